@@ -1,0 +1,367 @@
+"""CPU oracle for the rotated INT2 KV cache: append (rotate, clip, group-128 INT2
+quantise, BF16 sink/recent windows) and mixed INT2/BF16 decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+benchmark's CPU-baseline arm may import this module.  The product path (the
+CUDA library and its Python binding) never calls it and shares no code with it.
+
+It is deliberately plain: numpy, one pass, no blocking, no splits.  The codec is
+computed in float32 with the operation order written below (numpy float32
+element-wise ufuncs round every operation to nearest-even and never contract to
+FMA); everything attention-side is float64.
+
+Sources (titles of the pages describing OSCAR; section in brackets):
+
+* OSCAR-LLAMACPP-Qwen3-4B-Thinking-2507-INT2-KV model card [Run]: per-row
+  outlier clip before quantisation (clip ratio 0.96); first/last tokens kept
+  high-precision (sink 512 / recent 2048); [Files] note: the rotation is a
+  post-RoPE orthogonal transform applied to K and V.
+* OSCAR-LLAMACPP-Gemma-4-12B-it-INT2-KV card [Folders]: the rotation is applied
+  to Q/K (and V); per-layer 512x512 rotations exist (head_dim 512).
+* OSCAR-RotationZoo card [Available rotations]: G is the INT2 quant group size
+  along head_dim (group128); [How to use]: K clip 0.96, V clip 0.92, V
+  rotation absorbed, 64 prefix / 256 recent BF16 tokens, int2 KV dtype,
+  quant group size 128; [File format]: one head_dim x head_dim rotation per
+  layer, shared by the heads of the layer.
+* hysenlabs article on FutureMLS-Lab/OSCAR [What OSCAR compresses]: bulk of the
+  cache INT2, small BF16 sink and recent window; [How the offline rotation is
+  fit]: clipping thresholds bound the values before they are rounded; fused
+  mixed INT2+BF16 flash attention instead of dequantise-then-attend.
+
+Readings taken where the pages are silent (each listed in the design doc):
+
+* quantiser: asymmetric per group of 128 along head_dim, scale=(max-min)/3,
+  zero=min, both stored as IEEE fp16 (round-to-nearest-even);
+* clip: t = ratio * max_j |r_j| over the whole rotated row (one token, one KV
+  head, all head_dim channels), x = clamp(r, -t, t), before grouping;
+* constant group (scale rounds to 0): every code is 0 and the value is zero;
+* code = clamp(rint_half_even((x - zero) * (1 / scale)), 0, 3), with the
+  reciprocal correctly rounded and no fused multiply-add;
+* row-vector rotation k' = k R with R stored [D][D] row-major; Q uses R_K;
+  the output is un-rotated once, o = o' R_V^T, unless the V rotation is
+  absorbed by the caller;
+* windows: sink = positions [0, S), ring = [max(S, T-W), T), INT2 = the rest;
+  BF16 window copies hold BF16(RNE) of the same float32 rotated row;
+* softmax scale 1/sqrt(D) unless given.
+
+The byte layout written by :func:`append` is the one the C header documents
+for the cache (regions, strides, code bit positions); it is implemented here
+from that description, independently of the CUDA code.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+GROUP = 128
+ALIGN = 256
+NCAP_ROUND = 64
+
+FLAG_ABSORB_V = 1
+FLAG_IN_FP32 = 2
+FLAG_OUT_FP32 = 4
+
+
+# --------------------------------------------------------------------------
+# configuration and layout
+# --------------------------------------------------------------------------
+@dataclass
+class Config:
+    num_layers: int
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    sink: int
+    recent: int
+    capacity: int
+    k_clip: float = 0.96
+    v_clip: float = 0.92
+    flags: int = 0
+    group_size: int = GROUP
+
+    @property
+    def G(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+
+def _align(x: int) -> int:
+    return (x + ALIGN - 1) // ALIGN * ALIGN
+
+
+def layout(cfg: Config) -> dict:
+    """Byte sizes of one layer's cache, per the header's documented formulas.
+
+    Per layer: K role then V role.  Per role: sink [B][Hkv][S][D] bf16, ring
+    [B][Hkv][W][D] bf16, codes [B][Hkv][Ncap][D/4] u8, sz [B][Hkv][Ncap][D/128]
+    x (fp16 scale, fp16 zero); Ncap = round_up(max(capacity - S, 0), 64); each
+    region starts on a 256-byte boundary.
+    """
+    B, H, D, S, W = cfg.batch, cfg.num_kv_heads, cfg.head_dim, cfg.sink, cfg.recent
+    ncap = -(-max(cfg.capacity - S, 0) // NCAP_ROUND) * NCAP_ROUND
+    sink = _align(B * H * S * D * 2)
+    ring = _align(B * H * W * D * 2)
+    codes = _align(B * H * ncap * (D // 4))
+    sz = _align(B * H * ncap * (D // GROUP) * 4)
+    role = sink + ring + codes + sz
+    return dict(ncap=ncap, sink_bytes=sink, ring_bytes=ring, codes_bytes=codes,
+                sz_bytes=sz, role_bytes=role, layer_bytes=2 * role,
+                total_bytes=2 * role * cfg.num_layers)
+
+
+# --------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bits.
+
+    bf16 is the top half of a float32; rounding adds 0x7FFF plus the lowest kept
+    bit before truncating, which is round-half-to-even on the dropped 16 bits.
+    NaN stays a quiet NaN.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    r[nan] = 0x7FC0
+    return r
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# rotation and codec
+# --------------------------------------------------------------------------
+def rotate_rows(x: np.ndarray, R: np.ndarray) -> np.ndarray:
+    """r = x R (row vectors, R [D][D] row-major), exact float64 product rounded
+    once to float32."""
+    return (np.asarray(x, np.float64) @ np.asarray(R, np.float64)).astype(np.float32)
+
+
+def quantize_rows(r: np.ndarray, ratio: float):
+    """Clip then group-128 asymmetric INT2 quantisation of float32 rows.
+
+    r: [N, D] float32 rotated rows.  Returns (codes [N, D] uint8 in 0..3,
+    scale [N, D/128] float16, zero [N, D/128] float16).
+
+    Steps, each a float32 round-to-nearest operation:
+      a = max_j |r_j| ; t = ratio * a ; x = min(max(r, -t), t)
+      per group: mn = min x, mx = max x ; s32 = (mx - mn) / 3
+      scale = fp16(s32) ; zero = fp16(mn)
+      scale == 0      -> code 0
+      otherwise inv = 1 / scale ; code = clamp(rint((x - zero) * inv), 0, 3)
+    A non-finite scale or zero also yields code 0.
+    """
+    r = np.ascontiguousarray(r, dtype=np.float32)
+    n, d = r.shape
+    ng = d // GROUP
+    a = np.max(np.abs(r), axis=1)
+    t = (np.float32(ratio) * a).astype(np.float32)
+    x = np.minimum(np.maximum(r, -t[:, None]), t[:, None])
+    xg = x.reshape(n, ng, GROUP)
+    mn = xg.min(axis=2)
+    mx = xg.max(axis=2)
+    s32 = ((mx - mn) / np.float32(3.0)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        scale = s32.astype(np.float16)
+        zero = mn.astype(np.float16)
+    sf = scale.astype(np.float32)
+    zf = zero.astype(np.float32)
+    ok = (sf != 0) & np.isfinite(sf) & np.isfinite(zf)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        inv = np.where(ok, np.float32(1.0) / np.where(ok, sf, np.float32(1.0)), np.float32(0.0))
+        inv = inv.astype(np.float32)
+        y = ((xg - zf[:, :, None]).astype(np.float32) * inv[:, :, None]).astype(np.float32)
+        q = np.rint(y)
+    q = np.where(ok[:, :, None], q, 0.0)
+    codes = np.clip(q, 0, 3).astype(np.uint8).reshape(n, d)
+    return codes, scale, zero
+
+
+def dequantize_rows(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """x_hat = zero + scale * code, exact in float64 (fp16 inputs)."""
+    n, d = codes.shape
+    s = scale.astype(np.float64).repeat(GROUP, axis=1)
+    z = zero.astype(np.float64).repeat(GROUP, axis=1)
+    return z + s * codes.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# physical code packing (the header's bit layout)
+# --------------------------------------------------------------------------
+def pack_codes(codes: np.ndarray, role: int) -> np.ndarray:
+    """Pack [N, D] codes (0..3) into [N, D/4] bytes.
+
+    A row is D/16 little-endian 32-bit words; word w, bit b holds the code of
+    one dim.  With j the 128-dim group:
+      K (role 0): word j*8 + 2*c + i (c 0..3, i 0..1); for p in 0..7 with
+        kk = 4*i + p//2 and h = p%2: bit 2p <- dim 128j + 16kk + 2c + 8h,
+        bit 16+2p <- that dim + 1.
+      V (role 1): word j*8 + g (g 0..7); bit 2n (n 0..15) <- dim 128j + 8n + g.
+    """
+    n, d = codes.shape
+    words = np.zeros((n, d // 16), dtype=np.uint32)
+    for dim, word, bit in _bit_map(d, role):
+        words[:, word] |= codes[:, dim].astype(np.uint32) << np.uint32(bit)
+    return words.view(np.uint8).reshape(n, d // 4)
+
+
+def unpack_codes(packed: np.ndarray, d: int, role: int) -> np.ndarray:
+    n = packed.shape[0]
+    words = np.ascontiguousarray(packed, dtype=np.uint8).reshape(n, d // 4).view(np.uint32)
+    codes = np.zeros((n, d), dtype=np.uint8)
+    for dim, word, bit in _bit_map(d, role):
+        codes[:, dim] = (words[:, word] >> np.uint32(bit)) & np.uint32(3)
+    return codes
+
+
+def _bit_map(d: int, role: int):
+    """(dim, word, bit) triples for every dim of a row."""
+    out = []
+    for j in range(d // GROUP):
+        if role == 0:
+            for c in range(4):
+                for i in range(2):
+                    for p in range(8):
+                        kk = 4 * i + p // 2
+                        h = p % 2
+                        dim = GROUP * j + 16 * kk + 2 * c + 8 * h
+                        word = j * 8 + 2 * c + i
+                        out.append((dim, word, 2 * p))
+                        out.append((dim + 1, word, 16 + 2 * p))
+        else:
+            for g in range(8):
+                for n in range(16):
+                    out.append((GROUP * j + 8 * n + g, j * 8 + g, 2 * n))
+    return out
+
+
+# --------------------------------------------------------------------------
+# cache views
+# --------------------------------------------------------------------------
+class CacheView:
+    """numpy views of one (layer, role) of a cache byte buffer."""
+
+    def __init__(self, cfg: Config, buf: np.ndarray, layer: int, role: int):
+        lay = layout(cfg)
+        B, H, D, S, W = cfg.batch, cfg.num_kv_heads, cfg.head_dim, cfg.sink, cfg.recent
+        base = layer * lay["layer_bytes"] + role * lay["role_bytes"]
+        ncap = lay["ncap"]
+        o = base
+        self.sink = buf[o:o + B * H * S * D * 2].view(np.uint16).reshape(B, H, S, D)
+        o += lay["sink_bytes"]
+        self.ring = buf[o:o + B * H * W * D * 2].view(np.uint16).reshape(B, H, W, D)
+        o += lay["ring_bytes"]
+        self.codes = buf[o:o + B * H * ncap * D // 4].reshape(B, H, ncap, D // 4)
+        o += lay["codes_bytes"]
+        self.sz = buf[o:o + B * H * ncap * (D // GROUP) * 4].view(np.float16).reshape(
+            B, H, ncap, D // GROUP, 2)
+
+
+def new_cache(cfg: Config) -> np.ndarray:
+    return np.zeros(layout(cfg)["total_bytes"], dtype=np.uint8)
+
+
+# --------------------------------------------------------------------------
+# append
+# --------------------------------------------------------------------------
+def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new: np.ndarray,
+           start_pos, R_K: np.ndarray, R_V: np.ndarray, return_rot: bool = False):
+    """Write n new tokens per sequence at positions start_pos[b] .. +n-1.
+
+    k_new, v_new: [B][n][Hkv][D] float (bf16 values as float32, or float32).
+    R_K, R_V: [D][D] rotations of this layer.  Every position p >= S gets its
+    INT2 row; p < S also goes to the BF16 sink; p >= start_pos[b] + n - W also
+    goes to the BF16 ring slot p mod W.
+    """
+    B, n, H, D = k_new.shape
+    S, W = cfg.sink, cfg.recent
+    rots = []
+    for role, (x, R, ratio) in enumerate(((k_new, R_K, cfg.k_clip), (v_new, R_V, cfg.v_clip))):
+        view = CacheView(cfg, cache, layer, role)
+        r = rotate_rows(np.asarray(x, np.float32).reshape(-1, D), R).reshape(B, n, H, D)
+        rots.append(r)
+        codes, scale, zero = quantize_rows(r.reshape(-1, D), ratio)
+        packed = pack_codes(codes, role).reshape(B, n, H, D // 4)
+        scale = scale.reshape(B, n, H, -1)
+        zero = zero.reshape(B, n, H, -1)
+        rb = f32_to_bf16_bits(r.reshape(-1, D)).reshape(B, n, H, D)
+        for b in range(B):
+            newlen = int(start_pos[b]) + n
+            for t in range(n):
+                p = int(start_pos[b]) + t
+                if p < S:
+                    view.sink[b, :, p, :] = rb[b, t]
+                else:
+                    view.codes[b, :, p - S, :] = packed[b, t]
+                    view.sz[b, :, p - S, :, 0] = scale[b, t]
+                    view.sz[b, :, p - S, :, 1] = zero[b, t]
+                if W > 0 and p >= newlen - W:
+                    view.ring[b, :, p % W, :] = rb[b, t]
+    if return_rot:
+        return rots[0], rots[1]
+    return None
+
+
+# --------------------------------------------------------------------------
+# decode
+# --------------------------------------------------------------------------
+def regions(T: int, S: int, W: int):
+    """(n_sink, Tq, n_int2, n_ring): sink [0, n_sink), INT2 [S, Tq), ring [Tq, T)."""
+    if T <= S:
+        return T, T, 0, 0
+    tq = max(S, T - W)
+    return S, tq, tq - S, T - tq
+
+
+def dequant_history(cfg: Config, cache: np.ndarray, layer: int, role: int, b: int, h: int, T: int):
+    """[T, D] float64 values the decode attends to for one (b, kv head)."""
+    view = CacheView(cfg, cache, layer, role)
+    D, S, W = cfg.head_dim, cfg.sink, cfg.recent
+    n_sink, tq, n_int, n_ring = regions(T, S, W)
+    out = np.zeros((T, D), dtype=np.float64)
+    if n_sink:
+        out[:n_sink] = bf16_bits_to_f32(view.sink[b, h, :n_sink])
+    if n_int:
+        codes = unpack_codes(view.codes[b, h, :n_int], D, role)
+        sc = view.sz[b, h, :n_int, :, 0]
+        ze = view.sz[b, h, :n_int, :, 1]
+        out[S:tq] = dequantize_rows(codes, sc, ze)
+    for p in range(tq, T):
+        out[p] = bf16_bits_to_f32(view.ring[b, h, p % W])
+    return out
+
+
+def decode(cfg: Config, cache: np.ndarray, layer: int, q: np.ndarray, seq_lens, R_K: np.ndarray,
+           R_V: np.ndarray, sm_scale: float = 0.0, absorb_v: bool = False):
+    """One decode step of attention over the mixed cache, float64.
+
+    q: [B][Hq][D] (bf16 values as float).  Query head i reads KV head i // G.
+    Returns (out [B][Hq][D] float64, lse [B][Hq] float64 natural log).
+    """
+    B, Hq, D = q.shape
+    G = cfg.G
+    scale = sm_scale if sm_scale > 0 else 1.0 / math.sqrt(D)
+    RK = np.asarray(R_K, np.float64)
+    RV = np.asarray(R_V, np.float64)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64)
+    for b in range(B):
+        T = int(seq_lens[b])
+        for h in range(cfg.num_kv_heads):
+            K = dequant_history(cfg, cache, layer, 0, b, h, T)
+            V = dequant_history(cfg, cache, layer, 1, b, h, T)
+            for i in range(h * G, (h + 1) * G):
+                qr = np.asarray(q[b, i], np.float64) @ RK
+                s = scale * (K @ qr)
+                m = s.max()
+                e = np.exp(s - m)
+                l = e.sum()
+                o_rot = (e @ V) / l
+                out[b, i] = o_rot if absorb_v else o_rot @ RV.T
+                lse[b, i] = m + math.log(l)
+    return out, lse

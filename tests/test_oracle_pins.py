@@ -1,0 +1,426 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix (hand-derived examples, closed forms, invariants, library routines, brute
+force on tiny inputs).  CPU only."""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oscar_oracle as O
+from int2_kv_cache_append_gb300 import synth as S
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")))
+
+
+# --------------------------------------------------------------------------
+# number formats against library conversions
+# --------------------------------------------------------------------------
+def _tricky_f32(n=20000, seed=0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(n).astype(np.float32) * np.float32(10.0) ** rng.integers(-6, 6, n).astype(np.float32)
+    # exact bf16 ties: low 16 bits 0x8000, both parities of the kept lsb
+    ties = (rng.integers(0, 2 ** 15, 256).astype(np.uint32) << 16 | 0x8000).view(np.float32)
+    return np.concatenate([x, ties, np.array([0.0, -0.0, 1.0, -2.5, 65504.0, 1e-40], np.float32)])
+
+
+def test_bf16_rounding_matches_torch():
+    x = _tricky_f32()
+    ours = O.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_fp16_rounding_matches_torch():
+    x = _tricky_f32(seed=1)
+    x = x[np.abs(x) < 60000]
+    ours = x.astype(np.float16).view(np.uint16)
+    ref = torch.from_numpy(x).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# --------------------------------------------------------------------------
+# codec: hand-derived rows
+# --------------------------------------------------------------------------
+def _row(vals, d=128):
+    r = np.zeros((1, d), np.float32)
+    r[0, :len(vals)] = vals
+    return r
+
+
+def test_codec_hand_example_ties_to_even():
+    # mn=-3, mx=3 -> scale=(3-(-3))/3=2, zero=-3; (x+3)/2: -3->0, -1->1, 1->2, 3->3,
+    # 0 -> 1.5 -> 2 (even), -2 -> 0.5 -> 0 (even), 2 -> 2.5 -> 2 (even)
+    r = _row([-3, -1, 1, 3, 0, -2, 2])
+    codes, sc, ze = O.quantize_rows(r, 1.0)
+    assert float(sc[0, 0]) == 2.0 and float(ze[0, 0]) == -3.0
+    assert list(codes[0, :7]) == [0, 1, 2, 3, 2, 0, 2]
+    assert (codes[0, 7:] == 2).all()  # the zero padding also sits on a tie
+
+
+def test_codec_clip_bounds_outlier_per_row_not_per_group():
+    # D=256: outlier 10 in group 0; group 1 holds values in [-5, 5].
+    # Row threshold t = fl32(0.96) * 10 = 9.6 (as float32); group 0's max becomes t,
+    # group 1 is untouched because 5 < t.  A per-group clip would shrink group 1.
+    d = 256
+    r = np.zeros((1, d), np.float32)
+    r[0, 0] = 10.0
+    r[0, 1] = -1.0
+    r[0, 128] = 5.0
+    r[0, 129] = -5.0
+    codes, sc, ze = O.quantize_rows(r, 0.96)
+    t = np.float32(0.96) * np.float32(10.0)
+    xh = O.dequantize_rows(codes, sc, ze)
+    # group 0: mn=-1, mx=t -> top code reconstructs t up to fp16 rounding of scale/zero
+    assert codes[0, 0] == 3
+    assert abs(xh[0, 0] - float(t)) <= 3 * abs(float(sc[0, 0]) - (float(t) + 1) / 3) + abs(float(ze[0, 0]) + 1) + 1e-6
+    assert abs(xh[0, 0] - 10.0) > 0.3
+    # group 1 keeps its full range: zero=-5, scale=10/3 in fp16
+    assert float(ze[0, 1]) == -5.0
+    assert float(sc[0, 1]) == float(np.float16(np.float32(10.0) / np.float32(3.0)))
+
+
+def test_codec_constant_group():
+    r = np.full((1, 128), 1.5, np.float32)
+    codes, sc, ze = O.quantize_rows(r, 1.0)
+    assert float(sc[0, 0]) == 0.0 and float(ze[0, 0]) == 1.5 and (codes == 0).all()
+    # with a clip ratio the constant row is clipped to ratio*1.5 first
+    codes, sc, ze = O.quantize_rows(r, 0.92)
+    assert float(ze[0, 0]) == float(np.float16(np.float32(0.92) * np.float32(1.5)))
+
+
+def test_codec_lattice_rows_round_trip_exactly():
+    # x = z + s*c with fp16-exact s and z, extremes present, ratio 1: exact.
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        d = int(rng.choice([128, 256, 512]))
+        rows = []
+        for _g in range(d // 128):
+            s = float(np.float16(rng.uniform(0.01, 4.0)))
+            z = float(np.float16(rng.uniform(-8, 0)))
+            c = rng.integers(0, 4, 128)
+            c[0], c[1] = 0, 3
+            rows.append(z + s * c)
+        r = np.concatenate(rows)[None].astype(np.float32)
+        # keep the whole row's max |x| as the top value so ratio=1 clips nothing
+        codes, sc, ze = O.quantize_rows(r, 1.0)
+        xh = O.dequantize_rows(codes, sc, ze)
+        assert np.array_equal(xh.astype(np.float32), r), "lattice row not reproduced"
+
+
+def test_codec_error_bound_and_code_range_random():
+    rng = np.random.default_rng(4)
+    r = S.activations(rng, (400, 256), [3, 100, 200], kind="t3")
+    for ratio in (1.0, 0.96, 0.92):
+        codes, sc, ze = O.quantize_rows(r, ratio)
+        assert codes.max() <= 3
+        a = np.abs(r).max(axis=1)
+        t = (np.float32(ratio) * a)[:, None]
+        x = np.clip(r, -t, t).astype(np.float64)
+        xh = O.dequantize_rows(codes, sc, ze)
+        xg = x.reshape(400, 2, 128)
+        mn, mx = xg.min(2), xg.max(2)
+        s32 = (mx - mn) / 3
+        s16 = sc.astype(np.float64)
+        z16 = ze.astype(np.float64)
+        slack = s16 / 2 + 3 * np.abs(s16 - s32) + np.abs(z16 - mn) + 4 * np.spacing(np.abs(mx).astype(np.float32))
+        err = np.abs(xh - x).reshape(400, 2, 128).max(2)
+        assert (err <= slack + 1e-7).all()
+        # rounding to nearest: most elements sit well inside s/2
+        assert np.mean(np.abs(xh - x).reshape(400, 2, 128) <= s16[:, :, None] / 2 + 1e-6) > 0.99
+
+
+def test_codec_multiplies_by_correctly_rounded_reciprocal():
+    # scale 0.88671875 (fp16 0x3B18), zero -0.68408203125 (fp16 0xB979) and the
+    # float32 x with bits 0xBE767FFE (found by search): the product with the
+    # float32 reciprocal rounds to exactly 0.5, a tie that goes to the even code
+    # 0, whereas a true division rounds just above 0.5 and gives code 1.
+    s = np.float32(np.uint16(15128).view(np.float16))
+    z = np.float32(np.uint16(47481).view(np.float16))
+    x = np.array([3195437054], np.uint32).view(np.float32)[0]
+    dx = np.float32(x - z)
+    via_rcp = np.rint(np.float32(dx * (np.float32(1.0) / s)))
+    via_div = np.rint(np.float32(dx / s))
+    assert via_rcp == 0.0 and via_div == 1.0          # the two readings disagree here
+    # exact rational check of the reciprocal path: 1/s rounded to float32 first,
+    # the exact product lies within half a float32 ulp of 1/2, so it rounds to 1/2
+    inv = Fraction(float(np.float32(1.0) / s))
+    prod = Fraction(float(dx)) * inv
+    assert abs(prod - Fraction(1, 2)) <= Fraction(1, 2 ** 26)
+    assert Fraction(float(dx)) / Fraction(float(s)) > Fraction(1, 2) + Fraction(1, 2 ** 26)
+    row = np.full((1, 128), x, np.float32)
+    row[0, 0] = z
+    row[0, 1] = np.float32(z + np.float32(3) * s)     # max: scale comes out exactly s
+    codes, sc, ze = O.quantize_rows(row, 1.0)
+    assert np.float32(sc[0, 0]) == s and np.float32(ze[0, 0]) == z
+    assert codes[0, 2] == 0
+
+
+# --------------------------------------------------------------------------
+# physical packing: bytes derived by hand from the documented bit layout
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("role,dim,byte,val", [
+    (0, 0, 0, 0x01),     # K: dim 0 -> word 0 bit 0
+    (0, 1, 2, 0x01),     # K: dim 1 -> word 0 bit 16
+    (0, 8, 0, 0x04),     # K: dim 8 = 16*0 + 2*0 + 8*1 -> p=1 -> bit 2
+    (0, 2, 8, 0x01),     # K: dim 2 -> c=1 -> word 2 -> byte 8
+    (0, 16, 0, 0x10),    # K: dim 16 -> kk=1 -> p=2 -> bit 4
+    (0, 64, 4, 0x01),    # K: dim 64 -> kk=4 -> word 1 bit 0
+    (0, 15, 14, 0x40),   # K: dim 15 = 14+1 -> c=3,h=1 -> word 6 bit 16+2 -> byte 26? see below
+    (1, 0, 0, 0x01),     # V: dim 0 -> word 0 bit 0
+    (1, 1, 4, 0x01),     # V: dim 1 -> word 1 (g=1) bit 0
+    (1, 8, 0, 0x04),     # V: dim 8 -> g=0, n=1 -> bit 2
+    (1, 127, 31, 0x40),  # V: dim 127 = 8*15+7 -> word 7 bit 30 -> byte 31 bit 6
+])
+def test_pack_layout_hand_bytes(role, dim, byte, val):
+    if role == 0 and dim == 15:
+        # dim 15 = 16*0 + 2*3 + 8*1 + 1 -> c=3, i=0, p=1 (kk=0,h=1): word 6, bit 16+2=18
+        byte, val = 6 * 4 + 2, 0x04
+    codes = np.zeros((1, 128), np.uint8)
+    codes[0, dim] = 1
+    packed = O.pack_codes(codes, role)
+    expect = np.zeros(32, np.uint8)
+    expect[byte] = val
+    assert np.array_equal(packed[0], expect)
+
+
+def test_pack_second_group_offsets():
+    codes = np.zeros((1, 256), np.uint8)
+    codes[0, 129] = 3          # V: group 1, g=1, n=0 -> word 9, bits 0-1
+    p = O.pack_codes(codes, 1)
+    assert p[0, 36] == 3 and p[0].sum() == 3
+    p = O.pack_codes(codes, 0)  # K: group 1 dim 1 -> word 8 bit 16 -> byte 34
+    assert p[0, 34] == 3 and p[0].sum() == 3
+
+
+# --------------------------------------------------------------------------
+# rotations (generator) and rotation invariance
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [128, 256, 512])
+def test_hadamard_bitrev_closed_forms(d):
+    h = S.hadamard(d)
+    assert np.abs(h @ h.T - np.eye(d)).max() < 1e-12
+    assert np.all(np.abs(np.abs(h) - 1 / math.sqrt(d)) < 1e-15)
+    p = S.bit_reversal(d)
+    assert np.array_equal(p @ p, np.eye(d))  # involution
+
+
+def test_eig_rotation_sorted_eigvecs_and_orthogonal():
+    w = S.WORKLOADS["tiny"]
+    calib = S.activations(S.rng_for(0, 0, S.ROLE_CALIB), (4096, 128), [3, 17, 90], kind="scale")
+    r = S.eig_rotation(calib)
+    e = r @ S.bit_reversal(128).T @ S.hadamard(128).T     # undo H P_br
+    sig = calib.astype(np.float64).T @ calib.astype(np.float64)
+    lam = np.diag(e.T @ sig @ e)
+    assert np.all(np.diff(lam) <= 1e-6 * lam[0])
+    assert np.abs(sig @ e - e * lam).max() < 1e-6 * lam[0]
+    rk, rv = S.rotations(w, 0)
+    for R in (rk, rv):
+        assert np.abs(R.astype(np.float64) @ R.T.astype(np.float64) - np.eye(128)).max() <= 1e-5
+
+
+def test_rotation_invariance_of_scores():
+    w = S.WORKLOADS["tiny"]
+    rk, _ = S.rotations(w, 0)
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((8, 128))
+    k = rng.standard_normal((64, 128))
+    R = rk.astype(np.float64)
+    assert np.abs((q @ R) @ (k @ R).T - q @ k.T).max() < 1e-4  # fp32 R: |RR^T - I| ~ 1e-8
+    Rx = S.eig_rotation(S.activations(S.rng_for(0, 0, S.ROLE_CALIB), (4096, 128), [3, 17, 90], "scale"))
+    assert np.abs((q @ Rx) @ (k @ Rx).T - q @ k.T).max() < 1e-10
+
+
+# --------------------------------------------------------------------------
+# layout against the pages' numbers
+# --------------------------------------------------------------------------
+def test_layout_compression_matches_pages():
+    assert GOLD["group_size"]["value"] == O.GROUP
+    d = 128
+    int2_row = d // 4 + 4 * (d // O.GROUP)      # codes + fp16 scale + fp16 zero
+    ratio = (2 * d) / int2_row
+    assert abs(ratio - GOLD["compression_vs_16bit"]["value"]) < 0.25     # "~7x"
+    assert (2 * d) / (d // 4) == GOLD["reduction_vs_bf16"]["value"]       # code bits alone: 8x
+    layers, hd = GOLD["qwen3_4b_layers_head_dim"]["value"]
+    mb = layers * hd * hd * 4 / 1e6                                       # fp32 matrices
+    assert abs(mb - GOLD["qwen3_4b_rotation_file_mb"]["value"]) < 0.1
+    g = GOLD["gemma_rotation"]["value"]
+    assert 512 * 512 * 4 * 18 / 1e6 == pytest.approx(g["size_mb_each"], rel=0.06)  # 48 layers? ~18.9MB
+
+
+def test_layout_sizes():
+    cfg = O.Config(2, 3, 8, 2, 256, 5, 7, 100)
+    lay = O.layout(cfg)
+    assert lay["ncap"] == 128
+    assert lay["sink_bytes"] == O._align(3 * 2 * 5 * 256 * 2)
+    assert lay["codes_bytes"] == O._align(3 * 2 * 128 * 64)
+    assert lay["sz_bytes"] == O._align(3 * 2 * 128 * 2 * 4)
+    assert lay["total_bytes"] == 2 * 2 * lay["role_bytes"]
+
+
+# --------------------------------------------------------------------------
+# append semantics
+# --------------------------------------------------------------------------
+def _small_cfg(S_=2, W=3, cap=40, D=128, G=2, Hkv=2, B=2):
+    return O.Config(1, B, Hkv * G, Hkv, D, S_, W, cap, 0.96, 0.92)
+
+
+def test_append_ring_slots_hand_example():
+    cfg = _small_cfg(S_=2, W=3, B=1, Hkv=1, G=1)
+    cache = O.new_cache(cfg)
+    I = np.eye(128, dtype=np.float32)
+    for p in range(7):
+        k = np.full((1, 1, 1, 128), p + 1.0, np.float32)
+        O.append(cfg, cache, 0, k, k, [p], I, I)
+    v = O.CacheView(cfg, cache, 0, 0)
+    got = O.bf16_bits_to_f32(v.ring[0, 0, :, 0])
+    assert list(got) == [7.0, 5.0, 6.0]      # slots 0,1,2 <- tokens 6,4,5 (values p+1)
+    assert list(O.bf16_bits_to_f32(v.sink[0, 0, :, 0])) == [1.0, 2.0]
+
+
+def test_append_chunking_invariance():
+    cfg = _small_cfg(S_=3, W=5, cap=64)
+    rng = np.random.default_rng(6)
+    rk = S.qr_rotation(rng, 128).astype(np.float32)
+    rv = S.qr_rotation(rng, 128).astype(np.float32)
+    T = 29
+    k = S.to_bf16_values(rng.standard_normal((2, T, 2, 128)).astype(np.float32))
+    v = S.to_bf16_values(rng.standard_normal((2, T, 2, 128)).astype(np.float32))
+    c1 = O.new_cache(cfg)
+    O.append(cfg, c1, 0, k, v, [0, 0], rk, rv)
+    c2 = O.new_cache(cfg)
+    pos = 0
+    for n in (1, 4, 2, 7, 1, 14):
+        O.append(cfg, c2, 0, k[:, pos:pos + n], v[:, pos:pos + n], [pos, pos], rk, rv)
+        pos += n
+    assert pos == T
+    q = S.to_bf16_values(rng.standard_normal((2, 4, 128)).astype(np.float32))
+    o1, l1 = O.decode(cfg, c1, 0, q, [T, T], rk, rv)
+    o2, l2 = O.decode(cfg, c2, 0, q, [T, T], rk, rv)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# --------------------------------------------------------------------------
+# attention: library routine, closed forms, brute force
+# --------------------------------------------------------------------------
+def test_all_bf16_window_equals_library_sdpa():
+    # S + W >= T: every token is BF16; with R = I the result is plain scaled
+    # dot-product attention over BF16(K), BF16(V) (torch reference, float64).
+    cfg = _small_cfg(S_=8, W=16, cap=64, G=3, Hkv=2, B=2)
+    rng = np.random.default_rng(7)
+    T = 20
+    k = S.to_bf16_values(rng.standard_normal((2, T, 2, 128)).astype(np.float32) * 2)
+    v = S.to_bf16_values(rng.standard_normal((2, T, 2, 128)).astype(np.float32))
+    I = np.eye(128, dtype=np.float32)
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, v, [0, 0], I, I)
+    q = S.to_bf16_values(rng.standard_normal((2, 6, 128)).astype(np.float32))
+    out, lse = O.decode(cfg, cache, 0, q, [T, T], I, I)
+    qt = torch.from_numpy(q.astype(np.float64))[:, :, None, :]             # B,Hq,1,D
+    kt = torch.from_numpy(k.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(3, dim=1)
+    vt = torch.from_numpy(v.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(3, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, :, 0].numpy()
+    assert np.abs(out - ref).max() < 1e-12
+    sc = torch.einsum("bhd,bhtd->bht", qt[:, :, 0], kt) / math.sqrt(128)
+    assert np.abs(lse - torch.logsumexp(sc, dim=-1).numpy()).max() < 1e-12
+
+
+def test_uniform_attention_window_boundaries_closed_form():
+    # K = 0 -> uniform attention; V rows constant p+1 per token.  BF16 tokens keep
+    # p+1; INT2 tokens hold the constant-row codec value fp16(fl32(ratio*(p+1))).
+    for (S_, W, T) in [(4, 6, 30), (0, 5, 17), (3, 0, 12), (5, 5, 9), (8, 4, 6), (2, 3, 3)]:
+        cfg = _small_cfg(S_=S_, W=W, cap=64, G=1, Hkv=1, B=1)
+        I = np.eye(128, dtype=np.float32)
+        cache = O.new_cache(cfg)
+        k = np.zeros((1, T, 1, 128), np.float32)
+        v = np.broadcast_to((np.arange(T, dtype=np.float32) + 1)[None, :, None, None], (1, T, 1, 128)).copy()
+        O.append(cfg, cache, 0, k, v, [0], I, I)
+        q = np.ones((1, 1, 128), np.float32)
+        out, lse = O.decode(cfg, cache, 0, q, [T], I, I)
+        total = 0.0
+        for p in range(T):
+            in_sink = p < S_
+            in_ring = p >= max(S_, T - W)
+            if in_sink or in_ring:
+                total += p + 1
+            else:
+                total += float(np.float16(np.float32(0.92) * np.float32(p + 1)))
+        assert abs(out[0, 0, 0] - total / T) < 1e-12, (S_, W, T)
+        assert abs(lse[0, 0] - math.log(T)) < 1e-12
+
+
+def test_one_hot_and_constant_v():
+    cfg = _small_cfg(S_=2, W=2, cap=64, G=2, Hkv=1, B=1)
+    rng = np.random.default_rng(8)
+    T = 40
+    I = np.eye(128, dtype=np.float32)
+    k = S.to_bf16_values(rng.standard_normal((1, T, 1, 128)).astype(np.float32))
+    k[0, 17, 0, :] = 0
+    k[0, 17, 0, 5] = 200.0      # one token with a huge logit (INT2 region)
+    vrow = np.float32(0.5) * np.arange(128, dtype=np.float32) % np.float32(4.0) - np.float32(1.0)
+    v = np.broadcast_to(vrow, (1, T, 1, 128)).copy()
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, v, [0], I, I)
+    q = np.zeros((1, 2, 128), np.float32)
+    q[0, 0, 5] = 50.0
+    out, _ = O.decode(cfg, cache, 0, q, [T], I, I)
+    # head 0: all weight on token 17 -> its INT2 reconstruction of vrow
+    expect17 = O.dequant_history(cfg, cache, 0, 1, 0, 0, T)[17]
+    assert np.abs(out[0, 0] - expect17).max() < 1e-9
+    # head 1 (q=0): uniform average; the constant V row: BF16 tokens give vrow,
+    # INT2 tokens give the same reconstruction each -> a closed-form mean
+    nb = 2 + 2
+    expect = (nb * vrow.astype(np.float64) + (T - nb) * expect17) / T
+    assert np.abs(out[0, 1] - expect).max() < 1e-12
+
+
+def test_decode_brute_force_tiny():
+    # Pure-Python loops, independent of the oracle's vectorised path.
+    cfg = _small_cfg(S_=2, W=3, cap=64, G=2, Hkv=2, B=2)
+    rng = np.random.default_rng(9)
+    T = [11, 7]
+    rk = S.qr_rotation(rng, 128).astype(np.float32)
+    rv = S.qr_rotation(rng, 128).astype(np.float32)
+    k = S.to_bf16_values(rng.standard_normal((2, 11, 2, 128)).astype(np.float32))
+    v = S.to_bf16_values(rng.standard_normal((2, 11, 2, 128)).astype(np.float32))
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k[:, :7], v[:, :7], [0, 0], rk, rv)
+    # both rows get 4 more tokens; row b=1 is then decoded with T=7, which must
+    # ignore every position >= 7
+    c2 = cache.copy()
+    O.append(cfg, c2, 0, k[:, 7:], v[:, 7:], [7, 7], rk, rv)
+    # row b=1 must look as if it had 7 tokens: decode with T=7 ignores positions >= 7
+    q = S.to_bf16_values(rng.standard_normal((2, 4, 128)).astype(np.float32))
+    out, lse = O.decode(cfg, c2, 0, q, T, rk, rv, absorb_v=False)
+    for b in range(2):
+        for i in range(4):
+            h = i // 2
+            K = O.dequant_history(cfg, c2, 0, 0, b, h, T[b])
+            V = O.dequant_history(cfg, c2, 0, 1, b, h, T[b])
+            qr = [sum(float(q[b, i, a]) * float(rk[a, j]) for a in range(128)) for j in range(128)]
+            sc = [sum(qr[j] * K[t, j] for j in range(128)) / math.sqrt(128) for t in range(T[b])]
+            m = max(sc)
+            e = [math.exp(s - m) for s in sc]
+            l = sum(e)
+            orot = [sum(e[t] * V[t, j] for t in range(T[b])) / l for j in range(128)]
+            o = [sum(orot[j] * float(rv[a, j]) for j in range(128)) for a in range(128)]
+            assert max(abs(o[a] - out[b, i, a]) for a in range(128)) < 1e-11
+            assert abs(m + math.log(l) - lse[b, i]) < 1e-11
+
+
+def test_absorb_v_is_output_in_rotated_basis():
+    cfg = _small_cfg(S_=2, W=3, cap=64)
+    rng = np.random.default_rng(10)
+    rk = S.qr_rotation(rng, 128).astype(np.float32)
+    rv = S.qr_rotation(rng, 128).astype(np.float32)
+    k = S.to_bf16_values(rng.standard_normal((2, 20, 2, 128)).astype(np.float32))
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, k[:, ::-1].copy(), [0, 0], rk, rv)
+    q = S.to_bf16_values(rng.standard_normal((2, 4, 128)).astype(np.float32))
+    o_abs, l1 = O.decode(cfg, cache, 0, q, [20, 13], rk, rv, absorb_v=True)
+    o, l2 = O.decode(cfg, cache, 0, q, [20, 13], rk, rv, absorb_v=False)
+    assert np.abs(o_abs @ rv.astype(np.float64).T - o).max() < 1e-12
+    assert np.array_equal(l1, l2)
