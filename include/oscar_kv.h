@@ -1,0 +1,199 @@
+/*
+ * oscar_kv.h — C ABI of a rotated 2-bit (INT2) KV cache with a BF16 sink and
+ * recent window, and of the decode attention that reads it, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * What it computes (sources are the pages describing OSCAR; page title and
+ * section in brackets):
+ *
+ *  - kv_append: for every new token and KV head, rotate the post-RoPE key and
+ *    value rows by the layer's orthogonal matrices, k' = k R_K, v' = v R_V
+ *    ["OSCAR-LLAMACPP-Qwen3-4B-Thinking-2507-INT2-KV" model card, note under
+ *    Files: in-graph post-RoPE orthogonal transform on K and V;
+ *    "OSCAR-RotationZoo" card, File format: one head_dim x head_dim rotation
+ *    per layer], clip the row to ratio * max|x| [model card, Run:
+ *    LLAMA_KV_CLIP_RATIO, per-row outlier clip before quant; RotationZoo, How
+ *    to use: K clip 0.96, V clip 0.92], quantise each group of 128 channels
+ *    along head_dim to 2-bit codes with an fp16 scale and zero [RotationZoo,
+ *    Available rotations: group128 along head_dim; How to use:
+ *    --kv-cache-dtype int2 --kv-cache-quant-group-size 128], and keep the
+ *    first `sink` and the last `recent` tokens as BF16 [model card, Run:
+ *    LLAMA_KV_HP_SINK / LLAMA_KV_HP_RECENT; hysenlabs article, What OSCAR
+ *    compresses: INT2 bulk with a small BF16 sink and recent window].
+ *
+ *  - attn_decode: one decode step of attention over that mixed cache without
+ *    a separate dequantise pass [hysenlabs article, How the offline rotation
+ *    is fit: fused mixed-precision flash attention]: the query is rotated by
+ *    R_K (the same rotation as K, so q'.k' = q.k) ["OSCAR-LLAMACPP-Gemma-4-
+ *    12B-it-INT2-KV" card, Folders: applied to Q/K (and V)], softmax over all
+ *    cached positions, and the value rotation is undone once at the output,
+ *    o = o' R_V^T, unless the caller absorbs it [RotationZoo, How to use:
+ *    SGLANG_OSCAR_ABSORB_V_ROTATION].
+ *
+ * Quantiser (the pages fix group, clip and 2-bit codes; the asymmetric
+ * min/max form and the exact operation order are this library's definition):
+ *   a = max_j |r_j| over the float32 rotated row; t = ratio * a;
+ *   x_j = min(max(r_j, -t), t);
+ *   per group of 128: mn = min x, mx = max x; s = fp16((mx - mn) / 3);
+ *   z = fp16(mn); code = 0 if s == 0, else
+ *   clamp(rint_half_even((x - z) * fl(1/s)), 0, 3);
+ *   every step is a float32 round-to-nearest operation without FMA.
+ *   Dequantised value: z + s * code.
+ *
+ * Cache layout (bytes; every region starts on a 256-byte boundary; the cache
+ * base pointer must be 256-byte aligned).  For layer l and role r (0 = K,
+ * 1 = V) the role block starts at l * layer_bytes + r * role_bytes and holds,
+ * in order:
+ *   sink  [B][Hkv][S][D]    bf16   position p < S
+ *   ring  [B][Hkv][W][D]    bf16   slot p mod W for the last W positions
+ *   codes [B][Hkv][Ncap][D/4] u8   row p - S for every position p >= S
+ *   sz    [B][Hkv][Ncap][D/128] x {fp16 scale, fp16 zero}, row p - S
+ *   with Ncap = round_up(max(capacity - S, 0), 64).
+ *   BF16 rows hold the round-to-nearest-even bf16 of the float32 rotated row.
+ *   A code row is D/16 little-endian 32-bit words; with j the 128-channel
+ *   group, word w bit b holds one channel's code:
+ *     K: word 8j + 2c + i (c = 0..3, i = 0..1); for p = 0..7, kk = 4i + p/2,
+ *        h = p % 2: bit 2p = channel 128j + 16kk + 2c + 8h, bit 16 + 2p =
+ *        that channel + 1.
+ *     V: word 8j + g (g = 0..7); bit 2n (n = 0..15) = channel 128j + 8n + g.
+ *   These orders let the decode kernel feed codes straight into tensor-core
+ *   fragments.
+ *
+ * Windows at decode time for a sequence of length T: sink = [0, min(S, T)),
+ * ring = [max(S, T - W), T), INT2 = [S, max(S, T - W)).
+ *
+ * Ownership: the caller owns every buffer (cache, inputs, rotations, outputs,
+ * workspace, status word); the library allocates nothing, keeps no state
+ * between calls beyond per-device launch settings, and only enqueues work on
+ * the given stream (a cudaStream_t passed as void*; NULL = legacy default).
+ * Calls may be captured in CUDA graphs.
+ *
+ * Errors: every entry point returns an oscar_status.  Argument checks happen
+ * on the host before anything is launched.  Conditions only the device can see
+ * are OR-ed into *dev_status (an int32 in device memory, may be NULL); kernels
+ * never trap.
+ */
+#ifndef OSCAR_KV_H
+#define OSCAR_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSCAR_KV_GROUP 128       /* quant group along head_dim */
+#define OSCAR_KV_MAX_SPLITS 64   /* upper bound on decode context splits */
+
+/* config flags */
+enum {
+  OSCAR_FLAG_ABSORB_V = 1, /* attn_decode returns o' (rotated basis); caller folds R_V^T into W_o */
+  OSCAR_FLAG_IN_FP32 = 2,  /* k_new, v_new and q are float32 instead of bf16 */
+  OSCAR_FLAG_OUT_FP32 = 4  /* attn_decode writes float32 instead of bf16 */
+};
+
+/* return codes */
+typedef enum {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID = -1,     /* null pointer, bad shape, clip not in (0,1], negative window, ... */
+  OSCAR_ERR_CAPACITY = -2,    /* n_new or the seq-length hint exceeds capacity */
+  OSCAR_ERR_WORKSPACE = -3,   /* workspace smaller than one split needs */
+  OSCAR_ERR_LAUNCH = -4,      /* a CUDA launch or attribute call failed */
+  OSCAR_ERR_UNSUPPORTED = -5  /* head_dim not in {128, 256, 512}, group != 128, G > 8 */
+} oscar_status;
+
+/* bits OR-ed into *dev_status by the kernels */
+enum {
+  OSCAR_DEV_OVER_CAPACITY = 1, /* a position or seq_len was >= capacity (row skipped / clamped) */
+  OSCAR_DEV_NONFINITE = 2,     /* a non-finite input row */
+  OSCAR_DEV_FP16_RANGE = 4,    /* a scale, zero or scaled query component left the fp16 range */
+  OSCAR_DEV_TIMEOUT = 8,       /* a pipeline wait gave up (the kernel returned early) */
+  OSCAR_DEV_EMPTY = 16         /* a sequence had seq_len < 1 (its output is zero) */
+};
+
+typedef struct {
+  int32_t num_layers;
+  int32_t batch;         /* B */
+  int32_t num_q_heads;   /* Hq; query head i uses KV head i / (Hq / Hkv) */
+  int32_t num_kv_heads;  /* Hkv */
+  int32_t head_dim;      /* D: 128, 256 or 512 */
+  int32_t group_size;    /* must be 128 */
+  int32_t sink;          /* S >= 0: first positions kept BF16 */
+  int32_t recent;        /* W >= 0: last positions kept BF16 */
+  int32_t capacity;      /* max positions per sequence (> 0) */
+  float k_clip;          /* clip ratio for K rows, in (0, 1] */
+  float v_clip;          /* clip ratio for V rows, in (0, 1] */
+  uint32_t flags;        /* OSCAR_FLAG_* */
+} oscar_kv_config;
+
+typedef struct {
+  uint64_t ncap;         /* INT2 rows per (sequence, KV head) */
+  uint64_t sink_bytes, ring_bytes, codes_bytes, sz_bytes; /* one role of one layer */
+  uint64_t role_bytes;   /* sink + ring + codes + sz */
+  uint64_t layer_bytes;  /* 2 * role_bytes (K then V) */
+  uint64_t total_bytes;  /* num_layers * layer_bytes */
+  uint64_t decode_workspace_bytes; /* attn_decode workspace for OSCAR_KV_MAX_SPLITS splits */
+  int32_t max_splits;    /* OSCAR_KV_MAX_SPLITS */
+  int32_t reserved;
+} oscar_kv_layout;
+
+/*
+ * kv_layout_query — sizes and offsets of the cache and of the decode
+ * workspace.  Host only, pure arithmetic.  Returns OSCAR_ERR_INVALID or
+ * OSCAR_ERR_UNSUPPORTED on a bad config, else fills *out.
+ * attn_decode with n splits needs
+ *   align256(B*Hq*D*4) + align256(B*Hq*(D/128)*4) + align256(B*Hq*n*D*4)
+ *   + align256(B*Hq*n*2*4) bytes of workspace.
+ */
+int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out);
+
+/*
+ * kv_append — write n_new new tokens per sequence into layer `layer`.
+ *   cache      device, layout above (written).
+ *   k_new,v_new device [B][n_new][Hkv][D] post-RoPE rows, bf16 (float32 with
+ *              OSCAR_FLAG_IN_FP32).
+ *   start_pos  device int32 [B]: position of each sequence's first new token.
+ *   R_K, R_V   device float32 [D][D] row-major rotations of this layer.
+ *   debug_rot_out device float32 [B][n_new][Hkv][2][D] or NULL: receives the
+ *              float32 rotated rows the quantiser saw (K then V).
+ *   dev_status device int32 or NULL.
+ * Position p = start_pos[b] + t gets its INT2 row when p >= S, its sink row
+ * when p < S and its ring slot p mod W when p >= start_pos[b] + n_new - W.
+ * Rows with p >= capacity are skipped and flagged OSCAR_DEV_OVER_CAPACITY.
+ * Enqueued on `stream`; inputs must stay valid until it completes.
+ */
+int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new,
+              const void* v_new, const int32_t* start_pos, int32_t n_new, const float* R_K,
+              const float* R_V, float* debug_rot_out, int32_t* dev_status, void* stream);
+
+/*
+ * attn_decode — one query token per sequence attends to all seq_lens[b]
+ * cached positions of layer `layer` (append the current token first).
+ *   q          device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_IN_FP32), not rotated.
+ *   seq_lens   device int32 [B], 1 <= seq_len <= capacity.
+ *   seq_len_hint host upper bound on seq_lens (0 = capacity); only used to
+ *              choose the number of context splits.
+ *   R_K, R_V   device float32 [D][D] rotations of this layer.
+ *   sm_scale   softmax scale; <= 0 means 1/sqrt(D).
+ *   num_splits 0 = automatic, else the number of context splits per
+ *              (sequence, KV head), at most OSCAR_KV_MAX_SPLITS.
+ *   out        device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_OUT_FP32);
+ *              o = o' R_V^T, or o' with OSCAR_FLAG_ABSORB_V.
+ *   lse        device float32 [B][Hq] or NULL: natural-log log-sum-exp of the
+ *              scaled scores.
+ *   workspace  device scratch of workspace_bytes (see kv_layout_query); the
+ *              automatic split count never needs more than is given.
+ * Launches three kernels on `stream` (query rotation, split attention, split
+ * merge + un-rotation).  Concurrent calls must not share a workspace.
+ */
+int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
+                const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
+                float sm_scale, int32_t num_splits, void* out, float* lse, void* workspace,
+                uint64_t workspace_bytes, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_KV_H */

@@ -1,0 +1,812 @@
+// attn_decode: one decode step of attention over the mixed INT2 / BF16 cache.
+//
+// Source: hysenlabs article on FutureMLS-Lab/OSCAR (How the offline rotation
+// is fit: a fused mixed-precision flash attention over the INT2 + BF16 layout,
+// no dequantise-then-attend pass); "OSCAR-LLAMACPP-Gemma-4-12B-it-INT2-KV"
+// card (Folders: the rotation applies to Q/K and V); "OSCAR-RotationZoo" (How
+// to use: V rotation absorbed into the output).
+//
+// Three kernels per call:
+//   qrot   q' = q R_K * sm_scale * log2(e) (float32) and per-group sums of q'.
+//   split  grid (splits, Hkv, B).  Four consumer warps and one producer warp.
+//          The producer streams 64-token INT2 blocks (codes + scale/zero) and
+//          16-token BF16 blocks (sink, ring) into a shared-memory ring with
+//          cp.async.bulk + mbarriers.  Consumers compute scores and P.V with
+//          mma.sync m16n8k16 in "swap-AB" form: tokens (QK) or channels (PV)
+//          on the M side, query heads on N, with each head's hi and lo fp16
+//          (bf16 for BF16 blocks) split in adjacent columns so that the
+//          products keep ~22 bits.  INT2 codes are unpacked straight into
+//          A fragments (exact small integers); per-token scale/zero are
+//          applied algebraically:
+//            s_t = scale_t * (q'.c_t) + zero_t * sum(q'),
+//            o  += (p_t * scale_t) . c_t  and  zeta += p_t * zero_t.
+//          Online softmax in log2 units; teams of D/128 warps split the
+//          channels of a block by quant group and exchange partial scores.
+//   merge  grid (B * Hkv): log-sum-exp merge of the splits, o = o' R_V^T
+//          (skipped when absorbed), store bf16/fp32 and lse.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kNCW = 4;                    // consumer warps
+constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
+constexpr int kI2Tok = 64;                 // tokens per INT2 block
+constexpr int kBfTok = 16;                 // tokens per BF16 block
+
+template <int D, int NQT>
+struct DecCfg {
+  static constexpr int Dg = D / kGroup;
+  static constexpr int TS = Dg;              // warps per team (one quant group each)
+  static constexpr int NTEAMS = kNCW / TS;
+  static constexpr int ROWB = D / 4;         // code bytes per token
+  static constexpr int BF_STRIDE = 2 * D + 16;
+  static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
+  static constexpr int BF_BYTES = 2 * kBfTok * BF_STRIDE;
+  static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 127) / 128 * 128;
+  static constexpr int NST = D == 128 ? 8 : (D == 256 ? 6 : 4);
+  static constexpr int HEADS = 4 * NQT;      // head slots per (b, kv head)
+  // shared memory carve-up (bytes)
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_QBF = OFF_STAGE + NST * STAGE;           // bf16 q fragments per warp
+  static constexpr int QBF_BYTES = kNCW * 8 * NQT * 32 * 8;
+  static constexpr int OFF_XCH = OFF_QBF + QBF_BYTES;               // team score exchange
+  static constexpr int XCH_BYTES = TS > 1 ? NTEAMS * 2 * TS * kI2Tok * HEADS * 4 : 0;
+  static constexpr int OFF_PART = OFF_XCH + XCH_BYTES;              // team partials
+  static constexpr int PART_BYTES = NTEAMS * HEADS * (D + 2) * 4;
+  static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
+  static constexpr int SMEM = OFF_BAR + 2 * NST * 8 + 16;
+};
+
+// Per-(b, kv head) region sizes and the block list
+struct Regions {
+  int T, n_sink, tq, n_int, n_ring;
+  int nsb, nib, nrb;
+  int64_t cbf, ci2;
+};
+
+__device__ __forceinline__ Regions make_regions(int T, int S, int W, int D) {
+  Regions r;
+  r.T = T;
+  if (T <= S) {
+    r.n_sink = T; r.tq = T; r.n_int = 0; r.n_ring = 0;
+  } else {
+    r.n_sink = S;
+    r.tq = max(S, T - W);
+    r.n_int = r.tq - S;
+    r.n_ring = T - r.tq;
+  }
+  r.nsb = (r.n_sink + kBfTok - 1) / kBfTok;
+  r.nib = (r.n_int + kI2Tok - 1) / kI2Tok;
+  r.nrb = (r.n_ring + kBfTok - 1) / kBfTok;
+  r.cbf = int64_t(2) * kBfTok * 2 * D;
+  r.ci2 = int64_t(2) * kI2Tok * (D / 4 + 4 * (D / kGroup));
+  return r;
+}
+
+// Smallest block index whose starting cost is >= x.
+__device__ __forceinline__ int first_block_at(const Regions& r, int64_t x) {
+  const int64_t c0 = r.nsb * r.cbf, c1 = c0 + r.nib * r.ci2;
+  if (x <= 0) return 0;
+  if (x <= c0) return int((x + r.cbf - 1) / r.cbf);
+  if (x <= c1) return r.nsb + int((x - c0 + r.ci2 - 1) / r.ci2);
+  const int k = r.nsb + r.nib + int((x - c1 + r.cbf - 1) / r.cbf);
+  return min(k, r.nsb + r.nib + r.nrb);
+}
+
+struct Blk {
+  int type;   // 0 sink, 1 int2, 2 ring
+  int first;  // sink/ring: first position; int2: first row (position - S)
+  int count;
+};
+
+__device__ __forceinline__ Blk block_at(const Regions& r, int k) {
+  Blk b;
+  if (k < r.nsb) {
+    b.type = 0; b.first = k * kBfTok; b.count = min(kBfTok, r.n_sink - b.first);
+  } else if (k < r.nsb + r.nib) {
+    b.type = 1; b.first = (k - r.nsb) * kI2Tok; b.count = min(kI2Tok, r.n_int - b.first);
+  } else {
+    b.type = 2; b.first = r.tq + (k - r.nsb - r.nib) * kBfTok; b.count = min(kBfTok, r.T - b.first);
+  }
+  return b;
+}
+
+// AND of `v` over the `n` threads meeting at named barrier `id`.
+__device__ __forceinline__ int team_all(int v, int id, int n) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n selp.s32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(v), "r"(id), "r"(n)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b) {
+  int T = a.seq_lens[b];
+  if (T > a.g.cap) T = a.g.cap;
+  if (T < 0) T = 0;
+  return T;
+}
+
+// ---------------------------------------------------------------------------
+// qrot: q' = q R_K * qscale, and per-group sums
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(D) qrot_kernel(const DecodeArgs a) {
+  __shared__ float qs[D];
+  __shared__ float red[D / 32];
+  const int bq = blockIdx.x;  // b * Hq + head
+  const int d = threadIdx.x;
+  if (a.in_fp32)
+    qs[d] = static_cast<const float*>(a.q)[int64_t(bq) * D + d];
+  else
+    qs[d] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[int64_t(bq) * D + d]);
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < D; ++i) acc = fmaf(qs[i], __ldg(a.R_K + i * D + d), acc);
+  acc *= a.qscale;
+  if (!(fabsf(acc) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
+  a.qprime[int64_t(bq) * D + d] = acc;
+  float s = acc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((d & 31) == 0) red[d >> 5] = s;
+  __syncthreads();
+  if (d < D / kGroup) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) t += red[d * 4 + w];
+    a.qsum[int64_t(bq) * (D / kGroup) + d] = t;
+  }
+  pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// split kernel
+// ---------------------------------------------------------------------------
+template <int D, int NQT>
+__global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
+  using C = DecCfg<D, NQT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  __shared__ int abort_flag;
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const Geom& g = a.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = clamp_seq_len(a, b);
+  const Regions rg = make_regions(T, g.S, g.W, D);
+  const int64_t total = rg.nsb * rg.cbf + rg.nib * rg.ci2 + rg.nrb * rg.cbf;
+  const int kb = first_block_at(rg, (int64_t(split) * total + a.ns - 1) / a.ns);
+  const int ke = first_block_at(rg, (int64_t(split + 1) * total + a.ns - 1) / a.ns);
+  const int nblk = ke - kb;
+  const int64_t bh = int64_t(b) * g.Hkv + h;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);                  // full: producer arrival + tx bytes
+      mbar_init(smem_u32(&bars[C::NST + s]), C::TS);     // empty: one arrival per team warp
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const uint8_t* kbase = a.layer_base;
+  const uint8_t* vbase = a.layer_base + g.role_bytes;
+  const uint64_t codes_off = g.sink_bytes + g.ring_bytes;
+  const uint64_t sz_off = codes_off + g.codes_bytes;
+
+  if (warp == kNCW) {
+    // ------------------------------- producer -------------------------------
+    int issued = 0;
+    for (int kl = 0; kl < nblk; ++kl) {
+      const int stage = kl % C::NST;
+      const uint32_t full = smem_u32(&bars[stage]);
+      const uint32_t empty = smem_u32(&bars[C::NST + stage]);
+      int ok = 1;
+      if (lane == 0) {
+        if (kl >= C::NST) ok = mbar_wait(empty, ((kl / C::NST) - 1) & 1);
+        if (!ok) status_or(a.status, OSCAR_DEV_TIMEOUT);
+        if (*((volatile int*)&abort_flag)) ok = 0;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);  // one decision for the whole warp
+      if (!ok) {
+        if (lane == 0) abort_flag = 1;
+        break;
+      }
+      const Blk bk = block_at(rg, kb + kl);
+      const uint32_t dst = smem_u32(smem + C::OFF_STAGE + stage * C::STAGE);
+      if (bk.type == 1) {
+        if (lane == 0) {
+          const int n4 = (bk.count + 3) & ~3;
+          const uint32_t cb = n4 * C::ROWB, sb = n4 * C::Dg * 4;
+          mbar_arrive_expect_tx(full, 2 * cb + 2 * sb);
+          const int64_t row = bh * g.ncap + bk.first;
+          bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
+          bulk_g2s(dst + kI2Tok * C::ROWB, vbase + codes_off + row * C::ROWB, cb, full);
+          bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
+          bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb,
+                   full);
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(full, 2 * bk.count * 2 * D);
+        __syncwarp();
+        const int r = lane & 15;
+        if (r < bk.count) {
+          const int pos = bk.first + r;
+          const uint8_t* base = lane < 16 ? kbase : vbase;
+          const uint8_t* src = bk.type == 0 ? base + (bh * g.S + pos) * (2 * D)
+                                            : base + g.sink_bytes + (bh * g.W + pos % g.W) * (2 * D);
+          bulk_g2s(dst + (lane < 16 ? 0 : kBfTok * C::BF_STRIDE) + r * C::BF_STRIDE, src, 2 * D, full);
+        }
+      }
+      issued = kl + 1;
+    }
+    // make sure nothing is still landing in shared memory before exiting
+    if (lane == 0) {
+      const int from = issued > C::NST ? issued - C::NST : 0;
+      for (int kl = from; kl < issued; ++kl)
+        if (!mbar_wait(smem_u32(&bars[kl % C::NST]), (kl / C::NST) & 1)) {
+          status_or(a.status, OSCAR_DEV_TIMEOUT);
+          break;
+        }
+    }
+    return;
+  }
+
+  // ------------------------------- consumers --------------------------------
+  const int team = warp / C::TS, wt = warp % C::TS;  // wt = quant group handled
+  const int gq = lane >> 2, cq = lane & 3;
+  const int Gh = g.G;
+  const int head0 = h * Gh;  // first query head of this kv head
+
+  pdl_wait();  // q' comes from the preceding kernel
+
+  // B fragments of q' for this warp's group: column n <-> (head n/2, hi|lo by n%2)
+  uint32_t qf[8][NQT][2];
+  float qsum[NQT];
+  uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + warp * 8 * NQT * 64;
+  {
+    const int hs_b = gq >> 1, lohalf = gq & 1;
+#pragma unroll
+    for (int nq = 0; nq < NQT; ++nq) {
+      const int hb = 4 * nq + hs_b;  // head slot of this lane's B column
+      const bool hv = hb < Gh;
+      const float* qp = a.qprime + (int64_t(b) * g.Hq + head0 + (hv ? hb : 0)) * D + wt * kGroup;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int d0 = 16 * kk + 2 * cq + 8 * half;
+          const float x0 = hv ? qp[d0] : 0.f, x1 = hv ? qp[d0 + 1] : 0.f;
+          const uint32_t s0 = split_f16(x0), s1 = split_f16(x1);
+          const uint32_t t0 = split_bf16(x0), t1 = split_bf16(x1);
+          // pick hi (low half) or lo (high half) of each split
+          const uint32_t v16 = lohalf ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
+          const uint32_t vbf = lohalf ? ((t0 >> 16) | (t1 & 0xffff0000u)) : ((t0 & 0xffffu) | (t1 << 16));
+          qf[kk][nq][half] = v16;
+          qbf[(kk * NQT + nq) * 64 + half * 32 + lane] = vbf;
+        }
+      }
+      const int hc = 4 * nq + cq;  // head owned by this lane in C fragments
+      qsum[nq] = hc < Gh ? a.qsum[(int64_t(b) * g.Hq + head0 + hc) * C::Dg + wt] : 0.f;
+    }
+  }
+  __syncwarp();
+
+  float o[8][NQT][4];
+  float m_run[NQT], l_run[NQT], zeta[NQT];
+#pragma unroll
+  for (int nq = 0; nq < NQT; ++nq) {
+    m_run[nq] = -INFINITY; l_run[nq] = 0.f; zeta[nq] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nq][e] = 0.f;
+  }
+
+  float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+  int xbuf = 0;
+
+  for (int kl = team; kl < nblk; kl += C::NTEAMS) {
+    const int stage = kl % C::NST;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (kl / C::NST) & 1);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    // the warps of a team must take the same decision: they meet at team barriers below
+    if constexpr (C::TS > 1) ok = team_all(ok, 1 + team, 32 * C::TS);
+    if (!ok) {
+      if (lane == 0) { abort_flag = 1; status_or(a.status, OSCAR_DEV_TIMEOUT); }
+      break;
+    }
+    const Blk bk = block_at(rg, kb + kl);
+    const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
+    const bool is_i2 = bk.type == 1;
+    constexpr int MT_MAX = kI2Tok / 16;
+    const int nmt = is_i2 ? MT_MAX : 1;
+
+    // ---- scores: s[mt][nq][0] token 16mt+gq, [1] token 16mt+gq+8
+    float s[MT_MAX][NQT][2];
+    float ksc[MT_MAX][2], kze[MT_MAX][2];
+    if (is_i2) {
+      const uint8_t* kc = st;
+      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB);
+#pragma unroll
+      for (int mt = 0; mt < MT_MAX; ++mt) {
+        const int t0 = 16 * mt + gq, t1 = t0 + 8;
+        const uint2 w0 = *reinterpret_cast<const uint2*>(kc + t0 * C::ROWB + wt * 32 + cq * 8);
+        const uint2 w1 = *reinterpret_cast<const uint2*>(kc + t1 * C::ROWB + wt * 32 + cq * 8);
+        float acc[NQT][4];
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nq][e] = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+          uint32_t r0[8], r1[8];
+          unpack16(wi ? w0.y : w0.x, r0);
+          unpack16(wi ? w1.y : w1.x, r1);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * wi + k4;
+#pragma unroll
+            for (int nq = 0; nq < NQT; ++nq)
+              mma_f16(acc[nq], r0[2 * k4], r1[2 * k4], r0[2 * k4 + 1], r1[2 * k4 + 1], qf[kk][nq][0],
+                      qf[kk][nq][1]);
+          }
+        }
+        const uint32_t z0 = ksz[t0 * C::Dg + wt], z1 = ksz[t1 * C::Dg + wt];
+        ksc[mt][0] = __half2float(__ushort_as_half(z0 & 0xffff));
+        kze[mt][0] = __half2float(__ushort_as_half(z0 >> 16));
+        ksc[mt][1] = __half2float(__ushort_as_half(z1 & 0xffff));
+        kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq) {
+          s[mt][nq][0] = fmaf(ksc[mt][0], acc[nq][0] + acc[nq][1], kze[mt][0] * qsum[nq]);
+          s[mt][nq][1] = fmaf(ksc[mt][1], acc[nq][2] + acc[nq][3], kze[mt][1] * qsum[nq]);
+        }
+      }
+    } else {
+      const uint32_t kb_s = smem_u32(st);
+      float acc[NQT][4];
+#pragma unroll
+      for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nq][e] = 0.f;
+      const int mi = lane >> 3;
+      const int tok = (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int dim = wt * kGroup + 16 * kk + 8 * (mi >> 1);
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(kb_s + tok * C::BF_STRIDE + dim * 2, a0, a1, a2, a3);
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq) {
+          const uint32_t b0 = qbf[(kk * NQT + nq) * 64 + lane];
+          const uint32_t b1 = qbf[(kk * NQT + nq) * 64 + 32 + lane];
+          mma_bf16(acc[nq], a0, a1, a2, a3, b0, b1);
+        }
+      }
+#pragma unroll
+      for (int nq = 0; nq < NQT; ++nq) {
+        s[0][nq][0] = acc[nq][0] + acc[nq][1];
+        s[0][nq][1] = acc[nq][2] + acc[nq][3];
+      }
+    }
+
+    // ---- team exchange of partial scores (one quant group per warp)
+    if constexpr (C::TS > 1) {
+      float* xb = xch + ((team * 2 + xbuf) * C::TS) * kI2Tok * C::HEADS;
+#pragma unroll
+      for (int mt = 0; mt < MT_MAX; ++mt) {
+        if (mt < nmt) {
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            const int hs = 4 * nq + cq;
+            xb[(wt * kI2Tok + 16 * mt + gq) * C::HEADS + hs] = s[mt][nq][0];
+            xb[(wt * kI2Tok + 16 * mt + gq + 8) * C::HEADS + hs] = s[mt][nq][1];
+          }
+        }
+      }
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * C::TS) : "memory");
+#pragma unroll
+      for (int mt = 0; mt < MT_MAX; ++mt) {
+        if (mt < nmt) {
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            const int hs = 4 * nq + cq;
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::TS; ++w) {
+              t0 += xb[(w * kI2Tok + 16 * mt + gq) * C::HEADS + hs];
+              t1 += xb[(w * kI2Tok + 16 * mt + gq + 8) * C::HEADS + hs];
+            }
+            s[mt][nq][0] = t0;
+            s[mt][nq][1] = t1;
+          }
+        }
+      }
+      xbuf ^= 1;
+    }
+
+    // ---- online softmax (log2 units)
+    float p[MT_MAX][NQT][2];
+#pragma unroll
+    for (int nq = 0; nq < NQT; ++nq) {
+      float mb = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < MT_MAX; ++mt) {
+        if (mt < nmt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tk = 16 * mt + gq + 8 * e;
+            const float v = tk < bk.count ? s[mt][nq][e] : -INFINITY;
+            s[mt][nq][e] = v;
+            mb = fmaxf(mb, v);
+          }
+        }
+      }
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+      const float mnew = fmaxf(m_run[nq], mb);
+      const float corr = ex2(m_run[nq] - mnew);  // 0 on the first block
+      m_run[nq] = mnew;
+      if (__any_sync(0xffffffffu, corr != 1.f)) {
+        l_run[nq] *= corr;
+        zeta[nq] *= corr;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][nq][e] *= corr;
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT_MAX; ++mt) {
+        if (mt < nmt) {
+          p[mt][nq][0] = ex2(s[mt][nq][0] - mnew);
+          p[mt][nq][1] = ex2(s[mt][nq][1] - mnew);
+          l_run[nq] += p[mt][nq][0] + p[mt][nq][1];
+        }
+      }
+    }
+
+    // ---- P.V
+    if (is_i2) {
+      const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + kI2Tok * C::ROWB);
+#pragma unroll
+      for (int ks = 0; ks < MT_MAX; ++ks) {
+        uint32_t bw0[NQT], bw1[NQT];
+        // V scale/zero of this lane's two tokens (group wt)
+        const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB) + kI2Tok * C::Dg;
+        const int t0 = 16 * ks + gq, t1 = t0 + 8;
+        const uint32_t z0 = vsz[t0 * C::Dg + wt], z1 = vsz[t1 * C::Dg + wt];
+        const float vs0 = __half2float(__ushort_as_half(z0 & 0xffff));
+        const float vz0 = __half2float(__ushort_as_half(z0 >> 16));
+        const float vs1 = __half2float(__ushort_as_half(z1 & 0xffff));
+        const float vz1 = __half2float(__ushort_as_half(z1 >> 16));
+        const bool v0 = t0 < bk.count, v1 = t1 < bk.count;
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq) {
+          const float w0 = v0 ? p[ks][nq][0] * vs0 : 0.f;
+          const float w1 = v1 ? p[ks][nq][1] * vs1 : 0.f;
+          zeta[nq] += (v0 ? p[ks][nq][0] * vz0 : 0.f) + (v1 ? p[ks][nq][1] * vz1 : 0.f);
+          bw0[nq] = movmatrix_trans(split_f16(w0));
+          bw1[nq] = movmatrix_trans(split_f16(w1));
+        }
+        // codes of word (wt, gq) for tokens 2cq, 2cq+1, 2cq+8, 2cq+9 of this k-step
+        const int ta = 16 * ks + 2 * cq;
+        const uint32_t wa = vc[(ta + 0) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wb = vc[(ta + 1) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wc = vc[(ta + 8) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wd = vc[(ta + 9) * (C::ROWB / 4) + wt * 8 + gq];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t rx[8], ry[8];
+          unpack16(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
+          unpack16(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+#pragma unroll
+          for (int m4 = 0; m4 < 4; ++m4) {
+            const int mtd = 4 * hh + m4;
+#pragma unroll
+            for (int nq = 0; nq < NQT; ++nq)
+              mma_f16(o[mtd][nq], rx[2 * m4], rx[2 * m4 + 1], ry[2 * m4], ry[2 * m4 + 1], bw0[nq], bw1[nq]);
+          }
+        }
+      }
+    } else {
+      uint32_t bw0[NQT], bw1[NQT];
+#pragma unroll
+      for (int nq = 0; nq < NQT; ++nq) {
+        bw0[nq] = movmatrix_trans(split_bf16(p[0][nq][0]));
+        bw1[nq] = movmatrix_trans(split_bf16(p[0][nq][1]));
+      }
+      const uint32_t vb_s = smem_u32(st + kBfTok * C::BF_STRIDE);
+      const int mi = lane >> 3;
+      const int tok = (lane & 7) + 8 * (mi >> 1);
+      const bool partial = bk.count < kBfTok;
+      // tokens held by this lane's A fragment halves
+      const bool va = 2 * cq < bk.count, vb = 2 * cq + 1 < bk.count;
+      const bool vc8 = 2 * cq + 8 < bk.count, vd = 2 * cq + 9 < bk.count;
+      const uint32_t mask01 = (va ? 0xffffu : 0u) | (vb ? 0xffff0000u : 0u);
+      const uint32_t mask89 = (vc8 ? 0xffffu : 0u) | (vd ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int mtd = 0; mtd < 8; ++mtd) {
+        const int dim = wt * kGroup + 16 * mtd + 8 * (mi & 1);
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(vb_s + tok * C::BF_STRIDE + dim * 2, a0, a1, a2, a3);
+        if (partial) {
+          a0 &= mask01; a1 &= mask01; a2 &= mask89; a3 &= mask89;
+        }
+#pragma unroll
+        for (int nq = 0; nq < NQT; ++nq) mma_bf16(o[mtd][nq], a0, a1, a2, a3, bw0[nq], bw1[nq]);
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars[C::NST + stage]));
+  }
+
+  // ---- team partials -> shared memory
+#pragma unroll
+  for (int nq = 0; nq < NQT; ++nq) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l_run[nq] += __shfl_xor_sync(0xffffffffu, l_run[nq], off);
+      zeta[nq] += __shfl_xor_sync(0xffffffffu, zeta[nq], off);
+    }
+  }
+  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);  // [team][head][D + 2]
+#pragma unroll
+  for (int nq = 0; nq < NQT; ++nq) {
+    const int hs = 4 * nq + cq;
+    float* ph = part + (team * C::HEADS + hs) * (D + 2);
+#pragma unroll
+    for (int mtd = 0; mtd < 8; ++mtd) {
+      const int d0 = wt * kGroup + 16 * mtd + gq;
+      ph[d0] = o[mtd][nq][0] + o[mtd][nq][1] + zeta[nq];
+      ph[d0 + 8] = o[mtd][nq][2] + o[mtd][nq][3] + zeta[nq];
+    }
+    if (wt == 0 && gq == 0) {
+      ph[D] = m_run[nq];
+      ph[D + 1] = l_run[nq];
+    }
+  }
+  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+  pdl_trigger();
+
+  // ---- merge the teams of this CTA and write the split partial
+  for (int idx = threadIdx.x; idx < Gh * D; idx += 32 * kNCW) {
+    const int hs = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < C::NTEAMS; ++t) M = fmaxf(M, part[(t * C::HEADS + hs) * (D + 2) + D]);
+    float acc = 0.f, L = 0.f;
+#pragma unroll
+    for (int t = 0; t < C::NTEAMS; ++t) {
+      const float* ph = part + (t * C::HEADS + hs) * (D + 2);
+      const float w = M == -INFINITY ? 0.f : ex2(ph[D] - M);
+      acc += w * ph[d];
+      L += w * ph[D + 1];
+    }
+    const int64_t pi = (int64_t(b) * g.Hq + head0 + hs) * a.ns + split;
+    a.ws_acc[pi * D + d] = acc;
+    if (d == 0) {
+      a.ws_ml[pi * 2 + 0] = M;
+      a.ws_ml[pi * 2 + 1] = L;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// merge kernel: one CTA per (b, kv head)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
+  extern __shared__ float ms[];  // [G][D] o', then [G] M, [G] L
+  const Geom& g = a.g;
+  const int h = blockIdx.x % g.Hkv, b = blockIdx.x / g.Hkv;
+  const int G = g.G;
+  float* ob = ms;
+  float* Ms = ms + G * D;
+  float* Ls = Ms + G;
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = clamp_seq_len(a, b);
+  if (threadIdx.x == 0) {
+    if (a.seq_lens[b] > g.cap) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
+    if (T < 1) status_or(a.status, OSCAR_DEV_EMPTY);
+  }
+  for (int i = warp; i < G; i += 8) {
+    const int64_t base = (int64_t(b) * g.Hq + h * G + i) * a.ns;
+    float M = -INFINITY;
+    for (int s = lane; s < a.ns; s += 32) M = fmaxf(M, a.ws_ml[(base + s) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int s = lane; s < a.ns; s += 32) {
+      const float m = a.ws_ml[(base + s) * 2];
+      L += m == -INFINITY ? 0.f : ex2(m - M) * a.ws_ml[(base + s) * 2 + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) { Ms[i] = M; Ls[i] = L; }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int i = idx / D, d = idx % D;
+    const int64_t base = (int64_t(b) * g.Hq + h * G + i) * a.ns;
+    const float M = Ms[i], L = Ls[i];
+    float acc = 0.f;
+    if (M != -INFINITY && L > 0.f) {
+      for (int s = 0; s < a.ns; ++s) {
+        const float m = a.ws_ml[(base + s) * 2];
+        if (m != -INFINITY) acc += ex2(m - M) * a.ws_acc[(base + s) * D + d];
+      }
+      acc /= L;
+    }
+    ob[idx] = acc;
+  }
+  __syncthreads();
+  // o = o' R_V^T : o[r] = sum_j R_V[r][j] o'[j]; one warp per output channel r
+  for (int r = warp; r < D; r += 8) {
+    float res[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) res[i] = 0.f;
+    if (a.absorb_v) {
+      if (lane == 0)
+        for (int i = 0; i < G && i < 8; ++i) res[i] = ob[i * D + r];
+    } else {
+      for (int j = lane; j < D; j += 32) {
+        const float rv = __ldg(a.R_V + int64_t(r) * D + j);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < G) res[i] = fmaf(rv, ob[i * D + j], res[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) res[i] += __shfl_xor_sync(0xffffffffu, res[i], o);
+    }
+    if (lane == 0) {
+      for (int i = 0; i < G && i < 8; ++i) {
+        const int64_t oi = (int64_t(b) * g.Hq + h * G + i) * D + r;
+        if (a.out_fp32)
+          static_cast<float*>(a.out)[oi] = res[i];
+        else
+          static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(res[i]);
+      }
+    }
+  }
+  if (a.lse && threadIdx.x < G) {
+    const int i = threadIdx.x;
+    const float M = Ms[i], L = Ls[i];
+    a.lse[int64_t(b) * g.Hq + h * G + i] =
+        (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launch
+// ---------------------------------------------------------------------------
+template <typename K>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const DecodeArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+struct DevInfo {
+  int sms = 0;
+  int occ[3][2] = {{0, 0}, {0, 0}, {0, 0}};
+  bool ready = false;
+};
+DevInfo g_dev[64];
+
+template <int D, int NQT>
+int prepare_split(int dev) {
+  using C = DecCfg<D, NQT>;
+  if (cudaFuncSetAttribute(split_kernel<D, NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return -1;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<D, NQT>, kThreads, C::SMEM) !=
+      cudaSuccess)
+    return -1;
+  return occ;
+}
+
+int dinfo_init(int dev) {
+  DevInfo& di = g_dev[dev];
+  if (di.ready) return 0;
+  if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  const int o[6] = {prepare_split<128, 1>(dev), prepare_split<128, 2>(dev), prepare_split<256, 1>(dev),
+                    prepare_split<256, 2>(dev), prepare_split<512, 1>(dev), prepare_split<512, 2>(dev)};
+  for (int i = 0; i < 6; ++i) {
+    if (o[i] <= 0) return -1;
+    di.occ[i / 2][i % 2] = o[i];
+  }
+  di.ready = true;
+  return 0;
+}
+
+int didx(int D) { return D == 128 ? 0 : (D == 256 ? 1 : 2); }
+
+template <int D, int NQT>
+int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
+  using C = DecCfg<D, NQT>;
+  const Geom& g = a.g;
+  qrot_kernel<D><<<g.B * g.Hq, D, 0, stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  if (launch_pdl(split_kernel<D, NQT>, dim3(a.ns, g.Hkv, g.B), dim3(kThreads), C::SMEM, stream, a) !=
+      cudaSuccess)
+    return OSCAR_ERR_LAUNCH;
+  const size_t msmem = (size_t(g.G) * D + 2 * g.G) * sizeof(float);
+  if (launch_pdl(merge_kernel<D>, dim3(g.B * g.Hkv), dim3(256), msmem, stream, a) != cudaSuccess)
+    return OSCAR_ERR_LAUNCH;
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+uint64_t decode_workspace_bytes(const Geom& g, int ns) {
+  const uint64_t bq = uint64_t(g.B) * g.Hq;
+  return align256(bq * g.D * 4) + align256(bq * g.Dg * 4) + align256(bq * ns * g.D * 4) +
+         align256(bq * ns * 2 * 4);
+}
+
+int decode_auto_splits(const Geom& g, int seq_len_hint) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || dinfo_init(dev) != 0) return -1;
+  const DevInfo& di = g_dev[dev];
+  const int occ = di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
+  const int slots = di.sms * occ;
+  const int units = g.B * g.Hkv;
+  // at least ~4 INT2 blocks of work per split
+  const int max_by_len = std::max(1, seq_len_hint / (4 * kI2Tok));
+  int best = 1;
+  double best_eff = -1.0;
+  for (int waves = 1; waves <= 8; ++waves) {
+    int ns = std::max(1, (waves * slots) / units);
+    ns = std::min(ns, std::min(max_by_len, int(OSCAR_KV_MAX_SPLITS)));
+    const int64_t ctas = int64_t(ns) * units;
+    const int64_t wv = (ctas + slots - 1) / slots;
+    const double eff = double(ctas) / double(wv * slots);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || dinfo_init(dev) != 0) return OSCAR_ERR_LAUNCH;
+  const bool big = a.g.G > 4;
+  switch (a.g.D) {
+    case 128: return big ? launch_decode_d<128, 2>(a, stream) : launch_decode_d<128, 1>(a, stream);
+    case 256: return big ? launch_decode_d<256, 2>(a, stream) : launch_decode_d<256, 1>(a, stream);
+    case 512: return big ? launch_decode_d<512, 2>(a, stream) : launch_decode_d<512, 1>(a, stream);
+    default: return OSCAR_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace oscar

@@ -1,0 +1,52 @@
+// Host-side launch interface shared by the C-ABI translation unit and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace oscar {
+
+struct AppendArgs {
+  Geom g;
+  uint8_t* layer_base;   // cache + layer * layer_bytes
+  const void* k_new;
+  const void* v_new;
+  const int32_t* start_pos;
+  const float* R_K;
+  const float* R_V;
+  float* debug_rot;
+  int32_t* status;
+  int n_new;
+  int64_t rows;          // B * n_new * Hkv
+  float k_clip, v_clip;
+  int in_fp32;
+};
+
+struct DecodeArgs {
+  Geom g;
+  const uint8_t* layer_base;
+  const void* q;
+  const int32_t* seq_lens;
+  const float* R_K;
+  const float* R_V;
+  void* out;
+  float* lse;
+  int32_t* status;
+  float* qprime;   // [B][Hq][D]   scaled rotated query (log2 units)
+  float* qsum;     // [B][Hq][Dg]  per-group sums of qprime
+  float* ws_acc;   // [B][Hq][NS][D]
+  float* ws_ml;    // [B][Hq][NS][2]
+  int ns;          // context splits per (b, kv head)
+  float qscale;    // sm_scale * log2(e)
+  int in_fp32, out_fp32, absorb_v;
+};
+
+uint64_t decode_workspace_bytes(const Geom& g, int ns);
+int launch_append(const AppendArgs& a, cudaStream_t stream);
+int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+int decode_auto_splits(const Geom& g, int seq_len_hint);
+
+}  // namespace oscar

@@ -1,0 +1,154 @@
+// C ABI: argument validation, cache layout arithmetic and kernel dispatch.
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+using oscar::Geom;
+
+int validate(const oscar_kv_config* c) {
+  if (!c) return OSCAR_ERR_INVALID;
+  if (c->num_layers <= 0 || c->batch <= 0 || c->num_q_heads <= 0 || c->num_kv_heads <= 0 ||
+      c->capacity <= 0 || c->sink < 0 || c->recent < 0)
+    return OSCAR_ERR_INVALID;
+  if (c->num_q_heads % c->num_kv_heads != 0) return OSCAR_ERR_INVALID;
+  if (!(c->k_clip > 0.f && c->k_clip <= 1.f) || !(c->v_clip > 0.f && c->v_clip <= 1.f)) return OSCAR_ERR_INVALID;
+  if (c->flags & ~uint32_t(OSCAR_FLAG_ABSORB_V | OSCAR_FLAG_IN_FP32 | OSCAR_FLAG_OUT_FP32)) return OSCAR_ERR_INVALID;
+  if (c->group_size != OSCAR_KV_GROUP) return OSCAR_ERR_UNSUPPORTED;
+  if (c->head_dim != 128 && c->head_dim != 256 && c->head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
+  if (c->num_q_heads / c->num_kv_heads > 8) return OSCAR_ERR_UNSUPPORTED;
+  return OSCAR_OK;
+}
+
+Geom make_geom(const oscar_kv_config* c) {
+  Geom g;
+  g.B = c->batch;
+  g.Hq = c->num_q_heads;
+  g.Hkv = c->num_kv_heads;
+  g.D = c->head_dim;
+  g.G = g.Hq / g.Hkv;
+  g.Dg = g.D / OSCAR_KV_GROUP;
+  g.S = c->sink;
+  g.W = c->recent;
+  g.cap = c->capacity;
+  const int64_t n = c->capacity > c->sink ? c->capacity - c->sink : 0;
+  g.ncap = (n + oscar::kNcapRound - 1) / oscar::kNcapRound * oscar::kNcapRound;
+  const uint64_t bh = uint64_t(g.B) * g.Hkv;
+  g.sink_bytes = oscar::align256(bh * g.S * g.D * 2);
+  g.ring_bytes = oscar::align256(bh * g.W * g.D * 2);
+  g.codes_bytes = oscar::align256(bh * uint64_t(g.ncap) * (g.D / 4));
+  g.sz_bytes = oscar::align256(bh * uint64_t(g.ncap) * g.Dg * 4);
+  g.role_bytes = g.sink_bytes + g.ring_bytes + g.codes_bytes + g.sz_bytes;
+  g.layer_bytes = 2 * g.role_bytes;
+  return g;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out) {
+  const int v = validate(cfg);
+  if (v != OSCAR_OK) return v;
+  if (!out) return OSCAR_ERR_INVALID;
+  const Geom g = make_geom(cfg);
+  std::memset(out, 0, sizeof(*out));
+  out->ncap = uint64_t(g.ncap);
+  out->sink_bytes = g.sink_bytes;
+  out->ring_bytes = g.ring_bytes;
+  out->codes_bytes = g.codes_bytes;
+  out->sz_bytes = g.sz_bytes;
+  out->role_bytes = g.role_bytes;
+  out->layer_bytes = g.layer_bytes;
+  out->total_bytes = g.layer_bytes * uint64_t(cfg->num_layers);
+  out->decode_workspace_bytes = oscar::decode_workspace_bytes(g, OSCAR_KV_MAX_SPLITS);
+  out->max_splits = OSCAR_KV_MAX_SPLITS;
+  return OSCAR_OK;
+}
+
+int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
+              const int32_t* start_pos, int32_t n_new, const float* R_K, const float* R_V,
+              float* debug_rot_out, int32_t* dev_status, void* stream) {
+  const int v = validate(cfg);
+  if (v != OSCAR_OK) return v;
+  if (!cache || !k_new || !v_new || !start_pos || !R_K || !R_V) return OSCAR_ERR_INVALID;
+  if (layer < 0 || layer >= cfg->num_layers || n_new < 0) return OSCAR_ERR_INVALID;
+  if (!aligned(cache, 256) || !aligned(R_K, 16) || !aligned(R_V, 16) || !aligned(k_new, 16) ||
+      !aligned(v_new, 16) || (debug_rot_out && !aligned(debug_rot_out, 16)))
+    return OSCAR_ERR_INVALID;
+  if (n_new > cfg->capacity) return OSCAR_ERR_CAPACITY;
+  oscar::AppendArgs a;
+  a.g = make_geom(cfg);
+  a.layer_base = static_cast<uint8_t*>(cache) + uint64_t(layer) * a.g.layer_bytes;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.start_pos = start_pos;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.debug_rot = debug_rot_out;
+  a.status = dev_status;
+  a.n_new = n_new;
+  a.rows = int64_t(cfg->batch) * n_new * cfg->num_kv_heads;
+  a.k_clip = cfg->k_clip;
+  a.v_clip = cfg->v_clip;
+  a.in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
+  return oscar::launch_append(a, static_cast<cudaStream_t>(stream));
+}
+
+int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
+                const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
+                float sm_scale, int32_t num_splits, void* out, float* lse, void* workspace,
+                uint64_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const int v = validate(cfg);
+  if (v != OSCAR_OK) return v;
+  if (!cache || !q || !seq_lens || !R_K || !R_V || !out || !workspace) return OSCAR_ERR_INVALID;
+  if (layer < 0 || layer >= cfg->num_layers || num_splits < 0 || num_splits > OSCAR_KV_MAX_SPLITS ||
+      seq_len_hint < 0)
+    return OSCAR_ERR_INVALID;
+  if (!aligned(cache, 256) || !aligned(workspace, 256) || !aligned(R_K, 16) || !aligned(R_V, 16) ||
+      !aligned(q, 16) || !aligned(out, 16))
+    return OSCAR_ERR_INVALID;
+  if (seq_len_hint > cfg->capacity) return OSCAR_ERR_CAPACITY;
+  const Geom g = make_geom(cfg);
+  const int hint = seq_len_hint > 0 ? seq_len_hint : cfg->capacity;
+  int ns = num_splits;
+  if (ns == 0) {
+    ns = oscar::decode_auto_splits(g, hint);
+    if (ns < 1) return OSCAR_ERR_LAUNCH;
+    while (ns > 1 && oscar::decode_workspace_bytes(g, ns) > workspace_bytes) --ns;
+  }
+  if (oscar::decode_workspace_bytes(g, ns) > workspace_bytes) return OSCAR_ERR_WORKSPACE;
+
+  oscar::DecodeArgs a;
+  a.g = g;
+  a.layer_base = static_cast<const uint8_t*>(cache) + uint64_t(layer) * g.layer_bytes;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.R_K = R_K;
+  a.R_V = R_V;
+  a.out = out;
+  a.lse = lse;
+  a.status = dev_status;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint64_t bq = uint64_t(g.B) * g.Hq;
+  a.qprime = reinterpret_cast<float*>(ws);
+  ws += oscar::align256(bq * g.D * 4);
+  a.qsum = reinterpret_cast<float*>(ws);
+  ws += oscar::align256(bq * g.Dg * 4);
+  a.ws_acc = reinterpret_cast<float*>(ws);
+  ws += oscar::align256(bq * uint64_t(ns) * g.D * 4);
+  a.ws_ml = reinterpret_cast<float*>(ws);
+  a.ns = ns;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(float(g.D));
+  a.qscale = scale * 1.4426950408889634f;
+  a.in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
+  a.out_fp32 = (cfg->flags & OSCAR_FLAG_OUT_FP32) ? 1 : 0;
+  a.absorb_v = (cfg->flags & OSCAR_FLAG_ABSORB_V) ? 1 : 0;
+  return oscar::launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

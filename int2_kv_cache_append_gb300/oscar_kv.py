@@ -1,0 +1,137 @@
+"""Thin ctypes binding of liboscar_kv.so (argument marshalling only).
+
+Every computation runs in the library's CUDA kernels; this module converts
+torch tensors to pointers and checks return codes.  It raises if the library
+has not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "liboscar_kv.so")
+
+GROUP = 128
+MAX_SPLITS = 64
+FLAG_ABSORB_V = 1
+FLAG_IN_FP32 = 2
+FLAG_OUT_FP32 = 4
+
+DEV_OVER_CAPACITY = 1
+DEV_NONFINITE = 2
+DEV_FP16_RANGE = 4
+DEV_TIMEOUT = 8
+DEV_EMPTY = 16
+
+STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LAUNCH", -5: "UNSUPPORTED"}
+
+# every symbol include/oscar_kv.h declares
+EXPORTS = ("kv_layout_query", "kv_append", "attn_decode")
+
+
+class OscarError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({STATUS_NAMES.get(code, '?')})")
+        self.code = code
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("sink", ctypes.c_int32), ("recent", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("k_clip", ctypes.c_float), ("v_clip", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("ncap", ctypes.c_uint64), ("sink_bytes", ctypes.c_uint64), ("ring_bytes", ctypes.c_uint64),
+                ("codes_bytes", ctypes.c_uint64), ("sz_bytes", ctypes.c_uint64), ("role_bytes", ctypes.c_uint64),
+                ("layer_bytes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
+                ("decode_workspace_bytes", ctypes.c_uint64), ("max_splits", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+@dataclass
+class KVConfig:
+    num_layers: int
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    sink: int
+    recent: int
+    capacity: int
+    k_clip: float = 0.96
+    v_clip: float = 0.92
+    flags: int = 0
+    group_size: int = GROUP
+
+    def c(self) -> _Config:
+        return _Config(self.num_layers, self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim,
+                       self.group_size, self.sink, self.recent, self.capacity, self.k_clip, self.v_clip,
+                       self.flags)
+
+
+_lib = None
+
+
+def lib():
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with int2_kv_cache_append_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        L.kv_layout_query.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Layout)]
+        L.kv_layout_query.restype = ctypes.c_int
+        L.kv_append.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, P, ctypes.c_int32, P, P, P, P, P]
+        L.kv_append.restype = ctypes.c_int
+        L.attn_decode.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, ctypes.c_int32, P, P,
+                                  ctypes.c_float, ctypes.c_int32, P, P, P, ctypes.c_uint64, P, P]
+        L.attn_decode.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def layout_query(cfg: KVConfig) -> dict:
+    out = _Layout()
+    rc = lib().kv_layout_query(ctypes.byref(cfg.c()), ctypes.byref(out))
+    if rc != 0:
+        raise OscarError("kv_layout_query", rc)
+    return {name: getattr(out, name) for name, _ in _Layout._fields_}
+
+
+def kv_append(cfg: KVConfig, cache, layer: int, k_new, v_new, start_pos, R_K, R_V, debug_rot=None,
+              status=None, stream=None, check: bool = True) -> int:
+    rc = lib().kv_append(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(k_new), _ptr(v_new), _ptr(start_pos),
+                         int(k_new.shape[1]), _ptr(R_K), _ptr(R_V), _ptr(debug_rot), _ptr(status), _stream(stream))
+    if check and rc != 0:
+        raise OscarError("kv_append", rc)
+    return rc
+
+
+def attn_decode(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, out, workspace, lse=None,
+                seq_len_hint: int = 0, sm_scale: float = 0.0, num_splits: int = 0, status=None, stream=None,
+                check: bool = True) -> int:
+    rc = lib().attn_decode(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(q), _ptr(seq_lens), int(seq_len_hint),
+                           _ptr(R_K), _ptr(R_V), float(sm_scale), int(num_splits), _ptr(out), _ptr(lse),
+                           _ptr(workspace), int(workspace.numel() * workspace.element_size()), _ptr(status),
+                           _stream(stream))
+    if check and rc != 0:
+        raise OscarError("attn_decode", rc)
+    return rc

@@ -1,0 +1,63 @@
+"""Helpers for GPU parity tests: upload seeded inputs, call the C-ABI through the
+binding, download results.  Expected values always come from the oracle."""
+import numpy as np
+import torch
+
+from int2_kv_cache_append_gb300 import oscar_kv as K
+from oracle import oscar_oracle as O
+
+
+def kcfg(c: O.Config) -> K.KVConfig:
+    return K.KVConfig(c.num_layers, c.batch, c.num_q_heads, c.num_kv_heads, c.head_dim, c.sink, c.recent,
+                      c.capacity, c.k_clip, c.v_clip, c.flags)
+
+
+def dev(x, dtype=torch.bfloat16):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dtype).cuda()
+
+
+def dev_i32(x):
+    return torch.tensor(np.asarray(x, dtype=np.int32), dtype=torch.int32, device="cuda")
+
+
+def new_cache(c: O.Config):
+    return torch.zeros(O.layout(c)["total_bytes"], dtype=torch.uint8, device="cuda")
+
+
+def gpu_append(c: O.Config, cache, layer, k, v, start_pos, RK, RV, want_rot=False, status=None):
+    fp32 = bool(c.flags & K.FLAG_IN_FP32)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    kt, vt = dev(k, dt), dev(v, dt)
+    B, n, H, D = k.shape
+    rot = torch.empty((B, n, H, 2, D), dtype=torch.float32, device="cuda") if want_rot else None
+    K.kv_append(kcfg(c), cache, layer, kt, vt, dev_i32(start_pos), dev(RK, torch.float32),
+                dev(RV, torch.float32), debug_rot=rot, status=status)
+    torch.cuda.synchronize()
+    return rot
+
+
+def gpu_decode(c: O.Config, cache, layer, q, seq_lens, RK, RV, sm_scale=0.0, num_splits=0, hint=0,
+               status=None, out_fp32=None):
+    kc = kcfg(c)
+    if out_fp32 is not None:
+        kc.flags = (kc.flags & ~K.FLAG_OUT_FP32) | (K.FLAG_OUT_FP32 if out_fp32 else 0)
+    lay = K.layout_query(kc)
+    fp32_in = bool(c.flags & K.FLAG_IN_FP32)
+    qt = dev(q, torch.float32 if fp32_in else torch.bfloat16)
+    B, Hq, D = q.shape
+    out = torch.empty((B, Hq, D), dtype=torch.float32 if kc.flags & K.FLAG_OUT_FP32 else torch.bfloat16,
+                      device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
+    K.attn_decode(kc, cache, layer, qt, dev_i32(seq_lens), dev(RK, torch.float32), dev(RV, torch.float32), out,
+                  ws, lse=lse, seq_len_hint=hint, sm_scale=sm_scale, num_splits=num_splits, status=status)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def bf16_round64(x):
+    return O.bf16_bits_to_f32(O.f32_to_bf16_bits(np.asarray(x, np.float32))).astype(np.float64)
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm((a - b).ravel()) / max(np.linalg.norm(b.ravel()), 1e-30))

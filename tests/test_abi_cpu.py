@@ -1,0 +1,90 @@
+"""C-ABI library: loads, exports every declared symbol, host-only layout
+arithmetic and argument validation.  No GPU compute is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from int2_kv_cache_append_gb300 import oscar_kv as K
+from oracle import oscar_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int2_kv_cache_append_gb300 import build
+    build.build()
+    return K.lib()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "oscar_kv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^int\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    decl = _declared_symbols()
+    assert decl == sorted(K.EXPORTS)
+    for name in decl:
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 4, 1, 128, 64, 256, 1024), (2, 3, 8, 2, 256, 5, 7, 100), (36, 32, 32, 8, 128, 64, 256, 32768),
+    (1, 4, 16, 8, 512, 512, 2048, 65536), (1, 2, 2, 2, 128, 0, 0, 1), (1, 1, 8, 1, 128, 300, 0, 200)])
+def test_layout_matches_oracle(lib, shape):
+    L, B, Hq, Hkv, D, S, W, cap = shape
+    got = K.layout_query(K.KVConfig(L, B, Hq, Hkv, D, S, W, cap))
+    exp = O.layout(O.Config(L, B, Hq, Hkv, D, S, W, cap))
+    for key in ("ncap", "sink_bytes", "ring_bytes", "codes_bytes", "sz_bytes", "role_bytes", "layer_bytes",
+                "total_bytes"):
+        assert got[key] == exp[key], key
+    assert got["max_splits"] == K.MAX_SPLITS
+    # documented workspace formula
+    a = lambda x: (x + 255) // 256 * 256
+    bq = B * Hq
+    ws = a(bq * D * 4) + a(bq * (D // 128) * 4) + a(bq * 64 * D * 4) + a(bq * 64 * 8)
+    assert got["decode_workspace_bytes"] == ws
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 64, -5), ("head_dim", 192, -5), ("group_size", 64, -5), ("num_q_heads", 6, -1),
+    ("num_q_heads", 72, -5), ("k_clip", 0.0, -1), ("v_clip", 1.5, -1), ("sink", -1, -1), ("recent", -3, -1),
+    ("capacity", 0, -1), ("batch", 0, -1), ("flags", 64, -1)])
+def test_layout_rejects_bad_config(lib, field, value, code):
+    cfg = K.KVConfig(1, 2, 8, 4 if field == "num_q_heads" and value == 6 else 8, 128, 4, 8, 64)
+    if field == "num_q_heads" and value == 72:
+        cfg.num_kv_heads = 8
+    setattr(cfg, field, value)
+    out = K._Layout()
+    assert lib.kv_layout_query(ctypes.byref(cfg.c()), ctypes.byref(out)) == code
+
+
+def test_entry_points_validate_before_launch(lib):
+    cfg = K.KVConfig(1, 1, 4, 1, 128, 4, 8, 64)
+    c = cfg.c()
+    P = ctypes.c_void_p
+    big = P(1 << 20)  # never dereferenced: every call below fails validation first
+    # null cache
+    assert lib.kv_append(ctypes.byref(c), None, 0, big, big, big, 1, big, big, None, None, None) == -1
+    # layer out of range
+    assert lib.kv_append(ctypes.byref(c), big, 1, big, big, big, 1, big, big, None, None, None) == -1
+    # misaligned cache
+    assert lib.kv_append(ctypes.byref(c), P((1 << 20) + 16), 0, big, big, big, 1, big, big, None, None, None) == -1
+    # n_new beyond capacity
+    assert lib.kv_append(ctypes.byref(c), big, 0, big, big, big, 65, big, big, None, None, None) == -2
+    # decode: too many splits, hint beyond capacity, workspace too small for one split
+    assert lib.attn_decode(ctypes.byref(c), big, 0, big, big, 0, big, big, 0.0, 65, big, None, big, 1 << 30,
+                           None, None) == -1
+    assert lib.attn_decode(ctypes.byref(c), big, 0, big, big, 65, big, big, 0.0, 1, big, None, big, 1 << 30,
+                           None, None) == -2
+    assert lib.attn_decode(ctypes.byref(c), big, 0, big, big, 0, big, big, 0.0, 1, big, None, big, 16, None,
+                           None) == -3
+    # bad config passes through the same validation
+    bad = K.KVConfig(1, 1, 4, 1, 96, 4, 8, 64).c()
+    assert lib.attn_decode(ctypes.byref(bad), big, 0, big, big, 0, big, big, 0.0, 1, big, None, big, 1 << 30,
+                           None, None) == -5

@@ -1,0 +1,149 @@
+"""GPU parity: attn_decode against the oracle on identical cache bytes.
+
+The oracle builds the cache (its own append) from seeded inputs; the same bytes
+are uploaded and decoded on the GPU.  Tolerances (BF16 output compared with the
+oracle's float64 result rounded to BF16; float32 output with the float64 result):
+  rel-L2(bf16 out, bf16(oracle)) <= 1e-3
+  max |fp32 out - oracle| <= 5e-3 and rel-L2 <= 2e-4
+  |lse - oracle| <= 1e-4 (natural log)."""
+import numpy as np
+import pytest
+import torch
+
+from int2_kv_cache_append_gb300 import oscar_kv as K
+from int2_kv_cache_append_gb300 import synth as S
+from oracle import oscar_oracle as O
+from tests.gpu_helpers import bf16_round64, gpu_decode, rel_l2
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int2_kv_cache_append_gb300 import build
+    build.build()
+
+
+def _build(c, seq_lens, seed, rot="oscar", act="t3", layer=0):
+    D = c.head_dim
+    rng = np.random.default_rng(seed)
+    if rot == "oscar":
+        calib = S.activations(rng, (2048, D), rng.choice(D, 3, replace=False), kind=act)
+        RK = S.eig_rotation(calib).astype(np.float32)
+        RV = S.qr_rotation(rng, D).astype(np.float32)
+    elif rot == "identity":
+        RK = RV = np.eye(D, dtype=np.float32)
+    else:
+        RK = S.qr_rotation(rng, D).astype(np.float32)
+        RV = S.qr_rotation(rng, D).astype(np.float32)
+    ch = rng.choice(D, max(1, round(0.02 * D)), replace=False)
+    T = max(seq_lens)
+    fp32 = bool(c.flags & K.FLAG_IN_FP32)
+    k = S.activations(rng, (c.batch, T, c.num_kv_heads, D), ch, kind=act)
+    v = S.activations(rng, (c.batch, T, c.num_kv_heads, D), ch, kind=act)
+    q = S.activations(rng, (c.batch, c.num_q_heads, D), ch, kind=act)
+    if not fp32:
+        k, v, q = S.to_bf16_values(k), S.to_bf16_values(v), S.to_bf16_values(q)
+    cache = O.new_cache(c)
+    O.append(c, cache, layer, k, v, [0] * c.batch, RK, RV)
+    return cache, q, RK, RV
+
+
+def _check(c, cache, q, seq_lens, RK, RV, layer=0, num_splits=0, sm_scale=0.0, tol_fp32=2e-4):
+    absorb = bool(c.flags & K.FLAG_ABSORB_V)
+    ref, ref_lse = O.decode(c, cache, layer, q, seq_lens, RK, RV, sm_scale=sm_scale, absorb_v=absorb)
+    gc = torch.from_numpy(cache).cuda()
+    o16, lse = gpu_decode(c, gc, layer, q, seq_lens, RK, RV, sm_scale=sm_scale, num_splits=num_splits,
+                          out_fp32=False)
+    o32, lse32 = gpu_decode(c, gc, layer, q, seq_lens, RK, RV, sm_scale=sm_scale, num_splits=num_splits,
+                            out_fp32=True)
+    r16 = rel_l2(o16, bf16_round64(ref))
+    r32 = rel_l2(o32, ref)
+    m32 = float(np.abs(o32 - ref).max())
+    dl = float(np.abs(lse - ref_lse).max())
+    assert r16 <= 1e-3, f"bf16 rel-L2 {r16}"
+    assert m32 <= 5e-3 and r32 <= tol_fp32, f"fp32 max-abs {m32} rel-L2 {r32}"
+    assert dl <= 1e-4, f"lse {dl}"
+    assert np.array_equal(lse, lse32)
+    return r16, r32, m32
+
+
+DEC_CASES = [
+    # D, B, Hq, Hkv, S, W, seq_lens, flags
+    (128, 1, 4, 1, 64, 256, [1024], 0),
+    (128, 2, 8, 2, 16, 32, [700, 333], 0),                 # ragged
+    (128, 2, 4, 2, 64, 256, [200, 64], 0),                 # S+W >= T: all BF16
+    (128, 1, 8, 8, 512, 0, [2000], 0),                     # W = 0, G = 1
+    (128, 2, 16, 2, 0, 100, [1500, 900], 0),               # S = 0, G = 8
+    (128, 3, 6, 3, 20, 40, [30, 19, 1], 0),                # T <= S, T = 1
+    (128, 1, 16, 8, 64, 256, [4000], K.FLAG_ABSORB_V),     # G = 2, absorbed V
+    (256, 2, 8, 2, 32, 64, [900, 513], 0),
+    (512, 1, 4, 2, 512, 256, [2300], 0),
+    (512, 2, 16, 2, 8, 8, [333, 1000], 0),                 # D = 512, G = 8
+]
+
+
+@pytest.mark.parametrize("case", DEC_CASES)
+def test_decode_parity(case):
+    D, B, Hq, Hkv, S_, W, lens, flags = case
+    c = O.Config(1, B, Hq, Hkv, D, S_, W, max(lens) + 37, 0.96, 0.92, flags=flags)
+    cache, q, RK, RV = _build(c, lens, seed=D * 7 + B + Hq)
+    _check(c, cache, q, lens, RK, RV)
+
+
+def test_decode_tiny_fp32_inputs():
+    w = S.WORKLOADS["tiny"]
+    c = O.Config(1, 1, 4, 1, 128, 64, 256, 1024, 0.96, 0.92, flags=K.FLAG_IN_FP32)
+    RK, RV = S.rotations(w, 0)
+    k, v = S.kv_rows(w, 0, 1024)
+    q = S.queries(w, 0)
+    cache = O.new_cache(c)
+    O.append(c, cache, 0, k, v, [0], RK, RV)
+    _check(c, cache, q, [1024], RK, RV)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_decode_split_counts_agree(splits):
+    c = O.Config(1, 2, 8, 2, 128, 64, 128, 3000, 0.96, 0.92)
+    lens = [2900, 1700]
+    cache, q, RK, RV = _build(c, lens, seed=11)
+    _check(c, cache, q, lens, RK, RV, num_splits=splits)
+
+
+def test_decode_custom_scale_and_layer():
+    c = O.Config(3, 1, 4, 2, 128, 16, 16, 400, 0.96, 0.92)
+    cache, q, RK, RV = _build(c, [390], seed=12, layer=2)
+    _check(c, cache, q, [390], RK, RV, layer=2, sm_scale=0.05)
+
+
+def test_decode_constant_v_gives_constant():
+    # V rows all equal to a lattice row (exact in INT2 and in BF16), R_V = I
+    D = 128
+    c = O.Config(1, 1, 4, 1, D, 8, 8, 600)
+    rng = np.random.default_rng(13)
+    T = 500
+    row = (-1.0 + 0.5 * (np.arange(D) % 4)).astype(np.float32)   # z=-1, s=0.5, codes 0..3
+    row[0], row[1] = -1.5, 1.5                                   # keep clip inert: |max| stays first
+    k = S.to_bf16_values(rng.standard_normal((1, T, 1, D)).astype(np.float32))
+    v = np.broadcast_to(row, (1, T, 1, D)).copy()
+    I = np.eye(D, dtype=np.float32)
+    cache = O.new_cache(c)
+    O.append(c, cache, 0, k, v, [0], I, I)
+    q = S.to_bf16_values(rng.standard_normal((1, 4, D)).astype(np.float32))
+    gc = torch.from_numpy(cache).cuda()
+    o32, _ = gpu_decode(c, gc, 0, q, [T], I, I, out_fp32=True)
+    ref, _ = O.decode(c, cache, 0, q, [T], I, I)
+    # every token reconstructs the same row, so the output is that row
+    assert np.abs(ref - ref[0, 0]).max() < 1e-12
+    assert np.abs(o32 - ref).max() < 1e-5
+
+
+def test_decode_empty_sequence_status():
+    c = O.Config(1, 2, 4, 1, 128, 4, 4, 64)
+    cache, q, RK, RV = _build(c, [10, 10], seed=14)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o32, lse = gpu_decode(c, torch.from_numpy(cache).cuda(), 0, q, [10, 0], RK, RV, out_fp32=True, status=st)
+    assert int(st.item()) & K.DEV_EMPTY
+    assert np.all(o32[1] == 0) and np.all(np.isneginf(lse[1]))
+    ref, _ = O.decode(c, cache, 0, q[:1], [10], RK, RV)
+    assert np.abs(o32[0] - ref[0]).max() < 5e-3
