@@ -1,0 +1,397 @@
+"""Benchmark: one decode step of the rotated INT2 KV cache on GB300.
+
+A step is the whole hot path for one batch: kv_append of the current token of
+every sequence (rotate, clip, INT2 pack, BF16 window write) followed by
+attn_decode over the full mixed INT2/BF16 cache (query rotation, split-K
+attention, LSE merge, V un-rotation).  Inputs are synthetic (seeded normal
+activations with heavy outlier channels) and resident in HBM; the cache is
+pre-filled by untimed appends.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT2+BF16 KV decode-attn tokens/s and KV GB/s (% of HBM peak), 1 GB300"
+DEFAULT_WORKLOAD = "qwen3-4b-layer"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: B{w.batch} Hq{w.num_q_heads} Hkv{w.num_kv_heads} D{w.head_dim} T{w.context} "
+            f"S{w.sink} W{w.recent} g128 clip{w.k_clip}/{w.v_clip} layers{w.num_layers}"
+            f"{' absorbV' if w.absorb_v else ''}")
+
+
+def kv_bytes_per_bh(w, T: int) -> int:
+    """Algorithmic K+V bytes one decode step reads for one (sequence, KV head)."""
+    D = w.head_dim
+    S, W = w.sink, w.recent
+    if T <= S:
+        n_bf, n_i2 = T, 0
+    else:
+        tq = max(S, T - W)
+        n_i2 = tq - S
+        n_bf = S + (T - tq)
+    return n_i2 * 2 * (D // 4 + 4 * (D // 128)) + n_bf * 2 * 2 * D
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def split_kernel_traffic(workload: str):
+    """ncu DRAM bytes per split-kernel launch from the committed profile summary,
+    or None if absent or taken on a different kernel source."""
+    src = os.path.join(ROOT, "int2_kv_cache_append_gb300", "csrc", "attn_decode.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    p = os.path.join(ROOT, "profiles", f"split_kernel_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle sample (test infrastructure, timed as the CPU baseline)
+# --------------------------------------------------------------------------
+def cpu_sample_worker(workload: str, steps: int, warmup: int):
+    """Run inside a single-threaded child process: time the oracle's decode step
+    (append of the current token + attention) for batch row 0 of the workload."""
+    import numpy as np
+    from int2_kv_cache_append_gb300 import synth as S
+    from oracle import oscar_oracle as O
+
+    w = S.WORKLOADS[workload]
+    T = w.context
+    c = O.Config(1, 1, w.num_q_heads, w.num_kv_heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip)
+    RK, RV = S.rotations(w, 0)
+    k, v = S.kv_rows(w, 0, T, batch=1)
+    cache = O.new_cache(c)
+    O.append(c, cache, 0, k[:, :T - 1], v[:, :T - 1], [0], RK, RV)
+    q = S.queries(w, 0, batch=1)
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        O.append(c, cache, 0, k[:, T - 1:], v[:, T - 1:], [T - 1], RK, RV)
+        O.decode(c, cache, 0, q, [T], RK, RV, absorb_v=w.absorb_v)
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    print(json.dumps({"sec_per_step": statistics.mean(times), "steps": len(times)}))
+
+
+def run_cpu_sample(workload: str, steps: int, warmup: int):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", "--workload", workload,
+           "--steps", str(steps), "--warmup", str(warmup)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args):
+    """The oracle as the reference implementation, timed on this host's cores."""
+    from int2_kv_cache_append_gb300 import synth as S
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = S.WORKLOADS[args.workload]
+    steps = max(1, args.steps)
+    t0 = time.time()
+    res = run_cpu_sample(args.workload, steps, args.warmup)
+    sec = res["sec_per_step"]
+    value = 1.0 / sec  # one sequence per sample step
+    sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}: append of the current "
+              f"token + decode over T={w.context} for all {w.num_q_heads} query heads; single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w), "sample": "1 sequence per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.time() - t0}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def ours(args):
+    import numpy as np
+    import torch
+
+    from int2_kv_cache_append_gb300 import build as B
+    from int2_kv_cache_append_gb300 import oscar_kv as K
+    from int2_kv_cache_append_gb300 import synth as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        B.build()
+    if dist is not None:
+        dist.barrier()
+    K.lib()
+
+    w = S.WORKLOADS[args.workload]
+    L, Bsz, Hq, Hkv, D, T = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.context
+    flags = K.FLAG_ABSORB_V if w.absorb_v else 0
+    cfg = K.KVConfig(L, Bsz, Hq, Hkv, D, w.sink, w.recent, T, w.k_clip, w.v_clip, flags)
+    lay = K.layout_query(cfg)
+    stream = torch.cuda.current_stream()
+
+    # ---- setup (untimed): rotations, cache pre-fill of T-1 tokens per sequence
+    gen = torch.Generator(device=dev)
+    cache = torch.empty(lay["total_bytes"], dtype=torch.uint8, device=dev)
+    rots = []
+    for layer in range(L):
+        RK, RV = S.rotations(w, layer if L == 1 else layer % 4)
+        rots.append((torch.from_numpy(RK).to(dev), torch.from_numpy(RV).to(dev)))
+    ch = S.outlier_channels(w.config_id, 0, D)
+    chunk = max(1, min(T - 1, (1 << 27) // (Bsz * Hkv * D)))
+    for layer in range(L):
+        gen.manual_seed(1000 * w.config_id + layer + 7919 * rank)
+        pos = 0
+        while pos < T - 1:
+            n = min(chunk, T - 1 - pos)
+            k = S.activations_torch(gen, (Bsz, n, Hkv, D), ch, dtype=torch.bfloat16, device=dev)
+            v = S.activations_torch(gen, (Bsz, n, Hkv, D), ch, dtype=torch.bfloat16, device=dev)
+            K.kv_append(cfg, cache, layer, k, v, torch.full((Bsz,), pos, dtype=torch.int32, device=dev),
+                        rots[layer][0], rots[layer][1])
+            pos += n
+    torch.cuda.synchronize()
+    gen.manual_seed(99 + rank)
+    q = S.activations_torch(gen, (Bsz, Hq, D), ch, dtype=torch.bfloat16, device=dev)
+    k1 = S.activations_torch(gen, (Bsz, 1, Hkv, D), ch, dtype=torch.bfloat16, device=dev)
+    v1 = S.activations_torch(gen, (Bsz, 1, Hkv, D), ch, dtype=torch.bfloat16, device=dev)
+    start = torch.full((Bsz,), T - 1, dtype=torch.int32, device=dev)
+    seq = torch.full((Bsz,), T, dtype=torch.int32, device=dev)
+    out = torch.empty((Bsz, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Bsz, Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(qq=q, kk=k1, vv=v1, oo=out):
+        for layer in range(L):
+            RK, RV = rots[layer]
+            K.kv_append(cfg, cache, layer, kk, vv, start, RK, RV, status=status)
+            K.attn_decode(cfg, cache, layer, qq, seq, RK, RV, oo, ws, lse=lse, seq_len_hint=T, status=status)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    # clocks: sample across a short untimed load phase and the timed region
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        flush.zero_()
+        step()
+        torch.cuda.synchronize()
+
+    K_ = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_ * L)]
+    for a_, b_ in kev:  # torch creates the CUDA event on first record; the library re-records them
+        a_.record(stream)
+        b_.record(stream)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K_):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for layer in range(L):
+            RK, RV = rots[layer]
+            K.kv_append(cfg, cache, layer, k1, v1, start, RK, RV, status=status)
+            ks, ke = kev[i * L + layer]
+            K.set_profile_events(ks, ke)
+            K.attn_decode(cfg, cache, layer, q, seq, RK, RV, out, ws, lse=lse, seq_len_hint=T, status=status)
+            K.set_profile_events(None, None)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    split_ms = [a.elapsed_time(b) for a, b in kev]
+    ms = statistics.mean(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks.stop()
+
+    # ---- end-to-end through the public API with host buffers
+    q_h = q.cpu().pin_memory()
+    k_h = k1.cpu().pin_memory()
+    v_h = v1.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(k1), torch.empty_like(v1)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_)]
+    for i in range(K_):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        step(q_d, k_d, v_d, out)
+        out_h.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    h2d = (q.numel() * q.element_size() + 2 * k1.numel() * k1.element_size()) * L
+    d2h = out.numel() * out.element_size() * L
+    st = int(status.item())
+
+    if rank != 0:
+        return
+    kv_bytes = kv_bytes_per_bh(w, T) * Bsz * Hkv * L
+    tokens_per_s = world * Bsz / (ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    split_avg_ms = statistics.mean(split_ms)
+    achieved = kv_bytes / L / (split_avg_ms / 1e3) / 1e9
+    step_gbs = kv_bytes / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        res = run_cpu_sample(args.workload, steps=3, warmup=1)
+        cpu = {"value": 1.0 / res["sec_per_step"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"oracle decode step (append + attention) for 1 of {Bsz} sequences of {args.workload}, "
+                         f"T={T}, {res['steps']} timed steps, single thread"}
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K_,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "step": "kv_append(1 token/seq) + attn_decode per layer",
+                   "l2": "flushed between steps (512 MiB write)", "cache": "int2+bf16", "parallelism":
+                       f"replica x{world}" if world > 1 else "single"},
+        "kv_gbs": step_gbs, "kv_pct_hbm": step_gbs / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": split_kernel_traffic(args.workload), "kernel": "split_kernel (attn_decode)",
+                     "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": kv_bytes // L},
+        "e2e": {"value": world * Bsz / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * L * K_,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+        "dev_status": st,
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.cpu_sample_worker:
+        cpu_sample_worker(args.workload, args.steps, args.warmup)
+        return
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    ours(args)
+
+
+if __name__ == "__main__":
+    main()

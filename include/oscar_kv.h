@@ -64,7 +64,8 @@
  *
  * Ownership: the caller owns every buffer (cache, inputs, rotations, outputs,
  * workspace, status word); the library allocates nothing, keeps no state
- * between calls beyond per-device launch settings, and only enqueues work on
+ * between calls beyond per-device launch settings (and the optional per-thread
+ * profiling events below), and only enqueues work on
  * the given stream (a cudaStream_t passed as void*; NULL = legacy default).
  * Calls may be captured in CUDA graphs.
  *
@@ -191,6 +192,17 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
                 const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
                 float sm_scale, int32_t num_splits, void* out, float* lse, void* workspace,
                 uint64_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * oscar_kv_set_profile_events — measurement hook (no counterpart on the pages).
+ * While both events are non-NULL (cudaEvent_t passed as void*), every
+ * attn_decode call made from the calling host thread records `split_start` on
+ * its stream immediately before launching the split-attention kernel and
+ * `split_stop` immediately after it, so that cudaEventElapsedTime gives that
+ * kernel's device time.  Recording between kernels removes the launch overlap
+ * of that call.  Pass NULL, NULL to stop.  The setting is per host thread.
+ */
+int oscar_kv_set_profile_events(void* split_start, void* split_stop);
 
 #ifdef __cplusplus
 }

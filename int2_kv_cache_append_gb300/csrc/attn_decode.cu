@@ -49,12 +49,13 @@ struct DecCfg {
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
   static constexpr int BF_BYTES = 2 * kBfTok * BF_STRIDE;
   static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 127) / 128 * 128;
-  static constexpr int NST = D == 128 ? 8 : (D == 256 ? 6 : 4);
+  static constexpr int NST = D == 128 ? (NQT == 1 ? 8 : 6) : (D == 256 ? 6 : 4);
   static constexpr int HEADS = 4 * NQT;      // head slots per (b, kv head)
   // shared memory carve-up (bytes)
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_QBF = OFF_STAGE + NST * STAGE;           // bf16 q fragments per warp
-  static constexpr int QBF_BYTES = kNCW * 8 * NQT * 32 * 8;
+  static constexpr int NQB = 2 * NQT;       // bf16 n-tiles: (hi, mid) and (lo, -) per 4 heads
+  static constexpr int QBF_BYTES = kNCW * 8 * NQB * 32 * 8;
   static constexpr int OFF_XCH = OFF_QBF + QBF_BYTES;               // team score exchange
   static constexpr int XCH_BYTES = TS > 1 ? NTEAMS * 2 * TS * kI2Tok * HEADS * 4 : 0;
   static constexpr int OFF_PART = OFF_XCH + XCH_BYTES;              // team partials
@@ -274,7 +275,9 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
   // B fragments of q' for this warp's group: column n <-> (head n/2, hi|lo by n%2)
   uint32_t qf[8][NQT][2];
   float qsum[NQT];
-  uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + warp * 8 * NQT * 64;
+  // bf16 B fragments for BF16 blocks: n-tile 2nq holds (hi, mid) and n-tile
+  // 2nq+1 holds (lo, 0) of each head's three-way bf16 split (~24 bits)
+  uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + warp * 8 * C::NQB * 64;
   {
     const int hs_b = gq >> 1, lohalf = gq & 1;
 #pragma unroll
@@ -289,12 +292,16 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
           const int d0 = 16 * kk + 2 * cq + 8 * half;
           const float x0 = hv ? qp[d0] : 0.f, x1 = hv ? qp[d0 + 1] : 0.f;
           const uint32_t s0 = split_f16(x0), s1 = split_f16(x1);
-          const uint32_t t0 = split_bf16(x0), t1 = split_bf16(x1);
           // pick hi (low half) or lo (high half) of each split
           const uint32_t v16 = lohalf ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
-          const uint32_t vbf = lohalf ? ((t0 >> 16) | (t1 & 0xffff0000u)) : ((t0 & 0xffffu) | (t1 << 16));
           qf[kk][nq][half] = v16;
-          qbf[(kk * NQT + nq) * 64 + half * 32 + lane] = vbf;
+          uint32_t p0[3], p1[3];
+          split3_bf16(x0, p0);
+          split3_bf16(x1, p1);
+          const uint32_t va = lohalf ? (p0[1] | (p1[1] << 16)) : (p0[0] | (p1[0] << 16));
+          const uint32_t vb = lohalf ? 0u : (p0[2] | (p1[2] << 16));
+          qbf[(kk * C::NQB + 2 * nq) * 64 + half * 32 + lane] = va;
+          qbf[(kk * C::NQB + 2 * nq + 1) * 64 + half * 32 + lane] = vb;
         }
       }
       const int hc = 4 * nq + cq;  // head owned by this lane in C fragments
@@ -377,11 +384,11 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
       }
     } else {
       const uint32_t kb_s = smem_u32(st);
-      float acc[NQT][4];
+      float acc[C::NQB][4];
 #pragma unroll
-      for (int nq = 0; nq < NQT; ++nq)
+      for (int nb = 0; nb < C::NQB; ++nb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nq][e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
       const int mi = lane >> 3;
       const int tok = (lane & 7) + 8 * (mi & 1);
 #pragma unroll
@@ -390,16 +397,16 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(kb_s + tok * C::BF_STRIDE + dim * 2, a0, a1, a2, a3);
 #pragma unroll
-        for (int nq = 0; nq < NQT; ++nq) {
-          const uint32_t b0 = qbf[(kk * NQT + nq) * 64 + lane];
-          const uint32_t b1 = qbf[(kk * NQT + nq) * 64 + 32 + lane];
-          mma_bf16(acc[nq], a0, a1, a2, a3, b0, b1);
+        for (int nb = 0; nb < C::NQB; ++nb) {
+          const uint32_t b0 = qbf[(kk * C::NQB + nb) * 64 + lane];
+          const uint32_t b1 = qbf[(kk * C::NQB + nb) * 64 + 32 + lane];
+          mma_bf16(acc[nb], a0, a1, a2, a3, b0, b1);
         }
       }
 #pragma unroll
       for (int nq = 0; nq < NQT; ++nq) {
-        s[0][nq][0] = acc[nq][0] + acc[nq][1];
-        s[0][nq][1] = acc[nq][2] + acc[nq][3];
+        s[0][nq][0] = acc[2 * nq][0] + acc[2 * nq][1] + acc[2 * nq + 1][0];
+        s[0][nq][1] = acc[2 * nq][2] + acc[2 * nq][3] + acc[2 * nq + 1][2];
       }
     }
 
@@ -755,9 +762,12 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   const Geom& g = a.g;
   qrot_kernel<D><<<g.B * g.Hq, D, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
+  if (prof && cudaEventRecord(g_prof_start, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   if (launch_pdl(split_kernel<D, NQT>, dim3(a.ns, g.Hkv, g.B), dim3(kThreads), C::SMEM, stream, a) !=
       cudaSuccess)
     return OSCAR_ERR_LAUNCH;
+  if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   const size_t msmem = (size_t(g.G) * D + 2 * g.G) * sizeof(float);
   if (launch_pdl(merge_kernel<D>, dim3(g.B * g.Hkv), dim3(256), msmem, stream, a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
@@ -765,6 +775,8 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns) {
   const uint64_t bq = uint64_t(g.B) * g.Hq;

@@ -144,6 +144,17 @@ __device__ __forceinline__ uint32_t split_bf16(float x) {
   return pack_bf162(h, l);
 }
 
+// Three-way bf16 split: x ~ p[0] + p[1] + p[2] (bf16 bit patterns), ~24 bits.
+__device__ __forceinline__ void split3_bf16(float x, uint32_t (&p)[3]) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+  p[0] = __bfloat16_as_ushort(h);
+  p[1] = __bfloat16_as_ushort(m);
+  p[2] = __bfloat16_as_ushort(l);
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier + bulk copy (TMA engine, non-tensor form)
 // ---------------------------------------------------------------------------

@@ -45,7 +45,10 @@ struct DecodeArgs {
 };
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns);
+// optional events recorded around the split kernel (per host thread)
+extern thread_local cudaEvent_t g_prof_start, g_prof_stop;
 int launch_append(const AppendArgs& a, cudaStream_t stream);
+int launch_append_tc(const AppendArgs& a, cudaStream_t stream);  // D = 128, bf16 inputs
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 int decode_auto_splits(const Geom& g, int seq_len_hint);
 

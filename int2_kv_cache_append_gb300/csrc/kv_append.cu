@@ -221,6 +221,7 @@ int launch_append_d(const AppendArgs& a, cudaStream_t stream) {
 
 int launch_append(const AppendArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return OSCAR_OK;
+  if (a.g.D == 128 && !a.in_fp32) return launch_append_tc(a, stream);
   switch (a.g.D) {
     case 128: return launch_append_d<128>(a, stream);
     case 256: return launch_append_d<256>(a, stream);

@@ -1,0 +1,396 @@
+// kv_append on the 5th-generation tensor cores (head_dim 128, bf16 inputs).
+//
+// Same computation as kv_append.cu (rotate, clip, group-128 INT2 codes, BF16
+// windows; see the Qwen3-4B model card, Run, and OSCAR-RotationZoo, How to use),
+// organised as a GEMM [rows x 128] x [128 x 128] per role:
+//
+//   * R (float32) is split once per CTA into three bf16 matrices whose sum is R
+//     exactly (8 + 8 + 8 mantissa bits); each bf16 product with a bf16 input is
+//     exact, so the fp32 accumulation gives the rotation to float32 accuracy.
+//     The pieces are written to shared memory transposed (N x K, K-major) in the
+//     128-byte swizzled layout the MMA descriptors expect.
+//   * A tiles of 128 rows are fetched with TMA tensor loads (cp.async.bulk.tensor,
+//     SWIZZLE_128B) into a 2-stage ring.
+//   * One thread of the producer warp issues 3 x 8 tcgen05.mma (M128 N128 K16,
+//     kind::f16, bf16 operands, fp32 accumulate) per tile into a double-buffered
+//     TMEM accumulator and signals completion with tcgen05.commit.
+//   * Four epilogue warps read their 32 TMEM lanes (one row per thread) with
+//     tcgen05.ld and run the codec exactly as the CUDA-core kernel does.
+//
+// Every wait is bounded; on a timeout the kernel flags OSCAR_DEV_TIMEOUT, stops
+// issuing work, waits (bounded) for its own copies and MMAs and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTileRows = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kThreadsTc = (kEpiWarps + 1) * 32;
+constexpr uint32_t kKBlockBytes = kTileRows * 128;  // 128 rows x 64 bf16 (128 B), swizzled
+constexpr uint32_t kOperandBytes = 2 * kKBlockBytes; // K = 128 -> two K-blocks
+constexpr uint32_t kOffB = 0;                          // 3 pieces of R^T
+constexpr uint32_t kOffA = 3 * kOperandBytes;          // 2 stages of A
+constexpr uint32_t kOffBar = kOffA + 2 * kOperandBytes;
+constexpr uint32_t kSmemTc = kOffBar + 128 + 1024;     // + alignment slack
+constexpr uint32_t kTmemCols = 256;                    // two 128-column fp32 accumulators
+
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFF);        // start address
+  d |= uint64_t(1) << 16;                       // leading byte offset (unused for swizzled K-major)
+  d |= uint64_t(1024 >> 4) << 32;               // stride byte offset
+  d |= uint64_t(1) << 46;                       // descriptor version
+  d |= uint64_t(2) << 61;                       // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, bf16 A/B, fp32 D, K-major A and B, M=128, N=128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kD >> 3) << 17) |
+                            (uint32_t(kTileRows >> 4) << 24);
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Byte offset of element (row, k) of a K-major, 128-byte-swizzled operand with
+// 128 rows and K = 128 (two 64-element K-blocks).
+__device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
+  const int kb = k >> 6, kin = k & 63;
+  const int chunk = (kin >> 3) ^ (row & 7);
+  return uint32_t(kb) * kKBlockBytes + uint32_t(row) * 128 + uint32_t(chunk) * 16 + uint32_t(kin & 7) * 2;
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    kv_append_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const AppendArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sB = base + kOffB, sA = base + kOffA;
+  const uint32_t bar0 = base + kOffBar;
+  auto full_a = [&](int s) { return bar0 + 8u * s; };
+  auto empty_a = [&](int s) { return bar0 + 16u + 8u * s; };
+  auto acc_full = [&](int s) { return bar0 + 32u + 8u * s; };
+  auto acc_empty = [&](int s) { return bar0 + 48u + 8u * s; };
+
+  const int role = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* __restrict__ R = role ? a.R_V : a.R_K;
+  const CUtensorMap* tmap = role ? &tmV : &tmK;
+  const int64_t ntiles = (a.rows + kTileRows - 1) / kTileRows;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(empty_a(s), 1);
+      mbar_init(acc_full(s), 1);
+      mbar_init(acc_empty(s), kEpiWarps);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // B operand: piece p holds B_p[n][k] with R[k][n] = B_0 + B_1 + B_2 (bf16)
+  if (threadIdx.x < kD) {
+    const int n = threadIdx.x;
+    for (int k = 0; k < kD; ++k) {
+      const float x = __ldg(R + k * kD + n);
+      const __nv_bfloat16 h = __float2bfloat16_rn(x);
+      const float r1 = x - __bfloat162float(h);
+      const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+      const uint32_t off = sw128_offset(n, k);
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 0 * kOperandBytes + off) = h;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 1 * kOperandBytes + off) = m;
+      *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 2 * kOperandBytes + off) = l;
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make generic smem writes visible to the MMA
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kEpiWarps) {
+    // ------------------------- producer + MMA issuer -------------------------
+    if (lane == 0) {
+      int it = 0;
+      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        bool ok = true;
+        if (it >= 2) ok = mbar_wait(empty_a(s), ph ^ 1);
+        if (ok && !*((volatile int*)&abort_flag)) {
+          mbar_arrive_expect_tx(full_a(s), kOperandBytes);
+          const uint32_t dst = sA + s * kOperandBytes;
+          tma_load_2d(dst, tmap, 0, int(tile * kTileRows), full_a(s));
+          tma_load_2d(dst + kKBlockBytes, tmap, 64, int(tile * kTileRows), full_a(s));
+          ok = mbar_wait(full_a(s), ph);
+        } else {
+          ok = false;
+        }
+        if (ok && it >= 2) ok = mbar_wait(acc_empty(s), ph ^ 1);
+        if (!ok) {
+          abort_flag = 1;
+          status_or(a.status, OSCAR_DEV_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dcol = tmem + uint32_t(s) * kD;
+        const uint32_t a_base = sA + s * kOperandBytes;
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t koff = uint32_t(k >> 2) * kKBlockBytes + uint32_t(k & 3) * 32;
+            umma_bf16(dcol, umma_desc_sw128(a_base + koff), umma_desc_sw128(sB + p * kOperandBytes + koff),
+                      (p | k) != 0);
+          }
+        }
+        umma_commit(acc_full(s));
+        umma_commit(empty_a(s));
+      }
+      // drain: the last (up to two) commits must have landed before TMEM is freed
+      for (int j = (it >= 2 ? it - 2 : 0); j < it; ++j) mbar_wait(acc_full(j & 1), (j >> 1) & 1);
+    }
+  } else {
+    // ------------------------------- epilogue --------------------------------
+    const Geom& g = a.g;
+    const float ratio = role ? a.v_clip : a.k_clip;
+    uint8_t* role_base = a.layer_base + role * g.role_bytes;
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int s = it & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(acc_full(s), (it >> 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) { abort_flag = 1; status_or(a.status, OSCAR_DEV_TIMEOUT); }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem + (uint32_t(32 * warp) << 16) + uint32_t(s) * kD;
+      const int64_t row = tile * kTileRows + 32 * warp + lane;
+      const bool valid = row < a.rows;
+      float v[32];
+
+      // pass 1: row max |r|
+      float amax = 0.f;
+      bool finite = true;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(taddr + 32 * c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          finite &= isfinite(v[j]);
+          amax = fmaxf(amax, fabsf(v[j]));
+        }
+      }
+      const float tclip = __fmul_rn(ratio, amax);
+      // pass 2: clipped min / max (one group of 128)
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(taddr + 32 * c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = fminf(fmaxf(v[j], -tclip), tclip);
+          mn = fminf(mn, x);
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      const __half sh = __float2half_rn(s32);
+      const __half zh = __float2half_rn(mn);
+      const float sf = __half2float(sh), zf = __half2float(zh);
+      const bool rng_ok = isfinite(sf) && isfinite(zf);
+      const bool qok = rng_ok && sf != 0.f;
+      const float inv = qok ? __frcp_rn(sf) : 0.f;
+
+      int b = 0, p = -1, newlen = 0;
+      int64_t bh = 0;
+      if (valid) {
+        const int h = int(row % g.Hkv);
+        const int64_t bt = row / g.Hkv;
+        const int t = int(bt % a.n_new);
+        b = int(bt / a.n_new);
+        p = a.start_pos[b] + t;
+        newlen = a.start_pos[b] + a.n_new;
+        bh = int64_t(b) * g.Hkv + h;
+        if (!finite) status_or(a.status, OSCAR_DEV_NONFINITE);
+        if (!rng_ok) status_or(a.status, OSCAR_DEV_FP16_RANGE);
+        if (p < 0 || p >= g.cap) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
+      }
+      const bool in_cache = valid && p >= 0 && p < g.cap;
+      const bool to_sink = in_cache && p < g.S;
+      const bool to_ring = in_cache && g.W > 0 && p >= newlen - g.W;
+      uint4* sink4 = to_sink ? reinterpret_cast<uint4*>(role_base + (bh * g.S + p) * (2 * kD)) : nullptr;
+      uint4* ring4 =
+          to_ring ? reinterpret_cast<uint4*>(role_base + g.sink_bytes + (bh * g.W + (p % g.W)) * (2 * kD)) : nullptr;
+      float4* dbg = (valid && a.debug_rot) ? reinterpret_cast<float4*>(a.debug_rot + (row * 2 + role) * kD) : nullptr;
+
+      // pass 3: codes, BF16 windows, debug rows
+      uint32_t words[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) words[w] = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(taddr + 32 * c, v);
+        if (dbg) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) dbg[(32 * c + j) / 4] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+        if (sink4 || ring4) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 q;
+            q.x = pack_bf162(__float2bfloat16_rn(v[j + 0]), __float2bfloat16_rn(v[j + 1]));
+            q.y = pack_bf162(__float2bfloat16_rn(v[j + 2]), __float2bfloat16_rn(v[j + 3]));
+            q.z = pack_bf162(__float2bfloat16_rn(v[j + 4]), __float2bfloat16_rn(v[j + 5]));
+            q.w = pack_bf162(__float2bfloat16_rn(v[j + 6]), __float2bfloat16_rn(v[j + 7]));
+            if (sink4) sink4[(32 * c + j) / 8] = q;
+            if (ring4) ring4[(32 * c + j) / 8] = q;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = fminf(fmaxf(v[j], -tclip), tclip);
+          int code = __float2int_rn(__fmul_rn(__fsub_rn(x, zf), inv));
+          code = qok ? min(max(code, 0), 3) : 0;
+          const int d = 32 * c + j;
+          if (role == 0) {
+            const int kk = d >> 4, r16 = d & 15, hh = r16 >> 3, e = r16 & 7;
+            const int word = 2 * (e >> 1) + (kk >> 2);
+            const int bit = 2 * (2 * (kk & 3) + hh) + 16 * (e & 1);
+            words[word] |= uint32_t(code) << bit;
+          } else {
+            words[d & 7] |= uint32_t(code) << (2 * (d >> 3));
+          }
+        }
+      }
+      if (in_cache && p >= g.S) {
+        const int64_t irow = bh * g.ncap + (p - g.S);
+        uint4* c4 = reinterpret_cast<uint4*>(role_base + g.sink_bytes + g.ring_bytes + irow * (kD / 4));
+        c4[0] = make_uint4(words[0], words[1], words[2], words[3]);
+        c4[1] = make_uint4(words[4], words[5], words[6], words[7]);
+        reinterpret_cast<uint32_t*>(role_base + g.sink_bytes + g.ring_bytes + g.codes_bytes)[irow] =
+            pack_half2(sh, zh);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(s));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_rows_map(CUtensorMap* m, const void* ptr, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(kD), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(kD * 2)};
+  const cuuint32_t box[2] = {64, kTileRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_append_tc(const AppendArgs& a, cudaStream_t stream) {
+  static int attr_set[64] = {0};
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return OSCAR_ERR_LAUNCH;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kv_append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return OSCAR_ERR_LAUNCH;
+    attr_set[dev] = 1;
+  }
+  CUtensorMap mk, mv;
+  if (!make_rows_map(&mk, a.k_new, a.rows) || !make_rows_map(&mv, a.v_new, a.rows)) return OSCAR_ERR_LAUNCH;
+  const int64_t ntiles = (a.rows + kTileRows - 1) / kTileRows;
+  const int per_role = int(std::min<int64_t>(ntiles, std::max(1, sms[dev] / 2)));
+  kv_append_tc_kernel<<<dim3(per_role, 2, 1), kThreadsTc, kSmemTc, stream>>>(mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
+}
+
+}  // namespace oscar

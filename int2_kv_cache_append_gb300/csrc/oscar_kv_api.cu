@@ -151,4 +151,10 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   return oscar::launch_decode(a, static_cast<cudaStream_t>(stream));
 }
 
+int oscar_kv_set_profile_events(void* split_start, void* split_stop) {
+  oscar::g_prof_start = static_cast<cudaEvent_t>(split_start);
+  oscar::g_prof_stop = static_cast<cudaEvent_t>(split_stop);
+  return OSCAR_OK;
+}
+
 }  // extern "C"

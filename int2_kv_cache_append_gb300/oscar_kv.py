@@ -28,7 +28,7 @@ DEV_EMPTY = 16
 STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LAUNCH", -5: "UNSUPPORTED"}
 
 # every symbol include/oscar_kv.h declares
-EXPORTS = ("kv_layout_query", "kv_append", "attn_decode")
+EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "oscar_kv_set_profile_events")
 
 
 class OscarError(RuntimeError):
@@ -91,6 +91,8 @@ def lib():
         L.attn_decode.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, ctypes.c_int32, P, P,
                                   ctypes.c_float, ctypes.c_int32, P, P, P, ctypes.c_uint64, P, P]
         L.attn_decode.restype = ctypes.c_int
+        L.oscar_kv_set_profile_events.argtypes = [P, P]
+        L.oscar_kv_set_profile_events.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -135,3 +137,9 @@ def attn_decode(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, out, wo
     if check and rc != 0:
         raise OscarError("attn_decode", rc)
     return rc
+
+
+def set_profile_events(start=None, stop=None) -> None:
+    """Record torch.cuda.Event pair around the split kernel of later attn_decode calls (None, None stops)."""
+    lib().oscar_kv_set_profile_events(None if start is None else ctypes.c_void_p(start.cuda_event),
+                                      None if stop is None else ctypes.c_void_p(stop.cuda_event))

@@ -203,3 +203,27 @@ def queries(w: Workload, layer: int, batch: int | None = None, extra: int = 0):
     q = activations(rng_for(w.config_id, layer, ROLE_Q, extra), (b, w.num_q_heads, w.head_dim), ch,
                     kind=w.act_kind)
     return q if w.in_fp32 else to_bf16_values(q)
+
+
+# --------------------------------------------------------------------------
+# device-side generation for large workloads (torch RNG on the GPU)
+# --------------------------------------------------------------------------
+def activations_torch(gen, shape, channels, kind: str = "t3", mag: float = 8.0, dtype=None, device="cuda"):
+    """Same distribution as :func:`activations`, drawn with a seeded torch generator.
+
+    Student-t(3) is drawn as z / sqrt(chi2_3 / 3) from four standard normals.
+    """
+    import torch
+
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    ch = torch.as_tensor(np.asarray(channels), device=device, dtype=torch.long)
+    if ch.numel():
+        sub = list(shape[:-1]) + [ch.numel()]
+        if kind == "scale":
+            x[..., ch] *= mag
+        else:
+            z = torch.randn(sub, generator=gen, device=device)
+            n = torch.randn([3] + sub, generator=gen, device=device)
+            t3 = z / torch.sqrt((n * n).sum(0) / 3.0)
+            x[..., ch] += mag * t3
+    return x if dtype is None else x.to(dtype)

@@ -276,10 +276,11 @@ def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new:
     k_new, v_new: [B][n][Hkv][D] float (bf16 values as float32, or float32).
     R_K, R_V: [D][D] rotations of this layer.  Every position p >= S gets its
     INT2 row; p < S also goes to the BF16 sink; p >= start_pos[b] + n - W also
-    goes to the BF16 ring slot p mod W.
+    goes to the BF16 ring slot p mod W.  Positions outside [0, capacity) are
+    not stored.
     """
     B, n, H, D = k_new.shape
-    S, W = cfg.sink, cfg.recent
+    S, W, cap = cfg.sink, cfg.recent, cfg.capacity
     rots = []
     for role, (x, R, ratio) in enumerate(((k_new, R_K, cfg.k_clip), (v_new, R_V, cfg.v_clip))):
         view = CacheView(cfg, cache, layer, role)
@@ -294,6 +295,8 @@ def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new:
             newlen = int(start_pos[b]) + n
             for t in range(n):
                 p = int(start_pos[b]) + t
+                if p < 0 or p >= cap:
+                    continue  # outside the cache: not stored
                 if p < S:
                     view.sink[b, :, p, :] = rb[b, t]
                 else:

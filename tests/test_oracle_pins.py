@@ -281,6 +281,23 @@ def test_append_ring_slots_hand_example():
     assert list(O.bf16_bits_to_f32(v.sink[0, 0, :, 0])) == [1.0, 2.0]
 
 
+def test_append_skips_positions_beyond_capacity():
+    # capacity 5, S=2, W=2: tokens at positions 3..7 -> only 3 and 4 are stored
+    cfg = _small_cfg(S_=2, W=2, cap=5, B=1, Hkv=1, G=1)
+    cache = O.new_cache(cfg)
+    I = np.eye(128, dtype=np.float32)
+    k = (np.arange(5, dtype=np.float32) + 10.0)[None, :, None, None] * np.ones((1, 5, 1, 128), np.float32)
+    O.append(cfg, cache, 0, k, k, [3], I, I)
+    v = O.CacheView(cfg, cache, 0, 0)
+    assert O.layout(cfg)["ncap"] == 64      # rows exist past capacity in memory ...
+    zq = v.sz[0, 0, :, 0, 1].astype(np.float64)
+    assert zq[1] != 0 and zq[2] != 0       # positions 3, 4 (rows 1, 2) written
+    assert np.all(zq[3:] == 0)             # ... but positions 5.. are never written
+    # ring slots hold the last W=2 stored tokens only if they are in the cache:
+    # newlen - W = 6 -> positions 6, 7 are beyond capacity, so the ring stays empty
+    assert np.all(v.ring == 0)
+
+
 def test_append_chunking_invariance():
     cfg = _small_cfg(S_=3, W=5, cap=64)
     rng = np.random.default_rng(6)
