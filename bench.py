@@ -65,6 +65,23 @@ def kv_bytes_per_bh(w, T: int) -> int:
     return n_i2 * 2 * (D // 4 + 4 * (D // 128)) + n_bf * 2 * 2 * D
 
 
+def max_over_ranks(ms: float) -> float:
+    """Slowest rank's time when torch.distributed is initialised (any backend), else ms."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(batch_per_rank: int, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank decodes its own batch; the job's rate uses the slowest rank."""
+    return world * batch_per_rank / (ms_max / 1e3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -314,11 +331,7 @@ def ours(args):
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     split_ms = [a.elapsed_time(b) for a, b in kev]
-    ms = statistics.mean(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms))
     clocks.stop()
 
     # ---- end-to-end through the public API with host buffers
@@ -346,7 +359,7 @@ def ours(args):
     if rank != 0:
         return
     kv_bytes = kv_bytes_per_bh(w, T) * Bsz * Hkv * L
-    tokens_per_s = world * Bsz / (ms / 1e3)
+    tokens_per_s = whole_job_tokens_per_s(Bsz, world, ms)
     peak, peak_kind = measured_peaks()
     split_avg_ms = statistics.mean(split_ms)
     achieved = kv_bytes / L / (split_avg_ms / 1e3) / 1e9
@@ -382,6 +395,110 @@ def ours(args):
         dist.destroy_process_group()
 
 
+def ours_append(args):
+    """Append-phase workload: every step appends n new tokens per sequence at the
+    end of the context (rotation GEMM on the tensor cores, clip, INT2 pack, ring)."""
+    import torch
+
+    from int2_kv_cache_append_gb300 import build as B
+    from int2_kv_cache_append_gb300 import oscar_kv as K
+    from int2_kv_cache_append_gb300 import synth as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    w = S.WORKLOADS[args.workload]
+    Bsz, H, D, T, n = w.batch, w.num_kv_heads, w.head_dim, w.context, w.append_tokens
+    cfg = K.KVConfig(1, Bsz, w.num_q_heads, H, D, w.sink, w.recent, T, w.k_clip, w.v_clip)
+    lay = K.layout_query(cfg)
+    cache = torch.zeros(lay["total_bytes"], dtype=torch.uint8, device=dev)
+    RK, RV = S.rotations(w, 0)
+    RK, RV = torch.from_numpy(RK).to(dev), torch.from_numpy(RV).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5 + rank)
+    ch = S.outlier_channels(w.config_id, 0, D)
+    k = S.activations_torch(gen, (Bsz, n, H, D), ch, dtype=torch.bfloat16, device=dev)
+    v = S.activations_torch(gen, (Bsz, n, H, D), ch, dtype=torch.bfloat16, device=dev)
+    start = torch.full((Bsz,), T - n, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        K.kv_append(cfg, cache, 0, k, v, start, RK, RV, status=status)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        flush.zero_()
+        K.kv_append(cfg, cache, 0, k, v, start, RK, RV, status=status)
+        torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a_, b_ in ev:
+        flush.zero_()
+        a_.record(stream)
+        K.kv_append(cfg, cache, 0, k, v, start, RK, RV, status=status)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    ms = max_over_ranks(statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev))
+    # e2e: inputs copied from pinned host memory every step, status word read back
+    k_h, v_h = k.cpu().pin_memory(), v.cpu().pin_memory()
+    st_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    k_d, v_d = torch.empty_like(k), torch.empty_like(v)
+    e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in e2e:
+        flush.zero_()
+        a_.record(stream)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        K.kv_append(cfg, cache, 0, k_d, v_d, start, RK, RV, status=status)
+        st_h.copy_(status, non_blocking=True)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in e2e)
+    if rank != 0:
+        return
+    rows = Bsz * n * H * 2
+    tokens = world * Bsz * n
+    ring_rows = Bsz * H * min(n, w.recent) * 2
+    hbm_bytes = rows * (2 * D + D // 4 + 4 * (D // 128)) + ring_rows * 2 * D
+    flops = rows * 2 * D * D
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+    gbs = hbm_bytes / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "INT2 KV append tokens/s (rotate + clip + INT2 pack), 1 GB300", "value": tokens / (ms / 1e3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w) + f" append{n}", "l2": "flushed between steps (512 MiB write)"},
+        "roofline": {"bound": "hbm" if gbs / peaks["hbm_gbs"] >= tfs / peaks["bf16_tflops"] else "tensor",
+                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": None, "kernel": "kv_append_tc_kernel",
+                     "tensor_tflops_algorithmic": tfs, "tensor_frac_algorithmic": tfs / peaks["bf16_tflops"],
+                     "tensor_frac_issued_3piece": 3 * tfs / peaks["bf16_tflops"],
+                     "algorithmic_bytes_per_launch": hbm_bytes, "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * k.numel() * k.element_size(), "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps, "clocks": clocks.summary(), "cpu_baseline": None,
+        "dev_status": int(status.item()),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.cpu_sample_worker:
@@ -389,6 +506,10 @@ def main():
         return
     if args.impl == "reference":
         reference_arm(args)
+        return
+    from int2_kv_cache_append_gb300 import synth as S
+    if S.WORKLOADS[args.workload].append_tokens > 0:
+        ours_append(args)
         return
     ours(args)
 

@@ -65,14 +65,16 @@ def test_append_exact_chain_bitwise(case, fp32):
     assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
 
 
-def test_append_calibrated_rotation_codec_exact_where_inputs_agree():
-    """Calibrated rotations: the GPU's float32 rotated rows are within a few ulp
-    of the oracle's exactly rounded rows.  The codec is then checked where its
-    inputs agree: for every group whose scale and zero match the oracle's bit
-    for bit, each channel whose rotated value matches bit for bit must carry
-    the oracle's code; mismatching groups differ by at most one fp16 ulp.  BF16
-    window values must be bit-equal where the rotated value is, else within
-    one bf16 ulp."""
+def test_append_calibrated_rotation_close_to_oracle():
+    """Calibrated rotations: the GPU rotation (tensor cores, R split into three
+    bf16 pieces, fp32 accumulation) is within 2e-6 of the float64 product, but
+    not correctly rounded, so the stored cache can differ from the oracle's where
+    a value sits next to a rounding boundary.  Checked: scale/zero equal for
+    almost every group and within one fp16 ulp otherwise; codes equal except
+    where the oracle's own pre-rounding value (x - zero) / scale lies within
+    1e-3 of a half-integer, and never off by more than one; BF16 window values
+    within one bf16 ulp.  Bit-exactness of the codec itself is covered by the
+    exact-rotation tests above."""
     w = S.WORKLOADS["qwen3-4b-layer"]
     D, B, H, n, S_ = 128, 2, 8, 300, 64
     c = O.Config(1, B, 32, H, D, S_, 128, 512, 0.96, 0.92)
@@ -83,31 +85,32 @@ def test_append_calibrated_rotation_codec_exact_where_inputs_agree():
     gcache = new_cache(c)
     rot = gpu_append(c, gcache, 0, k, v, [0, 0], RK, RV, want_rot=True).cpu().numpy()
     g = gcache.cpu().numpy()
-    for role, (ro, R, x) in enumerate(((rk_o, RK, k), (rv_o, RV, v))):
-        rg = rot[:, :, :, role]                                     # [B][n][H][D]
+    for role, (ro, R, x, ratio) in enumerate(((rk_o, RK, k, c.k_clip), (rv_o, RV, v, c.v_clip))):
         exact = x.astype(np.float64).reshape(-1, D) @ R.astype(np.float64)
-        assert np.abs(rg.reshape(-1, D) - exact).max() <= 2e-6 * np.abs(exact).max()
-        eq = rg.view(np.uint32) == ro.view(np.uint32)              # per element
-        assert eq.mean() > 0.5
+        assert np.abs(rot[:, :, :, role].reshape(-1, D) - exact).max() <= 2e-6 * np.abs(exact).max()
         gv, ov = O.CacheView(c, g, 0, role), O.CacheView(c, ocache, 0, role)
-        # INT2 rows: positions S..n-1
-        gsz = gv.sz[:, :, :n - S_].transpose(0, 2, 1, 3, 4)          # [B][t][H][groups][2]
-        osz = ov.sz[:, :, :n - S_].transpose(0, 2, 1, 3, 4)
-        gcodes = O.unpack_codes(gv.codes[:, :, :n - S_].transpose(0, 2, 1, 3).reshape(-1, D // 4), D, role)
-        ocodes = O.unpack_codes(ov.codes[:, :, :n - S_].transpose(0, 2, 1, 3).reshape(-1, D // 4), D, role)
-        same_sz = np.all(gsz.view(np.uint16) == osz.view(np.uint16), axis=-1).reshape(-1, D // 128)
-        assert same_sz.mean() > 0.9
-        d16 = np.abs(gsz.view(np.uint16).astype(np.int64) - osz.view(np.uint16).astype(np.int64))
-        assert d16.max() <= 1
-        gate = eq[:, S_:].reshape(-1, D) & np.repeat(same_sz, 128, axis=1)
-        assert np.array_equal(gcodes[gate], ocodes[gate])
-        assert np.abs(gcodes.astype(int) - ocodes.astype(int)).max() <= 1
-        # BF16 sink rows: positions 0..S-1
-        gs = gv.sink[:, :, :S_].transpose(0, 2, 1, 3)
-        os_ = ov.sink[:, :, :S_].transpose(0, 2, 1, 3)
-        e2 = eq[:, :S_]
-        assert np.array_equal(gs[e2], os_[e2])
-        assert np.abs(gs.astype(np.int64) - os_.astype(np.int64)).max() <= 1
+        gsz = gv.sz[:, :, :n - S_].view(np.uint16).astype(np.int64)
+        osz = ov.sz[:, :, :n - S_].view(np.uint16).astype(np.int64)
+        assert np.mean(np.all(gsz == osz, axis=-1)) > 0.95
+        assert np.abs(gsz - osz).max() <= 1
+        gcodes = O.unpack_codes(gv.codes[:, :, :n - S_].reshape(-1, D // 4), D, role).astype(int)
+        ocodes = O.unpack_codes(ov.codes[:, :, :n - S_].reshape(-1, D // 4), D, role).astype(int)
+        # the oracle's pre-rounding value of each code, from its own rows
+        r = ro[:, S_:].transpose(0, 2, 1, 3).reshape(-1, D)
+        t = (np.float32(ratio) * np.abs(r).max(axis=1)).astype(np.float32)[:, None]
+        xc = np.minimum(np.maximum(r, -t), t)
+        sc = ov.sz[:, :, :n - S_, 0, 0].reshape(-1, 1).astype(np.float64)
+        ze = ov.sz[:, :, :n - S_, 0, 1].reshape(-1, 1).astype(np.float64)
+        y = (xc - ze) / np.where(sc == 0, 1.0, sc)
+        near_tie = np.abs(y - np.floor(y) - 0.5) < 1e-3
+        same_sz = np.repeat(np.all(gsz == osz, axis=-1).reshape(-1, 1), D, axis=1)
+        bad = (gcodes != ocodes) & same_sz & ~near_tie
+        assert not bad.any(), f"{bad.sum()} codes differ away from a rounding tie"
+        assert np.abs(gcodes - ocodes).max() <= 1
+        assert np.mean(gcodes != ocodes) < 1e-3
+        gs = gv.sink[:, :, :S_].astype(np.int64)
+        os_ = ov.sink[:, :, :S_].astype(np.int64)
+        assert np.abs(gs - os_).max() <= 1 and np.mean(gs != os_) < 0.05
 
 
 def test_append_over_capacity_sets_status_and_skips():

@@ -112,7 +112,7 @@ def _run(wname, samples, layers=(0,), rot="perm", T=None, check_bytes=True):
             r16 = rel_l2(o16[b, sl], bf16_round64(ref))
             r32 = rel_l2(o32[b, sl], ref)
             m32 = float(np.abs(o32[b, sl] - ref).max())
-            dl = float(np.abs(l32[b, sl] - ref_lse).max())
+            dl = float(np.max(np.abs(l32[b, sl] - ref_lse) - 1e-5 * np.abs(ref_lse)))
             tol32 = 2e-4 if check_bytes else 2e-3
             assert r16 <= (1e-3 if check_bytes else 3e-3), (wname, layer, b, h, r16)
             assert m32 <= 5e-3 and r32 <= tol32, (wname, layer, b, h, m32, r32)
