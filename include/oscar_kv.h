@@ -145,7 +145,7 @@ typedef struct {
  * OSCAR_ERR_UNSUPPORTED on a bad config, else fills *out.
  * attn_decode with n splits needs
  *   align256(B*Hq*D*4) + align256(B*Hq*(D/128)*4) + align256(B*Hq*n*D*4)
- *   + align256(B*Hq*n*2*4) bytes of workspace.
+ *   + align256(B*Hq*n*2*4) + align256(B*Hkv*4) bytes of workspace.
  */
 int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out);
 
@@ -185,8 +185,10 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  *              scaled scores.
  *   workspace  device scratch of workspace_bytes (see kv_layout_query); the
  *              automatic split count never needs more than is given.
- * Launches three kernels on `stream` (query rotation, split attention, split
- * merge + un-rotation).  Concurrent calls must not share a workspace.
+ * Launches two kernels on `stream`: query rotation, then split attention
+ * whose last CTA per (sequence, KV head) merges the splits and un-rotates V.
+ * Both use programmatic dependent launch; the first waits for all prior work
+ * on the stream before reading q.  Concurrent calls must not share a workspace.
  */
 int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
                 const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,

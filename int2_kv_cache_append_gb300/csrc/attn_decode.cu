@@ -6,7 +6,7 @@
 // card (Folders: the rotation applies to Q/K and V); "OSCAR-RotationZoo" (How
 // to use: V rotation absorbed into the output).
 //
-// Three kernels per call:
+// Two kernels per call:
 //   qrot   q' = q R_K * sm_scale * log2(e) (float32) and per-group sums of q'.
 //   split  grid (splits, Hkv, B).  Four consumer warps and one producer warp.
 //          The producer streams 64-token INT2 blocks (codes + scale/zero) and
@@ -22,8 +22,10 @@
 //            o  += (p_t * scale_t) . c_t  and  zeta += p_t * zero_t.
 //          Online softmax in log2 units; teams of D/128 warps split the
 //          channels of a block by quant group and exchange partial scores.
-//   merge  grid (B * Hkv): log-sum-exp merge of the splits, o = o' R_V^T
-//          (skipped when absorbed), store bf16/fp32 and lse.
+//          Each CTA writes one partial (m, l, o') per head; the last CTA of a
+//          (b, kv head) to finish (an atomic ticket, never a wait) merges the
+//          splits by log-sum-exp, applies o = o' R_V^T (skipped when absorbed)
+//          and stores bf16/fp32 output and lse.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -49,7 +51,7 @@ struct DecCfg {
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
   static constexpr int BF_BYTES = 2 * kBfTok * BF_STRIDE;
   static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 127) / 128 * 128;
-  static constexpr int NST = D == 128 ? (NQT == 1 ? 8 : 6) : (D == 256 ? 6 : 4);
+  static constexpr int NST = D == 128 ? 6 : (D == 256 ? 6 : 4);
   static constexpr int HEADS = 4 * NQT;      // head slots per (b, kv head)
   // shared memory carve-up (bytes)
   static constexpr int OFF_STAGE = 0;
@@ -137,35 +139,54 @@ __device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b) {
 }
 
 // ---------------------------------------------------------------------------
-// qrot: q' = q R_K * qscale, and per-group sums
+// qrot: q' = q R_K * qscale and per-group sums, for the G query heads of one
+// (b, kv head); also zeroes that unit's merge ticket.  Launched with PDL: it
+// waits for the preceding kernel before reading anything (q may be produced
+// right before this call) and lets the split kernel launch when it is done.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(D) qrot_kernel(const DecodeArgs a) {
-  __shared__ float qs[D];
-  __shared__ float red[D / 32];
-  const int bq = blockIdx.x;  // b * Hq + head
+  __shared__ float qs[8][D];
+  __shared__ float red[8][D / 32];
+  const int bh = blockIdx.x;  // b * Hkv + h
+  const int G = a.g.G;
   const int d = threadIdx.x;
-  if (a.in_fp32)
-    qs[d] = static_cast<const float*>(a.q)[int64_t(bq) * D + d];
-  else
-    qs[d] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[int64_t(bq) * D + d]);
+  const int64_t q0 = int64_t(bh) * G * D;  // first query head of this kv head
+  pdl_wait();
+  for (int i = 0; i < G; ++i)
+    qs[i][d] = a.in_fp32 ? static_cast<const float*>(a.q)[q0 + i * D + d]
+                         : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[q0 + i * D + d]);
   __syncthreads();
-  float acc = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < D; ++i) acc = fmaf(qs[i], __ldg(a.R_K + i * D + d), acc);
-  acc *= a.qscale;
-  if (!(fabsf(acc) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
-  a.qprime[int64_t(bq) * D + d] = acc;
-  float s = acc;
+  float acc[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((d & 31) == 0) red[d >> 5] = s;
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 16
+  for (int k = 0; k < D; ++k) {
+    const float r = __ldg(a.R_K + k * D + d);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < G) acc[i] = fmaf(qs[i][k], r, acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < G) {
+      const float v = acc[i] * a.qscale;
+      if (!(fabsf(v) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
+      a.qprime[q0 + i * D + d] = v;
+      float t = v;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if ((d & 31) == 0) red[i][d >> 5] = t;
+    }
+  }
+  if (d == 0) a.ticket[bh] = 0;
   __syncthreads();
-  if (d < D / kGroup) {
+  for (int idx = d; idx < G * (D / kGroup); idx += D) {
+    const int i = idx / (D / kGroup), j = idx % (D / kGroup);
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) t += red[d * 4 + w];
-    a.qsum[int64_t(bq) * (D / kGroup) + d] = t;
+    for (int w = 0; w < 4; ++w) t += red[i][j * 4 + w];
+    a.qsum[(q0 / D + i) * (D / kGroup) + j] = t;
   }
   pdl_trigger();
 }
@@ -174,7 +195,7 @@ __global__ void __launch_bounds__(D) qrot_kernel(const DecodeArgs a) {
 // split kernel
 // ---------------------------------------------------------------------------
 template <int D, int NQT>
-__global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, (D == 128 ? (NQT == 1 ? 3 : 2) : 1)) split_kernel(const DecodeArgs a) {
   using C = DecCfg<D, NQT>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -611,81 +632,82 @@ __global__ void __launch_bounds__(kThreads) split_kernel(const DecodeArgs a) {
       a.ws_ml[pi * 2 + 1] = L;
     }
   }
-}
 
-// ---------------------------------------------------------------------------
-// merge kernel: one CTA per (b, kv head)
-// ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
-  extern __shared__ float ms[];  // [G][D] o', then [G] M, [G] L
-  const Geom& g = a.g;
-  const int h = blockIdx.x % g.Hkv, b = blockIdx.x / g.Hkv;
-  const int G = g.G;
-  float* ob = ms;
-  float* Ms = ms + G * D;
-  float* Ls = Ms + G;
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = clamp_seq_len(a, b);
-  if (threadIdx.x == 0) {
-    if (a.seq_lens[b] > g.cap) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
-    if (T < 1) status_or(a.status, OSCAR_DEV_EMPTY);
-  }
-  for (int i = warp; i < G; i += 8) {
-    const int64_t base = (int64_t(b) * g.Hq + h * G + i) * a.ns;
+  // ---- the last CTA of this (b, kv head) to finish merges all splits (a ticket,
+  // no waiting on other CTAs), un-rotates V and stores the output
+  __shared__ int is_last;
+  __threadfence();
+  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket + bh, 1) == a.ns - 1;
+  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+  if (!is_last) return;
+  __threadfence();
+  float* ob = part;                    // [G][D] merged o' (rotated basis)
+  float* Ms = part + C::HEADS * D;     // [G] max, [G] sum
+  float* Ls = Ms + C::HEADS;
+  for (int i = warp; i < Gh; i += kNCW) {
+    const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
     float M = -INFINITY;
-    for (int s = lane; s < a.ns; s += 32) M = fmaxf(M, a.ws_ml[(base + s) * 2]);
+    for (int sp = lane; sp < a.ns; sp += 32) M = fmaxf(M, __ldcg(a.ws_ml + (base + sp) * 2));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
     float L = 0.f;
-    for (int s = lane; s < a.ns; s += 32) {
-      const float m = a.ws_ml[(base + s) * 2];
-      L += m == -INFINITY ? 0.f : ex2(m - M) * a.ws_ml[(base + s) * 2 + 1];
+    for (int sp = lane; sp < a.ns; sp += 32) {
+      const float m = __ldcg(a.ws_ml + (base + sp) * 2);
+      L += m == -INFINITY ? 0.f : ex2(m - M) * __ldcg(a.ws_ml + (base + sp) * 2 + 1);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) { Ms[i] = M; Ls[i] = L; }
+    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    if (lane == 0) {
+      Ms[i] = M;
+      Ls[i] = L;
+    }
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+  for (int idx = threadIdx.x; idx < Gh * D; idx += 32 * kNCW) {
     const int i = idx / D, d = idx % D;
-    const int64_t base = (int64_t(b) * g.Hq + h * G + i) * a.ns;
+    const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
     const float M = Ms[i], L = Ls[i];
     float acc = 0.f;
     if (M != -INFINITY && L > 0.f) {
-      for (int s = 0; s < a.ns; ++s) {
-        const float m = a.ws_ml[(base + s) * 2];
-        if (m != -INFINITY) acc += ex2(m - M) * a.ws_acc[(base + s) * D + d];
+#pragma unroll 4
+      for (int sp = 0; sp < a.ns; ++sp) {
+        const float m = __ldcg(a.ws_ml + (base + sp) * 2);
+        const float v = __ldcg(a.ws_acc + (base + sp) * D + d);
+        acc += m == -INFINITY ? 0.f : ex2(m - M) * v;
       }
       acc /= L;
     }
     ob[idx] = acc;
   }
-  __syncthreads();
-  // o = o' R_V^T : o[r] = sum_j R_V[r][j] o'[j]; one warp per output channel r
-  for (int r = warp; r < D; r += 8) {
+  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+  // o = o' R_V^T: o[r] = sum_j R_V[r][j] o'[j]; one thread per output channel r
+  for (int r = threadIdx.x; r < D; r += 32 * kNCW) {
     float res[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) res[i] = 0.f;
     if (a.absorb_v) {
-      if (lane == 0)
-        for (int i = 0; i < G && i < 8; ++i) res[i] = ob[i * D + r];
-    } else {
-      for (int j = lane; j < D; j += 32) {
-        const float rv = __ldg(a.R_V + int64_t(r) * D + j);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < G) res[i] = fmaf(rv, ob[i * D + j], res[i]);
-      }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
+        if (i < Gh) res[i] = ob[i * D + r];
+    } else {
+      const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);
+#pragma unroll 8
+      for (int j4 = 0; j4 < D / 4; ++j4) {
+        const float4 rv = __ldg(rv4 + j4);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) res[i] += __shfl_xor_sync(0xffffffffu, res[i], o);
+        for (int i = 0; i < 8; ++i) {
+          if (i < Gh) {
+            const float* oi = ob + i * D + 4 * j4;
+            res[i] = fmaf(rv.x, oi[0], fmaf(rv.y, oi[1], fmaf(rv.z, oi[2], fmaf(rv.w, oi[3], res[i]))));
+          }
+        }
+      }
     }
-    if (lane == 0) {
-      for (int i = 0; i < G && i < 8; ++i) {
-        const int64_t oi = (int64_t(b) * g.Hq + h * G + i) * D + r;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < Gh) {
+        const int64_t oi = (int64_t(b) * g.Hq + head0 + i) * D + r;
         if (a.out_fp32)
           static_cast<float*>(a.out)[oi] = res[i];
         else
@@ -693,11 +715,17 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
       }
     }
   }
-  if (a.lse && threadIdx.x < G) {
+  if (threadIdx.x < Gh) {
     const int i = threadIdx.x;
-    const float M = Ms[i], L = Ls[i];
-    a.lse[int64_t(b) * g.Hq + h * G + i] =
-        (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+    if (a.lse) {
+      const float M = Ms[i], L = Ls[i];
+      a.lse[int64_t(b) * g.Hq + head0 + i] =
+          (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+    }
+    if (i == 0 && h == 0) {
+      if (a.seq_lens[b] > g.cap) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
+      if (T < 1) status_or(a.status, OSCAR_DEV_EMPTY);
+    }
   }
 }
 
@@ -760,17 +788,13 @@ template <int D, int NQT>
 int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = DecCfg<D, NQT>;
   const Geom& g = a.g;
-  qrot_kernel<D><<<g.B * g.Hq, D, 0, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  if (launch_pdl(qrot_kernel<D>, dim3(g.B * g.Hkv), dim3(D), 0, stream, a) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
   if (prof && cudaEventRecord(g_prof_start, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   if (launch_pdl(split_kernel<D, NQT>, dim3(a.ns, g.Hkv, g.B), dim3(kThreads), C::SMEM, stream, a) !=
       cudaSuccess)
     return OSCAR_ERR_LAUNCH;
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
-  const size_t msmem = (size_t(g.G) * D + 2 * g.G) * sizeof(float);
-  if (launch_pdl(merge_kernel<D>, dim3(g.B * g.Hkv), dim3(256), msmem, stream, a) != cudaSuccess)
-    return OSCAR_ERR_LAUNCH;
   return OSCAR_OK;
 }
 
@@ -781,7 +805,7 @@ thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 uint64_t decode_workspace_bytes(const Geom& g, int ns) {
   const uint64_t bq = uint64_t(g.B) * g.Hq;
   return align256(bq * g.D * 4) + align256(bq * g.Dg * 4) + align256(bq * ns * g.D * 4) +
-         align256(bq * ns * 2 * 4);
+         align256(bq * ns * 2 * 4) + align256(uint64_t(g.B) * g.Hkv * 4);
 }
 
 int decode_auto_splits(const Geom& g, int seq_len_hint) {

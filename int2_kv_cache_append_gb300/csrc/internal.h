@@ -39,6 +39,7 @@ struct DecodeArgs {
   float* qsum;     // [B][Hq][Dg]  per-group sums of qprime
   float* ws_acc;   // [B][Hq][NS][D]
   float* ws_ml;    // [B][Hq][NS][2]
+  int32_t* ticket; // [B][Hkv] split-completion counters (zeroed by qrot)
   int ns;          // context splits per (b, kv head)
   float qscale;    // sm_scale * log2(e)
   int in_fp32, out_fp32, absorb_v;

@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendA
   float* xs = smem;                 // [RPC][LD] inputs
   float* rs = smem + C::RPC * C::LD;  // [RPC][LD] rotated rows
 
+  pdl_trigger();  // a dependent kernel may be scheduled now; it waits for our completion itself
   const int role = blockIdx.y;
   const float* __restrict__ R = role ? a.R_V : a.R_K;
   const float ratio = role ? a.v_clip : a.k_clip;

@@ -142,6 +142,8 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   a.ws_acc = reinterpret_cast<float*>(ws);
   ws += oscar::align256(bq * uint64_t(ns) * g.D * 4);
   a.ws_ml = reinterpret_cast<float*>(ws);
+  ws += oscar::align256(bq * uint64_t(ns) * 2 * 4);
+  a.ticket = reinterpret_cast<int32_t*>(ws);
   a.ns = ns;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(float(g.D));
   a.qscale = scale * 1.4426950408889634f;

@@ -47,7 +47,7 @@ def test_layout_matches_oracle(lib, shape):
     # documented workspace formula
     a = lambda x: (x + 255) // 256 * 256
     bq = B * Hq
-    ws = a(bq * D * 4) + a(bq * (D // 128) * 4) + a(bq * 64 * D * 4) + a(bq * 64 * 8)
+    ws = a(bq * D * 4) + a(bq * (D // 128) * 4) + a(bq * 64 * D * 4) + a(bq * 64 * 8) + a(B * Hkv * 4)
     assert got["decode_workspace_bytes"] == ws
 
 
