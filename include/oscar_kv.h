@@ -196,6 +196,29 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
                 uint64_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * attn_decode_static — attn_decode for callers that cannot allocate device
+ * memory (no counterpart on the pages).  Plugin hosts that own every device
+ * allocation, and serving loops that must not call cudaMalloc while other
+ * streams run, can call this instead: its scratch is a file-scope __device__
+ * array of OSCAR_KV_STATIC_SCRATCH_BYTES inside the library, which every GPU
+ * that loads the library holds until the process exits.  Arguments are those of
+ * attn_decode without workspace / workspace_bytes; the caller still passes all
+ * inputs and outputs.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Returns OSCAR_ERR_WORKSPACE when even one context split needs more
+ * scratch than the array holds, or when an explicit num_splits does not fit;
+ * the automatic split count is reduced to what fits.  Every call shares the
+ * array, so calls whose work overlaps on the GPU race; nothing in it needs to
+ * start at zero (each call zeroes its own counters and writes every partial
+ * before reading it).
+ */
+#define OSCAR_KV_STATIC_SCRATCH_BYTES (16u << 20)
+int attn_decode_static(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
+                       const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
+                       float sm_scale, int32_t num_splits, void* out, float* lse, int32_t* dev_status,
+                       void* stream);
+
+/*
  * oscar_kv_set_profile_events — measurement hook (no counterpart on the pages).
  * While both events are non-NULL (cudaEvent_t passed as void*), every
  * attn_decode call made from the calling host thread records `split_start` on

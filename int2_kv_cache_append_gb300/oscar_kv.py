@@ -28,7 +28,8 @@ DEV_EMPTY = 16
 STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LAUNCH", -5: "UNSUPPORTED"}
 
 # every symbol include/oscar_kv.h declares
-EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "oscar_kv_set_profile_events")
+EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "attn_decode_static", "oscar_kv_set_profile_events")
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class OscarError(RuntimeError):
@@ -91,6 +92,9 @@ def lib():
         L.attn_decode.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, ctypes.c_int32, P, P,
                                   ctypes.c_float, ctypes.c_int32, P, P, P, ctypes.c_uint64, P, P]
         L.attn_decode.restype = ctypes.c_int
+        L.attn_decode_static.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, ctypes.c_int32, P, P,
+                                         ctypes.c_float, ctypes.c_int32, P, P, P, P]
+        L.attn_decode_static.restype = ctypes.c_int
         L.oscar_kv_set_profile_events.argtypes = [P, P]
         L.oscar_kv_set_profile_events.restype = ctypes.c_int
         _lib = L
@@ -136,6 +140,18 @@ def attn_decode(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, out, wo
                            _stream(stream))
     if check and rc != 0:
         raise OscarError("attn_decode", rc)
+    return rc
+
+
+def attn_decode_static(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, out, lse=None,
+                       seq_len_hint: int = 0, sm_scale: float = 0.0, num_splits: int = 0, status=None, stream=None,
+                       check: bool = True) -> int:
+    """attn_decode with the library's fixed scratch array (no workspace argument)."""
+    rc = lib().attn_decode_static(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(q), _ptr(seq_lens),
+                                  int(seq_len_hint), _ptr(R_K), _ptr(R_V), float(sm_scale), int(num_splits),
+                                  _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    if check and rc != 0:
+        raise OscarError("attn_decode_static", rc)
     return rc
 
 
