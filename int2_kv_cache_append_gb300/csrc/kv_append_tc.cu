@@ -14,8 +14,11 @@
 //   * One thread of the producer warp issues 3 x 8 tcgen05.mma (M128 N128 K16,
 //     kind::f16, bf16 operands, fp32 accumulate) per tile into a double-buffered
 //     TMEM accumulator and signals completion with tcgen05.commit.
-//   * Four epilogue warps read their 32 TMEM lanes (one row per thread) with
-//     tcgen05.ld and run the codec exactly as the CUDA-core kernel does.
+//   * Eight epilogue warps in two groups (even and odd tiles, one TMEM
+//     accumulator each) read their 32 TMEM lanes (one row per thread) with
+//     tcgen05.ld and run the codec exactly as the CUDA-core kernel does, in two
+//     passes: row min/max (which give max|x| and, clamping being monotone, the
+//     clipped group min/max), then codes and BF16 copies.
 //
 // Every wait is bounded; on a timeout the kernel flags OSCAR_DEV_TIMEOUT, stops
 // issuing work, waits (bounded) for its own copies and MMAs and frees TMEM.
@@ -32,7 +35,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTileRows = 128;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;                 // two groups of four: even / odd tiles
 constexpr int kThreadsTc = (kEpiWarps + 1) * 32;
 constexpr uint32_t kKBlockBytes = kTileRows * 128;  // 128 rows x 64 bf16 (128 B), swizzled
 constexpr uint32_t kOperandBytes = 2 * kKBlockBytes; // K = 128 -> two K-blocks
@@ -121,6 +124,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   auto acc_full = [&](int s) { return bar0 + 32u + 8u * s; };
   auto acc_empty = [&](int s) { return bar0 + 48u + 8u * s; };
 
+  pdl_trigger();  // a dependent kernel may be scheduled now; it waits for our completion itself
   const int role = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* __restrict__ R = role ? a.R_V : a.R_K;
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(full_a(s), 1);
       mbar_init(empty_a(s), 1);
       mbar_init(acc_full(s), 1);
-      mbar_init(acc_empty(s), kEpiWarps);
+      mbar_init(acc_empty(s), kEpiWarps / 2);
     }
     mbar_fence_init();
   }
@@ -144,18 +148,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // B operand: piece p holds B_p[n][k] with R[k][n] = B_0 + B_1 + B_2 (bf16)
-  if (threadIdx.x < kD) {
-    const int n = threadIdx.x;
-    for (int k = 0; k < kD; ++k) {
-      const float x = __ldg(R + k * kD + n);
-      const __nv_bfloat16 h = __float2bfloat16_rn(x);
-      const float r1 = x - __bfloat162float(h);
-      const __nv_bfloat16 m = __float2bfloat16_rn(r1);
-      const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
-      const uint32_t off = sw128_offset(n, k);
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 0 * kOperandBytes + off) = h;
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 1 * kOperandBytes + off) = m;
-      *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 2 * kOperandBytes + off) = l;
+  {
+    // all 160 threads; float4 loads along rows of R (coalesced, many in flight)
+    const float4* R4 = reinterpret_cast<const float4*>(R);
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < kD * kD / 4; idx += kThreadsTc) {
+      const float4 x4 = __ldg(R4 + idx);
+      const int k = (idx * 4) / kD, n0 = (idx * 4) % kD;
+      const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = xs[e];
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const float r1 = x - __bfloat162float(h);
+        const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+        const uint32_t off = sw128_offset(n0 + e, k);
+        *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 0 * kOperandBytes + off) = h;
+        *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 1 * kOperandBytes + off) = m;
+        *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 2 * kOperandBytes + off) = l;
+      }
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make generic smem writes visible to the MMA
@@ -211,8 +223,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const Geom& g = a.g;
     const float ratio = role ? a.v_clip : a.k_clip;
     uint8_t* role_base = a.layer_base + role * g.role_bytes;
-    int it = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    const int grp = warp >> 2, quarter = warp & 3;  // tile parity handled, TMEM lane quarter
+    int it = grp;
+    for (int64_t tile = blockIdx.x + int64_t(grp) * gridDim.x; tile < ntiles;
+         tile += 2 * int64_t(gridDim.x), it += 2) {
       const int s = it & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(acc_full(s), (it >> 1) & 1);
@@ -222,36 +236,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem + (uint32_t(32 * warp) << 16) + uint32_t(s) * kD;
-      const int64_t row = tile * kTileRows + 32 * warp + lane;
+      const uint32_t taddr = tmem + (uint32_t(32 * quarter) << 16) + uint32_t(s) * kD;
+      const int64_t row = tile * kTileRows + 32 * quarter + lane;
       const bool valid = row < a.rows;
       float v[32];
 
-      // pass 1: row max |r|
-      float amax = 0.f;
-      bool finite = true;
+      // pass 1: raw row min / max (NaN-propagating, so a NaN row shows as non-finite)
+      float rmn = INFINITY, rmx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(taddr + 32 * c, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          finite &= isfinite(v[j]);
-          amax = fmaxf(amax, fabsf(v[j]));
+          rmn = fmin_nan(rmn, v[j]);
+          rmx = fmax_nan(rmx, v[j]);
         }
       }
+      const bool finite = isfinite(rmn) && isfinite(rmx);
+      const float amax = fmaxf(fabsf(rmn), fabsf(rmx));          // max_j |r_j|
       const float tclip = __fmul_rn(ratio, amax);
-      // pass 2: clipped min / max (one group of 128)
-      float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(taddr + 32 * c, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = fminf(fmaxf(v[j], -tclip), tclip);
-          mn = fminf(mn, x);
-          mx = fmaxf(mx, x);
-        }
-      }
+      const float mn = fminf(fmaxf(rmn, -tclip), tclip);           // min_j clamp(r_j)
+      const float mx = fminf(fmaxf(rmx, -tclip), tclip);           // max_j clamp(r_j)
       const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
       const __half sh = __float2half_rn(s32);
       const __half zh = __float2half_rn(mn);
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           to_ring ? reinterpret_cast<uint4*>(role_base + g.sink_bytes + (bh * g.W + (p % g.W)) * (2 * kD)) : nullptr;
       float4* dbg = (valid && a.debug_rot) ? reinterpret_cast<float4*>(a.debug_rot + (row * 2 + role) * kD) : nullptr;
 
-      // pass 3: codes, BF16 windows, debug rows
+      // pass 2: codes, BF16 windows, debug rows
       uint32_t words[8];
 #pragma unroll
       for (int w = 0; w < 8; ++w) words[w] = 0;
