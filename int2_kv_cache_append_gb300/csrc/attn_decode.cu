@@ -51,7 +51,12 @@ struct DecCfg {
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
   static constexpr int BF_BYTES = 2 * kBfTok * BF_STRIDE;
   static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 127) / 128 * 128;
-  static constexpr int NST = D == 128 ? 6 : (D == 256 ? 6 : 4);
+  // Block k uses stage k % NST and is consumed by team k % NTEAMS.  NST must be a
+  // multiple of NTEAMS so that every stage is always consumed by the same team:
+  // a team then waits on a stage only after it has itself consumed that stage's
+  // previous phase, so the phase parity it waits on cannot alias an older phase.
+  static constexpr int NST = D == 128 ? 8 : (D == 256 ? 6 : 4);
+  static_assert(NST % NTEAMS == 0, "every stage must belong to one team");
   static constexpr int HEADS = 4 * NQT;      // head slots per (b, kv head)
   // shared memory carve-up (bytes)
   static constexpr int OFF_STAGE = 0;
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(D) qrot_kernel(const DecodeArgs a) {
 // split kernel
 // ---------------------------------------------------------------------------
 template <int D, int NQT>
-__global__ void __launch_bounds__(kThreads, (D == 128 ? (NQT == 1 ? 3 : 2) : 1)) split_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(const DecodeArgs a) {
   using C = DecCfg<D, NQT>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
