@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--sample-heads", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -158,21 +159,24 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # CPU oracle sample (test infrastructure, timed as the CPU baseline)
 # --------------------------------------------------------------------------
-def cpu_sample_worker(workload: str, steps: int, warmup: int):
+def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int):
     """Run inside a single-threaded child process: time the oracle's decode step
-    (append of the current token + attention) for batch row 0 of the workload."""
+    (append of the current token + attention) for batch row 0 of the workload,
+    restricted to its first `heads` KV heads (and their query heads)."""
     import numpy as np
     from int2_kv_cache_append_gb300 import synth as S
     from oracle import oscar_oracle as O
 
     w = S.WORKLOADS[workload]
     T = w.context
-    c = O.Config(1, 1, w.num_q_heads, w.num_kv_heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip)
+    G = w.num_q_heads // w.num_kv_heads
+    c = O.Config(1, 1, G * heads, heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip)
     RK, RV = S.rotations(w, 0)
     k, v = S.kv_rows(w, 0, T, batch=1)
+    k, v = k[:, :, :heads], v[:, :, :heads]
     cache = O.new_cache(c)
     O.append(c, cache, 0, k[:, :T - 1], v[:, :T - 1], [0], RK, RV)
-    q = S.queries(w, 0, batch=1)
+    q = S.queries(w, 0, batch=1)[:, :G * heads]
     times = []
     for i in range(warmup + steps):
         t0 = time.perf_counter()
@@ -183,11 +187,11 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int):
     print(json.dumps({"sec_per_step": statistics.mean(times), "steps": len(times)}))
 
 
-def run_cpu_sample(workload: str, steps: int, warmup: int):
+def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", "--workload", workload,
-           "--steps", str(steps), "--warmup", str(warmup)]
+           "--steps", str(steps), "--warmup", str(warmup), "--sample-heads", str(heads)]
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
@@ -202,16 +206,19 @@ def reference_arm(args):
         return
     w = S.WORKLOADS[args.workload]
     steps = max(1, args.steps)
+    # about 75 ms of oracle work per KV head and step at T=16384: keep the run near two minutes
+    heads = max(1, min(w.num_kv_heads, int(120.0 / (0.075 * (steps + args.warmup) * w.context / 16384))))
     t0 = time.time()
-    res = run_cpu_sample(args.workload, steps, args.warmup)
+    res = run_cpu_sample(args.workload, steps, args.warmup, heads)
     sec = res["sec_per_step"]
-    value = 1.0 / sec  # one sequence per sample step
-    sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}: append of the current "
-              f"token + decode over T={w.context} for all {w.num_q_heads} query heads; single thread")
+    value = (heads / w.num_kv_heads) / sec  # the sample is heads/Hkv of one sequence's decode step
+    sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}, {heads} of "
+              f"{w.num_kv_heads} KV heads: append of the current token + decode over T={w.context}; "
+              f"single thread; tokens/s scaled by the fraction of a sequence sampled")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "sample": "1 sequence per step"},
+            "config": {"workload": workload_desc(w), "sample": f"{heads} of {w.num_kv_heads} KV heads of one sequence per step"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.time() - t0}
@@ -366,7 +373,7 @@ def ours(args):
     step_gbs = kv_bytes / (ms / 1e3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        res = run_cpu_sample(args.workload, steps=3, warmup=1)
+        res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv)
         cpu = {"value": 1.0 / res["sec_per_step"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"oracle decode step (append + attention) for 1 of {Bsz} sequences of {args.workload}, "
                          f"T={T}, {res['steps']} timed steps, single thread"}
@@ -502,7 +509,7 @@ def ours_append(args):
 def main():
     args = parse()
     if args.cpu_sample_worker:
-        cpu_sample_worker(args.workload, args.steps, args.warmup)
+        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads)
         return
     if args.impl == "reference":
         reference_arm(args)
