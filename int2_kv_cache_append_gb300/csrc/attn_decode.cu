@@ -36,8 +36,8 @@
 namespace oscar {
 namespace {
 
-constexpr int kNCW = 4;                    // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;  // + one producer warp
+constexpr int kNCW = 4;                    // warps per CTA (each team issues its own copies)
+constexpr int kThreads = kNCW * 32;
 constexpr int kI2Tok = 64;                 // tokens per INT2 block
 constexpr int kBfTok = 16;                 // tokens per BF16 block
 
@@ -51,12 +51,12 @@ struct DecCfg {
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
   static constexpr int BF_BYTES = 2 * kBfTok * BF_STRIDE;
   static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 127) / 128 * 128;
-  // Block k uses stage k % NST and is consumed by team k % NTEAMS.  NST must be a
-  // multiple of NTEAMS so that every stage is always consumed by the same team:
-  // a team then waits on a stage only after it has itself consumed that stage's
-  // previous phase, so the phase parity it waits on cannot alias an older phase.
+  // Each team owns NSTW private stages: it issues the bulk copies of its own
+  // blocks into them and consumes them in order, so a stage's barrier phases
+  // are produced and awaited by one team only.
   static constexpr int NST = D == 128 ? 8 : (D == 256 ? 6 : 4);
   static_assert(NST % NTEAMS == 0, "every stage must belong to one team");
+  static constexpr int NSTW = NST / NTEAMS;
   static constexpr int HEADS = 4 * NQT;      // head slots per (b, kv head)
   // shared memory carve-up (bytes)
   static constexpr int OFF_STAGE = 0;
@@ -68,7 +68,7 @@ struct DecCfg {
   static constexpr int OFF_PART = OFF_XCH + XCH_BYTES;              // team partials
   static constexpr int PART_BYTES = NTEAMS * HEADS * (D + 2) * 4;
   static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
-  static constexpr int SMEM = OFF_BAR + 2 * NST * 8 + 16;
+  static constexpr int SMEM = OFF_BAR + NST * 8 + 16;
 };
 
 // Per-(b, kv head) region sizes and the block list
@@ -219,10 +219,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(smem_u32(&bars[s]), 1);                  // full: producer arrival + tx bytes
-      mbar_init(smem_u32(&bars[C::NST + s]), C::TS);     // empty: one arrival per team warp
-    }
+    for (int s = 0; s < C::NST; ++s) mbar_init(smem_u32(&bars[s]), 1);  // issuer's arrival + tx bytes
     mbar_fence_init();
   }
   __syncthreads();
@@ -232,69 +229,50 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
   const uint64_t codes_off = g.sink_bytes + g.ring_bytes;
   const uint64_t sz_off = codes_off + g.codes_bytes;
 
-  if (warp == kNCW) {
-    // ------------------------------- producer -------------------------------
-    int issued = 0;
-    for (int kl = 0; kl < nblk; ++kl) {
-      const int stage = kl % C::NST;
-      const uint32_t full = smem_u32(&bars[stage]);
-      const uint32_t empty = smem_u32(&bars[C::NST + stage]);
-      int ok = 1;
+  // Bulk copies of block kl into stage `stage`, issued by the calling warp (lane
+  // 0 arms the barrier with the byte count first).
+  auto issue_block = [&](int kl, int stage) {
+    const Blk bk = block_at(rg, kb + kl);
+    const uint32_t full = smem_u32(&bars[stage]);
+    const uint32_t dst = smem_u32(smem + C::OFF_STAGE + stage * C::STAGE);
+    if (bk.type == 1) {
       if (lane == 0) {
-        if (kl >= C::NST) ok = mbar_wait(empty, ((kl / C::NST) - 1) & 1);
-        if (!ok) status_or(a.status, OSCAR_DEV_TIMEOUT);
-        if (*((volatile int*)&abort_flag)) ok = 0;
+        const int n4 = (bk.count + 3) & ~3;
+        const uint32_t cb = n4 * C::ROWB, sb = n4 * C::Dg * 4;
+        mbar_arrive_expect_tx(full, 2 * cb + 2 * sb);
+        const int64_t row = bh * g.ncap + bk.first;
+        bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
+        bulk_g2s(dst + kI2Tok * C::ROWB, vbase + codes_off + row * C::ROWB, cb, full);
+        bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
+        bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb, full);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);  // one decision for the whole warp
-      if (!ok) {
-        if (lane == 0) abort_flag = 1;
-        break;
+    } else {
+      if (lane == 0) mbar_arrive_expect_tx(full, 2 * bk.count * 2 * D);
+      __syncwarp();
+      const int r = lane & 15;
+      if (r < bk.count) {
+        const int pos = bk.first + r;
+        const uint8_t* base = lane < 16 ? kbase : vbase;
+        const uint8_t* src = bk.type == 0 ? base + (bh * g.S + pos) * (2 * D)
+                                          : base + g.sink_bytes + (bh * g.W + pos % g.W) * (2 * D);
+        bulk_g2s(dst + (lane < 16 ? 0 : kBfTok * C::BF_STRIDE) + r * C::BF_STRIDE, src, 2 * D, full);
       }
-      const Blk bk = block_at(rg, kb + kl);
-      const uint32_t dst = smem_u32(smem + C::OFF_STAGE + stage * C::STAGE);
-      if (bk.type == 1) {
-        if (lane == 0) {
-          const int n4 = (bk.count + 3) & ~3;
-          const uint32_t cb = n4 * C::ROWB, sb = n4 * C::Dg * 4;
-          mbar_arrive_expect_tx(full, 2 * cb + 2 * sb);
-          const int64_t row = bh * g.ncap + bk.first;
-          bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
-          bulk_g2s(dst + kI2Tok * C::ROWB, vbase + codes_off + row * C::ROWB, cb, full);
-          bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
-          bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb,
-                   full);
-        }
-      } else {
-        if (lane == 0) mbar_arrive_expect_tx(full, 2 * bk.count * 2 * D);
-        __syncwarp();
-        const int r = lane & 15;
-        if (r < bk.count) {
-          const int pos = bk.first + r;
-          const uint8_t* base = lane < 16 ? kbase : vbase;
-          const uint8_t* src = bk.type == 0 ? base + (bh * g.S + pos) * (2 * D)
-                                            : base + g.sink_bytes + (bh * g.W + pos % g.W) * (2 * D);
-          bulk_g2s(dst + (lane < 16 ? 0 : kBfTok * C::BF_STRIDE) + r * C::BF_STRIDE, src, 2 * D, full);
-        }
-      }
-      issued = kl + 1;
     }
-    // make sure nothing is still landing in shared memory before exiting
-    if (lane == 0) {
-      const int from = issued > C::NST ? issued - C::NST : 0;
-      for (int kl = from; kl < issued; ++kl)
-        if (!mbar_wait(smem_u32(&bars[kl % C::NST]), (kl / C::NST) & 1)) {
-          status_or(a.status, OSCAR_DEV_TIMEOUT);
-          break;
-        }
-    }
-    return;
-  }
+  };
 
   // ------------------------------- consumers --------------------------------
   const int team = warp / C::TS, wt = warp % C::TS;  // wt = quant group handled
   const int gq = lane >> 2, cq = lane & 3;
   const int Gh = g.G;
   const int head0 = h * Gh;  // first query head of this kv head
+  const int nmine = nblk > team ? (nblk - team + C::NTEAMS - 1) / C::NTEAMS : 0;  // this team's blocks
+  auto my_stage = [&](int j) { return team * C::NSTW + j % C::NSTW; };
+  int issued = 0;  // blocks of this team whose copies are in flight or done
+
+  // the cache is complete once this kernel runs (the preceding kernel waited
+  // for it); start streaming before waiting for q'
+  if (wt == 0)
+    for (; issued < nmine && issued < C::NSTW; ++issued) issue_block(team + issued * C::NTEAMS, my_stage(issued));
 
   pdl_wait();  // q' comes from the preceding kernel
 
@@ -350,10 +328,11 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
   float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
   int xbuf = 0;
 
-  for (int kl = team; kl < nblk; kl += C::NTEAMS) {
-    const int stage = kl % C::NST;
+  for (int j = 0; j < nmine; ++j) {
+    const int kl = team + j * C::NTEAMS;
+    const int stage = my_stage(j);
     int ok = 1;
-    if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (kl / C::NST) & 1);
+    if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (j / C::NSTW) & 1);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     // the warps of a team must take the same decision: they meet at team barriers below
     if constexpr (C::TS > 1) ok = team_all(ok, 1 + team, 32 * C::TS);
@@ -373,39 +352,58 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
     if (is_i2) {
       const uint8_t* kc = st;
       const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB);
+      // m-tiles are processed in groups whose MMAs interleave (independent
+      // accumulators), so the k-step chain of one m-tile never runs alone
+      constexpr int MG = NQT == 1 ? 4 : 2;
 #pragma unroll
-      for (int mt = 0; mt < MT_MAX; ++mt) {
-        const int t0 = 16 * mt + gq, t1 = t0 + 8;
-        const uint2 w0 = *reinterpret_cast<const uint2*>(kc + t0 * C::ROWB + wt * 32 + cq * 8);
-        const uint2 w1 = *reinterpret_cast<const uint2*>(kc + t1 * C::ROWB + wt * 32 + cq * 8);
-        float acc[NQT][4];
+      for (int m0 = 0; m0 < MT_MAX; m0 += MG) {
+        uint2 w[MG][2];
 #pragma unroll
-        for (int nq = 0; nq < NQT; ++nq)
+        for (int i = 0; i < MG; ++i) {
+          const int t0 = 16 * (m0 + i) + gq;
+          w[i][0] = *reinterpret_cast<const uint2*>(kc + t0 * C::ROWB + wt * 32 + cq * 8);
+          w[i][1] = *reinterpret_cast<const uint2*>(kc + (t0 + 8) * C::ROWB + wt * 32 + cq * 8);
+        }
+        float acc[MG][NQT][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nq][e] = 0.f;
+        for (int i = 0; i < MG; ++i)
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][nq][e] = 0.f;
 #pragma unroll
         for (int wi = 0; wi < 2; ++wi) {
-          uint32_t r0[8], r1[8];
-          unpack16(wi ? w0.y : w0.x, r0);
-          unpack16(wi ? w1.y : w1.x, r1);
+          uint32_t r[MG][2][8];
+#pragma unroll
+          for (int i = 0; i < MG; ++i) {
+            unpack16(wi ? w[i][0].y : w[i][0].x, r[i][0]);
+            unpack16(wi ? w[i][1].y : w[i][1].x, r[i][1]);
+          }
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = 4 * wi + k4;
 #pragma unroll
             for (int nq = 0; nq < NQT; ++nq)
-              mma_f16(acc[nq], r0[2 * k4], r1[2 * k4], r0[2 * k4 + 1], r1[2 * k4 + 1], qf[kk][nq][0],
-                      qf[kk][nq][1]);
+#pragma unroll
+              for (int i = 0; i < MG; ++i)
+                mma_f16(acc[i][nq], r[i][0][2 * k4], r[i][1][2 * k4], r[i][0][2 * k4 + 1], r[i][1][2 * k4 + 1],
+                        qf[kk][nq][0], qf[kk][nq][1]);
           }
         }
-        const uint32_t z0 = ksz[t0 * C::Dg + wt], z1 = ksz[t1 * C::Dg + wt];
-        ksc[mt][0] = __half2float(__ushort_as_half(z0 & 0xffff));
-        kze[mt][0] = __half2float(__ushort_as_half(z0 >> 16));
-        ksc[mt][1] = __half2float(__ushort_as_half(z1 & 0xffff));
-        kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
 #pragma unroll
-        for (int nq = 0; nq < NQT; ++nq) {
-          s[mt][nq][0] = fmaf(ksc[mt][0], acc[nq][0] + acc[nq][1], kze[mt][0] * qsum[nq]);
-          s[mt][nq][1] = fmaf(ksc[mt][1], acc[nq][2] + acc[nq][3], kze[mt][1] * qsum[nq]);
+        for (int i = 0; i < MG; ++i) {
+          const int mt = m0 + i;
+          const int t0 = 16 * mt + gq, t1 = t0 + 8;
+          const uint32_t z0 = ksz[t0 * C::Dg + wt], z1 = ksz[t1 * C::Dg + wt];
+          ksc[mt][0] = __half2float(__ushort_as_half(z0 & 0xffff));
+          kze[mt][0] = __half2float(__ushort_as_half(z0 >> 16));
+          ksc[mt][1] = __half2float(__ushort_as_half(z1 & 0xffff));
+          kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            s[mt][nq][0] = fmaf(ksc[mt][0], acc[i][nq][0] + acc[i][nq][1], kze[mt][0] * qsum[nq]);
+            s[mt][nq][1] = fmaf(ksc[mt][1], acc[i][nq][2] + acc[i][nq][3], kze[mt][1] * qsum[nq]);
+          }
         }
       }
     } else {
@@ -584,8 +582,22 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
       }
     }
 
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars[C::NST + stage]));
+    // every warp of the team is done with this stage: refill it
+    if constexpr (C::TS > 1) {
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * C::TS) : "memory");
+    } else {
+      __syncwarp();
+    }
+    if (wt == 0 && issued < nmine) {
+      issue_block(team + issued * C::NTEAMS, my_stage(issued));
+      ++issued;
+    }
+  }
+  // after an early exit, wait (bounded) for copies still landing in our stages
+  if (wt == 0 && lane == 0) {
+    const int consumed = *((volatile int*)&abort_flag) ? 0 : nmine;
+    for (int jj = (issued > C::NSTW ? issued - C::NSTW : 0); jj < issued; ++jj)
+      if (jj >= consumed && !mbar_wait(smem_u32(&bars[my_stage(jj)]), (jj / C::NSTW) & 1)) break;
   }
 
   // ---- team partials -> shared memory
