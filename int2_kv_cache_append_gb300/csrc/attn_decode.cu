@@ -38,7 +38,8 @@ namespace {
 
 constexpr int kNCW = 4;                    // warps per CTA (each team issues its own copies)
 constexpr int kThreads = kNCW * 32;
-constexpr int kI2Tok = 64;                 // tokens per INT2 block
+constexpr int kI2Tok = 128;                // tokens per INT2 block (one set of bulk copies)
+constexpr int kSub = 64;                   // tokens per INT2 compute sub-block
 constexpr int kBfTok = 16;                 // tokens per BF16 block
 
 template <int D, int NQT>
@@ -64,11 +65,15 @@ struct DecCfg {
   static constexpr int NQB = 2 * NQT;       // bf16 n-tiles: (hi, mid) and (lo, -) per 4 heads
   static constexpr int QBF_BYTES = kNCW * 8 * NQB * 32 * 8;
   static constexpr int OFF_XCH = OFF_QBF + QBF_BYTES;               // team score exchange
-  static constexpr int XCH_BYTES = TS > 1 ? NTEAMS * 2 * TS * kI2Tok * HEADS * 4 : 0;
+  static constexpr int XCH_BYTES = TS > 1 ? NTEAMS * 2 * TS * kSub * HEADS * 4 : 0;
   static constexpr int OFF_PART = OFF_XCH + XCH_BYTES;              // team partials
-  static constexpr int PART_BYTES = NTEAMS * HEADS * (D + 2) * 4;
+  // team partials [team][head][D + 2]; reused by the merging CTA for o' [head][D],
+  // max/sum [2][head] and split weights [head][OSCAR_KV_MAX_SPLITS]
+  static constexpr int PART_A = NTEAMS * HEADS * (D + 2);
+  static constexpr int PART_B = HEADS * (D + 2 + OSCAR_KV_MAX_SPLITS);
+  static constexpr int PART_BYTES = (PART_A > PART_B ? PART_A : PART_B) * 4;
   static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
-  static constexpr int SMEM = OFF_BAR + NST * 8 + 16;
+  static constexpr int SMEM = OFF_BAR + (NST + 1) * 8 + 16;
 };
 
 // Per-(b, kv head) region sizes and the block list
@@ -220,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < C::NST; ++s) mbar_init(smem_u32(&bars[s]), 1);  // issuer's arrival + tx bytes
+    mbar_init(smem_u32(&bars[C::NST]), 1);  // R_V prefetch of the merging CTA
     mbar_fence_init();
   }
   __syncthreads();
@@ -343,8 +349,12 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
     const Blk bk = block_at(rg, kb + kl);
     const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
     const bool is_i2 = bk.type == 1;
-    constexpr int MT_MAX = kI2Tok / 16;
+    constexpr int MT_MAX = kSub / 16;
     const int nmt = is_i2 ? MT_MAX : 1;
+    const int nsub = is_i2 ? (bk.count + kSub - 1) / kSub : 1;
+    for (int sbk = 0; sbk < nsub; ++sbk) {
+    const int cnt = is_i2 ? min(kSub, bk.count - sbk * kSub) : bk.count;  // tokens in this sub-block
+    const int tb = sbk * kSub;  // its first token within the stage
 
     // ---- scores: s[mt][nq][0] token 16mt+gq, [1] token 16mt+gq+8
     float s[MT_MAX][NQT][2];
@@ -361,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
 #pragma unroll
         for (int i = 0; i < MG; ++i) {
           const int t0 = 16 * (m0 + i) + gq;
-          w[i][0] = *reinterpret_cast<const uint2*>(kc + t0 * C::ROWB + wt * 32 + cq * 8);
-          w[i][1] = *reinterpret_cast<const uint2*>(kc + (t0 + 8) * C::ROWB + wt * 32 + cq * 8);
+          w[i][0] = *reinterpret_cast<const uint2*>(kc + (tb + t0) * C::ROWB + wt * 32 + cq * 8);
+          w[i][1] = *reinterpret_cast<const uint2*>(kc + (tb + t0 + 8) * C::ROWB + wt * 32 + cq * 8);
         }
         float acc[MG][NQT][4];
 #pragma unroll
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
         for (int i = 0; i < MG; ++i) {
           const int mt = m0 + i;
           const int t0 = 16 * mt + gq, t1 = t0 + 8;
-          const uint32_t z0 = ksz[t0 * C::Dg + wt], z1 = ksz[t1 * C::Dg + wt];
+          const uint32_t z0 = ksz[(tb + t0) * C::Dg + wt], z1 = ksz[(tb + t1) * C::Dg + wt];
           ksc[mt][0] = __half2float(__ushort_as_half(z0 & 0xffff));
           kze[mt][0] = __half2float(__ushort_as_half(z0 >> 16));
           ksc[mt][1] = __half2float(__ushort_as_half(z1 & 0xffff));
@@ -436,15 +446,15 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
 
     // ---- team exchange of partial scores (one quant group per warp)
     if constexpr (C::TS > 1) {
-      float* xb = xch + ((team * 2 + xbuf) * C::TS) * kI2Tok * C::HEADS;
+      float* xb = xch + ((team * 2 + xbuf) * C::TS) * kSub * C::HEADS;
 #pragma unroll
       for (int mt = 0; mt < MT_MAX; ++mt) {
         if (mt < nmt) {
 #pragma unroll
           for (int nq = 0; nq < NQT; ++nq) {
             const int hs = 4 * nq + cq;
-            xb[(wt * kI2Tok + 16 * mt + gq) * C::HEADS + hs] = s[mt][nq][0];
-            xb[(wt * kI2Tok + 16 * mt + gq + 8) * C::HEADS + hs] = s[mt][nq][1];
+            xb[(wt * kSub + 16 * mt + gq) * C::HEADS + hs] = s[mt][nq][0];
+            xb[(wt * kSub + 16 * mt + gq + 8) * C::HEADS + hs] = s[mt][nq][1];
           }
         }
       }
@@ -458,8 +468,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
             float t0 = 0.f, t1 = 0.f;
 #pragma unroll
             for (int w = 0; w < C::TS; ++w) {
-              t0 += xb[(w * kI2Tok + 16 * mt + gq) * C::HEADS + hs];
-              t1 += xb[(w * kI2Tok + 16 * mt + gq + 8) * C::HEADS + hs];
+              t0 += xb[(w * kSub + 16 * mt + gq) * C::HEADS + hs];
+              t1 += xb[(w * kSub + 16 * mt + gq + 8) * C::HEADS + hs];
             }
             s[mt][nq][0] = t0;
             s[mt][nq][1] = t1;
@@ -480,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int tk = 16 * mt + gq + 8 * e;
-            const float v = tk < bk.count ? s[mt][nq][e] : -INFINITY;
+            const float v = tk < cnt ? s[mt][nq][e] : -INFINITY;
             s[mt][nq][e] = v;
             mb = fmaxf(mb, v);
           }
@@ -519,12 +529,12 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
         // V scale/zero of this lane's two tokens (group wt)
         const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB) + kI2Tok * C::Dg;
         const int t0 = 16 * ks + gq, t1 = t0 + 8;
-        const uint32_t z0 = vsz[t0 * C::Dg + wt], z1 = vsz[t1 * C::Dg + wt];
+        const uint32_t z0 = vsz[(tb + t0) * C::Dg + wt], z1 = vsz[(tb + t1) * C::Dg + wt];
         const float vs0 = __half2float(__ushort_as_half(z0 & 0xffff));
         const float vz0 = __half2float(__ushort_as_half(z0 >> 16));
         const float vs1 = __half2float(__ushort_as_half(z1 & 0xffff));
         const float vz1 = __half2float(__ushort_as_half(z1 >> 16));
-        const bool v0 = t0 < bk.count, v1 = t1 < bk.count;
+        const bool v0 = t0 < cnt, v1 = t1 < cnt;
 #pragma unroll
         for (int nq = 0; nq < NQT; ++nq) {
           const float w0 = v0 ? p[ks][nq][0] * vs0 : 0.f;
@@ -535,10 +545,10 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
         }
         // codes of word (wt, gq) for tokens 2cq, 2cq+1, 2cq+8, 2cq+9 of this k-step
         const int ta = 16 * ks + 2 * cq;
-        const uint32_t wa = vc[(ta + 0) * (C::ROWB / 4) + wt * 8 + gq];
-        const uint32_t wb = vc[(ta + 1) * (C::ROWB / 4) + wt * 8 + gq];
-        const uint32_t wc = vc[(ta + 8) * (C::ROWB / 4) + wt * 8 + gq];
-        const uint32_t wd = vc[(ta + 9) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wa = vc[(tb + ta + 0) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wb = vc[(tb + ta + 1) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wc = vc[(tb + ta + 8) * (C::ROWB / 4) + wt * 8 + gq];
+        const uint32_t wd = vc[(tb + ta + 9) * (C::ROWB / 4) + wt * 8 + gq];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t rx[8], ry[8];
@@ -563,10 +573,10 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
       const uint32_t vb_s = smem_u32(st + kBfTok * C::BF_STRIDE);
       const int mi = lane >> 3;
       const int tok = (lane & 7) + 8 * (mi >> 1);
-      const bool partial = bk.count < kBfTok;
+      const bool partial = cnt < kBfTok;
       // tokens held by this lane's A fragment halves
-      const bool va = 2 * cq < bk.count, vb = 2 * cq + 1 < bk.count;
-      const bool vc8 = 2 * cq + 8 < bk.count, vd = 2 * cq + 9 < bk.count;
+      const bool va = 2 * cq < cnt, vb = 2 * cq + 1 < cnt;
+      const bool vc8 = 2 * cq + 8 < cnt, vd = 2 * cq + 9 < cnt;
       const uint32_t mask01 = (va ? 0xffffu : 0u) | (vb ? 0xffff0000u : 0u);
       const uint32_t mask89 = (vc8 ? 0xffffu : 0u) | (vd ? 0xffff0000u : 0u);
 #pragma unroll
@@ -581,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
         for (int nq = 0; nq < NQT; ++nq) mma_bf16(o[mtd][nq], a0, a1, a2, a3, bw0[nq], bw1[nq]);
       }
     }
+    }  // sub-blocks
 
     // every warp of the team is done with this stage: refill it
     if constexpr (C::TS > 1) {
@@ -659,22 +670,37 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
   asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
   if (!is_last) return;
   __threadfence();
+  // D = 128: prefetch R_V (64 KB) into the now idle stage area with one bulk copy
+  constexpr bool kRvSmem = D == 128 && !(C::NST * C::STAGE < D * D * 4);
+  const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
+  const uint32_t rv_bar = smem_u32(&bars[C::NST]);
+  if constexpr (kRvSmem) {
+    if (threadIdx.x == 0 && !a.absorb_v) {
+      mbar_arrive_expect_tx(rv_bar, D * D * 4);
+      bulk_g2s(smem_u32(smem + C::OFF_STAGE), a.R_V, D * D * 4, rv_bar);
+    }
+  }
   float* ob = part;                    // [G][D] merged o' (rotated basis)
   float* Ms = part + C::HEADS * D;     // [G] max, [G] sum
   float* Ls = Ms + C::HEADS;
+  float* wts = Ls + C::HEADS;          // [G][splits] normalised split weights
   for (int i = warp; i < Gh; i += kNCW) {
     const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
-    float M = -INFINITY;
-    for (int sp = lane; sp < a.ns; sp += 32) M = fmaxf(M, __ldcg(a.ws_ml + (base + sp) * 2));
+    const float m0 = lane < a.ns ? __ldcg(a.ws_ml + (base + lane) * 2) : -INFINITY;
+    const float l0 = lane < a.ns ? __ldcg(a.ws_ml + (base + lane) * 2 + 1) : 0.f;
+    const float m1 = lane + 32 < a.ns ? __ldcg(a.ws_ml + (base + lane + 32) * 2) : -INFINITY;
+    const float l1 = lane + 32 < a.ns ? __ldcg(a.ws_ml + (base + lane + 32) * 2 + 1) : 0.f;
+    float M = fmaxf(m0, m1);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-    float L = 0.f;
-    for (int sp = lane; sp < a.ns; sp += 32) {
-      const float m = __ldcg(a.ws_ml + (base + sp) * 2);
-      L += m == -INFINITY ? 0.f : ex2(m - M) * __ldcg(a.ws_ml + (base + sp) * 2 + 1);
-    }
+    const float e0 = M == -INFINITY || m0 == -INFINITY ? 0.f : ex2(m0 - M);
+    const float e1 = M == -INFINITY || m1 == -INFINITY ? 0.f : ex2(m1 - M);
+    float L = e0 * l0 + e1 * l1;
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    if (lane < a.ns) wts[i * OSCAR_KV_MAX_SPLITS + lane] = e0 * inv;
+    if (lane + 32 < a.ns) wts[i * OSCAR_KV_MAX_SPLITS + lane + 32] = e1 * inv;
     if (lane == 0) {
       Ms[i] = M;
       Ls[i] = L;
@@ -684,20 +710,18 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
   for (int idx = threadIdx.x; idx < Gh * D; idx += 32 * kNCW) {
     const int i = idx / D, d = idx % D;
     const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
-    const float M = Ms[i], L = Ls[i];
+    const float* wi = wts + i * OSCAR_KV_MAX_SPLITS;
     float acc = 0.f;
-    if (M != -INFINITY && L > 0.f) {
-#pragma unroll 4
-      for (int sp = 0; sp < a.ns; ++sp) {
-        const float m = __ldcg(a.ws_ml + (base + sp) * 2);
-        const float v = __ldcg(a.ws_acc + (base + sp) * D + d);
-        acc += m == -INFINITY ? 0.f : ex2(m - M) * v;
-      }
-      acc /= L;
-    }
+#pragma unroll 8
+    for (int sp = 0; sp < a.ns; ++sp) acc = fmaf(wi[sp], __ldcg(a.ws_acc + (base + sp) * D + d), acc);
     ob[idx] = acc;
   }
   asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+  bool rv_ok = true;
+  if constexpr (kRvSmem) {
+    if (!a.absorb_v) rv_ok = mbar_wait(rv_bar, 0);
+    if (!rv_ok && threadIdx.x == 0) status_or(a.status, OSCAR_DEV_TIMEOUT);
+  }
   // o = o' R_V^T: o[r] = sum_j R_V[r][j] o'[j]; one thread per output channel r
   for (int r = threadIdx.x; r < D; r += 32 * kNCW) {
     float res[8];
@@ -707,6 +731,16 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         if (i < Gh) res[i] = ob[i * D + r];
+    } else if (kRvSmem && rv_ok) {
+      // skewed walk over j: thread r touches bank (r + jj) % 32, no conflicts
+#pragma unroll 4
+      for (int jj = 0; jj < D; ++jj) {
+        const int j = (jj + r) & (D - 1);
+        const float rv = rvs[r * D + j];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < Gh) res[i] = fmaf(rv, ob[i * D + j], res[i]);
+      }
     } else {
       const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);
 #pragma unroll 8
