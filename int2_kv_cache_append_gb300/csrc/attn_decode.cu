@@ -30,6 +30,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "internal.h"
 
@@ -48,10 +49,11 @@ struct DecCfg {
   static constexpr int TS = Dg;              // warps per team (one quant group each)
   static constexpr int NTEAMS = kNCW / TS;
   static constexpr int ROWB = D / 4;         // code bytes per token
-  static constexpr int BF_STRIDE = 2 * D + 16;
+  static constexpr int BOXES = D / 64;       // 16-row x 64-column TMA boxes per BF16 matrix
+  static constexpr int BOX_BYTES = kBfTok * 128;
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
-  static constexpr int BF_BYTES = 2 * kBfTok * BF_STRIDE;
-  static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 127) / 128 * 128;
+  static constexpr int BF_BYTES = 2 * BOXES * BOX_BYTES;
+  static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 1023) / 1024 * 1024;
   // Each team owns NSTW private stages: it issues the bulk copies of its own
   // blocks into them and consumes them in order, so a stage's barrier phases
   // are produced and awaited by one team only.
@@ -73,12 +75,13 @@ struct DecCfg {
   static constexpr int PART_B = HEADS * (D + 2 + OSCAR_KV_MAX_SPLITS);
   static constexpr int PART_BYTES = (PART_A > PART_B ? PART_A : PART_B) * 4;
   static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
-  static constexpr int SMEM = OFF_BAR + (NST + 1) * 8 + 16;
+  static constexpr int SMEM = OFF_BAR + (NST + 1) * 8 + 16 + 1024;  // + slack to align the base to 1 KB
 };
 
 // Per-(b, kv head) region sizes and the block list
 struct Regions {
   int T, n_sink, tq, n_int, n_ring;
+  int ra, rlen1, nrb1;  // ring: first slot, positions before the slot wrap, their blocks
   int nsb, nib, nrb;
   int64_t cbf, ci2;
 };
@@ -96,7 +99,12 @@ __device__ __forceinline__ Regions make_regions(int T, int S, int W, int D) {
   }
   r.nsb = (r.n_sink + kBfTok - 1) / kBfTok;
   r.nib = (r.n_int + kI2Tok - 1) / kI2Tok;
-  r.nrb = (r.n_ring + kBfTok - 1) / kBfTok;
+  // ring positions [tq, T) sit in slots p mod W: cut them where the slots wrap
+  // so that every block reads consecutive slots
+  r.ra = r.n_ring > 0 ? r.tq % W : 0;
+  r.rlen1 = r.n_ring > 0 ? min(r.n_ring, W - r.ra) : 0;
+  r.nrb1 = (r.rlen1 + kBfTok - 1) / kBfTok;
+  r.nrb = r.nrb1 + (r.n_ring - r.rlen1 + kBfTok - 1) / kBfTok;
   r.cbf = int64_t(2) * kBfTok * 2 * D;
   r.ci2 = int64_t(2) * kI2Tok * (D / 4 + 4 * (D / kGroup));
   return r;
@@ -114,7 +122,7 @@ __device__ __forceinline__ int first_block_at(const Regions& r, int64_t x) {
 
 struct Blk {
   int type;   // 0 sink, 1 int2, 2 ring
-  int first;  // sink/ring: first position; int2: first row (position - S)
+  int first;  // sink: first position; int2: first row (position - S); ring: first slot
   int count;
 };
 
@@ -125,7 +133,15 @@ __device__ __forceinline__ Blk block_at(const Regions& r, int k) {
   } else if (k < r.nsb + r.nib) {
     b.type = 1; b.first = (k - r.nsb) * kI2Tok; b.count = min(kI2Tok, r.n_int - b.first);
   } else {
-    b.type = 2; b.first = r.tq + (k - r.nsb - r.nib) * kBfTok; b.count = min(kBfTok, r.T - b.first);
+    const int kr = k - r.nsb - r.nib;
+    b.type = 2;
+    if (kr < r.nrb1) {
+      b.first = r.ra + kr * kBfTok;
+      b.count = min(kBfTok, r.rlen1 - kr * kBfTok);
+    } else {
+      b.first = (kr - r.nrb1) * kBfTok;
+      b.count = min(kBfTok, r.n_ring - r.rlen1 - b.first);
+    }
   }
   return b;
 }
@@ -205,9 +221,14 @@ __global__ void __launch_bounds__(D) qrot_kernel(const DecodeArgs a) {
 // split kernel
 // ---------------------------------------------------------------------------
 template <int D, int NQT>
-__global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
+    split_kernel(const __grid_constant__ CUtensorMap tks, const __grid_constant__ CUtensorMap tvs,
+                 const __grid_constant__ CUtensorMap tkr, const __grid_constant__ CUtensorMap tvr,
+                 const DecodeArgs a) {
   using C = DecCfg<D, NQT>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte-swizzled TMA destinations need 1 KB alignment
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   __shared__ int abort_flag;
 
@@ -253,15 +274,17 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
         bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb, full);
       }
     } else {
-      if (lane == 0) mbar_arrive_expect_tx(full, 2 * bk.count * 2 * D);
-      __syncwarp();
-      const int r = lane & 15;
-      if (r < bk.count) {
-        const int pos = bk.first + r;
-        const uint8_t* base = lane < 16 ? kbase : vbase;
-        const uint8_t* src = bk.type == 0 ? base + (bh * g.S + pos) * (2 * D)
-                                          : base + g.sink_bytes + (bh * g.W + pos % g.W) * (2 * D);
-        bulk_g2s(dst + (lane < 16 ? 0 : kBfTok * C::BF_STRIDE) + r * C::BF_STRIDE, src, 2 * D, full);
+      // 16 rows of K and V as 64-column boxes, 128-byte swizzled by the TMA unit
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, 2 * C::BOXES * C::BOX_BYTES);
+        const CUtensorMap* mk = bk.type == 0 ? &tks : &tkr;
+        const CUtensorMap* mv = bk.type == 0 ? &tvs : &tvr;
+        const int row0 = int(bk.type == 0 ? bh * g.S + bk.first : bh * g.W + bk.first);
+#pragma unroll
+        for (int q = 0; q < C::BOXES; ++q) {
+          tma_load_2d(dst + q * C::BOX_BYTES, mk, 64 * q, row0, full);
+          tma_load_2d(dst + (C::BOXES + q) * C::BOX_BYTES, mv, 64 * q, row0, full);
+        }
       }
     }
   };
@@ -429,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
       for (int kk = 0; kk < 8; ++kk) {
         const int dim = wt * kGroup + 16 * kk + 8 * (mi >> 1);
         uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(kb_s + tok * C::BF_STRIDE + dim * 2, a0, a1, a2, a3);
+        ldmatrix_x4(kb_s + (dim >> 6) * C::BOX_BYTES + tok * 128 + ((((dim & 63) >> 3) ^ (tok & 7)) << 4), a0, a1,
+                    a2, a3);
 #pragma unroll
         for (int nb = 0; nb < C::NQB; ++nb) {
           const uint32_t b0 = qbf[(kk * C::NQB + nb) * 64 + lane];
@@ -570,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
         bw0[nq] = movmatrix_trans(split_bf16(p[0][nq][0]));
         bw1[nq] = movmatrix_trans(split_bf16(p[0][nq][1]));
       }
-      const uint32_t vb_s = smem_u32(st + kBfTok * C::BF_STRIDE);
+      const uint32_t vb_s = smem_u32(st + C::BOXES * C::BOX_BYTES);
       const int mi = lane >> 3;
       const int tok = (lane & 7) + 8 * (mi >> 1);
       const bool partial = cnt < kBfTok;
@@ -583,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
       for (int mtd = 0; mtd < 8; ++mtd) {
         const int dim = wt * kGroup + 16 * mtd + 8 * (mi & 1);
         uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(vb_s + tok * C::BF_STRIDE + dim * 2, a0, a1, a2, a3);
+        ldmatrix_x4_trans(vb_s + (dim >> 6) * C::BOX_BYTES + tok * 128 + ((((dim & 63) >> 3) ^ (tok & 7)) << 4),
+                          a0, a1, a2, a3);
         if (partial) {
           a0 &= mask01; a1 &= mask01; a2 &= mask89; a3 &= mask89;
         }
@@ -783,9 +808,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1)) split_kernel(con
 // ---------------------------------------------------------------------------
 // host launch
 // ---------------------------------------------------------------------------
-template <typename K>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       const DecodeArgs& a) {
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -796,7 +820,7 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 struct DevInfo {
@@ -842,8 +866,20 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   if (launch_pdl(qrot_kernel<D>, dim3(g.B * g.Hkv), dim3(D), 0, stream, a) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
   if (prof && cudaEventRecord(g_prof_start, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
-  if (launch_pdl(split_kernel<D, NQT>, dim3(a.ns, g.Hkv, g.B), dim3(kThreads), C::SMEM, stream, a) !=
-      cudaSuccess)
+  // TMA maps of this layer's BF16 windows: [B*Hkv*S][D] sink and [B*Hkv*W][D] ring, per role
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof(maps));
+  const uint8_t* kb = a.layer_base;
+  const uint8_t* vb = a.layer_base + g.role_bytes;
+  const uint64_t bh = uint64_t(g.B) * g.Hkv;
+  if (g.S > 0 && (!encode_rows_bf16(&maps[0], kb, bh * g.S, D, 64, kBfTok) ||
+                  !encode_rows_bf16(&maps[1], vb, bh * g.S, D, 64, kBfTok)))
+    return OSCAR_ERR_LAUNCH;
+  if (g.W > 0 && (!encode_rows_bf16(&maps[2], kb + g.sink_bytes, bh * g.W, D, 64, kBfTok) ||
+                  !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)))
+    return OSCAR_ERR_LAUNCH;
+  if (launch_pdl(split_kernel<D, NQT>, dim3(a.ns, g.Hkv, g.B), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
+                 maps[2], maps[3], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   return OSCAR_OK;
@@ -866,21 +902,12 @@ int decode_auto_splits(const Geom& g, int seq_len_hint) {
   const int occ = di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
   const int slots = di.sms * occ;
   const int units = g.B * g.Hkv;
-  // at least ~4 INT2 blocks of work per split
-  const int max_by_len = std::max(1, seq_len_hint / (4 * kI2Tok));
-  int best = 1;
-  double best_eff = -1.0;
-  for (int waves = 1; waves <= 8; ++waves) {
-    int ns = std::max(1, (waves * slots) / units);
-    ns = std::min(ns, std::min(max_by_len, int(OSCAR_KV_MAX_SPLITS)));
-    const int64_t ctas = int64_t(ns) * units;
-    const int64_t wv = (ctas + slots - 1) / slots;
-    const double eff = double(ctas) / double(wv * slots);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = ns;
-    }
-  }
+  // at least ~2 INT2 blocks of work per split
+  const int max_by_len = std::max(1, seq_len_hint / (2 * kI2Tok));
+  // about two CTAs per slot: enough CTAs to balance the tail, few enough that
+  // the per-CTA start-up and the final merge stay small
+  int best = int((2 * slots + units / 2) / units);
+  best = std::max(1, std::min(best, std::min(max_by_len, int(OSCAR_KV_MAX_SPLITS))));
   return best;
 }
 

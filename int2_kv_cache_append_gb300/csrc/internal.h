@@ -2,6 +2,7 @@
 // kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -50,6 +51,9 @@ uint64_t decode_workspace_bytes(const Geom& g, int ns);
 extern thread_local cudaEvent_t g_prof_start, g_prof_stop;
 int launch_append(const AppendArgs& a, cudaStream_t stream);
 int launch_append_tc(const AppendArgs& a, cudaStream_t stream);  // D = 128, bf16 inputs
+// 2-D tiled TMA map of a row-major bf16 matrix [rows][cols], 128-byte swizzle
+bool encode_rows_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_cols,
+                      uint32_t box_rows);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 int decode_auto_splits(const Geom& g, int seq_len_hint);
 
