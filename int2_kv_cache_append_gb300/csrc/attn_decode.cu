@@ -65,7 +65,7 @@ struct DecCfg {
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_QBF = OFF_STAGE + NST * STAGE;           // bf16 q fragments per warp
   static constexpr int NQB = 2 * NQT;       // bf16 n-tiles: (hi, mid) and (lo, -) per 4 heads
-  static constexpr int QBF_BYTES = kNCW * 8 * NQB * 32 * 8;
+  static constexpr int QBF_BYTES = TS * 8 * NQB * 32 * 8;  // one copy per channel group, shared by teams
   static constexpr int OFF_XCH = OFF_QBF + QBF_BYTES;               // team score exchange
   static constexpr int XCH_BYTES = TS > 1 ? NTEAMS * 2 * TS * kSub * HEADS * 4 : 0;
   static constexpr int OFF_PART = OFF_XCH + XCH_BYTES;              // team partials
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
   float qsum[NQT];
   // bf16 B fragments for BF16 blocks: n-tile 2nq holds (hi, mid) and n-tile
   // 2nq+1 holds (lo, 0) of each head's three-way bf16 split (~24 bits)
-  uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + warp * 8 * C::NQB * 64;
+  uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + wt * 8 * C::NQB * 64;
   {
     const int hs_b = gq >> 1, lohalf = gq & 1;
 #pragma unroll
@@ -328,13 +328,15 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
           // pick hi (low half) or lo (high half) of each split
           const uint32_t v16 = lohalf ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
           qf[kk][nq][half] = v16;
-          uint32_t p0[3], p1[3];
-          split3_bf16(x0, p0);
-          split3_bf16(x1, p1);
-          const uint32_t va = lohalf ? (p0[1] | (p1[1] << 16)) : (p0[0] | (p1[0] << 16));
-          const uint32_t vb = lohalf ? 0u : (p0[2] | (p1[2] << 16));
-          qbf[(kk * C::NQB + 2 * nq) * 64 + half * 32 + lane] = va;
-          qbf[(kk * C::NQB + 2 * nq + 1) * 64 + half * 32 + lane] = vb;
+          if (team == 0) {  // the other teams hold the same fragments
+            uint32_t p0[3], p1[3];
+            split3_bf16(x0, p0);
+            split3_bf16(x1, p1);
+            const uint32_t va = lohalf ? (p0[1] | (p1[1] << 16)) : (p0[0] | (p1[0] << 16));
+            const uint32_t vb = lohalf ? 0u : (p0[2] | (p1[2] << 16));
+            qbf[(kk * C::NQB + 2 * nq) * 64 + half * 32 + lane] = va;
+            qbf[(kk * C::NQB + 2 * nq + 1) * 64 + half * 32 + lane] = vb;
+          }
         }
       }
       const int hc = 4 * nq + cq;  // head owned by this lane in C fragments
@@ -342,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
     }
   }
   __syncwarp();
+
+  asm volatile("bar.sync 14, %0;" ::"r"(32 * kNCW) : "memory");  // shared bf16 fragments written
 
   float o[8][NQT][4];
   float m_run[NQT], l_run[NQT], zeta[NQT];
@@ -904,10 +908,21 @@ int decode_auto_splits(const Geom& g, int seq_len_hint) {
   const int units = g.B * g.Hkv;
   // at least ~2 INT2 blocks of work per split
   const int max_by_len = std::max(1, seq_len_hint / (2 * kI2Tok));
-  // about two CTAs per slot: enough CTAs to balance the tail, few enough that
-  // the per-CTA start-up and the final merge stay small
-  int best = int((2 * slots + units / 2) / units);
-  best = std::max(1, std::min(best, std::min(max_by_len, int(OSCAR_KV_MAX_SPLITS))));
+  // best wave efficiency with at most two waves; a second wave must pay for its
+  // extra start-up and merge work with a clearly better fill
+  int best = 1;
+  double best_eff = -1.0;
+  const int cap = std::min(max_by_len, int(OSCAR_KV_MAX_SPLITS));
+  for (int ns = 1; ns <= cap; ++ns) {
+    const int64_t ctas = int64_t(ns) * units;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    if (waves > 2) break;
+    const double eff = double(ctas) / double(waves * slots) - (waves > 1 ? 0.05 : 0.0);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = ns;
+    }
+  }
   return best;
 }
 
