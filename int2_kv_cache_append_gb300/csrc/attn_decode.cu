@@ -165,56 +165,84 @@ __device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b) {
 }
 
 // ---------------------------------------------------------------------------
-// qrot: q' = q R_K * qscale and per-group sums, for the G query heads of one
-// (b, kv head); also zeroes that unit's merge ticket.  Launched with PDL: it
-// waits for the preceding kernel before reading anything (q may be produced
-// right before this call) and lets the split kernel launch when it is done.
+// qrot: q' = q R_K * qscale and per-group sums for the G query heads of one
+// (b, kv head) and one 128-column chunk of q'; the chunk-0 CTA also zeroes
+// that unit's merge ticket.  512 threads = 4 slices of the contraction index
+// x 128 output columns, so each thread has at most D/4 loads of R_K, issued
+// 32 at a time.  Launched with PDL: it waits for the preceding kernel before
+// reading anything (q may be produced right before this call) and then at
+// once lets the split kernel launch, whose CTAs start their cache copies
+// while this kernel computes; the split kernel reads q' only after its own
+// wait for this grid's completion.
 // ---------------------------------------------------------------------------
+constexpr int kQrotThreads = 512;
+
 template <int D>
-__global__ void __launch_bounds__(D) qrot_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) {
+  constexpr int KP = kQrotThreads / 128;  // slices of the contraction index
+  constexpr int KC = D / KP;              // contraction indices per slice
   __shared__ float qs[8][D];
-  __shared__ float red[8][D / 32];
+  __shared__ float part[KP - 1][8][128];
+  __shared__ float red[8][4];
   const int bh = blockIdx.x;  // b * Hkv + h
+  const int chunk = blockIdx.y;
   const int G = a.g.G;
-  const int d = threadIdx.x;
+  const int c = threadIdx.x & 127, kp = threadIdx.x >> 7;
+  const int col = chunk * 128 + c;
   const int64_t q0 = int64_t(bh) * G * D;  // first query head of this kv head
   pdl_wait();
-  for (int i = 0; i < G; ++i)
-    qs[i][d] = a.in_fp32 ? static_cast<const float*>(a.q)[q0 + i * D + d]
-                         : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[q0 + i * D + d]);
+  pdl_trigger();
+
+  int k0 = kp * KC;
+  float rr[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) rr[j] = __ldg(a.R_K + (k0 + j) * D + col);
+  for (int idx = threadIdx.x; idx < G * D; idx += kQrotThreads)
+    qs[idx / D][idx % D] = a.in_fp32 ? static_cast<const float*>(a.q)[q0 + idx]
+                                     : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[q0 + idx]);
   __syncthreads();
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll 16
-  for (int k = 0; k < D; ++k) {
-    const float r = __ldg(a.R_K + k * D + d);
+  for (;;) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < G) acc[i] = fmaf(qs[i][k0 + j], rr[j], acc[i]);
+    k0 += 32;
+    if (k0 >= (kp + 1) * KC) break;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) rr[j] = __ldg(a.R_K + (k0 + j) * D + col);
+  }
+  if (kp > 0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (i < G) acc[i] = fmaf(qs[i][k], r, acc[i]);
+      if (i < G) part[kp - 1][i][c] = acc[i];
   }
+  if (chunk == 0 && threadIdx.x == 0) a.ticket[bh] = 0;
+  __syncthreads();
+  if (kp == 0) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < G) {
-      const float v = acc[i] * a.qscale;
-      if (!(fabsf(v) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
-      a.qprime[q0 + i * D + d] = v;
-      float t = v;
+    for (int i = 0; i < 8; ++i) {
+      if (i < G) {
+        float sum = acc[i];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if ((d & 31) == 0) red[i][d >> 5] = t;
+        for (int p = 0; p < KP - 1; ++p) sum += part[p][i][c];
+        const float v = sum * a.qscale;
+        if (!(fabsf(v) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
+        a.qprime[q0 + i * D + col] = v;
+        float t = v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if ((c & 31) == 0) red[i][c >> 5] = t;
+      }
     }
   }
-  if (d == 0) a.ticket[bh] = 0;
   __syncthreads();
-  for (int idx = d; idx < G * (D / kGroup); idx += D) {
-    const int i = idx / (D / kGroup), j = idx % (D / kGroup);
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) t += red[i][j * 4 + w];
-    a.qsum[(q0 / D + i) * (D / kGroup) + j] = t;
-  }
-  pdl_trigger();
+  if (threadIdx.x < G)
+    a.qsum[(q0 / D + threadIdx.x) * (D / kGroup) + chunk] =
+        red[threadIdx.x][0] + red[threadIdx.x][1] + red[threadIdx.x][2] + red[threadIdx.x][3];
 }
 
 // ---------------------------------------------------------------------------
@@ -867,7 +895,7 @@ template <int D, int NQT>
 int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = DecCfg<D, NQT>;
   const Geom& g = a.g;
-  if (launch_pdl(qrot_kernel<D>, dim3(g.B * g.Hkv), dim3(D), 0, stream, a) != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  if (launch_pdl(qrot_kernel<D>, dim3(g.B * g.Hkv, D / 128), dim3(kQrotThreads), 0, stream, a) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   const bool prof = g_prof_start != nullptr && g_prof_stop != nullptr;
   if (prof && cudaEventRecord(g_prof_start, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   // TMA maps of this layer's BF16 windows: [B*Hkv*S][D] sink and [B*Hkv*W][D] ring, per role

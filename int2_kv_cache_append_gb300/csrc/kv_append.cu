@@ -7,12 +7,22 @@
 // high-precision sink/recent tokens) and "OSCAR-RotationZoo" (Available
 // rotations: group 128 along head_dim; How to use: K/V clip 0.96/0.92).
 //
-// One CTA of 128 threads handles RPC = 128*128/D rows of one role (K or V):
+// Two CUDA-core kernels (the tensor-core kernel for large head_dim-128 bf16
+// appends is in kv_append_tc.cu):
+//
+// kv_append_kernel, tiled: one CTA of 128 threads handles RPC = 128*128/D rows
+// of one role (K or V):
 //   1. stage the input rows in shared memory as float32;
 //   2. rotate: each row's D outputs are split over 128/RPC threads, each
 //      accumulating 32 columns at a time with fp32 FMAs (R is read through the
 //      L1 as warp-wide broadcasts);
 //   3. quantise: one thread per row, the row held in padded shared memory.
+//
+// kv_append_rows_kernel, row-parallel, for appends of a few rows (a decode
+// step appends one token per sequence): 4 or 8 rows per CTA, described below.
+//
+// Both accumulate each rotated value with fp32 FMAs in increasing input-channel
+// order and run the same codec operations, so they write identical bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -22,6 +32,8 @@ namespace oscar {
 namespace {
 
 constexpr int kAppendThreads = 128;
+// appends of at most this many rows per role take the row-parallel kernel
+constexpr int64_t kSmallAppendRows = 1024;
 
 template <int D>
 struct AppendCfg {
@@ -201,6 +213,266 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendA
   }
 }
 
+// ---------------------------------------------------------------------------
+// Row-parallel variant for small appends (decode: one or a few new tokens per
+// sequence).  The tiled kernels above amortise loading R over many rows and pay
+// a long serial prologue; with a few dozen rows that prologue is the whole cost.
+// Here each CTA takes only RPC rows of one role, so many CTAs share the work:
+//   1. thread 0 streams R into shared memory in 64 KB chunks (cp.async.bulk,
+//      two stages when R is larger than one chunk) while all threads stage the
+//      RPC input rows transposed ([D][RPC], so one channel of all rows is one
+//      broadcast load);
+//   2. thread t accumulates output columns t, t + 128, ... of all RPC rows with
+//      fp32 FMAs in increasing input-channel order (the same sums, in the same
+//      order, as the tiled CUDA-core kernel, so results are bit-identical);
+//   3. each warp quantises whole rows: lanes hold channels lane + 32e, row and
+//      group extrema come from warp reductions (max/min are exact in any
+//      order), and every 2-bit word is built by 32 / (8 * D/128) lanes that
+//      OR their slots together.
+// Waits on the copies are bounded; on a timeout the CTA flags
+// OSCAR_DEV_TIMEOUT, waits (bounded) for its copies in flight and returns.
+// ---------------------------------------------------------------------------
+template <int D, int RPC>
+struct RowsCfg {
+  static constexpr int CH_ROWS = (65536 / (D * 4)) < D ? 65536 / (D * 4) : D;  // rows of R per chunk
+  static constexpr int NCH = D / CH_ROWS;
+  static constexpr int NSTG = NCH > 1 ? 2 : 1;
+  static constexpr uint32_t CH_BYTES = uint32_t(CH_ROWS) * D * 4;
+  static constexpr int CPT = D / 128;  // output columns per thread
+  static constexpr uint32_t OFF_X = NSTG * CH_BYTES;
+  static constexpr uint32_t OFF_Y = OFF_X + uint32_t(D) * RPC * 4;
+  static constexpr uint32_t OFF_BAR = OFF_Y + uint32_t(RPC) * D * 4;
+  static constexpr uint32_t SMEM = OFF_BAR + 8 * NSTG;
+  static constexpr int NW = 8 * (D / kGroup);  // 32-bit code words per row
+  static constexpr int LPW = 32 / NW;          // lanes per word
+  static constexpr int SPL = 16 / LPW;         // 2-bit slots per lane
+  static_assert(RPC % 4 == 0, "rows per CTA must be a multiple of the warp count");
+};
+
+template <int D, int RPC>
+__global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const AppendArgs a) {
+  using C = RowsCfg<D, RPC>;
+  extern __shared__ __align__(128) unsigned char sm[];
+  float* Rs = reinterpret_cast<float*>(sm);
+  float* xs = reinterpret_cast<float*>(sm + C::OFF_X);  // [D][RPC]
+  float* ys = reinterpret_cast<float*>(sm + C::OFF_Y);  // [RPC][D]
+  const uint32_t bar0 = smem_u32(sm + C::OFF_BAR);
+
+  pdl_trigger();
+  const int role = blockIdx.y;
+  const float* __restrict__ R = role ? a.R_V : a.R_K;
+  const int64_t row0 = int64_t(blockIdx.x) * RPC;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NSTG; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_fence_init();
+    for (int s = 0; s < C::NSTG; ++s) {
+      mbar_arrive_expect_tx(bar0 + 8 * s, C::CH_BYTES);
+      bulk_g2s(smem_u32(Rs) + s * C::CH_BYTES, R + size_t(s) * C::CH_ROWS * D, C::CH_BYTES, bar0 + 8 * s);
+    }
+  }
+  // stage inputs transposed; rows past the end are zero
+  for (int idx = tid; idx < RPC * D; idx += kAppendThreads) {
+    const int r = idx / D, i = idx % D;
+    const int64_t row = row0 + r;
+    float v = 0.f;
+    if (row < a.rows)
+      v = a.in_fp32 ? static_cast<const float*>(role ? a.v_new : a.k_new)[row * D + i]
+                    : __bfloat162float(static_cast<const __nv_bfloat16*>(role ? a.v_new : a.k_new)[row * D + i]);
+    xs[i * RPC + r] = v;
+  }
+  __syncthreads();
+
+  float acc[RPC][C::CPT];
+#pragma unroll
+  for (int r = 0; r < RPC; ++r)
+#pragma unroll
+    for (int m = 0; m < C::CPT; ++m) acc[r][m] = 0.f;
+
+  bool abort = false;
+  int ch = 0;
+  for (; ch < C::NCH; ++ch) {
+    const int s = ch % C::NSTG;
+    const bool ok = mbar_wait(bar0 + 8 * s, (ch / C::NSTG) & 1);
+    if (__syncthreads_or(!ok)) {
+      abort = true;
+      break;
+    }
+    const float* Rc = Rs + size_t(s) * C::CH_ROWS * D;
+#pragma unroll 4
+    for (int kk = 0; kk < C::CH_ROWS; ++kk) {
+      const int k = ch * C::CH_ROWS + kk;
+      float xv[RPC];
+#pragma unroll
+      for (int r4 = 0; r4 < RPC / 4; ++r4) {
+        const float4 x4 = *reinterpret_cast<const float4*>(xs + k * RPC + 4 * r4);
+        xv[4 * r4 + 0] = x4.x;
+        xv[4 * r4 + 1] = x4.y;
+        xv[4 * r4 + 2] = x4.z;
+        xv[4 * r4 + 3] = x4.w;
+      }
+#pragma unroll
+      for (int m = 0; m < C::CPT; ++m) {
+        const float rv = Rc[kk * D + tid + 128 * m];
+#pragma unroll
+        for (int r = 0; r < RPC; ++r) acc[r][m] = fmaf(xv[r], rv, acc[r][m]);
+      }
+    }
+    __syncthreads();  // every thread is done with stage s
+    if (tid == 0 && ch + C::NSTG < C::NCH) {
+      mbar_arrive_expect_tx(bar0 + 8 * s, C::CH_BYTES);
+      bulk_g2s(smem_u32(Rs) + s * C::CH_BYTES, R + size_t(ch + C::NSTG) * C::CH_ROWS * D, C::CH_BYTES,
+               bar0 + 8 * s);
+    }
+  }
+  if (abort) {
+    if (tid == 0) {
+      status_or(a.status, OSCAR_DEV_TIMEOUT);
+      // chunks issued but not consumed: ch .. min(ch + NSTG, NCH) - 1
+      for (int c2 = ch; c2 < C::NCH && c2 < ch + C::NSTG; ++c2)
+        (void)mbar_wait(bar0 + 8 * (c2 % C::NSTG), (c2 / C::NSTG) & 1);
+    }
+    return;
+  }
+#pragma unroll
+  for (int r = 0; r < RPC; ++r)
+#pragma unroll
+    for (int m = 0; m < C::CPT; ++m) ys[r * D + tid + 128 * m] = acc[r][m];
+  __syncthreads();
+
+  const int warp = tid >> 5, lane = tid & 31;
+  const float ratio = role ? a.v_clip : a.k_clip;
+  const Geom& g = a.g;
+  uint8_t* role_base = a.layer_base + role * g.role_bytes;
+  for (int r = warp; r < RPC; r += kAppendThreads / 32) {
+    const int64_t row = row0 + r;
+    if (row >= a.rows) break;
+    const float* y = ys + r * D;
+    if (a.debug_rot) {
+      float* dst = a.debug_rot + (row * 2 + role) * D;
+      for (int d = lane; d < D; d += 32) dst[d] = y[d];
+    }
+    const int h = int(row % g.Hkv);
+    const int64_t bt = row / g.Hkv;
+    const int t = int(bt % a.n_new);
+    const int b = int(bt / a.n_new);
+    const int p = a.start_pos[b] + t;
+    const int newlen = a.start_pos[b] + a.n_new;
+    if (p < 0 || p >= g.cap) {
+      if (lane == 0) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
+      continue;
+    }
+    const int64_t bh = int64_t(b) * g.Hkv + h;
+
+    float v[D / 32];
+    float amax = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      v[e] = y[lane + 32 * e];
+      finite &= isfinite(v[e]);
+      amax = fmaxf(amax, fabsf(v[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    finite = __all_sync(0xffffffffu, finite);
+    if (!finite && lane == 0) status_or(a.status, OSCAR_DEV_NONFINITE);
+    const float tclip = __fmul_rn(ratio, amax);
+
+    const bool to_sink = p < g.S;
+    const bool to_ring = g.W > 0 && p >= newlen - g.W;
+    if (to_sink || to_ring) {
+      __nv_bfloat16* d0 = reinterpret_cast<__nv_bfloat16*>(
+          to_sink ? role_base + (bh * g.S + p) * (2 * D) : role_base + g.sink_bytes + (bh * g.W + (p % g.W)) * (2 * D));
+      __nv_bfloat16* d1 = (to_sink && to_ring)
+                              ? reinterpret_cast<__nv_bfloat16*>(role_base + g.sink_bytes + (bh * g.W + (p % g.W)) * (2 * D))
+                              : nullptr;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) {
+        const __nv_bfloat16 bv = __float2bfloat16_rn(v[e]);
+        d0[lane + 32 * e] = bv;
+        if (d1) d1[lane + 32 * e] = bv;
+      }
+    }
+    if (to_sink) continue;
+
+    // group statistics; each lane keeps those of the group its code word lies in
+    const int wi = lane / C::LPW, part = lane % C::LPW;
+    const int my_j = wi / 8, my_w = wi % 8;
+    float my_zf = 0.f, my_inv = 0.f;
+    bool my_ok = false;
+    uint32_t my_sz = 0;
+#pragma unroll
+    for (int j = 0; j < D / kGroup; ++j) {
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int e = 4 * j; e < 4 * j + 4; ++e) {
+        const float x = fminf(fmaxf(v[e], -tclip), tclip);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      const __half sh = __float2half_rn(s32);
+      const __half zh = __float2half_rn(mn);
+      const float sf = __half2float(sh), zf = __half2float(zh);
+      const bool rng_ok = isfinite(sf) && isfinite(zf);
+      if (!rng_ok && lane == 0) status_or(a.status, OSCAR_DEV_FP16_RANGE);
+      const bool ok = rng_ok && sf != 0.f;
+      if (j == my_j) {
+        my_zf = zf;
+        my_inv = ok ? __frcp_rn(sf) : 0.f;
+        my_ok = ok;
+      }
+      if (lane == j) my_sz = pack_half2(sh, zh);
+    }
+    const int64_t irow = bh * g.ncap + (p - g.S);
+    uint32_t* codes = reinterpret_cast<uint32_t*>(role_base + g.sink_bytes + g.ring_bytes + irow * (D / 4));
+    uint32_t* sz = reinterpret_cast<uint32_t*>(role_base + g.sink_bytes + g.ring_bytes + g.codes_bytes) +
+                   irow * (D / kGroup);
+    uint32_t word = 0;
+#pragma unroll
+    for (int k = 0; k < C::SPL; ++k) {
+      const int s = part * C::SPL + k;
+      const float x = fminf(fmaxf(y[my_j * kGroup + slot_channel(role, my_w, s)], -tclip), tclip);
+      int c = __float2int_rn(__fmul_rn(__fsub_rn(x, my_zf), my_inv));
+      c = my_ok ? min(max(c, 0), 3) : 0;
+      word |= uint32_t(c) << (2 * s);
+    }
+#pragma unroll
+    for (int o = 1; o < C::LPW; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
+    if (part == 0) codes[wi] = word;
+    if (lane < D / kGroup) sz[lane] = my_sz;
+  }
+}
+
+template <int D, int RPC>
+int launch_append_rows(const AppendArgs& a, cudaStream_t stream) {
+  using C = RowsCfg<D, RPC>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kv_append_rows_kernel<D, RPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return OSCAR_ERR_LAUNCH;
+    attr_set[dev] = 1;
+  }
+  const dim3 grid(unsigned((a.rows + RPC - 1) / RPC), 2, 1);
+  kv_append_rows_kernel<D, RPC><<<grid, kAppendThreads, C::SMEM, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
+}
+
+template <int D>
+int launch_append_small(const AppendArgs& a, cudaStream_t stream) {
+  return a.rows > 512 ? launch_append_rows<D, 8>(a, stream) : launch_append_rows<D, 4>(a, stream);
+}
+
 template <int D>
 int launch_append_d(const AppendArgs& a, cudaStream_t stream) {
   using C = AppendCfg<D>;
@@ -222,6 +494,14 @@ int launch_append_d(const AppendArgs& a, cudaStream_t stream) {
 
 int launch_append(const AppendArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return OSCAR_OK;
+  if (a.rows <= kSmallAppendRows) {
+    switch (a.g.D) {
+      case 128: return launch_append_small<128>(a, stream);
+      case 256: return launch_append_small<256>(a, stream);
+      case 512: return launch_append_small<512>(a, stream);
+      default: return OSCAR_ERR_UNSUPPORTED;
+    }
+  }
   if (a.g.D == 128 && !a.in_fp32) return launch_append_tc(a, stream);
   switch (a.g.D) {
     case 128: return launch_append_d<128>(a, stream);

@@ -41,6 +41,12 @@ CASES = [
     (128, 2, 8, 64, 256, 1024, [600, 1], [0, 100]),
     (256, 2, 2, 5, 9, 200, [33, 17, 2], [1, 0]),
     (512, 2, 2, 8, 16, 160, [50, 31, 1], [0, 7]),
+    # row counts per call chosen to reach every append kernel: <= 512 rows and
+    # 513..1024 rows (row-parallel kernel, 4 and 8 rows per CTA), > 1024 rows
+    # (tiled kernels: tensor cores at D = 128 with bf16 input, CUDA cores otherwise)
+    (128, 2, 4, 16, 64, 400, [100, 1, 50], [0, 2]),
+    (256, 2, 4, 8, 32, 720, [600, 100], [0, 5]),
+    (512, 1, 4, 4, 8, 460, [300, 150], [3]),
 ]
 
 
