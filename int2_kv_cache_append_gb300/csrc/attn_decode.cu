@@ -333,9 +333,14 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
 
   pdl_wait();  // q' comes from the preceding kernel
 
-  // B fragments of q' for this warp's group: column n <-> (head n/2, hi|lo by n%2)
+  // B fragments of q' for this warp's group: column n <-> (head n/2, hi|lo by n%2).
+  // INT2 codes reach the MMAs as fp16 subnormals code * 4^k * 2^-24 (see
+  // unpack16), so the q' entry meeting a code at mantissa bit 2k is stored as
+  // q' * 4^-k * 2^X, with 2^X per (head, group) chosen so that the largest
+  // |q'| * 2^X lies in [2^13, 2^14): every product is then code * q' * 2^(X-24)
+  // and the score is rescaled by qF = 2^(24-X) (exact powers of two throughout).
   uint32_t qf[8][NQT][2];
-  float qsum[NQT];
+  float qsum[NQT], qF[NQT];
   // bf16 B fragments for BF16 blocks: n-tile 2nq holds (hi, mid) and n-tile
   // 2nq+1 holds (lo, 0) of each head's three-way bf16 split (~24 bits)
   uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + wt * 8 * C::NQB * 64;
@@ -346,13 +351,30 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
       const int hb = 4 * nq + hs_b;  // head slot of this lane's B column
       const bool hv = hb < Gh;
       const float* qp = a.qprime + (int64_t(b) * g.Hq + head0 + (hv ? hb : 0)) * D + wt * kGroup;
+      float xq[8][2][2];
+      float mx = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int d0 = 16 * kk + 2 * cq + 8 * half;
+          xq[kk][half][0] = hv ? qp[d0] : 0.f;
+          xq[kk][half][1] = hv ? qp[d0 + 1] : 0.f;
+          mx = fmaxf(mx, fmaxf(fabsf(xq[kk][half][0]), fabsf(xq[kk][half][1])));
+        }
+      // the four lanes of a B column hold all 128 channels of the group
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      int ex = 0;
+      (void)frexpf(mx, &ex);  // mx < 2^ex
+      const int X = mx > 0.f ? min(14 - ex, 100) : 0;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const int d0 = 16 * kk + 2 * cq + 8 * half;
-          const float x0 = hv ? qp[d0] : 0.f, x1 = hv ? qp[d0 + 1] : 0.f;
-          const uint32_t s0 = split_f16(x0), s1 = split_f16(x1);
+          const float f = ldexpf(1.f, X - 2 * unpack_k(2 * (kk & 3) + half));
+          const float x0 = xq[kk][half][0], x1 = xq[kk][half][1];
+          const uint32_t s0 = split_f16(x0 * f), s1 = split_f16(x1 * f);
           // pick hi (low half) or lo (high half) of each split
           const uint32_t v16 = lohalf ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
           qf[kk][nq][half] = v16;
@@ -368,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
         }
       }
       const int hc = 4 * nq + cq;  // head owned by this lane in C fragments
+      // lane 8 * cq holds B column 2 * cq, i.e. head slot cq of this n-tile
+      qF[nq] = ldexpf(1.f, 24 - __shfl_sync(0xffffffffu, X, 8 * cq));
       qsum[nq] = hc < Gh ? a.qsum[(int64_t(b) * g.Hq + head0 + hc) * C::Dg + wt] : 0.f;
     }
   }
@@ -389,6 +413,26 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
   float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
   int xbuf = 0;
 
+  // INT2 P.V takes V codes from unpack16_v: the code of output row r arrives
+  // as code * 2^e(r), e(r) = unpack_v_exp(p) with p = 2 * (mtd % 4) for rows gq
+  // and 2 * (mtd % 4) + 1 for rows gq + 8.  While INT2 blocks are consumed, row
+  // r of o holds (real value) * 2^e(r); it is converted by exact powers of two
+  // at a switch between INT2 and BF16 blocks and at the end.
+  bool o_i2 = false;
+  auto scale_o = [&](int sign) {  // o *= 2^(sign * e(r)) per row
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const float f0 = ldexpf(1.f, sign * unpack_v_exp(2 * (mt & 3)));
+      const float f1 = ldexpf(1.f, sign * unpack_v_exp(2 * (mt & 3) + 1));
+#pragma unroll
+      for (int nq = 0; nq < NQT; ++nq) {
+        o[mt][nq][0] *= f0; o[mt][nq][1] *= f0;
+        o[mt][nq][2] *= f1; o[mt][nq][3] *= f1;
+      }
+    }
+  };
+
+
   for (int j = 0; j < nmine; ++j) {
     const int kl = team + j * C::NTEAMS;
     const int stage = my_stage(j);
@@ -404,6 +448,10 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
     const Blk bk = block_at(rg, kb + kl);
     const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
     const bool is_i2 = bk.type == 1;
+    if (is_i2 != o_i2) {
+      scale_o(is_i2 ? 1 : -1);
+      o_i2 = is_i2;
+    }
     constexpr int MT_MAX = kSub / 16;
     const int nmt = is_i2 ? MT_MAX : 1;
     const int nsub = is_i2 ? (bk.count + kSub - 1) / kSub : 1;
@@ -466,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
           kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
 #pragma unroll
           for (int nq = 0; nq < NQT; ++nq) {
-            s[mt][nq][0] = fmaf(ksc[mt][0], acc[i][nq][0] + acc[i][nq][1], kze[mt][0] * qsum[nq]);
-            s[mt][nq][1] = fmaf(ksc[mt][1], acc[i][nq][2] + acc[i][nq][3], kze[mt][1] * qsum[nq]);
+            s[mt][nq][0] = fmaf(ksc[mt][0], (acc[i][nq][0] + acc[i][nq][1]) * qF[nq], kze[mt][0] * qsum[nq]);
+            s[mt][nq][1] = fmaf(ksc[mt][1], (acc[i][nq][2] + acc[i][nq][3]) * qF[nq], kze[mt][1] * qsum[nq]);
           }
         }
       }
@@ -608,8 +656,8 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t rx[8], ry[8];
-          unpack16(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
-          unpack16(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+          unpack16_v(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
+          unpack16_v(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
 #pragma unroll
           for (int m4 = 0; m4 < 4; ++m4) {
             const int mtd = 4 * hh + m4;
@@ -661,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
       ++issued;
     }
   }
+  if (o_i2) scale_o(-1);
   // after an early exit, wait (bounded) for copies still landing in our stages
   if (wt == 0 && lane == 0) {
     const int consumed = *((volatile int*)&abort_flag) ? 0 : nmine;

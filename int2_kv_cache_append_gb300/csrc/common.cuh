@@ -34,48 +34,61 @@ __device__ __forceinline__ void status_or(int32_t* st, int32_t bits) {
   if (st) atomicOr(st, bits);
 }
 
-// (a & b) | c
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
 
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
+// Unpack 16 two-bit codes into 8 f16x2 registers of fp16 subnormals.
+// Register p holds the codes at bits 2p and 16 + 2p (low and high half) for
+// p < 5, and the codes at bits 10 + 2(p-5) and 26 + 2(p-5) for p >= 5, each
+// left at mantissa bit 2k(p) of an otherwise zero half, k(p) = p < 5 ? p : p - 5:
+// the half's value is exactly code * 4^k(p) * 2^-24 (an fp16 subnormal; the
+// tensor cores multiply subnormal inputs exactly).  One AND per register (and
+// one shift for the top three): the factor 4^k(p) * 2^-24 is constant per
+// register index, so callers fold it into the other operand or the accumulator.
+// Precision: the tensor cores align the products of one MMA by the operands'
+// exponent fields, and a subnormal's field says 2^-14 whatever its leading bit,
+// so a code at bit 2k keeps about 15 + 2k significant bits of the accumulation
+// window instead of ~25 (measured on GB300: ~2e-5 relative error on sums of
+// k = 0 codes, ~2e-6 from k = 1 up).  unpack16_v therefore converts the two
+// k = 0 registers exactly instead.
+__device__ __forceinline__ constexpr int unpack_k(int p) { return p < 5 ? p : p - 5; }
+
+__device__ __forceinline__ void unpack16(uint32_t w, uint32_t (&r)[8]) {
+  r[0] = w & 0x00030003u;
+  r[1] = w & 0x000C000Cu;
+  r[2] = w & 0x00300030u;
+  r[3] = w & 0x00C000C0u;
+  r[4] = w & 0x03000300u;
+  const uint32_t w2 = w >> 10;
+  r[5] = w2 & 0x00030003u;
+  r[6] = w2 & 0x000C000Cu;
+  r[7] = w2 & 0x00300030u;
 }
 
-// Unpack 16 two-bit codes into 8 f16x2 registers holding the exact integers.
-// Register p holds (code at bit 2p, code at bit 16 + 2p) as (low, high) half.
-// Each code is OR-ed into the mantissa of fp16 1024 (0x6400), which gives
-// 1024 + 4^k * code exactly for a code at mantissa bit 2k (k <= 4); one fp16x2
-// fma by 4^-k and -1024 * 4^-k then yields the code with no rounding.
-__device__ __forceinline__ void unpack16(uint32_t w, uint32_t (&r)[8]) {
+// As unpack16, except registers 0 and 5 (the codes at bit 0 of each half) hold
+// the codes as exact fp16 integers: OR-ed into the mantissa of 1024 (0x6400)
+// and shifted back by one fp16x2 subtraction, which is exact.
+__device__ __forceinline__ void unpack16_v(uint32_t w, uint32_t (&r)[8]) {
   const uint32_t M = 0x64006400u;
-  // fp16x2 constants: scale 4^-k and offset -1024 * 4^-k for k = 0..4
-  const uint32_t S0 = 0x3C003C00u, O0 = 0xE400E400u;  // 1, -1024
-  const uint32_t S1 = 0x34003400u, O1 = 0xDC00DC00u;  // 1/4, -256
-  const uint32_t S2 = 0x2C002C00u, O2 = 0xD400D400u;  // 1/16, -64
-  const uint32_t S3 = 0x24002400u, O3 = 0xCC00CC00u;  // 1/64, -16
-  const uint32_t S4 = 0x1C001C00u, O4 = 0xC400C400u;  // 1/256, -4
-  r[0] = hfma2_u32(lop3_and_or(w, 0x00030003u, M), S0, O0);
-  r[1] = hfma2_u32(lop3_and_or(w, 0x000C000Cu, M), S1, O1);
-  r[2] = hfma2_u32(lop3_and_or(w, 0x00300030u, M), S2, O2);
-  r[3] = hfma2_u32(lop3_and_or(w, 0x00C000C0u, M), S3, O3);
-  r[4] = hfma2_u32(lop3_and_or(w, 0x03000300u, M), S4, O4);
+  uint32_t t0, t5;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t0) : "r"(w), "r"(0x00030003u), "r"(M));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(M));
+  r[1] = w & 0x000C000Cu;
+  r[2] = w & 0x00300030u;
+  r[3] = w & 0x00C000C0u;
+  r[4] = w & 0x03000300u;
   const uint32_t w2 = w >> 10;
-  r[5] = hfma2_u32(lop3_and_or(w2, 0x00030003u, M), S0, O0);
-  r[6] = hfma2_u32(lop3_and_or(w2, 0x000C000Cu, M), S1, O1);
-  r[7] = hfma2_u32(lop3_and_or(w2, 0x00300030u, M), S2, O2);
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t5) : "r"(w2), "r"(0x00030003u), "r"(M));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[5]) : "r"(t5), "r"(M));
+  r[6] = w2 & 0x000C000Cu;
+  r[7] = w2 & 0x00300030u;
 }
+
+// log2 of the value unpack16_v gives a code of register p, per unit of code
+__device__ __forceinline__ constexpr int unpack_v_exp(int p) { return (p == 0 || p == 5) ? 0 : 2 * unpack_k(p) - 24; }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
