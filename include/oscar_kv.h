@@ -143,9 +143,11 @@ typedef struct {
  * kv_layout_query — sizes and offsets of the cache and of the decode
  * workspace.  Host only, pure arithmetic.  Returns OSCAR_ERR_INVALID or
  * OSCAR_ERR_UNSUPPORTED on a bad config, else fills *out.
- * attn_decode with n splits needs
- *   align256(B*Hq*D*4) + align256(B*Hq*(D/128)*4) + align256(B*Hq*n*D*4)
- *   + align256(B*Hq*n*2*4) + align256(B*Hkv*4) bytes of workspace.
+ * attn_decode with n partial slots needs, with Dg = D/128 and NQT = 2 when
+ * Hq/Hkv > 4 else 1,
+ *   align256(B*Hkv*Dg*NQT*2048) + align256(B*Hkv*Dg*NQT*4096)
+ *   + 2 * align256(B*Hq*Dg*4) + align256(B*Hq*n*D*4) + align256(B*Hq*n*2*4)
+ *   + align256(B*Hkv*4) bytes of workspace.
  */
 int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out);
 
@@ -174,19 +176,27 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  *   q          device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_IN_FP32), not rotated.
  *   seq_lens   device int32 [B], 1 <= seq_len <= capacity.
  *   seq_len_hint host upper bound on seq_lens (0 = capacity); only used to
- *              choose the number of context splits.
+ *              size the grid when the contexts are short.
  *   R_K, R_V   device float32 [D][D] rotations of this layer.
  *   sm_scale   softmax scale; <= 0 means 1/sqrt(D).
- *   num_splits 0 = automatic, else the number of context splits per
- *              (sequence, KV head), at most OSCAR_KV_MAX_SPLITS.
+ *   num_splits 0 = automatic: one wave of CTAs (as many as are resident at
+ *              once).  Else num_splits * B * Hkv CTAs (at most
+ *              OSCAR_KV_MAX_SPLITS per unit): with equal seq_lens every
+ *              (sequence, KV head) is then split num_splits ways.  Either way
+ *              the cache of all (sequence, KV head) units, in unit order, is
+ *              cut into equal slices of work, one per CTA, so a CTA can cover
+ *              the tail of one unit and the head of the next.
  *   out        device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_OUT_FP32);
  *              o = o' R_V^T, or o' with OSCAR_FLAG_ABSORB_V.
  *   lse        device float32 [B][Hq] or NULL: natural-log log-sum-exp of the
  *              scaled scores.
- *   workspace  device scratch of workspace_bytes (see kv_layout_query); the
- *              automatic split count never needs more than is given.
- * Launches two kernels on `stream`: query rotation, then split attention
- * whose last CTA per (sequence, KV head) merges the splits and un-rotates V.
+ *   workspace  device scratch of workspace_bytes (see kv_layout_query); it
+ *              holds n = min(OSCAR_KV_MAX_SPLITS, what fits) partial slots per
+ *              query head, and no unit is shared by more CTAs than slots (an
+ *              explicit num_splits must fit in full).
+ * Launches two kernels on `stream`: query rotation (which writes q' as the
+ * split kernel's MMA fragments), then split attention whose last CTA per
+ * (sequence, KV head) merges that unit's partials and un-rotates V.
  * Both use programmatic dependent launch; the first waits for all prior work
  * on the stream before reading q.  Concurrent calls must not share a workspace.
  */

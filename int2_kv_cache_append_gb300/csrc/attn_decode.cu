@@ -7,25 +7,34 @@
 // to use: V rotation absorbed into the output).
 //
 // Two kernels per call:
-//   qrot   q' = q R_K * sm_scale * log2(e) (float32) and per-group sums of q'.
-//   split  grid (splits, Hkv, B).  Four consumer warps and one producer warp.
-//          The producer streams 64-token INT2 blocks (codes + scale/zero) and
-//          16-token BF16 blocks (sink, ring) into a shared-memory ring with
-//          cp.async.bulk + mbarriers.  Consumers compute scores and P.V with
-//          mma.sync m16n8k16 in "swap-AB" form: tokens (QK) or channels (PV)
-//          on the M side, query heads on N, with each head's hi and lo fp16
-//          (bf16 for BF16 blocks) split in adjacent columns so that the
-//          products keep ~22 bits.  INT2 codes are unpacked straight into
-//          A fragments (exact small integers); per-token scale/zero are
-//          applied algebraically:
+//   qrot   q' = q R_K * sm_scale * log2(e) (float32) and per-group sums of q';
+//          zeroes the merge tickets and writes the output of empty sequences.
+//   split  a persistent grid of P CTAs (by default as many as are resident at
+//          once).  The block lists of all (sequence, KV head) units, in unit
+//          order, are concatenated and cut by bytes into P equal slices, one
+//          per CTA, so every CTA streams the same amount of cache and the
+//          grid ends in one wave.  A slice covers the tail of one unit, whole
+//          units and the head of another; each such unit part is a segment.
+//          Four warps form teams (one warp per 128-channel quant group); each
+//          team issues the bulk copies of its own blocks (cp.async.bulk for
+//          128-token INT2 blocks: codes + scale/zero; 2-D TMA tensor loads for
+//          16-token BF16 sink/ring blocks) into its private stages, running
+//          ahead across segment boundaries, and consumes them with mma.sync
+//          m16n8k16 in "swap-AB" form: tokens (QK) or channels (PV) on the M
+//          side, query heads on N, with each head's hi and lo parts of q' / P
+//          in adjacent columns so that the products keep ~22 bits.  INT2 codes
+//          go from shared memory into A fragments with one AND per register
+//          (fp16 subnormals, see unpack16); per-token scale/zero are applied
+//          algebraically:
 //            s_t = scale_t * (q'.c_t) + zero_t * sum(q'),
 //            o  += (p_t * scale_t) . c_t  and  zeta += p_t * zero_t.
-//          Online softmax in log2 units; teams of D/128 warps split the
-//          channels of a block by quant group and exchange partial scores.
-//          Each CTA writes one partial (m, l, o') per head; the last CTA of a
-//          (b, kv head) to finish (an atomic ticket, never a wait) merges the
-//          splits by log-sum-exp, applies o = o' R_V^T (skipped when absorbed)
-//          and stores bf16/fp32 output and lse.
+//          Online softmax in log2 units; for D > 128 the warps of a team split
+//          a block's channels by quant group and exchange partial scores.  At
+//          the end of a segment the CTA merges its teams and writes one partial
+//          (m, l, o') per head into the segment's slot; the last CTA of a unit
+//          to finish (an atomic ticket, never a wait) merges the unit's slots
+//          by log-sum-exp, applies o = o' R_V^T (skipped when absorbed) and
+//          stores the bf16/fp32 output and lse.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,6 +51,7 @@ constexpr int kThreads = kNCW * 32;
 constexpr int kI2Tok = 128;                // tokens per INT2 block (one set of bulk copies)
 constexpr int kSub = 64;                   // tokens per INT2 compute sub-block
 constexpr int kBfTok = 16;                 // tokens per BF16 block
+constexpr int kMaxSeg = 64;                // segments (units) one window of a CTA's slice lists
 
 template <int D, int NQT>
 struct DecCfg {
@@ -74,8 +84,10 @@ struct DecCfg {
   static constexpr int PART_A = NTEAMS * HEADS * (D + 2);
   static constexpr int PART_B = HEADS * (D + 2 + OSCAR_KV_MAX_SPLITS);
   static constexpr int PART_BYTES = (PART_A > PART_B ? PART_A : PART_B) * 4;
-  static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
-  static constexpr int SMEM = OFF_BAR + (NST + 1) * 8 + 16 + 1024;  // + slack to align the base to 1 KB
+  static constexpr int OFF_SEG = OFF_PART + PART_BYTES;             // segment table of a window
+  static constexpr int OFF_BAR = OFF_SEG + kMaxSeg * 64;
+  static constexpr int SMEM = OFF_BAR + (NST + 2) * 8 + 16 + 1024;  // + slack to align the base to 1 KB
+  static_assert(SMEM + 4 * 1024 + 64 <= 227 * 1024, "dynamic + static shared memory of one CTA");
 };
 
 // Per-(b, kv head) region sizes and the block list
@@ -86,14 +98,17 @@ struct Regions {
   int64_t cbf, ci2;
 };
 
-__device__ __forceinline__ Regions make_regions(int T, int S, int W, int D) {
+__host__ __device__ inline int imin(int x, int y) { return x < y ? x : y; }
+__host__ __device__ inline int imax(int x, int y) { return x > y ? x : y; }
+
+__host__ __device__ inline Regions make_regions(int T, int S, int W, int D) {
   Regions r;
   r.T = T;
   if (T <= S) {
     r.n_sink = T; r.tq = T; r.n_int = 0; r.n_ring = 0;
   } else {
     r.n_sink = S;
-    r.tq = max(S, T - W);
+    r.tq = imax(S, T - W);
     r.n_int = r.tq - S;
     r.n_ring = T - r.tq;
   }
@@ -102,12 +117,21 @@ __device__ __forceinline__ Regions make_regions(int T, int S, int W, int D) {
   // ring positions [tq, T) sit in slots p mod W: cut them where the slots wrap
   // so that every block reads consecutive slots
   r.ra = r.n_ring > 0 ? r.tq % W : 0;
-  r.rlen1 = r.n_ring > 0 ? min(r.n_ring, W - r.ra) : 0;
+  r.rlen1 = r.n_ring > 0 ? imin(r.n_ring, W - r.ra) : 0;
   r.nrb1 = (r.rlen1 + kBfTok - 1) / kBfTok;
   r.nrb = r.nrb1 + (r.n_ring - r.rlen1 + kBfTok - 1) / kBfTok;
-  r.cbf = int64_t(2) * kBfTok * 2 * D;
-  r.ci2 = int64_t(2) * kI2Tok * (D / 4 + 4 * (D / kGroup));
+  // work weights of one block, in proportion to its measured processing time
+  // (a 128-token INT2 block takes ~1.7x a 16-token BF16 block for ~1.1x the
+  // bytes: the codes are unpacked and the scale/zero algebra is extra work)
+  r.cbf = int64_t(6) * D;
+  r.ci2 = int64_t(10) * D;
   return r;
+}
+
+// Work of one (sequence, KV head) unit of context length T: the summed
+// weights of its block list.
+__host__ __device__ inline int64_t unit_cost(const Regions& r) {
+  return r.nsb * r.cbf + r.nib * r.ci2 + r.nrb * r.cbf;
 }
 
 // Smallest block index whose starting cost is >= x.
@@ -125,26 +149,6 @@ struct Blk {
   int first;  // sink: first position; int2: first row (position - S); ring: first slot
   int count;
 };
-
-__device__ __forceinline__ Blk block_at(const Regions& r, int k) {
-  Blk b;
-  if (k < r.nsb) {
-    b.type = 0; b.first = k * kBfTok; b.count = min(kBfTok, r.n_sink - b.first);
-  } else if (k < r.nsb + r.nib) {
-    b.type = 1; b.first = (k - r.nsb) * kI2Tok; b.count = min(kI2Tok, r.n_int - b.first);
-  } else {
-    const int kr = k - r.nsb - r.nib;
-    b.type = 2;
-    if (kr < r.nrb1) {
-      b.first = r.ra + kr * kBfTok;
-      b.count = min(kBfTok, r.rlen1 - kr * kBfTok);
-    } else {
-      b.first = (kr - r.nrb1) * kBfTok;
-      b.count = min(kBfTok, r.n_ring - r.rlen1 - b.first);
-    }
-  }
-  return b;
-}
 
 // AND of `v` over the `n` threads meeting at named barrier `id`.
 __device__ __forceinline__ int team_all(int v, int id, int n) {
@@ -165,9 +169,237 @@ __device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b) {
 }
 
 // ---------------------------------------------------------------------------
-// qrot: q' = q R_K * qscale and per-group sums for the G query heads of one
-// (b, kv head) and one 128-column chunk of q'; the chunk-0 CTA also zeroes
-// that unit's merge ticket.  512 threads = 4 slices of the contraction index
+// Work plan of the split kernel.  Units u = b * Hkv + h in order; unit u costs
+// unit_cost(T_b) bytes and starts at the sum of the costs before it.  Slice c
+// of P is [cut(c), cut(c + 1)).  Normally cut(c) = ceil(c W / P) (W = total);
+// a unit [us, ue) is then shared by CTAs floor(us P / W) .. floor((ue-1) P / W),
+// and CTA c writes the partial of its segment into slot c - floor(us P / W).
+// P is capped so that no unit is shared by more CTAs than the workspace has
+// slots.  With fewer than 3 slots the cuts fall on unit boundaries instead
+// (cut(c) = start of unit ceil(c U / P)), so every unit has one CTA and slot 0.
+// Every CTA computes the same plan from seq_lens; warp-wide loops over B.
+// ---------------------------------------------------------------------------
+struct Plan {
+  int64_t W;     // total cost
+  int P;         // CTAs with a slice
+  bool aligned;  // cuts on unit boundaries
+};
+
+struct SegD {      // one segment: a unit's part of a CTA's slice
+  int b, h;        // unit
+  int kb, ke;      // block range within the unit's block list
+  int slot, nseg;  // partial slot of this CTA, CTAs sharing the unit
+  // the unit's block list (the fields of Regions that block_of reads)
+  int n_sink, n_int, n_ring, nsb, nib, ra, rlen1, nrb1;
+  int pad0, pad1;
+};
+
+// block_at on a segment's copy of its unit's block list
+__device__ __forceinline__ Blk block_of(const SegD& r, int k) {
+  Blk b;
+  if (k < r.nsb) {
+    b.type = 0; b.first = k * kBfTok; b.count = min(kBfTok, r.n_sink - b.first);
+  } else if (k < r.nsb + r.nib) {
+    b.type = 1; b.first = (k - r.nsb) * kI2Tok; b.count = min(kI2Tok, r.n_int - b.first);
+  } else {
+    const int kr = k - r.nsb - r.nib;
+    b.type = 2;
+    if (kr < r.nrb1) {
+      b.first = r.ra + kr * kBfTok;
+      b.count = min(kBfTok, r.rlen1 - kr * kBfTok);
+    } else {
+      b.first = (kr - r.nrb1) * kBfTok;
+      b.count = min(kBfTok, r.n_ring - r.rlen1 - b.first);
+    }
+  }
+  return b;
+}
+
+// 2^e as a float, for -126 <= e <= 127
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// the e with x < 2^e <= 2x for finite x > 0 (frexpf's exponent; -126 below the normal range)
+__device__ __forceinline__ int exp_above(float x) {
+  const int E = (__float_as_int(x) >> 23) & 255;
+  return E == 0 ? -126 : E - 126;
+}
+
+// floor(x / d) for 0 <= x < 2^62, 0 < d: three fp32 reciprocal estimates and an
+// exact int64 correction (FP64 and 64-bit integer division are long software
+// sequences on this GPU; this is a few instructions)
+__device__ __forceinline__ int64_t div_floor(int64_t x, int64_t d) {
+  const float inv = 1.0f / float(d);
+  int64_t q = int64_t(float(x) * inv);
+  int64_t r = x - q * d;
+  q += int64_t(floorf(float(r) * inv));  // each step leaves ~22 fewer bits of error
+  r = x - q * d;
+  q += int64_t(floorf(float(r) * inv));
+  r = x - q * d;
+  while (r < 0) { --q; r += d; }
+  while (r >= d) { ++q; r -= d; }
+  return q;
+}
+
+// clamped context lengths of the first kLenCache sequences, staged in shared
+// memory once per CTA; the rest are read from global memory
+constexpr int kLenCache = 1024;
+__device__ __forceinline__ int seq_len_at(const DecodeArgs& a, const int* lens, int b) {
+  return b < kLenCache ? lens[b] : clamp_seq_len(a, b);
+}
+
+// floor(x / d) when the quotient is known to be below 2^20 (one fp32 estimate,
+// off by at most one, then corrected exactly)
+__device__ __forceinline__ int64_t div_small(int64_t x, int64_t d) {
+  int64_t q = int64_t(float(x) * (1.0f / float(d)));
+  int64_t r = x - q * d;
+  while (r < 0) { --q; r += d; }
+  while (r >= d) { ++q; r -= d; }
+  return q;
+}
+
+template <int D>
+__device__ __forceinline__ int64_t seq_cost(const DecodeArgs& a, const int* lens, int b) {
+  return b < a.g.B ? unit_cost(make_regions(seq_len_at(a, lens, b), a.g.S, a.g.W, D)) : 0;
+}
+
+template <int D>
+__device__ Plan make_plan(const DecodeArgs& a, const int* lens, int lane) {
+  const Geom& g = a.g;
+  int64_t W = 0, cmax = 0;
+  for (int b0 = 0; b0 < g.B; b0 += 32) {
+    int64_t sm = seq_cost<D>(a, lens, b0 + lane), mx = sm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    W += sm * g.Hkv;
+    cmax = max(cmax, mx);
+  }
+  Plan pl;
+  pl.W = W;
+  pl.aligned = a.ns < 3;
+  int64_t P = gridDim.x;
+  if (pl.aligned) {
+    P = min(P, int64_t(g.B) * g.Hkv);
+  } else if (W > 0) {
+    P = min(P, W);
+    P = min(P, max(int64_t(1), div_floor((int64_t(a.ns) - 2) * W, cmax)));
+  }
+  pl.P = int(max(P, int64_t(1)));
+  return pl;
+}
+
+// Start cost of unit k (k <= B * Hkv).
+template <int D>
+__device__ int64_t unit_start(const DecodeArgs& a, const int* lens, int lane, int64_t k) {
+  const int Hkv = a.g.Hkv;
+  const int bk = int(k) / Hkv, hk = int(k) % Hkv;  // k <= B * Hkv < 2^31
+  int64_t base = 0;
+  for (int b0 = 0; b0 < bk; b0 += 32) {
+    int64_t c = b0 + lane < bk ? seq_cost<D>(a, lens, b0 + lane) * Hkv : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    base += c;
+  }
+  return base + (hk > 0 ? hk * seq_cost<D>(a, lens, bk) : 0);
+}
+
+// Unit holding cost x (0 <= x < W) and its start cost.
+template <int D>
+__device__ void locate(const DecodeArgs& a, const int* lens, int lane, int64_t x, int& u, int64_t& us) {
+  const int Hkv = a.g.Hkv;
+  int64_t base = 0;
+  u = 0;
+  us = 0;
+  for (int b0 = 0; b0 < a.g.B; b0 += 32) {
+    const int64_t per = seq_cost<D>(a, lens, b0 + lane);
+    int64_t incl = per * Hkv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, base + incl > x);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const int64_t pre = base + __shfl_sync(0xffffffffu, incl, l) - __shfl_sync(0xffffffffu, per, l) * Hkv;
+      const int64_t pl = __shfl_sync(0xffffffffu, per, l);
+      const int h = int(div_small(x - pre, pl));  // h < Hkv
+      u = (b0 + l) * Hkv + h;
+      us = pre + int64_t(h) * pl;
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+// Segment table of one window of slice [lo, hi) of CTA c, from unit u with
+// start cost us (warp-wide; lane 0's results are the ones used).  Lists at most
+// kMaxSeg segments; returns their number and leaves (u, us) at the first unit
+// not listed.
+template <int D>
+__device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& pl, int c, int64_t lo, int64_t hi,
+                              int& u, int64_t& us, SegD* seg, int lane) {
+  const Geom& g = a.g;
+  const int64_t U = int64_t(g.B) * g.Hkv;
+  int n = 0;
+  while (us < hi && u < U && n < kMaxSeg) {
+    const int64_t uu = u + lane;
+    const int b = int(uu) / g.Hkv, h = int(uu) % g.Hkv;
+    const int T = uu < U ? seq_len_at(a, lens, b) : 0;
+    const Regions rg = make_regions(T, g.S, g.W, D);
+    const int64_t cu = uu < U ? unit_cost(rg) : 0;
+    int64_t incl = cu;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int64_t s0 = us + incl - cu, e0 = us + incl;
+    const bool take = cu > 0 && s0 < hi;
+    const unsigned tk = __ballot_sync(0xffffffffu, take);
+    const int idx = n + __popc(tk & ((1u << lane) - 1u));
+    if (take && idx < kMaxSeg) {
+      SegD d;
+      d.b = b; d.h = h;
+      d.n_sink = rg.n_sink; d.n_int = rg.n_int; d.n_ring = rg.n_ring;
+      d.nsb = rg.nsb; d.nib = rg.nib; d.ra = rg.ra; d.rlen1 = rg.rlen1; d.nrb1 = rg.nrb1;
+      d.pad0 = 0; d.pad1 = 0;
+      d.kb = first_block_at(rg, max(lo, s0) - s0);
+      d.ke = first_block_at(rg, min(hi, e0) - s0);
+      if (pl.aligned) {
+        d.slot = 0; d.nseg = 1;
+      } else {
+        const int64_t cf = div_small(s0 * pl.P, pl.W), cl = div_small((e0 - 1) * pl.P, pl.W);  // < P
+        d.slot = int(c - cf);
+        d.nseg = int(cl - cf + 1);
+      }
+      seg[idx] = d;
+    }
+    // advance past the units listed (or skipped), stopping at a full table
+    const int room = kMaxSeg - n;
+    int adv = 32;
+    if (__popc(tk) > room) {
+      // the (room+1)-th taken lane is the first unit not listed
+      unsigned m = tk;
+      for (int i = 0; i < room; ++i) m &= m - 1;
+      adv = __ffs(m) - 1;
+    }
+    const int64_t consumed = adv > 0 ? __shfl_sync(0xffffffffu, incl, adv - 1) : 0;
+    n += min(__popc(tk), room);
+    us += consumed;
+    u += adv;
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// qrot: q' = q R_K * qscale for the G query heads of one (b, kv head) and one
+// 128-channel quant group, written as the split kernel's mma B fragments (see
+// the two layouts below) with per-group sums and score factors; the group-0
+// CTA also zeroes that unit's merge ticket.  For an empty sequence it writes the output
+// instead (zeros, lse = -inf) and flags OSCAR_DEV_EMPTY.  512 threads = 4 slices of the contraction index
 // x 128 output columns, so each thread has at most D/4 loads of R_K, issued
 // 32 at a time.  Launched with PDL: it waits for the preceding kernel before
 // reading anything (q may be produced right before this call) and then at
@@ -183,7 +415,9 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
   constexpr int KC = D / KP;              // contraction indices per slice
   __shared__ float qs[8][D];
   __shared__ float part[KP - 1][8][128];
-  __shared__ float red[8][4];
+  __shared__ float qv[8][128];  // q' of this group, per head
+  __shared__ float red[8][4], redm[8][4];
+  __shared__ int Xs[8];
   const int bh = blockIdx.x;  // b * Hkv + h
   const int chunk = blockIdx.y;
   const int G = a.g.G;
@@ -192,6 +426,25 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
   const int64_t q0 = int64_t(bh) * G * D;  // first query head of this kv head
   pdl_wait();
   pdl_trigger();
+
+  const int b = bh / a.g.Hkv;
+  const int T = clamp_seq_len(a, b);
+  if (chunk == 0 && threadIdx.x == 0 && bh % a.g.Hkv == 0) {
+    if (a.seq_lens[b] > a.g.cap) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
+    if (T < 1) status_or(a.status, OSCAR_DEV_EMPTY);
+  }
+  if (T < 1) {
+    // nothing to attend to (the split kernel has no work here): zero output, lse = -inf
+    for (int idx = threadIdx.x; idx < G * 128; idx += kQrotThreads) {
+      const int64_t oi = q0 + int64_t(idx / 128) * D + chunk * 128 + idx % 128;
+      if (a.out_fp32)
+        static_cast<float*>(a.out)[oi] = 0.f;
+      else
+        static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(0.f);
+    }
+    if (chunk == 0 && threadIdx.x < G && a.lse) a.lse[q0 / D + threadIdx.x] = -INFINITY;
+    return;
+  }
 
   int k0 = kp * KC;
   float rr[32];
@@ -231,18 +484,73 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
         for (int p = 0; p < KP - 1; ++p) sum += part[p][i][c];
         const float v = sum * a.qscale;
         if (!(fabsf(v) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
-        a.qprime[q0 + i * D + col] = v;
-        float t = v;
+        qv[i][c] = v;
+        float t = v, m = fabsf(v);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if ((c & 31) == 0) red[i][c >> 5] = t;
+        for (int o = 16; o > 0; o >>= 1) {
+          t += __shfl_xor_sync(0xffffffffu, t, o);
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        }
+        if ((c & 31) == 0) {
+          red[i][c >> 5] = t;
+          redm[i][c >> 5] = m;
+        }
       }
     }
   }
   __syncthreads();
-  if (threadIdx.x < G)
-    a.qsum[(q0 / D + threadIdx.x) * (D / kGroup) + chunk] =
-        red[threadIdx.x][0] + red[threadIdx.x][1] + red[threadIdx.x][2] + red[threadIdx.x][3];
+  // per head: sum of q' over the group, and the exponent X that puts the
+  // largest |q'| * 2^X in [2^13, 2^14) (the INT2 fragments are scaled by it)
+  if (threadIdx.x < G) {
+    const int i = threadIdx.x;
+    const float mx = fmaxf(fmaxf(redm[i][0], redm[i][1]), fmaxf(redm[i][2], redm[i][3]));
+    const int X = mx > 0.f ? max(-100, min(14 - exp_above(mx), 100)) : 0;
+    Xs[i] = X;
+    const int64_t qi = (q0 / D + i) * (D / kGroup) + chunk;
+    a.qsum[qi] = red[i][0] + red[i][1] + red[i][2] + red[i][3];
+    a.qF[qi] = pow2f(24 - X);
+  }
+  __syncthreads();
+
+  // B fragments of this (b, kv head, group) for the split kernel's mma.sync
+  // m16n8k16, in its lanes' order.  Column n of an n-tile nq is head slot
+  // 4 nq + n / 2, with the hi (n even) or lo (n odd) part; lane = 4 gq + cq
+  // holds column gq and k-rows 2cq, 2cq + 1 (+ 8 for the second register).
+  const int NQT = G > 4 ? 2 : 1, NQB = 2 * NQT;
+  const int64_t grp = int64_t(bh) * (D / kGroup) + chunk;
+  // INT2 blocks: channel d of a code at mantissa bit 2k meets q'[d] * 4^-k * 2^X
+  // as an fp16 hi/lo pair (see unpack16), entry ((nq * 8 + kk) * 2 + half) * 32 + lane
+  for (int e = threadIdx.x; e < NQT * 512; e += kQrotThreads) {
+    const int ln = e & 31, half = (e >> 5) & 1, kk = (e >> 6) & 7, nq = e >> 9;
+    const int gq = ln >> 2, cq = ln & 3, hb = 4 * nq + (gq >> 1);
+    const int d0 = 16 * kk + 2 * cq + 8 * half;
+    uint32_t v16 = 0;
+    if (hb < G) {
+      const float f = pow2f(Xs[hb] - 2 * unpack_k(2 * (kk & 3) + half));
+      const uint32_t s0 = split_f16(qv[hb][d0] * f), s1 = split_f16(qv[hb][d0 + 1] * f);
+      v16 = (gq & 1) ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
+    }
+    a.qfrag[grp * (NQT * 512) + e] = v16;
+  }
+  // BF16 blocks: n-tile 2nq holds the (hi, mid) and n-tile 2nq + 1 the (lo, 0)
+  // parts of each head's three-way bf16 split of q' (~24 bits), entry
+  // ((kk * NQB + nb) * 2 + half) * 32 + lane: the split kernel's shared image
+  for (int e = threadIdx.x; e < NQT * 1024; e += kQrotThreads) {
+    const int ln = e & 31, half = (e >> 5) & 1, nb = (e >> 6) % NQB, kk = (e >> 6) / NQB;
+    const int gq = ln >> 2, cq = ln & 3, hb = 4 * (nb >> 1) + (gq >> 1);
+    const int d0 = 16 * kk + 2 * cq + 8 * half;
+    uint32_t w = 0;
+    if (hb < G) {
+      uint32_t p0[3], p1[3];
+      split3_bf16(qv[hb][d0], p0);
+      split3_bf16(qv[hb][d0 + 1], p1);
+      if (nb & 1)
+        w = (gq & 1) ? 0u : (p0[2] | (p1[2] << 16));
+      else
+        w = (gq & 1) ? (p0[1] | (p1[1] << 16)) : (p0[0] | (p1[0] << 16));
+    }
+    a.qbfrag[grp * (NQT * 1024) + e] = w;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -258,36 +566,65 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
   // 128-byte-swizzled TMA destinations need 1 KB alignment
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  __shared__ int abort_flag;
+  SegD* seg = reinterpret_cast<SegD*>(smem + C::OFF_SEG);
+  __shared__ int abort_flag, is_last, win_n, win_more;
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  __shared__ int lens[kLenCache];
+
   const Geom& g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = clamp_seq_len(a, b);
-  const Regions rg = make_regions(T, g.S, g.W, D);
-  const int64_t total = rg.nsb * rg.cbf + rg.nib * rg.ci2 + rg.nrb * rg.cbf;
-  const int kb = first_block_at(rg, (int64_t(split) * total + a.ns - 1) / a.ns);
-  const int ke = first_block_at(rg, (int64_t(split + 1) * total + a.ns - 1) / a.ns);
-  const int nblk = ke - kb;
-  const int64_t bh = int64_t(b) * g.Hkv + h;
+  for (int i = threadIdx.x; i < g.B && i < kLenCache; i += kThreads) lens[i] = clamp_seq_len(a, i);
+  __syncthreads();
+
+  // ---- this CTA's slice [lo, hi) of the concatenated unit costs
+  const Plan pl = make_plan<D>(a, lens, lane);
+  const int c = blockIdx.x;
+  if (pl.W == 0 || c >= pl.P) return;
+  int64_t lo, hi, us_next = 0;
+  int u_next = 0;
+  if (pl.aligned) {
+    const int64_t U = int64_t(g.B) * g.Hkv;
+    const int64_t k0 = div_floor(int64_t(c) * U + pl.P - 1, pl.P), k1 = div_floor(int64_t(c + 1) * U + pl.P - 1, pl.P);
+    lo = unit_start<D>(a, lens, lane, k0);
+    hi = unit_start<D>(a, lens, lane, k1);
+    u_next = int(k0);
+    us_next = lo;
+  } else {
+    lo = div_floor(int64_t(c) * pl.W + pl.P - 1, pl.P);
+    hi = div_floor(int64_t(c + 1) * pl.W + pl.P - 1, pl.P);
+    if (lo < hi) locate<D>(a, lens, lane, lo, u_next, us_next);
+  }
+  if (lo >= hi) return;
+
+  pdl_wait();  // q' and the merge tickets come from the preceding kernel
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < C::NST; ++s) mbar_init(smem_u32(&bars[s]), 1);  // issuer's arrival + tx bytes
-    mbar_init(smem_u32(&bars[C::NST]), 1);  // R_V prefetch of the merging CTA
+    mbar_init(smem_u32(&bars[C::NST]), 1);      // R_V prefetch of a merge in the last segment
+    mbar_init(smem_u32(&bars[C::NST + 1]), 1);  // shared bf16 q' fragments
     mbar_fence_init();
   }
-  __syncthreads();
 
   const uint8_t* kbase = a.layer_base;
   const uint8_t* vbase = a.layer_base + g.role_bytes;
   const uint64_t codes_off = g.sink_bytes + g.ring_bytes;
   const uint64_t sz_off = codes_off + g.codes_bytes;
 
-  // Bulk copies of block kl into stage `stage`, issued by the calling warp (lane
-  // 0 arms the barrier with the byte count first).
-  auto issue_block = [&](int kl, int stage) {
-    const Blk bk = block_at(rg, kb + kl);
+  const int team = warp / C::TS, wt = warp % C::TS;  // wt = quant group handled
+  const int gq = lane >> 2, cq = lane & 3;
+  const int Gh = g.G;
+  auto my_stage = [&](int j) { return team * C::NSTW + j % C::NSTW; };
+  int issued = 0, consumed = 0;  // blocks of this team issued / consumed so far
+  int is_ = 0, ij = 0;           // issue cursor: segment, team-local block index
+  int nwin = 0;                  // segments in the current window
+
+  // Bulk copies of block k of segment si into stage `stage`, issued by the
+  // calling warp (lane 0 arms the barrier with the byte count first).
+  auto issue_block = [&](int si, int k, int stage) {
+    const SegD& sd = seg[si];
+    const Blk bk = block_of(sd, k);
+    const int64_t bh = int64_t(sd.b) * g.Hkv + sd.h;
     const uint32_t full = smem_u32(&bars[stage]);
     const uint32_t dst = smem_u32(smem + C::OFF_STAGE + stage * C::STAGE);
     if (bk.type == 1) {
@@ -317,573 +654,639 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
     }
   };
 
-  // ------------------------------- consumers --------------------------------
-  const int team = warp / C::TS, wt = warp % C::TS;  // wt = quant group handled
-  const int gq = lane >> 2, cq = lane & 3;
-  const int Gh = g.G;
-  const int head0 = h * Gh;  // first query head of this kv head
-  const int nmine = nblk > team ? (nblk - team + C::NTEAMS - 1) / C::NTEAMS : 0;  // this team's blocks
-  auto my_stage = [&](int j) { return team * C::NSTW + j % C::NSTW; };
-  int issued = 0;  // blocks of this team whose copies are in flight or done
-
-  // the cache is complete once this kernel runs (the preceding kernel waited
-  // for it); start streaming before waiting for q'
-  if (wt == 0)
-    for (; issued < nmine && issued < C::NSTW; ++issued) issue_block(team + issued * C::NTEAMS, my_stage(issued));
-
-  pdl_wait();  // q' comes from the preceding kernel
-
-  // B fragments of q' for this warp's group: column n <-> (head n/2, hi|lo by n%2).
-  // INT2 codes reach the MMAs as fp16 subnormals code * 4^k * 2^-24 (see
-  // unpack16), so the q' entry meeting a code at mantissa bit 2k is stored as
-  // q' * 4^-k * 2^X, with 2^X per (head, group) chosen so that the largest
-  // |q'| * 2^X lies in [2^13, 2^14): every product is then code * q' * 2^(X-24)
-  // and the score is rescaled by qF = 2^(24-X) (exact powers of two throughout).
-  uint32_t qf[8][NQT][2];
-  float qsum[NQT], qF[NQT];
-  // bf16 B fragments for BF16 blocks: n-tile 2nq holds (hi, mid) and n-tile
-  // 2nq+1 holds (lo, 0) of each head's three-way bf16 split (~24 bits)
-  uint32_t* qbf = reinterpret_cast<uint32_t*>(smem + C::OFF_QBF) + wt * 8 * C::NQB * 64;
-  {
-    const int hs_b = gq >> 1, lohalf = gq & 1;
-#pragma unroll
-    for (int nq = 0; nq < NQT; ++nq) {
-      const int hb = 4 * nq + hs_b;  // head slot of this lane's B column
-      const bool hv = hb < Gh;
-      const float* qp = a.qprime + (int64_t(b) * g.Hq + head0 + (hv ? hb : 0)) * D + wt * kGroup;
-      float xq[8][2][2];
-      float mx = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int d0 = 16 * kk + 2 * cq + 8 * half;
-          xq[kk][half][0] = hv ? qp[d0] : 0.f;
-          xq[kk][half][1] = hv ? qp[d0 + 1] : 0.f;
-          mx = fmaxf(mx, fmaxf(fabsf(xq[kk][half][0]), fabsf(xq[kk][half][1])));
-        }
-      // the four lanes of a B column hold all 128 channels of the group
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      int ex = 0;
-      (void)frexpf(mx, &ex);  // mx < 2^ex
-      const int X = mx > 0.f ? min(14 - ex, 100) : 0;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const float f = ldexpf(1.f, X - 2 * unpack_k(2 * (kk & 3) + half));
-          const float x0 = xq[kk][half][0], x1 = xq[kk][half][1];
-          const uint32_t s0 = split_f16(x0 * f), s1 = split_f16(x1 * f);
-          // pick hi (low half) or lo (high half) of each split
-          const uint32_t v16 = lohalf ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
-          qf[kk][nq][half] = v16;
-          if (team == 0) {  // the other teams hold the same fragments
-            uint32_t p0[3], p1[3];
-            split3_bf16(x0, p0);
-            split3_bf16(x1, p1);
-            const uint32_t va = lohalf ? (p0[1] | (p1[1] << 16)) : (p0[0] | (p1[0] << 16));
-            const uint32_t vb = lohalf ? 0u : (p0[2] | (p1[2] << 16));
-            qbf[(kk * C::NQB + 2 * nq) * 64 + half * 32 + lane] = va;
-            qbf[(kk * C::NQB + 2 * nq + 1) * 64 + half * 32 + lane] = vb;
-          }
-        }
+  // the team's next block in window order (blocks kb + team + j * NTEAMS of
+  // each segment), if any: issue it into the team's next stage
+  auto issue_next = [&]() {
+    while (is_ < nwin) {
+      const int k = seg[is_].kb + team + ij * C::NTEAMS;
+      if (k < seg[is_].ke) {
+        issue_block(is_, k, my_stage(issued));
+        ++issued;
+        ++ij;
+        return;
       }
-      const int hc = 4 * nq + cq;  // head owned by this lane in C fragments
-      // lane 8 * cq holds B column 2 * cq, i.e. head slot cq of this n-tile
-      qF[nq] = ldexpf(1.f, 24 - __shfl_sync(0xffffffffu, X, 8 * cq));
-      qsum[nq] = hc < Gh ? a.qsum[(int64_t(b) * g.Hq + head0 + hc) * C::Dg + wt] : 0.f;
-    }
-  }
-  __syncwarp();
-
-  asm volatile("bar.sync 14, %0;" ::"r"(32 * kNCW) : "memory");  // shared bf16 fragments written
-
-  float o[8][NQT][4];
-  float m_run[NQT], l_run[NQT], zeta[NQT];
-#pragma unroll
-  for (int nq = 0; nq < NQT; ++nq) {
-    m_run[nq] = -INFINITY; l_run[nq] = 0.f; zeta[nq] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][nq][e] = 0.f;
-  }
-
-  float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
-  int xbuf = 0;
-
-  // INT2 P.V takes V codes from unpack16_v: the code of output row r arrives
-  // as code * 2^e(r), e(r) = unpack_v_exp(p) with p = 2 * (mtd % 4) for rows gq
-  // and 2 * (mtd % 4) + 1 for rows gq + 8.  While INT2 blocks are consumed, row
-  // r of o holds (real value) * 2^e(r); it is converted by exact powers of two
-  // at a switch between INT2 and BF16 blocks and at the end.
-  bool o_i2 = false;
-  auto scale_o = [&](int sign) {  // o *= 2^(sign * e(r)) per row
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const float f0 = ldexpf(1.f, sign * unpack_v_exp(2 * (mt & 3)));
-      const float f1 = ldexpf(1.f, sign * unpack_v_exp(2 * (mt & 3) + 1));
-#pragma unroll
-      for (int nq = 0; nq < NQT; ++nq) {
-        o[mt][nq][0] *= f0; o[mt][nq][1] *= f0;
-        o[mt][nq][2] *= f1; o[mt][nq][3] *= f1;
-      }
+      ++is_;
+      ij = 0;
     }
   };
 
-
-  for (int j = 0; j < nmine; ++j) {
-    const int kl = team + j * C::NTEAMS;
-    const int stage = my_stage(j);
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (j / C::NSTW) & 1);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    // the warps of a team must take the same decision: they meet at team barriers below
-    if constexpr (C::TS > 1) ok = team_all(ok, 1 + team, 32 * C::TS);
-    if (!ok) {
-      if (lane == 0) { abort_flag = 1; status_or(a.status, OSCAR_DEV_TIMEOUT); }
-      break;
-    }
-    const Blk bk = block_at(rg, kb + kl);
-    const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
-    const bool is_i2 = bk.type == 1;
-    if (is_i2 != o_i2) {
-      scale_o(is_i2 ? 1 : -1);
-      o_i2 = is_i2;
-    }
-    constexpr int MT_MAX = kSub / 16;
-    const int nmt = is_i2 ? MT_MAX : 1;
-    const int nsub = is_i2 ? (bk.count + kSub - 1) / kSub : 1;
-    for (int sbk = 0; sbk < nsub; ++sbk) {
-    const int cnt = is_i2 ? min(kSub, bk.count - sbk * kSub) : bk.count;  // tokens in this sub-block
-    const int tb = sbk * kSub;  // its first token within the stage
-
-    // ---- scores: s[mt][nq][0] token 16mt+gq, [1] token 16mt+gq+8
-    float s[MT_MAX][NQT][2];
-    float ksc[MT_MAX][2], kze[MT_MAX][2];
-    if (is_i2) {
-      const uint8_t* kc = st;
-      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB);
-      // m-tiles are processed in groups whose MMAs interleave (independent
-      // accumulators), so the k-step chain of one m-tile never runs alone
-      constexpr int MG = NQT == 1 ? 4 : 2;
-#pragma unroll
-      for (int m0 = 0; m0 < MT_MAX; m0 += MG) {
-        uint2 w[MG][2];
-#pragma unroll
-        for (int i = 0; i < MG; ++i) {
-          const int t0 = 16 * (m0 + i) + gq;
-          w[i][0] = *reinterpret_cast<const uint2*>(kc + (tb + t0) * C::ROWB + wt * 32 + cq * 8);
-          w[i][1] = *reinterpret_cast<const uint2*>(kc + (tb + t0 + 8) * C::ROWB + wt * 32 + cq * 8);
-        }
-        float acc[MG][NQT][4];
-#pragma unroll
-        for (int i = 0; i < MG; ++i)
-#pragma unroll
-          for (int nq = 0; nq < NQT; ++nq)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[i][nq][e] = 0.f;
-#pragma unroll
-        for (int wi = 0; wi < 2; ++wi) {
-          uint32_t r[MG][2][8];
-#pragma unroll
-          for (int i = 0; i < MG; ++i) {
-            unpack16(wi ? w[i][0].y : w[i][0].x, r[i][0]);
-            unpack16(wi ? w[i][1].y : w[i][1].x, r[i][1]);
-          }
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = 4 * wi + k4;
-#pragma unroll
-            for (int nq = 0; nq < NQT; ++nq)
-#pragma unroll
-              for (int i = 0; i < MG; ++i)
-                mma_f16(acc[i][nq], r[i][0][2 * k4], r[i][1][2 * k4], r[i][0][2 * k4 + 1], r[i][1][2 * k4 + 1],
-                        qf[kk][nq][0], qf[kk][nq][1]);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < MG; ++i) {
-          const int mt = m0 + i;
-          const int t0 = 16 * mt + gq, t1 = t0 + 8;
-          const uint32_t z0 = ksz[(tb + t0) * C::Dg + wt], z1 = ksz[(tb + t1) * C::Dg + wt];
-          ksc[mt][0] = __half2float(__ushort_as_half(z0 & 0xffff));
-          kze[mt][0] = __half2float(__ushort_as_half(z0 >> 16));
-          ksc[mt][1] = __half2float(__ushort_as_half(z1 & 0xffff));
-          kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
-#pragma unroll
-          for (int nq = 0; nq < NQT; ++nq) {
-            s[mt][nq][0] = fmaf(ksc[mt][0], (acc[i][nq][0] + acc[i][nq][1]) * qF[nq], kze[mt][0] * qsum[nq]);
-            s[mt][nq][1] = fmaf(ksc[mt][1], (acc[i][nq][2] + acc[i][nq][3]) * qF[nq], kze[mt][1] * qsum[nq]);
-          }
-        }
-      }
-    } else {
-      const uint32_t kb_s = smem_u32(st);
-      float acc[C::NQB][4];
-#pragma unroll
-      for (int nb = 0; nb < C::NQB; ++nb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
-      const int mi = lane >> 3;
-      const int tok = (lane & 7) + 8 * (mi & 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int dim = wt * kGroup + 16 * kk + 8 * (mi >> 1);
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(kb_s + (dim >> 6) * C::BOX_BYTES + tok * 128 + ((((dim & 63) >> 3) ^ (tok & 7)) << 4), a0, a1,
-                    a2, a3);
-#pragma unroll
-        for (int nb = 0; nb < C::NQB; ++nb) {
-          const uint32_t b0 = qbf[(kk * C::NQB + nb) * 64 + lane];
-          const uint32_t b1 = qbf[(kk * C::NQB + nb) * 64 + 32 + lane];
-          mma_bf16(acc[nb], a0, a1, a2, a3, b0, b1);
-        }
-      }
-#pragma unroll
-      for (int nq = 0; nq < NQT; ++nq) {
-        s[0][nq][0] = acc[2 * nq][0] + acc[2 * nq][1] + acc[2 * nq + 1][0];
-        s[0][nq][1] = acc[2 * nq][2] + acc[2 * nq][3] + acc[2 * nq + 1][2];
-      }
-    }
-
-    // ---- team exchange of partial scores (one quant group per warp)
-    if constexpr (C::TS > 1) {
-      float* xb = xch + ((team * 2 + xbuf) * C::TS) * kSub * C::HEADS;
-#pragma unroll
-      for (int mt = 0; mt < MT_MAX; ++mt) {
-        if (mt < nmt) {
-#pragma unroll
-          for (int nq = 0; nq < NQT; ++nq) {
-            const int hs = 4 * nq + cq;
-            xb[(wt * kSub + 16 * mt + gq) * C::HEADS + hs] = s[mt][nq][0];
-            xb[(wt * kSub + 16 * mt + gq + 8) * C::HEADS + hs] = s[mt][nq][1];
-          }
-        }
-      }
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * C::TS) : "memory");
-#pragma unroll
-      for (int mt = 0; mt < MT_MAX; ++mt) {
-        if (mt < nmt) {
-#pragma unroll
-          for (int nq = 0; nq < NQT; ++nq) {
-            const int hs = 4 * nq + cq;
-            float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-            for (int w = 0; w < C::TS; ++w) {
-              t0 += xb[(w * kSub + 16 * mt + gq) * C::HEADS + hs];
-              t1 += xb[(w * kSub + 16 * mt + gq + 8) * C::HEADS + hs];
-            }
-            s[mt][nq][0] = t0;
-            s[mt][nq][1] = t1;
-          }
-        }
-      }
-      xbuf ^= 1;
-    }
-
-    // ---- online softmax (log2 units)
-    float p[MT_MAX][NQT][2];
+  // q' of a segment's unit, prepared by qrot: this lane's B fragments of group
+  // wt (INT2 blocks), and the per-group sums and score factors of the heads of
+  // its C fragments (head slot 4 nq + cq)
+  auto load_q = [&](int bx, int hx, uint32_t (&qfx)[8][NQT][2], float (&qsx)[NQT], float (&qFx)[NQT]) {
+    const int64_t unit = int64_t(bx) * g.Hkv + hx;
+    const uint32_t* src = a.qfrag + (unit * C::Dg + wt) * (NQT * 512);
 #pragma unroll
     for (int nq = 0; nq < NQT; ++nq) {
-      float mb = -INFINITY;
 #pragma unroll
-      for (int mt = 0; mt < MT_MAX; ++mt) {
-        if (mt < nmt) {
+      for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tk = 16 * mt + gq + 8 * e;
-            const float v = tk < cnt ? s[mt][nq][e] : -INFINITY;
-            s[mt][nq][e] = v;
-            mb = fmaxf(mb, v);
-          }
-        }
+        for (int half = 0; half < 2; ++half) qfx[kk][nq][half] = src[((nq * 8 + kk) * 2 + half) * 32 + lane];
+      const int hc = 4 * nq + cq;
+      const int64_t qi = (int64_t(bx) * g.Hq + hx * Gh + hc) * C::Dg + wt;
+      qsx[nq] = hc < Gh ? a.qsum[qi] : 0.f;
+      qFx[nq] = hc < Gh ? a.qF[qi] : 1.f;
+    }
+  };
+  // bf16 fragments of a unit (all its groups) into the shared image, one bulk
+  // copy issued by thread 0 on barrier NST + 1; every copy is awaited in order
+  const uint32_t qb_bar = smem_u32(&bars[C::NST + 1]);
+  int qb_issued = 0, qb_waited = 0;
+  auto qb_issue = [&](int bx, int hx) {
+    if (threadIdx.x == 0) {
+      const int64_t unit = int64_t(bx) * g.Hkv + hx;
+      mbar_arrive_expect_tx(qb_bar, C::QBF_BYTES);
+      bulk_g2s(smem_u32(smem + C::OFF_QBF), a.qbfrag + unit * (C::Dg * NQT * 1024), C::QBF_BYTES, qb_bar);
+    }
+    ++qb_issued;
+  };
+  auto qb_wait = [&]() {  // thread 0 waits; a CTA barrier must follow before others read
+    if (threadIdx.x == 0 && !mbar_wait(qb_bar, qb_waited & 1)) {
+      abort_flag = 1;
+      status_or(a.status, OSCAR_DEV_TIMEOUT);
+    }
+    ++qb_waited;
+  };
+
+
+  // the first window starts at unit u_next: its q' is loaded now, ahead of
+  // the window's copies, and lands while the segment table is built
+  uint32_t qf[8][NQT][2];
+  float qsum[NQT], qF[NQT];
+  const int pre_b = u_next / g.Hkv, pre_h = u_next % g.Hkv;
+  load_q(pre_b, pre_h, qf, qsum, qF);
+  qb_issue(pre_b, pre_h);
+  bool first = true, aborted = false;
+  for (;;) {
+    // ---- segment table of the next window (warp 0), then start streaming
+    if (warp == 0) {
+      const int n = build_segments<D>(a, lens, pl, c, lo, hi, u_next, us_next, seg, lane);
+      if (lane == 0) {
+        win_n = n;
+        win_more = us_next < hi && u_next < int64_t(g.B) * g.Hkv;
       }
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-      const float mnew = fmaxf(m_run[nq], mb);
-      const float corr = ex2(m_run[nq] - mnew);  // 0 on the first block
-      m_run[nq] = mnew;
-      if (__any_sync(0xffffffffu, corr != 1.f)) {
-        l_run[nq] *= corr;
-        zeta[nq] *= corr;
+    }
+    __syncthreads();
+    nwin = win_n;
+    const bool more = win_more;
+    is_ = 0;
+    ij = 0;
+    // (with cuts on unit boundaries the first unit listed can follow empty ones)
+    if (nwin > 0 && (!first || seg[0].b != pre_b || seg[0].h != pre_h)) {
+      load_q(seg[0].b, seg[0].h, qf, qsum, qF);
+      if (qb_issued > qb_waited) qb_wait();  // the shared image is rewritten only once landed
+      __syncthreads();
+      qb_issue(seg[0].b, seg[0].h);
+    }
+    first = false;
+    if (wt == 0)
+      for (int i = 0; i < C::NSTW; ++i) issue_next();
+
+    for (int sg = 0; sg < nwin; ++sg) {
+      const SegD& sd = seg[sg];
+      const int b = sd.b, h = sd.h;
+      const int head0 = h * Gh;  // first query head of this kv head
+      const int64_t bh = int64_t(b) * g.Hkv + h;
+      if (!more && sg == nwin - 1) pdl_trigger();
+      if (sg > 0) load_q(b, h, qf, qsum, qF);  // the shared image of this unit was issued at the previous segment's end
+
+      // bf16 fragments for BF16 blocks (shared by the teams): n-tile 2nq holds
+      // (hi, mid) and n-tile 2nq+1 holds (lo, 0) of each head's three-way split
+      const uint32_t* qbf = reinterpret_cast<const uint32_t*>(smem + C::OFF_QBF) + wt * 8 * C::NQB * 64;
+      qb_wait();
+      asm volatile("bar.sync 14, %0;" ::"r"(32 * kNCW) : "memory");  // shared bf16 fragments landed
+      if (abort_flag) {
+        aborted = true;
+        break;
+      }
+
+      float o[8][NQT][4];
+      float m_run[NQT], l_run[NQT], zeta[NQT];
+#pragma unroll
+      for (int nq = 0; nq < NQT; ++nq) {
+        m_run[nq] = -INFINITY; l_run[nq] = 0.f; zeta[nq] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[mt][nq][e] *= corr;
+          for (int e = 0; e < 4; ++e) o[mt][nq][e] = 0.f;
       }
-#pragma unroll
-      for (int mt = 0; mt < MT_MAX; ++mt) {
-        if (mt < nmt) {
-          p[mt][nq][0] = ex2(s[mt][nq][0] - mnew);
-          p[mt][nq][1] = ex2(s[mt][nq][1] - mnew);
-          l_run[nq] += p[mt][nq][0] + p[mt][nq][1];
-        }
-      }
-    }
 
-    // ---- P.V
-    if (is_i2) {
-      const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + kI2Tok * C::ROWB);
+      float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+      int xbuf = 0;
+
+      // INT2 P.V takes V codes from unpack16_v: the code of output row r arrives
+      // as code * 2^e(r), e(r) = unpack_v_exp(p) with p = 2 * (mtd % 4) for rows gq
+      // and 2 * (mtd % 4) + 1 for rows gq + 8.  While INT2 blocks are consumed, row
+      // r of o holds (real value) * 2^e(r); it is converted by exact powers of two
+      // at a switch between INT2 and BF16 blocks and at the end.
+      bool o_i2 = false;
+      auto scale_o = [&](int sign) {  // o *= 2^(sign * e(r)) per row
 #pragma unroll
-      for (int ks = 0; ks < MT_MAX; ++ks) {
-        uint32_t bw0[NQT], bw1[NQT];
-        // V scale/zero of this lane's two tokens (group wt)
-        const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB) + kI2Tok * C::Dg;
-        const int t0 = 16 * ks + gq, t1 = t0 + 8;
-        const uint32_t z0 = vsz[(tb + t0) * C::Dg + wt], z1 = vsz[(tb + t1) * C::Dg + wt];
-        const float vs0 = __half2float(__ushort_as_half(z0 & 0xffff));
-        const float vz0 = __half2float(__ushort_as_half(z0 >> 16));
-        const float vs1 = __half2float(__ushort_as_half(z1 & 0xffff));
-        const float vz1 = __half2float(__ushort_as_half(z1 >> 16));
-        const bool v0 = t0 < cnt, v1 = t1 < cnt;
+        for (int mt = 0; mt < 8; ++mt) {
+          const float f0 = pow2f(sign * unpack_v_exp(2 * (mt & 3)));
+          const float f1 = pow2f(sign * unpack_v_exp(2 * (mt & 3) + 1));
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            o[mt][nq][0] *= f0; o[mt][nq][1] *= f0;
+            o[mt][nq][2] *= f1; o[mt][nq][3] *= f1;
+          }
+        }
+      };
+
+
+      const int nb = sd.ke - sd.kb;
+      const int nmine = nb > team ? (nb - team + C::NTEAMS - 1) / C::NTEAMS : 0;  // this team's blocks
+      for (int j = 0; j < nmine; ++j) {
+        const int stage = my_stage(consumed);
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (consumed / C::NSTW) & 1);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // the warps of a team must take the same decision: they meet at team barriers below
+        if constexpr (C::TS > 1) ok = team_all(ok, 1 + team, 32 * C::TS);
+        if (!ok) {
+          if (lane == 0) { abort_flag = 1; status_or(a.status, OSCAR_DEV_TIMEOUT); }
+          break;
+        }
+        const Blk bk = block_of(sd, sd.kb + team + j * C::NTEAMS);
+        const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
+        const bool is_i2 = bk.type == 1;
+        if (is_i2 != o_i2) {
+          scale_o(is_i2 ? 1 : -1);
+          o_i2 = is_i2;
+        }
+        constexpr int MT_MAX = kSub / 16;
+        const int nmt = is_i2 ? MT_MAX : 1;
+        const int nsub = is_i2 ? (bk.count + kSub - 1) / kSub : 1;
+        for (int sbk = 0; sbk < nsub; ++sbk) {
+        const int cnt = is_i2 ? min(kSub, bk.count - sbk * kSub) : bk.count;  // tokens in this sub-block
+        const int tb = sbk * kSub;  // its first token within the stage
+
+        // ---- scores: s[mt][nq][0] token 16mt+gq, [1] token 16mt+gq+8
+        float s[MT_MAX][NQT][2];
+        float ksc[MT_MAX][2], kze[MT_MAX][2];
+        if (is_i2) {
+          const uint8_t* kc = st;
+          const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB);
+          // m-tiles are processed in groups whose MMAs interleave (independent
+          // accumulators), so the k-step chain of one m-tile never runs alone
+          constexpr int MG = NQT == 1 ? 4 : 2;
+#pragma unroll
+          for (int m0 = 0; m0 < MT_MAX; m0 += MG) {
+            uint2 w[MG][2];
+#pragma unroll
+            for (int i = 0; i < MG; ++i) {
+              const int t0 = 16 * (m0 + i) + gq;
+              w[i][0] = *reinterpret_cast<const uint2*>(kc + (tb + t0) * C::ROWB + wt * 32 + cq * 8);
+              w[i][1] = *reinterpret_cast<const uint2*>(kc + (tb + t0 + 8) * C::ROWB + wt * 32 + cq * 8);
+            }
+            float acc[MG][NQT][4];
+#pragma unroll
+            for (int i = 0; i < MG; ++i)
+#pragma unroll
+              for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][nq][e] = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 2; ++wi) {
+              uint32_t r[MG][2][8];
+#pragma unroll
+              for (int i = 0; i < MG; ++i) {
+                unpack16(wi ? w[i][0].y : w[i][0].x, r[i][0]);
+                unpack16(wi ? w[i][1].y : w[i][1].x, r[i][1]);
+              }
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = 4 * wi + k4;
+#pragma unroll
+                for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+                  for (int i = 0; i < MG; ++i)
+                    mma_f16(acc[i][nq], r[i][0][2 * k4], r[i][1][2 * k4], r[i][0][2 * k4 + 1], r[i][1][2 * k4 + 1],
+                            qf[kk][nq][0], qf[kk][nq][1]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < MG; ++i) {
+              const int mt = m0 + i;
+              const int t0 = 16 * mt + gq, t1 = t0 + 8;
+              const uint32_t z0 = ksz[(tb + t0) * C::Dg + wt], z1 = ksz[(tb + t1) * C::Dg + wt];
+              ksc[mt][0] = __half2float(__ushort_as_half(z0 & 0xffff));
+              kze[mt][0] = __half2float(__ushort_as_half(z0 >> 16));
+              ksc[mt][1] = __half2float(__ushort_as_half(z1 & 0xffff));
+              kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
+#pragma unroll
+              for (int nq = 0; nq < NQT; ++nq) {
+                s[mt][nq][0] = fmaf(ksc[mt][0], (acc[i][nq][0] + acc[i][nq][1]) * qF[nq], kze[mt][0] * qsum[nq]);
+                s[mt][nq][1] = fmaf(ksc[mt][1], (acc[i][nq][2] + acc[i][nq][3]) * qF[nq], kze[mt][1] * qsum[nq]);
+              }
+            }
+          }
+        } else {
+          const uint32_t kb_s = smem_u32(st);
+          float acc[C::NQB][4];
+#pragma unroll
+          for (int nb = 0; nb < C::NQB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+          const int mi = lane >> 3;
+          const int tok = (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int dim = wt * kGroup + 16 * kk + 8 * (mi >> 1);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(kb_s + (dim >> 6) * C::BOX_BYTES + tok * 128 + ((((dim & 63) >> 3) ^ (tok & 7)) << 4), a0, a1,
+                        a2, a3);
+#pragma unroll
+            for (int nb = 0; nb < C::NQB; ++nb) {
+              const uint32_t b0 = qbf[(kk * C::NQB + nb) * 64 + lane];
+              const uint32_t b1 = qbf[(kk * C::NQB + nb) * 64 + 32 + lane];
+              mma_bf16(acc[nb], a0, a1, a2, a3, b0, b1);
+            }
+          }
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            s[0][nq][0] = acc[2 * nq][0] + acc[2 * nq][1] + acc[2 * nq + 1][0];
+            s[0][nq][1] = acc[2 * nq][2] + acc[2 * nq][3] + acc[2 * nq + 1][2];
+          }
+        }
+
+        // ---- team exchange of partial scores (one quant group per warp)
+        if constexpr (C::TS > 1) {
+          float* xb = xch + ((team * 2 + xbuf) * C::TS) * kSub * C::HEADS;
+#pragma unroll
+          for (int mt = 0; mt < MT_MAX; ++mt) {
+            if (mt < nmt) {
+#pragma unroll
+              for (int nq = 0; nq < NQT; ++nq) {
+                const int hs = 4 * nq + cq;
+                xb[(wt * kSub + 16 * mt + gq) * C::HEADS + hs] = s[mt][nq][0];
+                xb[(wt * kSub + 16 * mt + gq + 8) * C::HEADS + hs] = s[mt][nq][1];
+              }
+            }
+          }
+          asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * C::TS) : "memory");
+#pragma unroll
+          for (int mt = 0; mt < MT_MAX; ++mt) {
+            if (mt < nmt) {
+#pragma unroll
+              for (int nq = 0; nq < NQT; ++nq) {
+                const int hs = 4 * nq + cq;
+                float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::TS; ++w) {
+                  t0 += xb[(w * kSub + 16 * mt + gq) * C::HEADS + hs];
+                  t1 += xb[(w * kSub + 16 * mt + gq + 8) * C::HEADS + hs];
+                }
+                s[mt][nq][0] = t0;
+                s[mt][nq][1] = t1;
+              }
+            }
+          }
+          xbuf ^= 1;
+        }
+
+        // ---- online softmax (log2 units)
+        float p[MT_MAX][NQT][2];
 #pragma unroll
         for (int nq = 0; nq < NQT; ++nq) {
-          const float w0 = v0 ? p[ks][nq][0] * vs0 : 0.f;
-          const float w1 = v1 ? p[ks][nq][1] * vs1 : 0.f;
-          zeta[nq] += (v0 ? p[ks][nq][0] * vz0 : 0.f) + (v1 ? p[ks][nq][1] * vz1 : 0.f);
-          bw0[nq] = movmatrix_trans(split_f16(w0));
-          bw1[nq] = movmatrix_trans(split_f16(w1));
-        }
-        // codes of word (wt, gq) for tokens 2cq, 2cq+1, 2cq+8, 2cq+9 of this k-step
-        const int ta = 16 * ks + 2 * cq;
-        const uint32_t wa = vc[(tb + ta + 0) * (C::ROWB / 4) + wt * 8 + gq];
-        const uint32_t wb = vc[(tb + ta + 1) * (C::ROWB / 4) + wt * 8 + gq];
-        const uint32_t wc = vc[(tb + ta + 8) * (C::ROWB / 4) + wt * 8 + gq];
-        const uint32_t wd = vc[(tb + ta + 9) * (C::ROWB / 4) + wt * 8 + gq];
+          float mb = -INFINITY;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t rx[8], ry[8];
-          unpack16_v(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
-          unpack16_v(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+          for (int mt = 0; mt < MT_MAX; ++mt) {
+            if (mt < nmt) {
 #pragma unroll
-          for (int m4 = 0; m4 < 4; ++m4) {
-            const int mtd = 4 * hh + m4;
+              for (int e = 0; e < 2; ++e) {
+                const int tk = 16 * mt + gq + 8 * e;
+                const float v = tk < cnt ? s[mt][nq][e] : -INFINITY;
+                s[mt][nq][e] = v;
+                mb = fmaxf(mb, v);
+              }
+            }
+          }
+          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+          const float mnew = fmaxf(m_run[nq], mb);
+          const float corr = ex2(m_run[nq] - mnew);  // 0 on the first block
+          m_run[nq] = mnew;
+          if (__any_sync(0xffffffffu, corr != 1.f)) {
+            l_run[nq] *= corr;
+            zeta[nq] *= corr;
 #pragma unroll
-            for (int nq = 0; nq < NQT; ++nq)
-              mma_f16(o[mtd][nq], rx[2 * m4], rx[2 * m4 + 1], ry[2 * m4], ry[2 * m4 + 1], bw0[nq], bw1[nq]);
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) o[mt][nq][e] *= corr;
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT_MAX; ++mt) {
+            if (mt < nmt) {
+              p[mt][nq][0] = ex2(s[mt][nq][0] - mnew);
+              p[mt][nq][1] = ex2(s[mt][nq][1] - mnew);
+              l_run[nq] += p[mt][nq][0] + p[mt][nq][1];
+            }
           }
         }
+
+        // ---- P.V
+        if (is_i2) {
+          const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + kI2Tok * C::ROWB);
+#pragma unroll
+          for (int ks = 0; ks < MT_MAX; ++ks) {
+            uint32_t bw0[NQT], bw1[NQT];
+            // V scale/zero of this lane's two tokens (group wt)
+            const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB) + kI2Tok * C::Dg;
+            const int t0 = 16 * ks + gq, t1 = t0 + 8;
+            const uint32_t z0 = vsz[(tb + t0) * C::Dg + wt], z1 = vsz[(tb + t1) * C::Dg + wt];
+            const float vs0 = __half2float(__ushort_as_half(z0 & 0xffff));
+            const float vz0 = __half2float(__ushort_as_half(z0 >> 16));
+            const float vs1 = __half2float(__ushort_as_half(z1 & 0xffff));
+            const float vz1 = __half2float(__ushort_as_half(z1 >> 16));
+            const bool v0 = t0 < cnt, v1 = t1 < cnt;
+#pragma unroll
+            for (int nq = 0; nq < NQT; ++nq) {
+              const float w0 = v0 ? p[ks][nq][0] * vs0 : 0.f;
+              const float w1 = v1 ? p[ks][nq][1] * vs1 : 0.f;
+              zeta[nq] += (v0 ? p[ks][nq][0] * vz0 : 0.f) + (v1 ? p[ks][nq][1] * vz1 : 0.f);
+              bw0[nq] = movmatrix_trans(split_f16(w0));
+              bw1[nq] = movmatrix_trans(split_f16(w1));
+            }
+            // codes of word (wt, gq) for tokens 2cq, 2cq+1, 2cq+8, 2cq+9 of this k-step
+            const int ta = 16 * ks + 2 * cq;
+            const uint32_t wa = vc[(tb + ta + 0) * (C::ROWB / 4) + wt * 8 + gq];
+            const uint32_t wb = vc[(tb + ta + 1) * (C::ROWB / 4) + wt * 8 + gq];
+            const uint32_t wc = vc[(tb + ta + 8) * (C::ROWB / 4) + wt * 8 + gq];
+            const uint32_t wd = vc[(tb + ta + 9) * (C::ROWB / 4) + wt * 8 + gq];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t rx[8], ry[8];
+              unpack16_v(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
+              unpack16_v(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+#pragma unroll
+              for (int m4 = 0; m4 < 4; ++m4) {
+                const int mtd = 4 * hh + m4;
+#pragma unroll
+                for (int nq = 0; nq < NQT; ++nq)
+                  mma_f16(o[mtd][nq], rx[2 * m4], rx[2 * m4 + 1], ry[2 * m4], ry[2 * m4 + 1], bw0[nq], bw1[nq]);
+              }
+            }
+          }
+        } else {
+          uint32_t bw0[NQT], bw1[NQT];
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            bw0[nq] = movmatrix_trans(split_bf16(p[0][nq][0]));
+            bw1[nq] = movmatrix_trans(split_bf16(p[0][nq][1]));
+          }
+          const uint32_t vb_s = smem_u32(st + C::BOXES * C::BOX_BYTES);
+          const int mi = lane >> 3;
+          const int tok = (lane & 7) + 8 * (mi >> 1);
+          const bool partial = cnt < kBfTok;
+          // tokens held by this lane's A fragment halves
+          const bool va = 2 * cq < cnt, vb = 2 * cq + 1 < cnt;
+          const bool vc8 = 2 * cq + 8 < cnt, vd = 2 * cq + 9 < cnt;
+          const uint32_t mask01 = (va ? 0xffffu : 0u) | (vb ? 0xffff0000u : 0u);
+          const uint32_t mask89 = (vc8 ? 0xffffu : 0u) | (vd ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int mtd = 0; mtd < 8; ++mtd) {
+            const int dim = wt * kGroup + 16 * mtd + 8 * (mi & 1);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(vb_s + (dim >> 6) * C::BOX_BYTES + tok * 128 + ((((dim & 63) >> 3) ^ (tok & 7)) << 4),
+                              a0, a1, a2, a3);
+            if (partial) {
+              a0 &= mask01; a1 &= mask01; a2 &= mask89; a3 &= mask89;
+            }
+#pragma unroll
+            for (int nq = 0; nq < NQT; ++nq) mma_bf16(o[mtd][nq], a0, a1, a2, a3, bw0[nq], bw1[nq]);
+          }
+        }
+        }  // sub-blocks
+
+        // every warp of the team is done with this stage: refill it
+        if constexpr (C::TS > 1) {
+          asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * C::TS) : "memory");
+        } else {
+          __syncwarp();
+        }
+        ++consumed;
+        if (wt == 0) issue_next();
       }
-    } else {
-      uint32_t bw0[NQT], bw1[NQT];
+      if (o_i2) scale_o(-1);
+      // ---- team partials -> shared memory
 #pragma unroll
       for (int nq = 0; nq < NQT; ++nq) {
-        bw0[nq] = movmatrix_trans(split_bf16(p[0][nq][0]));
-        bw1[nq] = movmatrix_trans(split_bf16(p[0][nq][1]));
-      }
-      const uint32_t vb_s = smem_u32(st + C::BOXES * C::BOX_BYTES);
-      const int mi = lane >> 3;
-      const int tok = (lane & 7) + 8 * (mi >> 1);
-      const bool partial = cnt < kBfTok;
-      // tokens held by this lane's A fragment halves
-      const bool va = 2 * cq < cnt, vb = 2 * cq + 1 < cnt;
-      const bool vc8 = 2 * cq + 8 < cnt, vd = 2 * cq + 9 < cnt;
-      const uint32_t mask01 = (va ? 0xffffu : 0u) | (vb ? 0xffff0000u : 0u);
-      const uint32_t mask89 = (vc8 ? 0xffffu : 0u) | (vd ? 0xffff0000u : 0u);
 #pragma unroll
-      for (int mtd = 0; mtd < 8; ++mtd) {
-        const int dim = wt * kGroup + 16 * mtd + 8 * (mi & 1);
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(vb_s + (dim >> 6) * C::BOX_BYTES + tok * 128 + ((((dim & 63) >> 3) ^ (tok & 7)) << 4),
-                          a0, a1, a2, a3);
-        if (partial) {
-          a0 &= mask01; a1 &= mask01; a2 &= mask89; a3 &= mask89;
+        for (int off = 4; off < 32; off <<= 1) {
+          l_run[nq] += __shfl_xor_sync(0xffffffffu, l_run[nq], off);
+          zeta[nq] += __shfl_xor_sync(0xffffffffu, zeta[nq], off);
         }
-#pragma unroll
-        for (int nq = 0; nq < NQT; ++nq) mma_bf16(o[mtd][nq], a0, a1, a2, a3, bw0[nq], bw1[nq]);
       }
-    }
-    }  // sub-blocks
-
-    // every warp of the team is done with this stage: refill it
-    if constexpr (C::TS > 1) {
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * C::TS) : "memory");
-    } else {
-      __syncwarp();
-    }
-    if (wt == 0 && issued < nmine) {
-      issue_block(team + issued * C::NTEAMS, my_stage(issued));
-      ++issued;
-    }
-  }
-  if (o_i2) scale_o(-1);
-  // after an early exit, wait (bounded) for copies still landing in our stages
-  if (wt == 0 && lane == 0) {
-    const int consumed = *((volatile int*)&abort_flag) ? 0 : nmine;
-    for (int jj = (issued > C::NSTW ? issued - C::NSTW : 0); jj < issued; ++jj)
-      if (jj >= consumed && !mbar_wait(smem_u32(&bars[my_stage(jj)]), (jj / C::NSTW) & 1)) break;
-  }
-
-  // ---- team partials -> shared memory
+      float* part = reinterpret_cast<float*>(smem + C::OFF_PART);  // [team][head][D + 2]
 #pragma unroll
-  for (int nq = 0; nq < NQT; ++nq) {
+      for (int nq = 0; nq < NQT; ++nq) {
+        const int hs = 4 * nq + cq;
+        float* ph = part + (team * C::HEADS + hs) * (D + 2);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l_run[nq] += __shfl_xor_sync(0xffffffffu, l_run[nq], off);
-      zeta[nq] += __shfl_xor_sync(0xffffffffu, zeta[nq], off);
-    }
-  }
-  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);  // [team][head][D + 2]
-#pragma unroll
-  for (int nq = 0; nq < NQT; ++nq) {
-    const int hs = 4 * nq + cq;
-    float* ph = part + (team * C::HEADS + hs) * (D + 2);
-#pragma unroll
-    for (int mtd = 0; mtd < 8; ++mtd) {
-      const int d0 = wt * kGroup + 16 * mtd + gq;
-      ph[d0] = o[mtd][nq][0] + o[mtd][nq][1] + zeta[nq];
-      ph[d0 + 8] = o[mtd][nq][2] + o[mtd][nq][3] + zeta[nq];
-    }
-    if (wt == 0 && gq == 0) {
-      ph[D] = m_run[nq];
-      ph[D + 1] = l_run[nq];
-    }
-  }
-  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
-  pdl_trigger();
-
-  // ---- merge the teams of this CTA and write the split partial
-  for (int idx = threadIdx.x; idx < Gh * D; idx += 32 * kNCW) {
-    const int hs = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < C::NTEAMS; ++t) M = fmaxf(M, part[(t * C::HEADS + hs) * (D + 2) + D]);
-    float acc = 0.f, L = 0.f;
-#pragma unroll
-    for (int t = 0; t < C::NTEAMS; ++t) {
-      const float* ph = part + (t * C::HEADS + hs) * (D + 2);
-      const float w = M == -INFINITY ? 0.f : ex2(ph[D] - M);
-      acc += w * ph[d];
-      L += w * ph[D + 1];
-    }
-    const int64_t pi = (int64_t(b) * g.Hq + head0 + hs) * a.ns + split;
-    a.ws_acc[pi * D + d] = acc;
-    if (d == 0) {
-      a.ws_ml[pi * 2 + 0] = M;
-      a.ws_ml[pi * 2 + 1] = L;
-    }
-  }
-
-  // ---- the last CTA of this (b, kv head) to finish merges all splits (a ticket,
-  // no waiting on other CTAs), un-rotates V and stores the output
-  __shared__ int is_last;
-  __threadfence();
-  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
-  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket + bh, 1) == a.ns - 1;
-  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
-  if (!is_last) return;
-  __threadfence();
-  // D = 128: prefetch R_V (64 KB) into the now idle stage area with one bulk copy
-  constexpr bool kRvSmem = D == 128 && !(C::NST * C::STAGE < D * D * 4);
-  const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
-  const uint32_t rv_bar = smem_u32(&bars[C::NST]);
-  if constexpr (kRvSmem) {
-    if (threadIdx.x == 0 && !a.absorb_v) {
-      mbar_arrive_expect_tx(rv_bar, D * D * 4);
-      bulk_g2s(smem_u32(smem + C::OFF_STAGE), a.R_V, D * D * 4, rv_bar);
-    }
-  }
-  float* ob = part;                    // [G][D] merged o' (rotated basis)
-  float* Ms = part + C::HEADS * D;     // [G] max, [G] sum
-  float* Ls = Ms + C::HEADS;
-  float* wts = Ls + C::HEADS;          // [G][splits] normalised split weights
-  for (int i = warp; i < Gh; i += kNCW) {
-    const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
-    const float m0 = lane < a.ns ? __ldcg(a.ws_ml + (base + lane) * 2) : -INFINITY;
-    const float l0 = lane < a.ns ? __ldcg(a.ws_ml + (base + lane) * 2 + 1) : 0.f;
-    const float m1 = lane + 32 < a.ns ? __ldcg(a.ws_ml + (base + lane + 32) * 2) : -INFINITY;
-    const float l1 = lane + 32 < a.ns ? __ldcg(a.ws_ml + (base + lane + 32) * 2 + 1) : 0.f;
-    float M = fmaxf(m0, m1);
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-    const float e0 = M == -INFINITY || m0 == -INFINITY ? 0.f : ex2(m0 - M);
-    const float e1 = M == -INFINITY || m1 == -INFINITY ? 0.f : ex2(m1 - M);
-    float L = e0 * l0 + e1 * l1;
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    if (lane < a.ns) wts[i * OSCAR_KV_MAX_SPLITS + lane] = e0 * inv;
-    if (lane + 32 < a.ns) wts[i * OSCAR_KV_MAX_SPLITS + lane + 32] = e1 * inv;
-    if (lane == 0) {
-      Ms[i] = M;
-      Ls[i] = L;
-    }
-  }
-  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
-  for (int idx = threadIdx.x; idx < Gh * D; idx += 32 * kNCW) {
-    const int i = idx / D, d = idx % D;
-    const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
-    const float* wi = wts + i * OSCAR_KV_MAX_SPLITS;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int sp = 0; sp < a.ns; ++sp) acc = fmaf(wi[sp], __ldcg(a.ws_acc + (base + sp) * D + d), acc);
-    ob[idx] = acc;
-  }
-  asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
-  bool rv_ok = true;
-  if constexpr (kRvSmem) {
-    if (!a.absorb_v) rv_ok = mbar_wait(rv_bar, 0);
-    if (!rv_ok && threadIdx.x == 0) status_or(a.status, OSCAR_DEV_TIMEOUT);
-  }
-  // o = o' R_V^T: o[r] = sum_j R_V[r][j] o'[j]; one thread per output channel r
-  for (int r = threadIdx.x; r < D; r += 32 * kNCW) {
-    float res[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) res[i] = 0.f;
-    if (a.absorb_v) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < Gh) res[i] = ob[i * D + r];
-    } else if (kRvSmem && rv_ok) {
-      // skewed walk over j: thread r touches bank (r + jj) % 32, no conflicts
-#pragma unroll 4
-      for (int jj = 0; jj < D; ++jj) {
-        const int j = (jj + r) & (D - 1);
-        const float rv = rvs[r * D + j];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < Gh) res[i] = fmaf(rv, ob[i * D + j], res[i]);
+        for (int mtd = 0; mtd < 8; ++mtd) {
+          const int d0 = wt * kGroup + 16 * mtd + gq;
+          ph[d0] = o[mtd][nq][0] + o[mtd][nq][1] + zeta[nq];
+          ph[d0 + 8] = o[mtd][nq][2] + o[mtd][nq][3] + zeta[nq];
+        }
+        if (wt == 0 && gq == 0) {
+          ph[D] = m_run[nq];
+          ph[D + 1] = l_run[nq];
+        }
       }
-    } else {
-      const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);
-#pragma unroll 8
-      for (int j4 = 0; j4 < D / 4; ++j4) {
-        const float4 rv = __ldg(rv4 + j4);
+      asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+      if (abort_flag) {
+        aborted = true;
+        break;
+      }
+
+      // ---- merge the teams of this CTA and write the segment's partial
+      for (int idx = threadIdx.x; idx < Gh * D; idx += 32 * kNCW) {
+        const int hs = idx / D, d = idx % D;
+        float M = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i < Gh) {
-            const float* oi = ob + i * D + 4 * j4;
-            res[i] = fmaf(rv.x, oi[0], fmaf(rv.y, oi[1], fmaf(rv.z, oi[2], fmaf(rv.w, oi[3], res[i]))));
+        for (int t = 0; t < C::NTEAMS; ++t) M = fmaxf(M, part[(t * C::HEADS + hs) * (D + 2) + D]);
+        float acc = 0.f, L = 0.f;
+#pragma unroll
+        for (int t = 0; t < C::NTEAMS; ++t) {
+          const float* ph = part + (t * C::HEADS + hs) * (D + 2);
+          const float w = M == -INFINITY ? 0.f : ex2(ph[D] - M);
+          acc += w * ph[d];
+          L += w * ph[D + 1];
+        }
+        const int64_t pi = (int64_t(b) * g.Hq + head0 + hs) * a.ns + sd.slot;
+        a.ws_acc[pi * D + d] = acc;
+        if (d == 0) {
+          a.ws_ml[pi * 2 + 0] = M;
+          a.ws_ml[pi * 2 + 1] = L;
+        }
+      }
+
+      // ---- the last CTA of this unit to finish merges its slots (a ticket, no
+      // waiting on other CTAs), un-rotates V and stores the output
+      __threadfence();
+      asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+      if (threadIdx.x == 0) is_last = atomicAdd(a.ticket + bh, 1) == sd.nseg - 1;
+      asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+      if (is_last) {
+        __threadfence();
+        const int nseg = sd.nseg;
+        // R_V: in the CTA's last segment no copy is in flight, so at D = 128 it
+        // comes into the idle stage area with one bulk copy, landing while the
+        // slots are merged; otherwise its rows are read through L2
+        const bool rv_smem = D == 128 && !a.absorb_v && !more && sg == nwin - 1 &&
+                             C::NST * C::STAGE >= D * D * 4;
+        const uint32_t rv_bar = smem_u32(&bars[C::NST]);
+        if (rv_smem && threadIdx.x == 0) {
+          mbar_arrive_expect_tx(rv_bar, D * D * 4);
+          bulk_g2s(smem_u32(smem + C::OFF_STAGE), a.R_V, D * D * 4, rv_bar);
+        }
+        float* ob = part;                    // [G][D] merged o' (rotated basis)
+        float* Ms = part + C::HEADS * D;     // [G] max, [G] sum
+        float* Ls = Ms + C::HEADS;
+        float* wts = Ls + C::HEADS;          // [G][splits] normalised split weights
+        for (int i = warp; i < Gh; i += kNCW) {
+          const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
+          const float m0 = lane < nseg ? __ldcg(a.ws_ml + (base + lane) * 2) : -INFINITY;
+          const float l0 = lane < nseg ? __ldcg(a.ws_ml + (base + lane) * 2 + 1) : 0.f;
+          const float m1 = lane + 32 < nseg ? __ldcg(a.ws_ml + (base + lane + 32) * 2) : -INFINITY;
+          const float l1 = lane + 32 < nseg ? __ldcg(a.ws_ml + (base + lane + 32) * 2 + 1) : 0.f;
+          float M = fmaxf(m0, m1);
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+          const float e0 = M == -INFINITY || m0 == -INFINITY ? 0.f : ex2(m0 - M);
+          const float e1 = M == -INFINITY || m1 == -INFINITY ? 0.f : ex2(m1 - M);
+          float L = e0 * l0 + e1 * l1;
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          if (lane < nseg) wts[i * OSCAR_KV_MAX_SPLITS + lane] = e0 * inv;
+          if (lane + 32 < nseg) wts[i * OSCAR_KV_MAX_SPLITS + lane + 32] = e1 * inv;
+          if (lane == 0) {
+            Ms[i] = M;
+            Ls[i] = L;
           }
         }
-      }
-    }
+        asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+        {
+          // (head, channel) pairs idx = threadIdx.x + kThreads * e: every slot
+          // load of a thread is issued before any is used
+          constexpr int IPT = C::HEADS * D / kThreads;
+          float acc[IPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < Gh) {
-        const int64_t oi = (int64_t(b) * g.Hq + head0 + i) * D + r;
-        if (a.out_fp32)
-          static_cast<float*>(a.out)[oi] = res[i];
-        else
-          static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(res[i]);
+          for (int e = 0; e < IPT; ++e) acc[e] = 0.f;
+#pragma unroll 2
+          for (int sp = 0; sp < nseg; ++sp) {
+#pragma unroll
+            for (int e = 0; e < IPT; ++e) {
+              const int idx = threadIdx.x + kThreads * e, i = idx / D, d = idx % D;
+              if (i < Gh) {
+                const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
+                acc[e] = fmaf(wts[i * OSCAR_KV_MAX_SPLITS + sp], __ldcg(a.ws_acc + (base + sp) * D + d), acc[e]);
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < IPT; ++e) {
+            const int idx = threadIdx.x + kThreads * e;
+            if (idx / D < Gh) ob[idx] = acc[e];
+          }
+        }
+        asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+        bool rv_ok = true;
+        if (rv_smem) {
+          rv_ok = mbar_wait(rv_bar, 0);
+          if (!rv_ok && threadIdx.x == 0) status_or(a.status, OSCAR_DEV_TIMEOUT);
+        }
+        auto store = [&](int i, int r, float v) {
+          const int64_t oi = (int64_t(b) * g.Hq + head0 + i) * D + r;
+          if (a.out_fp32)
+            static_cast<float*>(a.out)[oi] = v;
+          else
+            static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(v);
+        };
+        if (a.absorb_v || (rv_smem && rv_ok)) {
+          // o = o' R_V^T (or o' when absorbed): one thread per output channel r
+          const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
+          for (int r = threadIdx.x; r < D; r += 32 * kNCW) {
+            float res[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) res[i] = 0.f;
+            if (a.absorb_v) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (i < Gh) res[i] = ob[i * D + r];
+            } else {
+              // skewed walk over j: thread r touches bank (r + jj) % 32, no conflicts
+#pragma unroll 4
+              for (int jj = 0; jj < D; ++jj) {
+                const int j = (jj + r) & (D - 1);
+                const float rv = rvs[r * D + j];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  if (i < Gh) res[i] = fmaf(rv, ob[i * D + j], res[i]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i < Gh) store(i, r, res[i]);
+          }
+        } else {
+          // rows of R_V from L2: warp w takes rows w, w + 4, ...; lane l reads
+          // columns 4l .. 4l + 3 (+ 128 per step), so every load is coalesced
+#pragma unroll 4
+          for (int r = warp; r < D; r += kNCW) {
+            const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);
+            float res[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) res[i] = 0.f;
+#pragma unroll
+            for (int j4 = lane; j4 < D / 4; j4 += 32) {
+              const float4 rv = __ldg(rv4 + j4);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (i < Gh) {
+                  const float4 ov = reinterpret_cast<const float4*>(ob + i * D)[j4];
+                  res[i] = fmaf(rv.x, ov.x, fmaf(rv.y, ov.y, fmaf(rv.z, ov.z, fmaf(rv.w, ov.w, res[i]))));
+                }
+              }
+            }
+            float mine = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (i < Gh) {
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) res[i] += __shfl_xor_sync(0xffffffffu, res[i], o2);
+                if (lane == i) mine = res[i];
+              }
+            }
+            if (lane < Gh) store(lane, r, mine);
+          }
+        }
+        if (threadIdx.x < Gh && a.lse) {
+          const int i = threadIdx.x;
+          const float M = Ms[i], L = Ls[i];
+          a.lse[int64_t(b) * g.Hq + head0 + i] =
+              (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
+        }
       }
-    }
-  }
-  if (threadIdx.x < Gh) {
-    const int i = threadIdx.x;
-    if (a.lse) {
-      const float M = Ms[i], L = Ls[i];
-      a.lse[int64_t(b) * g.Hq + head0 + i] =
-          (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2f(L)) * 0.6931471805599453f;
-    }
-    if (i == 0 && h == 0) {
-      if (a.seq_lens[b] > g.cap) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
-      if (T < 1) status_or(a.status, OSCAR_DEV_EMPTY);
-    }
-  }
+      // part and the shared q' fragments are rewritten by the next segment
+      asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
+      if (sg + 1 < nwin) qb_issue(seg[sg + 1].b, seg[sg + 1].h);
+    }  // segments
+    if (aborted || !more) break;
+    __syncthreads();  // the table is rebuilt for the next window
+  }  // windows
+
+  // after an early exit, wait (bounded) for copies still landing in our stages
+  // and in the shared q' image
+  if (wt == 0 && lane == 0)
+    for (int jj = consumed; jj < issued; ++jj)
+      if (!mbar_wait(smem_u32(&bars[my_stage(jj)]), (jj / C::NSTW) & 1)) break;
+  if (threadIdx.x == 0)
+    for (; qb_waited < qb_issued; ++qb_waited)
+      if (!mbar_wait(qb_bar, qb_waited & 1)) break;
 }
 
 // ---------------------------------------------------------------------------
@@ -959,7 +1362,7 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   if (g.W > 0 && (!encode_rows_bf16(&maps[2], kb + g.sink_bytes, bh * g.W, D, 64, kBfTok) ||
                   !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)))
     return OSCAR_ERR_LAUNCH;
-  if (launch_pdl(split_kernel<D, NQT>, dim3(a.ns, g.Hkv, g.B), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
+  if (launch_pdl(split_kernel<D, NQT>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
                  maps[2], maps[3], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
@@ -971,36 +1374,25 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
 thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns) {
-  const uint64_t bq = uint64_t(g.B) * g.Hq;
-  return align256(bq * g.D * 4) + align256(bq * g.Dg * 4) + align256(bq * ns * g.D * 4) +
-         align256(bq * ns * 2 * 4) + align256(uint64_t(g.B) * g.Hkv * 4);
+  const uint64_t bq = uint64_t(g.B) * g.Hq, units = uint64_t(g.B) * g.Hkv;
+  const uint64_t nqt = g.G > 4 ? 2 : 1;
+  return align256(units * g.Dg * nqt * 2048) + align256(units * g.Dg * nqt * 4096) + align256(bq * g.Dg * 4) +
+         align256(bq * g.Dg * 4) + align256(bq * ns * g.D * 4) + align256(bq * ns * 2 * 4) + align256(units * 4);
 }
 
-int decode_auto_splits(const Geom& g, int seq_len_hint) {
+int decode_grid(const Geom& g, int seq_len_hint, int num_splits) {
+  const int64_t units = int64_t(g.B) * g.Hkv;
+  if (num_splits > 0) return int(std::min<int64_t>(int64_t(num_splits) * units, 1 << 30));
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || dinfo_init(dev) != 0) return -1;
   const DevInfo& di = g_dev[dev];
-  const int occ = di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
-  const int slots = di.sms * occ;
-  const int units = g.B * g.Hkv;
-  // at least ~2 INT2 blocks of work per split
-  const int max_by_len = std::max(1, seq_len_hint / (2 * kI2Tok));
-  // best wave efficiency with at most two waves; a second wave must pay for its
-  // extra start-up and merge work with a clearly better fill
-  int best = 1;
-  double best_eff = -1.0;
-  const int cap = std::min(max_by_len, int(OSCAR_KV_MAX_SPLITS));
-  for (int ns = 1; ns <= cap; ++ns) {
-    const int64_t ctas = int64_t(ns) * units;
-    const int64_t waves = (ctas + slots - 1) / slots;
-    if (waves > 2) break;
-    const double eff = double(ctas) / double(waves * slots) - (waves > 1 ? 0.05 : 0.0);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
-      best = ns;
-    }
-  }
-  return best;
+  // persistent: as many CTAs as are resident at once, each streaming at least
+  // two INT2 blocks per team of the cache a context of seq_len_hint implies
+  const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
+  const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D);
+  const int64_t min_cost = int64_t(2) * (kNCW / g.Dg) * r.ci2;
+  const int64_t by_work = std::max<int64_t>(1, unit_cost(r) * units / min_cost);
+  return int(std::max<int64_t>(1, std::min(resident, by_work)));
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {

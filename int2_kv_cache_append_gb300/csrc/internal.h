@@ -36,12 +36,15 @@ struct DecodeArgs {
   void* out;
   float* lse;
   int32_t* status;
-  float* qprime;   // [B][Hq][D]   scaled rotated query (log2 units)
-  float* qsum;     // [B][Hq][Dg]  per-group sums of qprime
+  uint32_t* qfrag;  // [B*Hkv][Dg][NQT*512]  mma B fragments of q' (fp16 hi/lo, scaled per head)
+  uint32_t* qbfrag; // [B*Hkv][Dg][NQT*1024] bf16 three-way B fragments of q', shared-memory image
+  float* qsum;      // [B][Hq][Dg]  per-group sums of q' (log2 units)
+  float* qF;        // [B][Hq][Dg]  score factor 2^(24 - X) of the scaled fragments
   float* ws_acc;   // [B][Hq][NS][D]
   float* ws_ml;    // [B][Hq][NS][2]
   int32_t* ticket; // [B][Hkv] split-completion counters (zeroed by qrot)
-  int ns;          // context splits per (b, kv head)
+  int ns;          // partial slots per (b, query head) in the workspace
+  int ctas;        // CTAs of the split kernel
   float qscale;    // sm_scale * log2(e)
   int in_fp32, out_fp32, absorb_v;
 };
@@ -55,6 +58,8 @@ int launch_append_tc(const AppendArgs& a, cudaStream_t stream);  // D = 128, bf1
 bool encode_rows_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_cols,
                       uint32_t box_rows);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
-int decode_auto_splits(const Geom& g, int seq_len_hint);
+// CTAs of the split kernel: num_splits * B * Hkv, or (num_splits = 0) as many
+// as are resident at once, fewer when a context of seq_len_hint is short.
+int decode_grid(const Geom& g, int seq_len_hint, int num_splits);
 
 }  // namespace oscar

@@ -115,13 +115,14 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   if (seq_len_hint > cfg->capacity) return OSCAR_ERR_CAPACITY;
   const Geom g = make_geom(cfg);
   const int hint = seq_len_hint > 0 ? seq_len_hint : cfg->capacity;
-  int ns = num_splits;
-  if (ns == 0) {
-    ns = oscar::decode_auto_splits(g, hint);
-    if (ns < 1) return OSCAR_ERR_LAUNCH;
-    while (ns > 1 && oscar::decode_workspace_bytes(g, ns) > workspace_bytes) --ns;
-  }
+  // partial slots per (sequence, query head): as many as the workspace holds,
+  // up to OSCAR_KV_MAX_SPLITS; an explicit split count must fit in full
+  if (num_splits > 0 && oscar::decode_workspace_bytes(g, num_splits) > workspace_bytes) return OSCAR_ERR_WORKSPACE;
+  int ns = OSCAR_KV_MAX_SPLITS;
+  while (ns > 1 && oscar::decode_workspace_bytes(g, ns) > workspace_bytes) --ns;
   if (oscar::decode_workspace_bytes(g, ns) > workspace_bytes) return OSCAR_ERR_WORKSPACE;
+  const int ctas = oscar::decode_grid(g, hint, num_splits);
+  if (ctas < 1) return OSCAR_ERR_LAUNCH;
 
   oscar::DecodeArgs a;
   a.g = g;
@@ -135,9 +136,14 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   a.status = dev_status;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const uint64_t bq = uint64_t(g.B) * g.Hq;
-  a.qprime = reinterpret_cast<float*>(ws);
-  ws += oscar::align256(bq * g.D * 4);
+  const uint64_t units = uint64_t(g.B) * g.Hkv, nqt = g.G > 4 ? 2 : 1;
+  a.qfrag = reinterpret_cast<uint32_t*>(ws);
+  ws += oscar::align256(units * g.Dg * nqt * 2048);
+  a.qbfrag = reinterpret_cast<uint32_t*>(ws);
+  ws += oscar::align256(units * g.Dg * nqt * 4096);
   a.qsum = reinterpret_cast<float*>(ws);
+  ws += oscar::align256(bq * g.Dg * 4);
+  a.qF = reinterpret_cast<float*>(ws);
   ws += oscar::align256(bq * g.Dg * 4);
   a.ws_acc = reinterpret_cast<float*>(ws);
   ws += oscar::align256(bq * uint64_t(ns) * g.D * 4);
@@ -145,6 +151,7 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   ws += oscar::align256(bq * uint64_t(ns) * 2 * 4);
   a.ticket = reinterpret_cast<int32_t*>(ws);
   a.ns = ns;
+  a.ctas = ctas;
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(float(g.D));
   a.qscale = scale * 1.4426950408889634f;
   a.in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;

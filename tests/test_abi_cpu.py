@@ -46,8 +46,10 @@ def test_layout_matches_oracle(lib, shape):
     assert got["max_splits"] == K.MAX_SPLITS
     # documented workspace formula
     a = lambda x: (x + 255) // 256 * 256
-    bq = B * Hq
-    ws = a(bq * D * 4) + a(bq * (D // 128) * 4) + a(bq * 64 * D * 4) + a(bq * 64 * 8) + a(B * Hkv * 4)
+    bq, units, Dg = B * Hq, B * Hkv, D // 128
+    nqt = 2 if Hq // Hkv > 4 else 1
+    ws = (a(units * Dg * nqt * 2048) + a(units * Dg * nqt * 4096) + 2 * a(bq * Dg * 4) + a(bq * 64 * D * 4)
+          + a(bq * 64 * 8) + a(units * 4))
     assert got["decode_workspace_bytes"] == ws
 
 
