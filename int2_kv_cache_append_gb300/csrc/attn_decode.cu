@@ -1218,14 +1218,20 @@ __global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
               for (int i = 0; i < 8; ++i)
                 if (i < Gh) res[i] = ob[i * D + r];
             } else {
-              // skewed walk over j: thread r touches bank (r + jj) % 32, no conflicts
+              // 16-byte loads in a skewed walk over j: thread r reads chunk
+              // (j4 + r) % (D / 4) of row r and of each o' row, so the eight
+              // threads of a quarter warp touch eight different chunks
 #pragma unroll 4
-              for (int jj = 0; jj < D; ++jj) {
-                const int j = (jj + r) & (D - 1);
-                const float rv = rvs[r * D + j];
+              for (int j4 = 0; j4 < D / 4; ++j4) {
+                const int jc = ((j4 + r) & (D / 4 - 1)) * 4;
+                const float4 rv = *reinterpret_cast<const float4*>(rvs + r * D + jc);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  if (i < Gh) res[i] = fmaf(rv, ob[i * D + j], res[i]);
+                for (int i = 0; i < 8; ++i) {
+                  if (i < Gh) {
+                    const float4 ov = *reinterpret_cast<const float4*>(ob + i * D + jc);
+                    res[i] = fmaf(rv.x, ov.x, fmaf(rv.y, ov.y, fmaf(rv.z, ov.z, fmaf(rv.w, ov.w, res[i]))));
+                  }
+                }
               }
             }
 #pragma unroll

@@ -36,8 +36,18 @@ def gpu_append(c: O.Config, cache, layer, k, v, start_pos, RK, RV, want_rot=Fals
     return rot
 
 
+def workspace_bytes(c: O.Config, slots: int) -> int:
+    """attn_decode workspace with `slots` partial slots per query head (the
+    formula documented with kv_layout_query)."""
+    a = lambda x: (x + 255) // 256 * 256
+    bq, units, Dg = c.batch * c.num_q_heads, c.batch * c.num_kv_heads, c.head_dim // 128
+    nqt = 2 if c.num_q_heads // c.num_kv_heads > 4 else 1
+    return (a(units * Dg * nqt * 2048) + a(units * Dg * nqt * 4096) + 2 * a(bq * Dg * 4)
+            + a(bq * slots * c.head_dim * 4) + a(bq * slots * 8) + a(units * 4))
+
+
 def gpu_decode(c: O.Config, cache, layer, q, seq_lens, RK, RV, sm_scale=0.0, num_splits=0, hint=0,
-               status=None, out_fp32=None):
+               status=None, out_fp32=None, ws_bytes=None):
     kc = kcfg(c)
     if out_fp32 is not None:
         kc.flags = (kc.flags & ~K.FLAG_OUT_FP32) | (K.FLAG_OUT_FP32 if out_fp32 else 0)
@@ -48,7 +58,7 @@ def gpu_decode(c: O.Config, cache, layer, q, seq_lens, RK, RV, sm_scale=0.0, num
     out = torch.empty((B, Hq, D), dtype=torch.float32 if kc.flags & K.FLAG_OUT_FP32 else torch.bfloat16,
                       device="cuda")
     lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
-    ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
+    ws = torch.empty(ws_bytes or lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
     K.attn_decode(kc, cache, layer, qt, dev_i32(seq_lens), dev(RK, torch.float32), dev(RV, torch.float32), out,
                   ws, lse=lse, seq_len_hint=hint, sm_scale=sm_scale, num_splits=num_splits, status=status)
     torch.cuda.synchronize()

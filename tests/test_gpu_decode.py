@@ -14,7 +14,7 @@ import torch
 from int2_kv_cache_append_gb300 import oscar_kv as K
 from int2_kv_cache_append_gb300 import synth as S
 from oracle import oscar_oracle as O
-from tests.gpu_helpers import bf16_round64, gpu_decode, rel_l2
+from tests.gpu_helpers import bf16_round64, gpu_decode, rel_l2, workspace_bytes
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
 
@@ -148,3 +148,91 @@ def test_decode_empty_sequence_status():
     assert np.all(o32[1] == 0) and np.all(np.isneginf(lse[1]))
     ref, _ = O.decode(c, cache, 0, q[:1], [10], RK, RV)
     assert np.abs(o32[0] - ref[0]).max() < 5e-3
+
+
+def _check_rows(c, cache, q, lens, RK, RV, **kw):
+    """Decode with the given lengths; non-empty sequences against the oracle,
+    empty ones against their defined output (zeros, lse = -inf, EMPTY flag)."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gc = torch.from_numpy(cache).cuda()
+    o32, lse = gpu_decode(c, gc, 0, q, lens, RK, RV, out_fp32=True, status=st, **kw)
+    ref, ref_lse = O.decode(c, cache, 0, q, [max(1, t) for t in lens], RK, RV)
+    for b, t in enumerate(lens):
+        if t == 0:
+            assert np.all(o32[b] == 0) and np.all(np.isneginf(lse[b]))
+            continue
+        assert np.abs(o32[b] - ref[b]).max() <= 5e-3 and rel_l2(o32[b], ref[b]) <= 2e-4, b
+        assert np.max(np.abs(lse[b] - ref_lse[b]) - 1e-5 * np.abs(ref_lse[b])) <= 1e-4, b
+    assert bool(int(st.item()) & K.DEV_EMPTY) == (0 in lens)
+
+
+def test_decode_ragged_batch_with_empty_and_full_sequences():
+    # the work of all sequences is cut into equal slices: slices cross sequence
+    # boundaries, skip empty sequences and cover one at full capacity
+    cap = 1500
+    c = O.Config(1, 6, 16, 4, 128, 16, 64, cap)
+    lens = [0, 1, 300, cap, 17, 0]
+    cache, q, RK, RV = _build(c, [cap], seed=31)
+    _check_rows(c, cache, q, lens, RK, RV)
+
+
+@pytest.mark.parametrize("slots", [1, 2, 3, 5])
+def test_decode_small_workspace(slots):
+    # fewer than 3 partial slots: slices are cut on unit boundaries; from 3 up
+    # no unit may be shared by more CTAs than there are slots
+    c = O.Config(1, 3, 8, 2, 128, 8, 32, 900)
+    lens = [900, 0, 257]
+    cache, q, RK, RV = _build(c, [900], seed=32 + slots)
+    _check_rows(c, cache, q, lens, RK, RV, ws_bytes=workspace_bytes(c, slots))
+
+
+def test_decode_many_units_per_cta():
+    """Thousands of short sequences: each CTA's slice spans more units than one
+    segment table holds, so the table is rebuilt in windows.  The cache is
+    built on the GPU; the automatic decomposition is compared with one CTA per
+    split (num_splits = 1) and sampled sequences with the oracle."""
+    B, Hq, Hkv, D, S_, W, cap = 16384, 8, 2, 128, 4, 8, 40
+    c = O.Config(1, B, Hq, Hkv, D, S_, W, cap)
+    kc = K.KVConfig(1, B, Hq, Hkv, D, S_, W, cap, 0.96, 0.92)
+    lay = K.layout_query(kc)
+    cache = torch.zeros(lay["total_bytes"], dtype=torch.uint8, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(33)
+    ch = np.array([3, 77])
+    k = S.activations_torch(gen, (B, cap, Hkv, D), ch, dtype=torch.bfloat16)
+    v = S.activations_torch(gen, (B, cap, Hkv, D), ch, dtype=torch.bfloat16)
+    q = S.activations_torch(gen, (B, Hq, D), ch, dtype=torch.bfloat16)
+    rng = np.random.default_rng(33)
+    RK = S.qr_rotation(rng, D).astype(np.float32)
+    RV = S.qr_rotation(rng, D).astype(np.float32)
+    rk, rv = torch.from_numpy(RK).cuda(), torch.from_numpy(RV).cuda()
+    K.kv_append(kc, cache, 0, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"), rk, rv)
+    lens = rng.integers(0, cap + 1, B).astype(np.int32)
+    lens[:4] = [0, 1, cap, 23]
+    seq = torch.from_numpy(lens).cuda()
+    outs = []
+    for ns in (0, 1):
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kc2 = K.KVConfig(1, B, Hq, Hkv, D, S_, W, cap, 0.96, 0.92, K.FLAG_OUT_FP32)
+        K.attn_decode(kc2, cache, 0, q, seq, rk, rv, out, ws, lse=lse, seq_len_hint=cap, num_splits=ns, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == K.DEV_EMPTY
+        outs.append((out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)))
+    # the two decompositions sum in different orders: each must be within the
+    # decode tolerance of the oracle, so they are compared with that tolerance
+    (o0, l0), (o1, l1) = outs
+    assert np.abs(o0 - o1).max() <= 5e-3 and rel_l2(o0, o1) <= 2e-4
+    fin = np.isfinite(l1)
+    assert np.array_equal(np.isfinite(l0), fin)
+    assert np.max(np.abs(l0[fin] - l1[fin]) - 1e-5 * np.abs(l1[fin])) <= 1e-4
+    assert np.all(o0[lens == 0] == 0)
+    for b in [1, 2, 3, int(np.argmax(lens))]:
+        oc = O.Config(1, 1, Hq, Hkv, D, S_, W, cap)
+        ocache = O.new_cache(oc)
+        O.append(oc, ocache, 0, k[b:b + 1].float().cpu().numpy(), v[b:b + 1].float().cpu().numpy(), [0], RK, RV)
+        ref, ref_lse = O.decode(oc, ocache, 0, q[b:b + 1].float().cpu().numpy(), [int(lens[b])], RK, RV)
+        assert np.abs(o0[b] - ref[0]).max() <= 5e-3 and rel_l2(o0[b], ref[0]) <= 2e-4, b
+        assert np.max(np.abs(l0[b] - ref_lse[0]) - 1e-5 * np.abs(ref_lse[0])) <= 1e-4, b
