@@ -1392,11 +1392,13 @@ int decode_grid(const Geom& g, int seq_len_hint, int num_splits) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || dinfo_init(dev) != 0) return -1;
   const DevInfo& di = g_dev[dev];
-  // persistent: as many CTAs as are resident at once, each streaming at least
-  // two INT2 blocks per team of the cache a context of seq_len_hint implies
+  // persistent: as many CTAs as are resident at once; for short contexts
+  // fewer, so that each team still gets about one block of the cache a
+  // context of seq_len_hint implies (a CTA's fixed cost, ~10 us of set-up and
+  // merge, runs in parallel with the others, so small problems spread wide)
   const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
   const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D);
-  const int64_t min_cost = int64_t(2) * (kNCW / g.Dg) * r.ci2;
+  const int64_t min_cost = int64_t(kNCW / g.Dg) * r.cbf;
   const int64_t by_work = std::max<int64_t>(1, unit_cost(r) * units / min_cost);
   return int(std::max<int64_t>(1, std::min(resident, by_work)));
 }
