@@ -51,7 +51,7 @@ constexpr int kThreads = kNCW * 32;
 constexpr int kI2Tok = 128;                // tokens per INT2 block (one set of bulk copies)
 constexpr int kSub = 64;                   // tokens per INT2 compute sub-block
 constexpr int kBfTok = 16;                 // tokens per BF16 block
-constexpr int kMaxSeg = 64;                // segments (units) one window of a CTA's slice lists
+constexpr int kMaxSeg = 48;                // segments (units) one window of a CTA's slice lists
 
 template <int D, int NQT>
 struct DecCfg {
@@ -67,7 +67,7 @@ struct DecCfg {
   // Each team owns NSTW private stages: it issues the bulk copies of its own
   // blocks into them and consumes them in order, so a stage's barrier phases
   // are produced and awaited by one team only.
-  static constexpr int NST = D == 128 ? 8 : (D == 256 ? 6 : 4);
+  static constexpr int NST = 2 * NTEAMS;  // two stages per team: with them two CTAs fit per SM
   static_assert(NST % NTEAMS == 0, "every stage must belong to one team");
   static constexpr int NSTW = NST / NTEAMS;
   static constexpr int HEADS = 4 * NQT;      // head slots per (b, kv head)
@@ -87,7 +87,7 @@ struct DecCfg {
   static constexpr int OFF_SEG = OFF_PART + PART_BYTES;             // segment table of a window
   static constexpr int OFF_BAR = OFF_SEG + kMaxSeg * 64;
   static constexpr int SMEM = OFF_BAR + (NST + 2) * 8 + 16 + 1024;  // + slack to align the base to 1 KB
-  static_assert(SMEM + 4 * 1024 + 64 <= 227 * 1024, "dynamic + static shared memory of one CTA");
+  static_assert(SMEM + 2 * 1024 + 64 <= 227 * 1024, "dynamic + static shared memory of one CTA");
 };
 
 // Per-(b, kv head) region sizes and the block list
@@ -242,7 +242,7 @@ __device__ __forceinline__ int64_t div_floor(int64_t x, int64_t d) {
 
 // clamped context lengths of the first kLenCache sequences, staged in shared
 // memory once per CTA; the rest are read from global memory
-constexpr int kLenCache = 1024;
+constexpr int kLenCache = 512;
 __device__ __forceinline__ int seq_len_at(const DecodeArgs& a, const int* lens, int b) {
   return b < kLenCache ? lens[b] : clamp_seq_len(a, b);
 }
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
 // split kernel
 // ---------------------------------------------------------------------------
 template <int D, int NQT>
-__global__ void __launch_bounds__(kThreads, (D == 128 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, 2)
     split_kernel(const __grid_constant__ CUtensorMap tks, const __grid_constant__ CUtensorMap tvs,
                  const __grid_constant__ CUtensorMap tkr, const __grid_constant__ CUtensorMap tvr,
                  const DecodeArgs a) {
