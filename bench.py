@@ -294,8 +294,8 @@ def ours(args):
     def step(qq=q, kk=k1, vv=v1, oo=out):
         for layer in range(L):
             RK, RV = rots[layer]
-            K.kv_append(cfg, cache, layer, kk, vv, start, RK, RV, status=status)
-            K.attn_decode(cfg, cache, layer, qq, seq, RK, RV, oo, ws, lse=lse, seq_len_hint=T, status=status)
+            K.decode_step(cfg, cache, layer, kk, vv, start, qq, seq, RK, RV, oo, ws, lse=lse, seq_len_hint=T,
+                          status=status)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -341,10 +341,10 @@ def ours(args):
         flush.zero_()
         for layer in range(L):
             RK, RV = rots[layer]
-            K.kv_append(cfg, cache, layer, k1, v1, start, RK, RV, status=status)
             ks, ke = kev[i * L + layer]
             K.set_profile_events(ks, ke)
-            K.attn_decode(cfg, cache, layer, q, seq, RK, RV, out, ws, lse=lse, seq_len_hint=T, status=status)
+            K.decode_step(cfg, cache, layer, k1, v1, start, q, seq, RK, RV, out, ws, lse=lse, seq_len_hint=T,
+                          status=status)
             K.set_profile_events(None, None)
     torch.cuda.synchronize()
     split_ms = [a.elapsed_time(b) for a, b in kev]
@@ -390,7 +390,7 @@ def ours(args):
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K_,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "step": "kv_append(1 token/seq) + attn_decode per layer",
+        "config": {"workload": workload_desc(w), "step": "decode_step per layer: kv_append(1 token/seq) + attn_decode in one call",
                    "l2": "flushed between steps (512 MiB write)", "cache": "int2+bf16", "parallelism":
                        f"replica x{world}" if world > 1 else "single"},
         "kv_gbs": step_gbs, "kv_pct_hbm": step_gbs / peak,

@@ -206,6 +206,30 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
                 uint64_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * decode_step — kv_append followed by attn_decode, in one call: the usual
+ * decode step of a serving loop (append the current token of every sequence,
+ * then attend over the whole context).  Same computation and results as the
+ * two calls made in sequence with the same arguments (kv_append of k_new,
+ * v_new at start_pos; attn_decode over seq_lens); the pages' append (Qwen3-4B
+ * card, Run; RotationZoo, How to use) and fused attention (hysenlabs article,
+ * How the offline rotation is fit) back to back.
+ * Because the call knows which cache locations the append writes (the sink
+ * positions and INT2 rows of [start_pos[b], start_pos[b] + n_new) and the ring
+ * slots of its last min(n_new, W) positions), the attention kernels start
+ * streaming every other part of the cache while the append runs, instead of
+ * after it.  seq_lens and start_pos must therefore be final when the call is
+ * made (they are read before the append completes); q may still be produced
+ * by the kernel preceding the call.  Arguments, errors and the workspace are
+ * those of kv_append and attn_decode; everything is validated before
+ * anything is launched.  Launches three kernels on `stream`.
+ */
+int decode_step(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
+                const int32_t* start_pos, int32_t n_new, const void* q, const int32_t* seq_lens,
+                int32_t seq_len_hint, const float* R_K, const float* R_V, float sm_scale, int32_t num_splits,
+                void* out, float* lse, void* workspace, uint64_t workspace_bytes, int32_t* dev_status,
+                void* stream);
+
+/*
  * attn_decode_static — attn_decode for callers that cannot allocate device
  * memory (no counterpart on the pages).  Plugin hosts that own every device
  * allocation, and serving loops that must not call cudaMalloc while other

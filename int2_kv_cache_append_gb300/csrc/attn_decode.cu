@@ -424,8 +424,12 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
   const int c = threadIdx.x & 127, kp = threadIdx.x >> 7;
   const int col = chunk * 128 + c;
   const int64_t q0 = int64_t(bh) * G * D;  // first query head of this kv head
+  // in a fused step (decode_step) the split kernel may launch at once: it only
+  // streams cache blocks the preceding append leaves untouched before waiting
+  // for this grid; otherwise it launches once everything before this call is done
+  if (a.fused) pdl_trigger();
   pdl_wait();
-  pdl_trigger();
+  if (!a.fused) pdl_trigger();
 
   const int b = bh / a.g.Hkv;
   const int T = clamp_seq_len(a, b);
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (lo >= hi) return;
 
-  pdl_wait();  // q' and the merge tickets come from the preceding kernel
+  if (!a.fused) pdl_wait();  // q' and the merge tickets come from the preceding kernel
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -654,20 +658,41 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
 
+  // In a fused step: does block k of a segment hold a location the preceding
+  // append writes (sink positions and INT2 rows of [new_pos, new_pos + new_n),
+  // ring slots of its last min(new_n, W) positions)?
+  auto written = [&](const SegD& sx, int k) -> bool {
+    const Blk bk = block_of(sx, k);
+    const int st = a.new_pos[sx.b], n = a.new_n;
+    if (n <= 0) return false;
+    if (bk.type == 0) return bk.first < min(st + n, g.S) && st < bk.first + bk.count;
+    if (bk.type == 1) {
+      const int p0 = g.S + bk.first;
+      return p0 < st + n && max(st, g.S) < p0 + bk.count;
+    }
+    const int w0 = max(max(st, st + n - g.W), 0), wn = st + n - w0;  // ring positions written
+    if (wn <= 0) return false;
+    if (wn >= g.W) return true;
+    const int a0 = w0 % g.W;
+    return (bk.first - a0 + g.W) % g.W < wn || (a0 - bk.first + g.W) % g.W < bk.count;
+  };
   // the team's next block in window order (blocks kb + team + j * NTEAMS of
-  // each segment), if any: issue it into the team's next stage
-  auto issue_next = [&]() {
+  // each segment), if any: issue it into the team's next stage (with
+  // old_only, not if the preceding append writes it)
+  auto issue_next = [&](bool old_only = false) {
     while (is_ < nwin) {
       const int k = seg[is_].kb + team + ij * C::NTEAMS;
       if (k < seg[is_].ke) {
+        if (old_only && written(seg[is_], k)) return false;
         issue_block(is_, k, my_stage(issued));
         ++issued;
         ++ij;
-        return;
+        return true;
       }
       ++is_;
       ij = 0;
     }
+    return false;
   };
 
   // q' of a segment's unit, prepared by qrot: this lane's B fragments of group
@@ -714,8 +739,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t qf[8][NQT][2];
   float qsum[NQT], qF[NQT];
   const int pre_b = u_next / g.Hkv, pre_h = u_next % g.Hkv;
-  load_q(pre_b, pre_h, qf, qsum, qF);
-  qb_issue(pre_b, pre_h);
+  if (!a.fused) {
+    load_q(pre_b, pre_h, qf, qsum, qF);
+    qb_issue(pre_b, pre_h);
+  }
   bool first = true, aborted = false;
   for (;;) {
     // ---- segment table of the next window (warp 0), then start streaming
@@ -731,16 +758,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool more = win_more;
     is_ = 0;
     ij = 0;
-    // (with cuts on unit boundaries the first unit listed can follow empty ones)
-    if (nwin > 0 && (!first || seg[0].b != pre_b || seg[0].h != pre_h)) {
-      load_q(seg[0].b, seg[0].h, qf, qsum, qF);
-      if (qb_issued > qb_waited) qb_wait();  // the shared image is rewritten only once landed
-      __syncthreads();
-      qb_issue(seg[0].b, seg[0].h);
+    if (first && a.fused) {
+      // blocks the append leaves alone stream while it and qrot run
+      if (wt == 0)
+        for (int i = 0; i < C::NSTW; ++i)
+          if (!issue_next(true)) break;
+      pdl_wait();  // the append, q' and the merge tickets are complete
+      if (nwin > 0) {
+        load_q(seg[0].b, seg[0].h, qf, qsum, qF);
+        qb_issue(seg[0].b, seg[0].h);
+      }
+      if (wt == 0)
+        while (issued < C::NSTW && issue_next()) {
+        }
+    } else {
+      // (with cuts on unit boundaries the first unit listed can follow empty ones)
+      if (nwin > 0 && (!first || seg[0].b != pre_b || seg[0].h != pre_h)) {
+        load_q(seg[0].b, seg[0].h, qf, qsum, qF);
+        if (qb_issued > qb_waited) qb_wait();  // the shared image is rewritten only once landed
+        __syncthreads();
+        qb_issue(seg[0].b, seg[0].h);
+      }
+      if (wt == 0)
+        for (int i = 0; i < C::NSTW; ++i) issue_next();
     }
     first = false;
-    if (wt == 0)
-      for (int i = 0; i < C::NSTW; ++i) issue_next();
 
     for (int sg = 0; sg < nwin; ++sg) {
       const SegD& sd = seg[sg];

@@ -43,6 +43,9 @@ struct DecodeArgs {
   float* ws_acc;   // [B][Hq][NS][D]
   float* ws_ml;    // [B][Hq][NS][2]
   int32_t* ticket; // [B][Hkv] split-completion counters (zeroed by qrot)
+  const int32_t* new_pos;  // with fused = 1: positions [new_pos[b], new_pos[b] + new_n) are being
+  int new_n;               // written by the preceding append kernel of the same call
+  int fused;
   int ns;          // partial slots per (b, query head) in the workspace
   int ctas;        // CTAs of the split kernel
   float qscale;    // sm_scale * log2(e)

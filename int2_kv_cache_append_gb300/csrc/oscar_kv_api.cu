@@ -49,30 +49,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out) {
-  const int v = validate(cfg);
-  if (v != OSCAR_OK) return v;
-  if (!out) return OSCAR_ERR_INVALID;
-  const Geom g = make_geom(cfg);
-  std::memset(out, 0, sizeof(*out));
-  out->ncap = uint64_t(g.ncap);
-  out->sink_bytes = g.sink_bytes;
-  out->ring_bytes = g.ring_bytes;
-  out->codes_bytes = g.codes_bytes;
-  out->sz_bytes = g.sz_bytes;
-  out->role_bytes = g.role_bytes;
-  out->layer_bytes = g.layer_bytes;
-  out->total_bytes = g.layer_bytes * uint64_t(cfg->num_layers);
-  out->decode_workspace_bytes = oscar::decode_workspace_bytes(g, OSCAR_KV_MAX_SPLITS);
-  out->max_splits = OSCAR_KV_MAX_SPLITS;
-  return OSCAR_OK;
-}
-
-int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
-              const int32_t* start_pos, int32_t n_new, const float* R_K, const float* R_V,
-              float* debug_rot_out, int32_t* dev_status, void* stream) {
+// Validates kv_append's arguments and fills *a; launches nothing.
+int prep_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
+                const int32_t* start_pos, int32_t n_new, const float* R_K, const float* R_V, float* debug_rot_out,
+                int32_t* dev_status, oscar::AppendArgs* a) {
   const int v = validate(cfg);
   if (v != OSCAR_OK) return v;
   if (!cache || !k_new || !v_new || !start_pos || !R_K || !R_V) return OSCAR_ERR_INVALID;
@@ -81,28 +63,29 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
       !aligned(v_new, 16) || (debug_rot_out && !aligned(debug_rot_out, 16)))
     return OSCAR_ERR_INVALID;
   if (n_new > cfg->capacity) return OSCAR_ERR_CAPACITY;
-  oscar::AppendArgs a;
-  a.g = make_geom(cfg);
-  a.layer_base = static_cast<uint8_t*>(cache) + uint64_t(layer) * a.g.layer_bytes;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.start_pos = start_pos;
-  a.R_K = R_K;
-  a.R_V = R_V;
-  a.debug_rot = debug_rot_out;
-  a.status = dev_status;
-  a.n_new = n_new;
-  a.rows = int64_t(cfg->batch) * n_new * cfg->num_kv_heads;
-  a.k_clip = cfg->k_clip;
-  a.v_clip = cfg->v_clip;
-  a.in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
-  return oscar::launch_append(a, static_cast<cudaStream_t>(stream));
+  a->g = make_geom(cfg);
+  a->layer_base = static_cast<uint8_t*>(cache) + uint64_t(layer) * a->g.layer_bytes;
+  a->k_new = k_new;
+  a->v_new = v_new;
+  a->start_pos = start_pos;
+  a->R_K = R_K;
+  a->R_V = R_V;
+  a->debug_rot = debug_rot_out;
+  a->status = dev_status;
+  a->n_new = n_new;
+  a->rows = int64_t(cfg->batch) * n_new * cfg->num_kv_heads;
+  a->k_clip = cfg->k_clip;
+  a->v_clip = cfg->v_clip;
+  a->in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
+  return OSCAR_OK;
 }
 
-int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
-                const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
-                float sm_scale, int32_t num_splits, void* out, float* lse, void* workspace,
-                uint64_t workspace_bytes, int32_t* dev_status, void* stream) {
+// Validates attn_decode's arguments and fills *a; launches nothing.
+int prep_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
+                const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V, float sm_scale,
+                int32_t num_splits, void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                int32_t* dev_status, oscar::DecodeArgs* ap) {
+  oscar::DecodeArgs& a = *ap;
   const int v = validate(cfg);
   if (v != OSCAR_OK) return v;
   if (!cache || !q || !seq_lens || !R_K || !R_V || !out || !workspace) return OSCAR_ERR_INVALID;
@@ -124,7 +107,6 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   const int ctas = oscar::decode_grid(g, hint, num_splits);
   if (ctas < 1) return OSCAR_ERR_LAUNCH;
 
-  oscar::DecodeArgs a;
   a.g = g;
   a.layer_base = static_cast<const uint8_t*>(cache) + uint64_t(layer) * g.layer_bytes;
   a.q = q;
@@ -157,7 +139,76 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   a.in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
   a.out_fp32 = (cfg->flags & OSCAR_FLAG_OUT_FP32) ? 1 : 0;
   a.absorb_v = (cfg->flags & OSCAR_FLAG_ABSORB_V) ? 1 : 0;
+  a.new_pos = nullptr;
+  a.new_n = 0;
+  a.fused = 0;
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out) {
+  const int v = validate(cfg);
+  if (v != OSCAR_OK) return v;
+  if (!out) return OSCAR_ERR_INVALID;
+  const Geom g = make_geom(cfg);
+  std::memset(out, 0, sizeof(*out));
+  out->ncap = uint64_t(g.ncap);
+  out->sink_bytes = g.sink_bytes;
+  out->ring_bytes = g.ring_bytes;
+  out->codes_bytes = g.codes_bytes;
+  out->sz_bytes = g.sz_bytes;
+  out->role_bytes = g.role_bytes;
+  out->layer_bytes = g.layer_bytes;
+  out->total_bytes = g.layer_bytes * uint64_t(cfg->num_layers);
+  out->decode_workspace_bytes = oscar::decode_workspace_bytes(g, OSCAR_KV_MAX_SPLITS);
+  out->max_splits = OSCAR_KV_MAX_SPLITS;
+  return OSCAR_OK;
+}
+
+int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
+              const int32_t* start_pos, int32_t n_new, const float* R_K, const float* R_V,
+              float* debug_rot_out, int32_t* dev_status, void* stream) {
+  oscar::AppendArgs a;
+  const int v = prep_append(cfg, cache, layer, k_new, v_new, start_pos, n_new, R_K, R_V, debug_rot_out, dev_status, &a);
+  if (v != OSCAR_OK) return v;
+  return oscar::launch_append(a, static_cast<cudaStream_t>(stream));
+}
+
+int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
+                const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
+                float sm_scale, int32_t num_splits, void* out, float* lse, void* workspace,
+                uint64_t workspace_bytes, int32_t* dev_status, void* stream) {
+  oscar::DecodeArgs a;
+  const int v = prep_decode(cfg, cache, layer, q, seq_lens, seq_len_hint, R_K, R_V, sm_scale, num_splits, out, lse,
+                            workspace, workspace_bytes, dev_status, &a);
+  if (v != OSCAR_OK) return v;
   return oscar::launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+int decode_step(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
+                const int32_t* start_pos, int32_t n_new, const void* q, const int32_t* seq_lens,
+                int32_t seq_len_hint, const float* R_K, const float* R_V, float sm_scale, int32_t num_splits,
+                void* out, float* lse, void* workspace, uint64_t workspace_bytes, int32_t* dev_status,
+                void* stream) {
+  oscar::AppendArgs aa;
+  oscar::DecodeArgs ad;
+  int v = prep_append(cfg, cache, layer, k_new, v_new, start_pos, n_new, R_K, R_V, nullptr, dev_status, &aa);
+  if (v != OSCAR_OK) return v;
+  v = prep_decode(cfg, cache, layer, q, seq_lens, seq_len_hint, R_K, R_V, sm_scale, num_splits, out, lse, workspace,
+                  workspace_bytes, dev_status, &ad);
+  if (v != OSCAR_OK) return v;
+  // the decode kernels know what the append writes: they start streaming the
+  // rest of the cache while it runs
+  ad.new_pos = start_pos;
+  ad.new_n = n_new;
+  ad.fused = 1;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  v = oscar::launch_append(aa, st);
+  if (v != OSCAR_OK) return v;
+  return oscar::launch_decode(ad, st);
 }
 
 int oscar_kv_set_profile_events(void* split_start, void* split_stop) {

@@ -28,7 +28,8 @@ DEV_EMPTY = 16
 STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LAUNCH", -5: "UNSUPPORTED"}
 
 # every symbol include/oscar_kv.h declares
-EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "attn_decode_static", "oscar_kv_set_profile_events")
+EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "decode_step", "attn_decode_static",
+           "oscar_kv_set_profile_events")
 STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -95,6 +96,9 @@ def lib():
         L.attn_decode_static.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, ctypes.c_int32, P, P,
                                          ctypes.c_float, ctypes.c_int32, P, P, P, P]
         L.attn_decode_static.restype = ctypes.c_int
+        L.decode_step.argtypes = [ctypes.POINTER(_Config), P, ctypes.c_int32, P, P, P, ctypes.c_int32, P, P,
+                                  ctypes.c_int32, P, P, ctypes.c_float, ctypes.c_int32, P, P, P, ctypes.c_uint64, P, P]
+        L.decode_step.restype = ctypes.c_int
         L.oscar_kv_set_profile_events.argtypes = [P, P]
         L.oscar_kv_set_profile_events.restype = ctypes.c_int
         _lib = L
@@ -140,6 +144,20 @@ def attn_decode(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, out, wo
                            _stream(stream))
     if check and rc != 0:
         raise OscarError("attn_decode", rc)
+    return rc
+
+
+def decode_step(cfg: KVConfig, cache, layer: int, k_new, v_new, start_pos, q, seq_lens, R_K, R_V, out, workspace,
+                lse=None, seq_len_hint: int = 0, sm_scale: float = 0.0, num_splits: int = 0, status=None,
+                stream=None, check: bool = True) -> int:
+    """kv_append of k_new/v_new ([B][n][Hkv][D]) at start_pos, then attn_decode, in one call."""
+    n_new = int(k_new.shape[1])
+    rc = lib().decode_step(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(k_new), _ptr(v_new), _ptr(start_pos),
+                           n_new, _ptr(q), _ptr(seq_lens), int(seq_len_hint), _ptr(R_K), _ptr(R_V), float(sm_scale),
+                           int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                           int(workspace.numel() * workspace.element_size()), _ptr(status), _stream(stream))
+    if check and rc != 0:
+        raise OscarError("decode_step", rc)
     return rc
 
 

@@ -86,6 +86,13 @@ def test_entry_points_validate_before_launch(lib):
                            None, None) == -2
     assert lib.attn_decode(ctypes.byref(c), big, 0, big, big, 0, big, big, 0.0, 1, big, None, big, 16, None,
                            None) == -3
+    # decode_step validates both halves before launching anything
+    assert lib.decode_step(ctypes.byref(c), None, 0, big, big, big, 1, big, big, 0, big, big, 0.0, 0, big, None,
+                           big, 1 << 30, None, None) == -1
+    assert lib.decode_step(ctypes.byref(c), big, 0, big, big, big, 65, big, big, 0, big, big, 0.0, 0, big, None,
+                           big, 1 << 30, None, None) == -2
+    assert lib.decode_step(ctypes.byref(c), big, 0, big, big, big, 1, big, big, 0, big, big, 0.0, 0, big, None,
+                           big, 16, None, None) == -3
     # bad config passes through the same validation
     bad = K.KVConfig(1, 1, 4, 1, 96, 4, 8, 64).c()
     assert lib.attn_decode(ctypes.byref(bad), big, 0, big, big, 0, big, big, 0.0, 1, big, None, big, 1 << 30,
