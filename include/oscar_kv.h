@@ -85,7 +85,7 @@ extern "C" {
 #endif
 
 #define OSCAR_KV_GROUP 128       /* quant group along head_dim */
-#define OSCAR_KV_MAX_SPLITS 64   /* upper bound on decode context splits */
+#define OSCAR_KV_MAX_SPLITS 64   /* upper bound on decode partial slots per query head */
 
 /* config flags */
 enum {
@@ -134,7 +134,7 @@ typedef struct {
   uint64_t role_bytes;   /* sink + ring + codes + sz */
   uint64_t layer_bytes;  /* 2 * role_bytes (K then V) */
   uint64_t total_bytes;  /* num_layers * layer_bytes */
-  uint64_t decode_workspace_bytes; /* attn_decode workspace for OSCAR_KV_MAX_SPLITS splits */
+  uint64_t decode_workspace_bytes; /* attn_decode workspace with OSCAR_KV_MAX_SPLITS slots */
   int32_t max_splits;    /* OSCAR_KV_MAX_SPLITS */
   int32_t reserved;
 } oscar_kv_layout;
