@@ -80,9 +80,9 @@ struct DecCfg {
   static constexpr int XCH_BYTES = TS > 1 ? NTEAMS * 2 * TS * kSub * HEADS * 4 : 0;
   static constexpr int OFF_PART = OFF_XCH + XCH_BYTES;              // team partials
   // team partials [team][head][D + 2]; reused by the merging CTA for o' [head][D],
-  // max/sum [2][head] and split weights [head][OSCAR_KV_MAX_SPLITS]
+  // and max/sum [2][head]
   static constexpr int PART_A = NTEAMS * HEADS * (D + 2);
-  static constexpr int PART_B = HEADS * (D + 2 + OSCAR_KV_MAX_SPLITS);
+  static constexpr int PART_B = HEADS * (D + 2);
   static constexpr int PART_BYTES = (PART_A > PART_B ? PART_A : PART_B) * 4;
   static constexpr int OFF_SEG = OFF_PART + PART_BYTES;             // segment table of a window
   static constexpr int OFF_BAR = OFF_SEG + kMaxSeg * 64;
@@ -1185,54 +1185,82 @@ __global__ void __launch_bounds__(kThreads, 2)
           bulk_g2s(smem_u32(smem + C::OFF_STAGE), a.R_V, D * D * 4, rv_bar);
         }
         float* ob = part;                    // [G][D] merged o' (rotated basis)
-        float* Ms = part + C::HEADS * D;     // [G] max, [G] sum
+        float* Ms = part + C::HEADS * D;     // [G] max, [G] sum of the merged partial
         float* Ls = Ms + C::HEADS;
-        float* wts = Ls + C::HEADS;          // [G][splits] normalised split weights
-        for (int i = warp; i < Gh; i += kNCW) {
-          const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
-          const float m0 = lane < nseg ? __ldcg(a.ws_ml + (base + lane) * 2) : -INFINITY;
-          const float l0 = lane < nseg ? __ldcg(a.ws_ml + (base + lane) * 2 + 1) : 0.f;
-          const float m1 = lane + 32 < nseg ? __ldcg(a.ws_ml + (base + lane + 32) * 2) : -INFINITY;
-          const float l1 = lane + 32 < nseg ? __ldcg(a.ws_ml + (base + lane + 32) * 2 + 1) : 0.f;
-          float M = fmaxf(m0, m1);
-#pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-          const float e0 = M == -INFINITY || m0 == -INFINITY ? 0.f : ex2(m0 - M);
-          const float e1 = M == -INFINITY || m1 == -INFINITY ? 0.f : ex2(m1 - M);
-          float L = e0 * l0 + e1 * l1;
-#pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          if (lane < nseg) wts[i * OSCAR_KV_MAX_SPLITS + lane] = e0 * inv;
-          if (lane + 32 < nseg) wts[i * OSCAR_KV_MAX_SPLITS + lane + 32] = e1 * inv;
-          if (lane == 0) {
-            Ms[i] = M;
-            Ls[i] = L;
-          }
-        }
-        asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
         {
-          // (head, channel) pairs idx = threadIdx.x + kThreads * e: every slot
-          // load of a thread is issued before any is used
-          constexpr int IPT = C::HEADS * D / kThreads;
-          float acc[IPT];
+          // (head, 4-channel chunk) pairs f = threadIdx.x + kThreads * e.  Each
+          // thread merges its head's slots online (running max, sums rescaled
+          // by 2^(old max - new max); every thread of a head takes the same
+          // steps), in groups of SU slots whose loads are all issued before
+          // any is used: a unit shared by many CTAs costs a few L2 round trips
+          constexpr int D4 = D / 4;
+          constexpr int IPT4 = C::HEADS * D4 / kThreads;
+          constexpr int SU = IPT4 >= 8 ? 2 : 16 / IPT4;
+          static_assert(IPT4 * kThreads == C::HEADS * D4, "whole float4 chunks per thread");
+          float4 acc[IPT4];
+          float Mr[IPT4], Lr[IPT4];
 #pragma unroll
-          for (int e = 0; e < IPT; ++e) acc[e] = 0.f;
-#pragma unroll 2
-          for (int sp = 0; sp < nseg; ++sp) {
+          for (int e = 0; e < IPT4; ++e) {
+            acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            Mr[e] = -INFINITY;
+            Lr[e] = 0.f;
+          }
+          for (int sp0 = 0; sp0 < nseg; sp0 += SU) {
+            float4 v[SU][IPT4];
+            float2 ml[SU][IPT4];
 #pragma unroll
-            for (int e = 0; e < IPT; ++e) {
-              const int idx = threadIdx.x + kThreads * e, i = idx / D, d = idx % D;
-              if (i < Gh) {
-                const int64_t base = (int64_t(b) * g.Hq + head0 + i) * a.ns;
-                acc[e] = fmaf(wts[i * OSCAR_KV_MAX_SPLITS + sp], __ldcg(a.ws_acc + (base + sp) * D + d), acc[e]);
+            for (int j = 0; j < SU; ++j)
+#pragma unroll
+              for (int e = 0; e < IPT4; ++e) {
+                const int f = threadIdx.x + kThreads * e, i = f / D4, d4 = f % D4;
+                v[j][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                ml[j][e] = make_float2(-INFINITY, 0.f);
+                if (i < Gh && sp0 + j < nseg) {
+                  const int64_t si = (int64_t(b) * g.Hq + head0 + i) * a.ns + sp0 + j;
+                  v[j][e] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + si * D) + d4);
+                  ml[j][e] = __ldcg(reinterpret_cast<const float2*>(a.ws_ml) + si);
+                }
+              }
+            // one rescale per group to the group's max, then independent
+            // weights (an empty partial or a missing slot carries (-inf, 0)
+            // and a zero vector, so its weight is 0)
+#pragma unroll
+            for (int e = 0; e < IPT4; ++e) {
+              float mg = Mr[e];
+#pragma unroll
+              for (int j = 0; j < SU; ++j) mg = fmaxf(mg, ml[j][e].x);
+              if (mg != -INFINITY) {
+                const float co = ex2(Mr[e] - mg);
+                acc[e].x *= co;
+                acc[e].y *= co;
+                acc[e].z *= co;
+                acc[e].w *= co;
+                Lr[e] *= co;
+#pragma unroll
+                for (int j = 0; j < SU; ++j) {
+                  const float cn = ex2(ml[j][e].x - mg);
+                  acc[e].x = fmaf(v[j][e].x, cn, acc[e].x);
+                  acc[e].y = fmaf(v[j][e].y, cn, acc[e].y);
+                  acc[e].z = fmaf(v[j][e].z, cn, acc[e].z);
+                  acc[e].w = fmaf(v[j][e].w, cn, acc[e].w);
+                  Lr[e] = fmaf(ml[j][e].y, cn, Lr[e]);
+                }
+                Mr[e] = mg;
               }
             }
           }
 #pragma unroll
-          for (int e = 0; e < IPT; ++e) {
-            const int idx = threadIdx.x + kThreads * e;
-            if (idx / D < Gh) ob[idx] = acc[e];
+          for (int e = 0; e < IPT4; ++e) {
+            const int f = threadIdx.x + kThreads * e, i = f / D4;
+            if (i < Gh) {
+              const float inv = Lr[e] > 0.f ? 1.f / Lr[e] : 0.f;
+              reinterpret_cast<float4*>(ob)[f] =
+                  make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
+              if (f % D4 == 0) {
+                Ms[i] = Mr[e];
+                Ls[i] = Lr[e];
+              }
+            }
           }
         }
         asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
