@@ -42,7 +42,11 @@ Readings taken where the pages are silent (each listed in the design doc):
   absorbed by the caller;
 * windows: sink = positions [0, S), ring = [max(S, T-W), T), INT2 = the rest;
   BF16 window copies hold BF16(RNE) of the same float32 rotated row;
-* softmax scale 1/sqrt(D) unless given.
+* softmax scale 1/sqrt(D) unless given;
+* data-free in-quant Hadamard (FLAG_HADAMARD): for a model with no calibrated
+  rotation, K and V are rotated by the Sylvester Hadamard matrix of order 128
+  (normalised by 1/sqrt(128)), block-diagonal over the head_dim groups, and Q
+  and the output use that same matrix in place of R_K and R_V.
 
 The byte layout written by :func:`append` is the one the C header documents
 for the cache (regions, strides, code bit positions); it is implemented here
@@ -62,6 +66,7 @@ NCAP_ROUND = 64
 FLAG_ABSORB_V = 1
 FLAG_IN_FP32 = 2
 FLAG_OUT_FP32 = 4
+FLAG_HADAMARD = 8
 
 
 # --------------------------------------------------------------------------
@@ -140,6 +145,37 @@ def rotate_rows(x: np.ndarray, R: np.ndarray) -> np.ndarray:
     """r = x R (row vectors, R [D][D] row-major), exact float64 product rounded
     once to float32."""
     return (np.asarray(x, np.float64) @ np.asarray(R, np.float64)).astype(np.float32)
+
+
+def hadamard_rotation(d: int) -> np.ndarray:
+    """Rotation of the data-free in-quant Hadamard, float64 [d][d].
+
+    The llama.cpp model card's environment table [Run] names an in-quant
+    Hadamard that models with a baked rotation skip, and a base model without
+    one falls back to data-free INT2 with it; the SGLang run command sets its
+    order to 128.  Read here as: block-diagonal over the d / 128 groups, each
+    block the Sylvester Hadamard matrix of order 128, H[i][k] =
+    (-1)^popcount(i & k), divided by sqrt(128) so that it is orthogonal.
+    """
+    n = GROUP
+    blk = np.empty((n, n), dtype=np.float64)
+    for i in range(n):
+        for k in range(n):
+            blk[i, k] = -1.0 if bin(i & k).count("1") % 2 else 1.0
+    blk /= math.sqrt(n)
+    R = np.zeros((d, d), dtype=np.float64)
+    for j in range(d // n):
+        R[j * n:(j + 1) * n, j * n:(j + 1) * n] = blk
+    return R
+
+
+def rotations_of(cfg: "Config", R_K, R_V):
+    """(R_K, R_V) a call uses: the given matrices, or the in-quant Hadamard for
+    both when cfg.flags has FLAG_HADAMARD (the given ones are then ignored)."""
+    if cfg.flags & FLAG_HADAMARD:
+        H = hadamard_rotation(cfg.head_dim)
+        return H, H
+    return R_K, R_V
 
 
 def quantize_rows(r: np.ndarray, ratio: float):
@@ -274,13 +310,15 @@ def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new:
     """Write n new tokens per sequence at positions start_pos[b] .. +n-1.
 
     k_new, v_new: [B][n][Hkv][D] float (bf16 values as float32, or float32).
-    R_K, R_V: [D][D] rotations of this layer.  Every position p >= S gets its
+    R_K, R_V: [D][D] rotations of this layer (ignored with FLAG_HADAMARD,
+    which rotates both by :func:`hadamard_rotation`).  Every position p >= S gets its
     INT2 row; p < S also goes to the BF16 sink; p >= start_pos[b] + n - W also
     goes to the BF16 ring slot p mod W.  Positions outside [0, capacity) are
     not stored.
     """
     B, n, H, D = k_new.shape
     S, W, cap = cfg.sink, cfg.recent, cfg.capacity
+    R_K, R_V = rotations_of(cfg, R_K, R_V)
     rots = []
     for role, (x, R, ratio) in enumerate(((k_new, R_K, cfg.k_clip), (v_new, R_V, cfg.v_clip))):
         view = CacheView(cfg, cache, layer, role)
@@ -349,6 +387,7 @@ def decode(cfg: Config, cache: np.ndarray, layer: int, q: np.ndarray, seq_lens, 
     B, Hq, D = q.shape
     G = cfg.G
     scale = sm_scale if sm_scale > 0 else 1.0 / math.sqrt(D)
+    R_K, R_V = rotations_of(cfg, R_K, R_V)
     RK = np.asarray(R_K, np.float64)
     RV = np.asarray(R_V, np.float64)
     out = np.zeros((B, Hq, D), dtype=np.float64)

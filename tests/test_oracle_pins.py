@@ -441,3 +441,77 @@ def test_absorb_v_is_output_in_rotated_basis():
     o, l2 = O.decode(cfg, cache, 0, q, [20, 13], rk, rv, absorb_v=False)
     assert np.abs(o_abs @ rv.astype(np.float64).T - o).max() < 1e-12
     assert np.array_equal(l1, l2)
+
+
+# --------------------------------------------------------------------------
+# data-free in-quant Hadamard (FLAG_HADAMARD)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [128, 256, 512])
+def test_in_quant_hadamard_is_block_diagonal_sylvester(d):
+    # each 128-channel block is scipy's Sylvester-ordered Hadamard matrix / sqrt(128);
+    # everything off the diagonal blocks is zero; the whole matrix is orthogonal
+    L = pytest.importorskip("scipy.linalg")
+    H = O.hadamard_rotation(d)
+    ref = L.hadamard(128).astype(np.float64) / math.sqrt(128)
+    for a in range(d // 128):
+        for b in range(d // 128):
+            blk = H[128 * a:128 * (a + 1), 128 * b:128 * (b + 1)]
+            assert np.array_equal(blk, ref if a == b else np.zeros((128, 128)))
+    assert np.abs(H @ H.T - np.eye(d)).max() < 1e-12
+    assert np.array_equal(H, H.T)
+
+
+def test_in_quant_hadamard_hand_entries():
+    # Walsh rows by hand: row 0 all +, row 1 alternates, row 2 in pairs, row 3 = row1*row2
+    H = O.hadamard_rotation(128) * math.sqrt(128)
+    assert np.all(H[0] == 1)
+    assert list(H[1, :4]) == [1, -1, 1, -1]
+    assert list(H[2, :4]) == [1, 1, -1, -1]
+    assert list(H[3, :4]) == [1, -1, -1, 1]
+    assert H[127, 127] == -1 and H[64, 63] == 1 and H[64, 64] == -1
+
+
+def test_hadamard_flag_ignores_given_rotations():
+    # the flag rotates by the Hadamard whatever R_K / R_V say: same bytes and
+    # outputs as passing the Hadamard explicitly without the flag
+    cfg = _small_cfg(S_=4, W=8, cap=64, G=2, Hkv=2, B=2)
+    cfg_h = _small_cfg(S_=4, W=8, cap=64, G=2, Hkv=2, B=2)
+    cfg_h.flags = O.FLAG_HADAMARD
+    rng = np.random.default_rng(21)
+    k = S.to_bf16_values(rng.standard_normal((2, 30, 2, 128)).astype(np.float32))
+    v = S.to_bf16_values(rng.standard_normal((2, 30, 2, 128)).astype(np.float32))
+    q = S.to_bf16_values(rng.standard_normal((2, 4, 128)).astype(np.float32))
+    H = O.hadamard_rotation(128)
+    junk = rng.standard_normal((128, 128)).astype(np.float32)
+    c1, c2 = O.new_cache(cfg), O.new_cache(cfg_h)
+    O.append(cfg, c1, 0, k, v, [0, 0], H, H)
+    O.append(cfg_h, c2, 0, k, v, [0, 0], junk, None)
+    assert np.array_equal(c1, c2)
+    o1, l1 = O.decode(cfg, c1, 0, q, [30, 17], H, H)
+    o2, l2 = O.decode(cfg_h, c2, 0, q, [30, 17], None, junk)
+    assert np.abs(o1 - o2).max() < 1e-12 and np.abs(l1 - l2).max() < 1e-12
+
+
+@pytest.mark.parametrize("j", [0, 1, 77])
+def test_hadamard_spreads_a_one_hot_row_to_two_levels(j):
+    # a one-hot row c e_j becomes c H[j] = +-c/sqrt(128) on every channel: after
+    # the 0.96 clip it has two levels, so every code is 0 or 3 (Walsh rows j > 0
+    # have 64 of each sign); row 0 is constant, so its group has scale 0, codes 0
+    cfg = _small_cfg(S_=0, W=0, cap=64, G=1, Hkv=1, B=1)
+    cfg.flags = O.FLAG_HADAMARD
+    x = np.zeros((1, 1, 1, 128), dtype=np.float32)
+    x[..., j] = 4.0
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, x, x, [0], None, None)
+    for role in (0, 1):
+        view = O.CacheView(cfg, cache, 0, role)
+        codes = O.unpack_codes(view.codes[0, 0, :1], 128, role)[0]
+        scale, zero = float(view.sz[0, 0, 0, 0, 0]), float(view.sz[0, 0, 0, 0, 1])
+        t = np.float32(0.96 if role == 0 else cfg.v_clip) * np.float32(4.0 / math.sqrt(128))
+        if j == 0:
+            assert np.all(codes == 0) and scale == 0.0 and zero == float(np.float16(t))
+        else:
+            assert set(np.unique(codes)) == {0, 3} and int((codes == 3).sum()) == 64
+            signs = O.hadamard_rotation(128)[j] > 0
+            assert np.array_equal(codes == 3, signs)
+            assert zero == float(np.float16(-t))
