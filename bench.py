@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hadamard", action="store_true",
+                    help="data-free in-quant Hadamard rotation instead of the calibrated R_K / R_V")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -51,6 +53,10 @@ def workload_desc(w) -> str:
     return (f"{w.name}: B{w.batch} Hq{w.num_q_heads} Hkv{w.num_kv_heads} D{w.head_dim} T{w.context} "
             f"S{w.sink} W{w.recent} g128 clip{w.k_clip}/{w.v_clip} layers{w.num_layers}"
             f"{' absorbV' if w.absorb_v else ''}")
+
+
+def rotation_desc(args) -> str:
+    return "in-quant Hadamard H_128 (data-free)" if getattr(args, "hadamard", False) else "calibrated R_K, R_V"
 
 
 def kv_bytes_per_bh(w, T: int) -> int:
@@ -159,7 +165,7 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # CPU oracle sample (test infrastructure, timed as the CPU baseline)
 # --------------------------------------------------------------------------
-def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int):
+def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False):
     """Run inside a single-threaded child process: time the oracle's decode step
     (append of the current token + attention) for batch row 0 of the workload,
     restricted to its first `heads` KV heads (and their query heads)."""
@@ -170,8 +176,9 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int):
     w = S.WORKLOADS[workload]
     T = w.context
     G = w.num_q_heads // w.num_kv_heads
-    c = O.Config(1, 1, G * heads, heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip)
-    RK, RV = S.rotations(w, 0)
+    c = O.Config(1, 1, G * heads, heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip,
+                 flags=O.FLAG_HADAMARD if hadamard else 0)
+    RK, RV = (None, None) if hadamard else S.rotations(w, 0)
     k, v = S.kv_rows(w, 0, T, batch=1)
     k, v = k[:, :, :heads], v[:, :, :heads]
     cache = O.new_cache(c)
@@ -187,11 +194,12 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int):
     print(json.dumps({"sec_per_step": statistics.mean(times), "steps": len(times)}))
 
 
-def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int):
+def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", "--workload", workload,
-           "--steps", str(steps), "--warmup", str(warmup), "--sample-heads", str(heads)]
+           "--steps", str(steps), "--warmup", str(warmup), "--sample-heads", str(heads)] + (
+               ["--hadamard"] if hadamard else [])
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
@@ -209,7 +217,7 @@ def reference_arm(args):
     # about 75 ms of oracle work per KV head and step at T=16384: keep the run near two minutes
     heads = max(1, min(w.num_kv_heads, int(120.0 / (0.075 * (steps + args.warmup) * w.context / 16384))))
     t0 = time.time()
-    res = run_cpu_sample(args.workload, steps, args.warmup, heads)
+    res = run_cpu_sample(args.workload, steps, args.warmup, heads, args.hadamard)
     sec = res["sec_per_step"]
     value = (heads / w.num_kv_heads) / sec  # the sample is heads/Hkv of one sequence's decode step
     sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}, {heads} of "
@@ -218,7 +226,8 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "sample": f"{heads} of {w.num_kv_heads} KV heads of one sequence per step"},
+            "config": {"workload": workload_desc(w), "rotation": rotation_desc(args),
+                       "sample": f"{heads} of {w.num_kv_heads} KV heads of one sequence per step"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.time() - t0}
@@ -254,7 +263,7 @@ def ours(args):
 
     w = S.WORKLOADS[args.workload]
     L, Bsz, Hq, Hkv, D, T = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.context
-    flags = K.FLAG_ABSORB_V if w.absorb_v else 0
+    flags = (K.FLAG_ABSORB_V if w.absorb_v else 0) | (K.FLAG_HADAMARD if args.hadamard else 0)
     cfg = K.KVConfig(L, Bsz, Hq, Hkv, D, w.sink, w.recent, T, w.k_clip, w.v_clip, flags)
     lay = K.layout_query(cfg)
     stream = torch.cuda.current_stream()
@@ -264,6 +273,9 @@ def ours(args):
     cache = torch.empty(lay["total_bytes"], dtype=torch.uint8, device=dev)
     rots = []
     for layer in range(L):
+        if args.hadamard:  # no matrices: the library applies the in-quant Hadamard itself
+            rots.append((None, None))
+            continue
         RK, RV = S.rotations(w, layer if L == 1 else layer % 4)
         rots.append((torch.from_numpy(RK).to(dev), torch.from_numpy(RV).to(dev)))
     ch = S.outlier_channels(w.config_id, 0, D)
@@ -382,7 +394,7 @@ def ours(args):
     step_gbs = kv_bytes / (ms / 1e3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv)
+        res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv, hadamard=args.hadamard)
         cpu = {"value": 1.0 / res["sec_per_step"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"oracle decode step (append + attention) for 1 of {Bsz} sequences of {args.workload}, "
                          f"T={T}, {res['steps']} timed steps, single thread"}
@@ -391,6 +403,7 @@ def ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(w), "step": "decode_step per layer: kv_append(1 token/seq) + attn_decode in one call",
+                   "rotation": rotation_desc(args),
                    "l2": "flushed between steps (512 MiB write)", "cache": "int2+bf16", "parallelism":
                        f"replica x{world}" if world > 1 else "single"},
         "kv_gbs": step_gbs, "kv_pct_hbm": step_gbs / peak,
@@ -518,7 +531,7 @@ def ours_append(args):
 def main():
     args = parse()
     if args.cpu_sample_worker:
-        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads)
+        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard)
         return
     if args.impl == "reference":
         reference_arm(args)

@@ -30,6 +30,17 @@
  *    o = o' R_V^T, unless the caller absorbs it [RotationZoo, How to use:
  *    SGLANG_OSCAR_ABSORB_V_ROTATION].
  *
+ *  - Data-free rotation (OSCAR_FLAG_HADAMARD): for a model without calibrated
+ *    rotations, K and V are rotated by the in-quant Hadamard instead
+ *    [model card, Run: LLAMA_KV_NO_HADAMARD skips the in-quant Hadamard of
+ *    models whose rotation is in-graph, and a base model falls back to
+ *    data-free INT2; RotationZoo, How to use: HADAMARD_ORDER=128]:
+ *    R_K = R_V = H, block-diagonal over the D/128 channel groups, each block
+ *    the Sylvester Hadamard matrix of order 128 divided by sqrt(128)
+ *    (H[i][k] = (-1)^popcount(i & k) / sqrt(128)).  The query and the output
+ *    use the same H.  H is applied with an in-register fast Walsh-Hadamard
+ *    transform; the R_K and R_V arguments are not read and may be NULL.
+ *
  * Quantiser (the pages fix group, clip and 2-bit codes; the asymmetric
  * min/max form and the exact operation order are this library's definition):
  *   a = max_j |r_j| over the float32 rotated row; t = ratio * a;
@@ -91,7 +102,9 @@ extern "C" {
 enum {
   OSCAR_FLAG_ABSORB_V = 1, /* attn_decode returns o' (rotated basis); caller folds R_V^T into W_o */
   OSCAR_FLAG_IN_FP32 = 2,  /* k_new, v_new and q are float32 instead of bf16 */
-  OSCAR_FLAG_OUT_FP32 = 4  /* attn_decode writes float32 instead of bf16 */
+  OSCAR_FLAG_OUT_FP32 = 4, /* attn_decode writes float32 instead of bf16 */
+  OSCAR_FLAG_HADAMARD = 8  /* rotate K, V, q and the output by the in-quant Hadamard H (above);
+                              R_K and R_V are ignored and may be NULL */
 };
 
 /* return codes */
@@ -157,7 +170,8 @@ int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out);
  *   k_new,v_new device [B][n_new][Hkv][D] post-RoPE rows, bf16 (float32 with
  *              OSCAR_FLAG_IN_FP32).
  *   start_pos  device int32 [B]: position of each sequence's first new token.
- *   R_K, R_V   device float32 [D][D] row-major rotations of this layer.
+ *   R_K, R_V   device float32 [D][D] row-major rotations of this layer
+ *              (not read with OSCAR_FLAG_HADAMARD; may then be NULL).
  *   debug_rot_out device float32 [B][n_new][Hkv][2][D] or NULL: receives the
  *              float32 rotated rows the quantiser saw (K then V).
  *   dev_status device int32 or NULL.
@@ -177,7 +191,8 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  *   seq_lens   device int32 [B], 1 <= seq_len <= capacity.
  *   seq_len_hint host upper bound on seq_lens (0 = capacity); only used to
  *              size the grid when the contexts are short.
- *   R_K, R_V   device float32 [D][D] rotations of this layer.
+ *   R_K, R_V   device float32 [D][D] rotations of this layer (not read
+ *              with OSCAR_FLAG_HADAMARD; may then be NULL).
  *   sm_scale   softmax scale; <= 0 means 1/sqrt(D).
  *   num_splits 0 = automatic: one wave of CTAs (as many as are resident at
  *              once).  Else num_splits * B * Hkv CTAs (at most

@@ -450,42 +450,73 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
     return;
   }
 
-  int k0 = kp * KC;
-  float rr[32];
+  // column c of this group before scaling: q R_K, or the in-quant Hadamard
+  // transform of the group (warp i transforms head i)
+  float hsum[8];
+  if (a.hadamard) {
+    const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    if (w < G) {
+      float x[4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) rr[j] = __ldg(a.R_K + (k0 + j) * D + col);
-  for (int idx = threadIdx.x; idx < G * D; idx += kQrotThreads)
-    qs[idx / D][idx % D] = a.in_fp32 ? static_cast<const float*>(a.q)[q0 + idx]
-                                     : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[q0 + idx]);
-  __syncthreads();
-  float acc[8];
+      for (int e = 0; e < 4; ++e) {
+        const int64_t qi = q0 + int64_t(w) * D + chunk * 128 + ln + 32 * e;
+        x[e] = a.in_fp32 ? static_cast<const float*>(a.q)[qi]
+                         : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qi]);
+      }
+      hadamard128_warp(x, ln);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (;;) {
+      for (int e = 0; e < 4; ++e) qv[w][ln + 32 * e] = x[e];
+    }
+    if (chunk == 0 && threadIdx.x == 0) a.ticket[bh] = 0;
+    __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < G) acc[i] = fmaf(qs[i][k0 + j], rr[j], acc[i]);
-    k0 += 32;
-    if (k0 >= (kp + 1) * KC) break;
+    for (int i = 0; i < 8; ++i) hsum[i] = (kp == 0 && i < G) ? qv[i][c] : 0.f;
+  } else {
+    int k0 = kp * KC;
+    float rr[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) rr[j] = __ldg(a.R_K + (k0 + j) * D + col);
-  }
-  if (kp > 0) {
+    for (int idx = threadIdx.x; idx < G * D; idx += kQrotThreads)
+      qs[idx / D][idx % D] = a.in_fp32 ? static_cast<const float*>(a.q)[q0 + idx]
+                                       : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[q0 + idx]);
+    __syncthreads();
+    float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < G) part[kp - 1][i][c] = acc[i];
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (;;) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < G) acc[i] = fmaf(qs[i][k0 + j], rr[j], acc[i]);
+      k0 += 32;
+      if (k0 >= (kp + 1) * KC) break;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) rr[j] = __ldg(a.R_K + (k0 + j) * D + col);
+    }
+    if (kp > 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < G) part[kp - 1][i][c] = acc[i];
+    }
+    if (chunk == 0 && threadIdx.x == 0) a.ticket[bh] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      hsum[i] = 0.f;
+      if (kp == 0 && i < G) {
+        float sum = acc[i];
+#pragma unroll
+        for (int p = 0; p < KP - 1; ++p) sum += part[p][i][c];
+        hsum[i] = sum;
+      }
+    }
   }
-  if (chunk == 0 && threadIdx.x == 0) a.ticket[bh] = 0;
-  __syncthreads();
   if (kp == 0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       if (i < G) {
-        float sum = acc[i];
-#pragma unroll
-        for (int p = 0; p < KP - 1; ++p) sum += part[p][i][c];
+        const float sum = hsum[i];
         const float v = sum * a.qscale;
         if (!(fabsf(v) < 60000.f)) status_or(a.status, OSCAR_DEV_FP16_RANGE);
         qv[i][c] = v;
@@ -1177,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // R_V: in the CTA's last segment no copy is in flight, so at D = 128 it
         // comes into the idle stage area with one bulk copy, landing while the
         // slots are merged; otherwise its rows are read through L2
-        const bool rv_smem = D == 128 && !a.absorb_v && !more && sg == nwin - 1 &&
+        const bool rv_smem = D == 128 && !a.absorb_v && !a.hadamard && !more && sg == nwin - 1 &&
                              C::NST * C::STAGE >= D * D * 4;
         const uint32_t rv_bar = smem_u32(&bars[C::NST]);
         if (rv_smem && threadIdx.x == 0) {
@@ -1276,7 +1307,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           else
             static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(v);
         };
-        if (a.absorb_v || (rv_smem && rv_ok)) {
+        if (a.hadamard && !a.absorb_v) {
+          // o = o' H (the in-quant Hadamard is symmetric): warp w transforms
+          // the (head, group) pairs w, w + kNCW, ... in registers
+          for (int pr = warp; pr < Gh * C::Dg; pr += kNCW) {
+            const int i = pr / C::Dg, j = pr % C::Dg;
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = ob[i * D + j * kGroup + lane + 32 * e];
+            hadamard128_warp(x, lane);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) store(i, j * kGroup + lane + 32 * e, x[e]);
+          }
+        } else if (a.absorb_v || (rv_smem && rv_ok)) {
           // o = o' R_V^T (or o' when absorbed): one thread per output channel r
           const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
           for (int r = threadIdx.x; r < D; r += 32 * kNCW) {

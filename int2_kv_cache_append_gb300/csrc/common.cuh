@@ -146,6 +146,34 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 1 / sqrt(128), rounded to float32
+constexpr float kInvSqrt128 = 0.0883883476483184405f;
+
+// In-quant Hadamard of one 128-channel group held by a warp: lane l holds
+// channels l + 32 e in x[e] (e = 0..3); on return x[e] holds output channel
+// l + 32 e of y = x H / sqrt(128), H[i][k] = (-1)^popcount(i & k) (Sylvester
+// order).  Fast Walsh-Hadamard transform: one butterfly (a, c) -> (a + c,
+// a - c) per channel-index bit, bits 5 and 6 inside the lane, bits 0-4 across
+// lanes; then one multiplication by 1/sqrt(128).
+__device__ __forceinline__ void hadamard128_warp(float (&x)[4], int lane) {
+  const float s0 = x[0] + x[1], d0 = x[0] - x[1], s1 = x[2] + x[3], d1 = x[2] - x[3];
+  x[0] = s0 + s1;
+  x[2] = s0 - s1;
+  x[1] = d0 + d1;
+  x[3] = d0 - d1;
+#pragma unroll
+  for (int bit = 1; bit < 32; bit <<= 1) {
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], bit);
+      x[e] = upper ? o - x[e] : x[e] + o;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] *= kInvSqrt128;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
   return static_cast<uint32_t>(__half_as_ushort(lo)) |
          (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);

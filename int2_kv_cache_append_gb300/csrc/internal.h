@@ -24,6 +24,7 @@ struct AppendArgs {
   int64_t rows;          // B * n_new * Hkv
   float k_clip, v_clip;
   int in_fp32;
+  int hadamard;          // rotate by the in-quant Hadamard (R_K, R_V unused)
 };
 
 struct DecodeArgs {
@@ -50,6 +51,7 @@ struct DecodeArgs {
   int ctas;        // CTAs of the split kernel
   float qscale;    // sm_scale * log2(e)
   int in_fp32, out_fp32, absorb_v;
+  int hadamard;    // q and the output use the in-quant Hadamard (R_K, R_V unused)
 };
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns);

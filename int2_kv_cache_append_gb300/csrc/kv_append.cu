@@ -231,6 +231,9 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendA
 //      OR their slots together.
 // Waits on the copies are bounded; on a timeout the CTA flags
 // OSCAR_DEV_TIMEOUT, waits (bounded) for its copies in flight and returns.
+// With HAD (the in-quant Hadamard) steps 1 and 2 are replaced: each warp loads
+// its rows and transforms every 128-channel group in registers
+// (hadamard128_warp); no rotation matrix is read.
 // ---------------------------------------------------------------------------
 template <int D, int RPC>
 struct RowsCfg {
@@ -243,26 +246,24 @@ struct RowsCfg {
   static constexpr uint32_t OFF_Y = OFF_X + uint32_t(D) * RPC * 4;
   static constexpr uint32_t OFF_BAR = OFF_Y + uint32_t(RPC) * D * 4;
   static constexpr uint32_t SMEM = OFF_BAR + 8 * NSTG;
+  static constexpr uint32_t SMEM_HAD = uint32_t(RPC) * D * 4;  // rotated rows only
   static constexpr int NW = 8 * (D / kGroup);  // 32-bit code words per row
   static constexpr int LPW = 32 / NW;          // lanes per word
   static constexpr int SPL = 16 / LPW;         // 2-bit slots per lane
   static_assert(RPC % 4 == 0, "rows per CTA must be a multiple of the warp count");
 };
 
+// Steps 1 and 2 with a rotation matrix R: stream R into shared memory, stage
+// the inputs transposed and accumulate ys = x R.  Returns false after a
+// timed-out copy (OSCAR_DEV_TIMEOUT flagged, copies in flight drained).
 template <int D, int RPC>
-__global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const AppendArgs a) {
+__device__ __forceinline__ bool rotate_by_matrix(const AppendArgs& a, unsigned char* sm, float* ys, int role,
+                                                 int64_t row0, int tid) {
   using C = RowsCfg<D, RPC>;
-  extern __shared__ __align__(128) unsigned char sm[];
   float* Rs = reinterpret_cast<float*>(sm);
   float* xs = reinterpret_cast<float*>(sm + C::OFF_X);  // [D][RPC]
-  float* ys = reinterpret_cast<float*>(sm + C::OFF_Y);  // [RPC][D]
   const uint32_t bar0 = smem_u32(sm + C::OFF_BAR);
-
-  pdl_trigger();
-  const int role = blockIdx.y;
   const float* __restrict__ R = role ? a.R_V : a.R_K;
-  const int64_t row0 = int64_t(blockIdx.x) * RPC;
-  const int tid = threadIdx.x;
 
   if (tid == 0) {
     for (int s = 0; s < C::NSTG; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -333,15 +334,51 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
       for (int c2 = ch; c2 < C::NCH && c2 < ch + C::NSTG; ++c2)
         (void)mbar_wait(bar0 + 8 * (c2 % C::NSTG), (c2 / C::NSTG) & 1);
     }
-    return;
+    return false;
   }
 #pragma unroll
   for (int r = 0; r < RPC; ++r)
 #pragma unroll
     for (int m = 0; m < C::CPT; ++m) ys[r * D + tid + 128 * m] = acc[r][m];
   __syncthreads();
+  return true;
+}
 
+template <int D, int RPC, bool HAD>
+__global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const AppendArgs a) {
+  using C = RowsCfg<D, RPC>;
+  extern __shared__ __align__(128) unsigned char sm[];
+  float* ys = reinterpret_cast<float*>(sm + (HAD ? 0 : C::OFF_Y));  // [RPC][D] rotated rows
+
+  pdl_trigger();
+  const int role = blockIdx.y;
+  const int64_t row0 = int64_t(blockIdx.x) * RPC;
+  const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+
+  if constexpr (HAD) {
+    for (int r = warp; r < RPC; r += kAppendThreads / 32) {
+      const int64_t row = row0 + r;
+      if (row >= a.rows) break;
+#pragma unroll
+      for (int j = 0; j < D / kGroup; ++j) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t i = row * D + j * kGroup + lane + 32 * e;
+          x[e] = a.in_fp32 ? static_cast<const float*>(role ? a.v_new : a.k_new)[i]
+                           : __bfloat162float(static_cast<const __nv_bfloat16*>(role ? a.v_new : a.k_new)[i]);
+        }
+        hadamard128_warp(x, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ys[r * D + j * kGroup + lane + 32 * e] = x[e];
+      }
+    }
+    __syncthreads();
+  } else {
+    if (!rotate_by_matrix<D, RPC>(a, sm, ys, role, row0, tid)) return;
+  }
+
   const float ratio = role ? a.v_clip : a.k_clip;
   const Geom& g = a.g;
   uint8_t* role_base = a.layer_base + role * g.role_bytes;
@@ -451,26 +488,34 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
   }
 }
 
-template <int D, int RPC>
+template <int D, int RPC, bool HAD>
 int launch_append_rows(const AppendArgs& a, cudaStream_t stream) {
   using C = RowsCfg<D, RPC>;
+  constexpr uint32_t smem = HAD ? C::SMEM_HAD : C::SMEM;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kv_append_rows_kernel<D, RPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(kv_append_rows_kernel<D, RPC, HAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
       return OSCAR_ERR_LAUNCH;
     attr_set[dev] = 1;
   }
   const dim3 grid(unsigned((a.rows + RPC - 1) / RPC), 2, 1);
-  kv_append_rows_kernel<D, RPC><<<grid, kAppendThreads, C::SMEM, stream>>>(a);
+  kv_append_rows_kernel<D, RPC, HAD><<<grid, kAppendThreads, smem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
 }
 
 template <int D>
 int launch_append_small(const AppendArgs& a, cudaStream_t stream) {
-  return a.rows > 512 ? launch_append_rows<D, 8>(a, stream) : launch_append_rows<D, 4>(a, stream);
+  return a.rows > 512 ? launch_append_rows<D, 8, false>(a, stream) : launch_append_rows<D, 4, false>(a, stream);
+}
+
+// the in-quant Hadamard reads no matrix, so every append takes the
+// row-parallel kernel
+template <int D>
+int launch_append_hadamard(const AppendArgs& a, cudaStream_t stream) {
+  return a.rows > 512 ? launch_append_rows<D, 8, true>(a, stream) : launch_append_rows<D, 4, true>(a, stream);
 }
 
 template <int D>
@@ -494,6 +539,14 @@ int launch_append_d(const AppendArgs& a, cudaStream_t stream) {
 
 int launch_append(const AppendArgs& a, cudaStream_t stream) {
   if (a.rows == 0) return OSCAR_OK;
+  if (a.hadamard) {
+    switch (a.g.D) {
+      case 128: return launch_append_hadamard<128>(a, stream);
+      case 256: return launch_append_hadamard<256>(a, stream);
+      case 512: return launch_append_hadamard<512>(a, stream);
+      default: return OSCAR_ERR_UNSUPPORTED;
+    }
+  }
   if (a.rows <= kSmallAppendRows) {
     switch (a.g.D) {
       case 128: return launch_append_small<128>(a, stream);

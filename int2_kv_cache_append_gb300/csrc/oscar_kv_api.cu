@@ -15,7 +15,8 @@ int validate(const oscar_kv_config* c) {
     return OSCAR_ERR_INVALID;
   if (c->num_q_heads % c->num_kv_heads != 0) return OSCAR_ERR_INVALID;
   if (!(c->k_clip > 0.f && c->k_clip <= 1.f) || !(c->v_clip > 0.f && c->v_clip <= 1.f)) return OSCAR_ERR_INVALID;
-  if (c->flags & ~uint32_t(OSCAR_FLAG_ABSORB_V | OSCAR_FLAG_IN_FP32 | OSCAR_FLAG_OUT_FP32)) return OSCAR_ERR_INVALID;
+  if (c->flags & ~uint32_t(OSCAR_FLAG_ABSORB_V | OSCAR_FLAG_IN_FP32 | OSCAR_FLAG_OUT_FP32 | OSCAR_FLAG_HADAMARD))
+    return OSCAR_ERR_INVALID;
   if (c->group_size != OSCAR_KV_GROUP) return OSCAR_ERR_UNSUPPORTED;
   if (c->head_dim != 128 && c->head_dim != 256 && c->head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
   if (c->num_q_heads / c->num_kv_heads > 8) return OSCAR_ERR_UNSUPPORTED;
@@ -57,7 +58,10 @@ int prep_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const vo
                 int32_t* dev_status, oscar::AppendArgs* a) {
   const int v = validate(cfg);
   if (v != OSCAR_OK) return v;
-  if (!cache || !k_new || !v_new || !start_pos || !R_K || !R_V) return OSCAR_ERR_INVALID;
+  // with the in-quant Hadamard the rotation matrices are not read (NULL allowed)
+  const bool had = (cfg->flags & OSCAR_FLAG_HADAMARD) != 0;
+  if (had) R_K = R_V = nullptr;
+  if (!cache || !k_new || !v_new || !start_pos || (!had && (!R_K || !R_V))) return OSCAR_ERR_INVALID;
   if (layer < 0 || layer >= cfg->num_layers || n_new < 0) return OSCAR_ERR_INVALID;
   if (!aligned(cache, 256) || !aligned(R_K, 16) || !aligned(R_V, 16) || !aligned(k_new, 16) ||
       !aligned(v_new, 16) || (debug_rot_out && !aligned(debug_rot_out, 16)))
@@ -77,6 +81,7 @@ int prep_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const vo
   a->k_clip = cfg->k_clip;
   a->v_clip = cfg->v_clip;
   a->in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
+  a->hadamard = had ? 1 : 0;
   return OSCAR_OK;
 }
 
@@ -88,7 +93,9 @@ int prep_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   oscar::DecodeArgs& a = *ap;
   const int v = validate(cfg);
   if (v != OSCAR_OK) return v;
-  if (!cache || !q || !seq_lens || !R_K || !R_V || !out || !workspace) return OSCAR_ERR_INVALID;
+  const bool had = (cfg->flags & OSCAR_FLAG_HADAMARD) != 0;
+  if (had) R_K = R_V = nullptr;
+  if (!cache || !q || !seq_lens || (!had && (!R_K || !R_V)) || !out || !workspace) return OSCAR_ERR_INVALID;
   if (layer < 0 || layer >= cfg->num_layers || num_splits < 0 || num_splits > OSCAR_KV_MAX_SPLITS ||
       seq_len_hint < 0)
     return OSCAR_ERR_INVALID;
@@ -139,6 +146,7 @@ int prep_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   a.in_fp32 = (cfg->flags & OSCAR_FLAG_IN_FP32) ? 1 : 0;
   a.out_fp32 = (cfg->flags & OSCAR_FLAG_OUT_FP32) ? 1 : 0;
   a.absorb_v = (cfg->flags & OSCAR_FLAG_ABSORB_V) ? 1 : 0;
+  a.hadamard = had ? 1 : 0;
   a.new_pos = nullptr;
   a.new_n = 0;
   a.fused = 0;

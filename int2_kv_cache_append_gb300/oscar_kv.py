@@ -18,6 +18,7 @@ MAX_SPLITS = 64
 FLAG_ABSORB_V = 1
 FLAG_IN_FP32 = 2
 FLAG_OUT_FP32 = 4
+FLAG_HADAMARD = 8  # rotate by the in-quant Hadamard; R_K / R_V may be None
 
 DEV_OVER_CAPACITY = 1
 DEV_NONFINITE = 2

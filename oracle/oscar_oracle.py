@@ -152,8 +152,8 @@ def hadamard_rotation(d: int) -> np.ndarray:
 
     The llama.cpp model card's environment table [Run] names an in-quant
     Hadamard that models with a baked rotation skip, and a base model without
-    one falls back to data-free INT2 with it; the SGLang run command sets its
-    order to 128.  Read here as: block-diagonal over the d / 128 groups, each
+    one falls back to data-free INT2 with it; the RotationZoo card's SGLang
+    launch [How to use] sets its order to 128.  Read here as: block-diagonal over the d / 128 groups, each
     block the Sylvester Hadamard matrix of order 128, H[i][k] =
     (-1)^popcount(i & k), divided by sqrt(128) so that it is orthogonal.
     """

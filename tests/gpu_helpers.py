@@ -20,6 +20,11 @@ def dev_i32(x):
     return torch.tensor(np.asarray(x, dtype=np.int32), dtype=torch.int32, device="cuda")
 
 
+def dev_rot(R):
+    """A rotation matrix on the device as float32, or None (in-quant Hadamard)."""
+    return None if R is None else dev(R, torch.float32)
+
+
 def new_cache(c: O.Config):
     return torch.zeros(O.layout(c)["total_bytes"], dtype=torch.uint8, device="cuda")
 
@@ -30,8 +35,8 @@ def gpu_append(c: O.Config, cache, layer, k, v, start_pos, RK, RV, want_rot=Fals
     kt, vt = dev(k, dt), dev(v, dt)
     B, n, H, D = k.shape
     rot = torch.empty((B, n, H, 2, D), dtype=torch.float32, device="cuda") if want_rot else None
-    K.kv_append(kcfg(c), cache, layer, kt, vt, dev_i32(start_pos), dev(RK, torch.float32),
-                dev(RV, torch.float32), debug_rot=rot, status=status)
+    K.kv_append(kcfg(c), cache, layer, kt, vt, dev_i32(start_pos), dev_rot(RK), dev_rot(RV),
+                debug_rot=rot, status=status)
     torch.cuda.synchronize()
     return rot
 
@@ -59,7 +64,7 @@ def gpu_decode(c: O.Config, cache, layer, q, seq_lens, RK, RV, sm_scale=0.0, num
                       device="cuda")
     lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
     ws = torch.empty(ws_bytes or lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
-    K.attn_decode(kc, cache, layer, qt, dev_i32(seq_lens), dev(RK, torch.float32), dev(RV, torch.float32), out,
+    K.attn_decode(kc, cache, layer, qt, dev_i32(seq_lens), dev_rot(RK), dev_rot(RV), out,
                   ws, lse=lse, seq_len_hint=hint, sm_scale=sm_scale, num_splits=num_splits, status=status)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)

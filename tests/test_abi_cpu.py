@@ -97,3 +97,22 @@ def test_entry_points_validate_before_launch(lib):
     bad = K.KVConfig(1, 1, 4, 1, 96, 4, 8, 64).c()
     assert lib.attn_decode(ctypes.byref(bad), big, 0, big, big, 0, big, big, 0.0, 1, big, None, big, 1 << 30,
                            None, None) == -5
+
+
+def test_hadamard_flag_makes_rotations_optional(lib):
+    P = ctypes.c_void_p
+    big = P(1 << 20)  # never dereferenced: every call below stops in validation
+    plain = K.KVConfig(1, 1, 4, 1, 128, 4, 8, 64).c()
+    had = K.KVConfig(1, 1, 4, 1, 128, 4, 8, 64, flags=K.FLAG_HADAMARD).c()
+    out = K._Layout()
+    assert lib.kv_layout_query(ctypes.byref(had), ctypes.byref(out)) == 0
+    # without the flag a NULL rotation is an invalid argument ...
+    assert lib.kv_append(ctypes.byref(plain), big, 0, big, big, big, 65, None, big, None, None, None) == -1
+    assert lib.attn_decode(ctypes.byref(plain), big, 0, big, big, 0, big, None, 0.0, 1, big, None, big, 16,
+                           None, None) == -1
+    # ... with it the NULLs pass and validation goes on to the next check
+    assert lib.kv_append(ctypes.byref(had), big, 0, big, big, big, 65, None, None, None, None, None) == -2
+    assert lib.attn_decode(ctypes.byref(had), big, 0, big, big, 0, None, None, 0.0, 1, big, None, big, 16,
+                           None, None) == -3
+    assert lib.decode_step(ctypes.byref(had), big, 0, big, big, big, 1, big, big, 0, None, None, 0.0, 0, big,
+                           None, big, 16, None, None) == -3
