@@ -46,7 +46,10 @@ Readings taken where the pages are silent (each listed in the design doc):
 * data-free in-quant Hadamard (FLAG_HADAMARD): for a model with no calibrated
   rotation, K and V are rotated by the Sylvester Hadamard matrix of order 128
   (normalised by 1/sqrt(128)), block-diagonal over the head_dim groups, and Q
-  and the output use that same matrix in place of R_K and R_V.
+  and the output use that same matrix in place of R_K and R_V;
+* K-only INT2 (FLAG_V_BF16): V is kept high precision, the BF16 of the
+  float32 rotated row for every position in a [B][Hkv][capacity][D] region;
+  K is stored as usual.
 
 The byte layout written by :func:`append` is the one the C header documents
 for the cache (regions, strides, code bit positions); it is implemented here
@@ -67,6 +70,7 @@ FLAG_ABSORB_V = 1
 FLAG_IN_FP32 = 2
 FLAG_OUT_FP32 = 4
 FLAG_HADAMARD = 8
+FLAG_V_BF16 = 16
 
 
 # --------------------------------------------------------------------------
@@ -99,7 +103,8 @@ def _align(x: int) -> int:
 def layout(cfg: Config) -> dict:
     """Byte sizes of one layer's cache, per the header's documented formulas.
 
-    Per layer: K role then V role.  Per role: sink [B][Hkv][S][D] bf16, ring
+    Per layer: K role then V role (with FLAG_V_BF16 the V role is instead
+    [B][Hkv][capacity][D] bf16, one row per position).  Per role: sink [B][Hkv][S][D] bf16, ring
     [B][Hkv][W][D] bf16, codes [B][Hkv][Ncap][D/4] u8, sz [B][Hkv][Ncap][D/128]
     x (fp16 scale, fp16 zero); Ncap = round_up(max(capacity - S, 0), 64); each
     region starts on a 256-byte boundary.
@@ -111,9 +116,11 @@ def layout(cfg: Config) -> dict:
     codes = _align(B * H * ncap * (D // 4))
     sz = _align(B * H * ncap * (D // GROUP) * 4)
     role = sink + ring + codes + sz
+    # with FLAG_V_BF16 the V role is one BF16 row per position
+    v_role = _align(B * H * cfg.capacity * D * 2) if cfg.flags & FLAG_V_BF16 else role
     return dict(ncap=ncap, sink_bytes=sink, ring_bytes=ring, codes_bytes=codes,
-                sz_bytes=sz, role_bytes=role, layer_bytes=2 * role,
-                total_bytes=2 * role * cfg.num_layers)
+                sz_bytes=sz, role_bytes=role, v_role_bytes=v_role, layer_bytes=role + v_role,
+                total_bytes=(role + v_role) * cfg.num_layers)
 
 
 # --------------------------------------------------------------------------
@@ -288,6 +295,12 @@ class CacheView:
         base = layer * lay["layer_bytes"] + role * lay["role_bytes"]
         ncap = lay["ncap"]
         o = base
+        self.full = None
+        if role == 1 and cfg.flags & FLAG_V_BF16:
+            cap = cfg.capacity
+            self.full = buf[o:o + B * H * cap * D * 2].view(np.uint16).reshape(B, H, cap, D)
+            self.sink = self.ring = self.codes = self.sz = None
+            return
         self.sink = buf[o:o + B * H * S * D * 2].view(np.uint16).reshape(B, H, S, D)
         o += lay["sink_bytes"]
         self.ring = buf[o:o + B * H * W * D * 2].view(np.uint16).reshape(B, H, W, D)
@@ -313,8 +326,9 @@ def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new:
     R_K, R_V: [D][D] rotations of this layer (ignored with FLAG_HADAMARD,
     which rotates both by :func:`hadamard_rotation`).  Every position p >= S gets its
     INT2 row; p < S also goes to the BF16 sink; p >= start_pos[b] + n - W also
-    goes to the BF16 ring slot p mod W.  Positions outside [0, capacity) are
-    not stored.
+    goes to the BF16 ring slot p mod W.  With FLAG_V_BF16 the V row of every
+    position goes to the V role's BF16 row p instead.  Positions outside
+    [0, capacity) are not stored.
     """
     B, n, H, D = k_new.shape
     S, W, cap = cfg.sink, cfg.recent, cfg.capacity
@@ -335,6 +349,9 @@ def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new:
                 p = int(start_pos[b]) + t
                 if p < 0 or p >= cap:
                     continue  # outside the cache: not stored
+                if view.full is not None:
+                    view.full[b, :, p, :] = rb[b, t]  # V kept BF16 at every position
+                    continue
                 if p < S:
                     view.sink[b, :, p, :] = rb[b, t]
                 else:
@@ -362,6 +379,8 @@ def regions(T: int, S: int, W: int):
 def dequant_history(cfg: Config, cache: np.ndarray, layer: int, role: int, b: int, h: int, T: int):
     """[T, D] float64 values the decode attends to for one (b, kv head)."""
     view = CacheView(cfg, cache, layer, role)
+    if view.full is not None:
+        return bf16_bits_to_f32(view.full[b, h, :T]).astype(np.float64)
     D, S, W = cfg.head_dim, cfg.sink, cfg.recent
     n_sink, tq, n_int, n_ring = regions(T, S, W)
     out = np.zeros((T, D), dtype=np.float64)

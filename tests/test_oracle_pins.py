@@ -515,3 +515,77 @@ def test_hadamard_spreads_a_one_hot_row_to_two_levels(j):
             signs = O.hadamard_rotation(128)[j] > 0
             assert np.array_equal(codes == 3, signs)
             assert zero == float(np.float16(-t))
+
+
+# --------------------------------------------------------------------------
+# K-only INT2 (FLAG_V_BF16): V kept BF16 at every position
+# --------------------------------------------------------------------------
+def test_v_bf16_layout_sizes():
+    base = O.Config(3, 2, 8, 4, 256, 16, 32, 1000, 0.96, 0.92)
+    vb = O.Config(3, 2, 8, 4, 256, 16, 32, 1000, 0.96, 0.92, flags=O.FLAG_V_BF16)
+    a, b = O.layout(base), O.layout(vb)
+    for key in ("ncap", "sink_bytes", "ring_bytes", "codes_bytes", "sz_bytes", "role_bytes"):
+        assert a[key] == b[key]                                   # the K role is unchanged
+    v = 2 * 4 * 1000 * 256 * 2                                    # one bf16 row per position
+    assert b["v_role_bytes"] == -(-v // 256) * 256
+    assert b["layer_bytes"] == b["role_bytes"] + b["v_role_bytes"]
+    assert b["total_bytes"] == 3 * b["layer_bytes"]
+    assert a["v_role_bytes"] == a["role_bytes"] and a["layer_bytes"] == 2 * a["role_bytes"]
+
+
+def _exact_lattice_rows(rng, shape):
+    # per 128-group x = z + s c with s, z and every x exact in fp16 and bf16 and
+    # codes 0 and 3 present: the codec (clip ratio 1) and the BF16 windows both
+    # return x exactly
+    B, T, H, D = shape
+    x = np.empty(shape, dtype=np.float32)
+    for idx in np.ndindex(B, T, H):
+        for j in range(D // 128):
+            s = float(rng.choice([0.25, 0.5, 0.75, 1.25]))
+            z = float(rng.choice([-3.0, -2.0, -1.5, -0.75]))
+            c = rng.integers(0, 4, 128)
+            c[0], c[1] = 0, 3
+            x[idx][128 * j:128 * (j + 1)] = z + s * c
+    return x
+
+
+def test_v_bf16_decode_equals_library_sdpa_on_exact_k():
+    # with K exact in every storage form and V kept BF16, the decode over every
+    # position (sink, INT2 region and ring alike) is plain attention over (K, V)
+    B, H, G, D, T = 2, 2, 2, 128, 40
+    cfg = O.Config(1, B, H * G, H, D, 4, 6, 64, 1.0, 0.92, flags=O.FLAG_V_BF16)
+    rng = np.random.default_rng(31)
+    k = _exact_lattice_rows(rng, (B, T, H, D))
+    v = S.to_bf16_values(rng.standard_normal((B, T, H, D)).astype(np.float32))
+    q = S.to_bf16_values(rng.standard_normal((B, H * G, D)).astype(np.float32))
+    I = np.eye(D, dtype=np.float32)
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, v, [0, 0], I, I)
+    lens = [T, T]  # the ring holds the last W appended positions: decode at the appended length
+    out, lse = O.decode(cfg, cache, 0, q, lens, I, I)
+    for b in range(B):
+        Tb = lens[b]
+        qt = torch.from_numpy(q[b].astype(np.float64))[:, None, :]                       # Hq,1,D
+        kt = torch.from_numpy(k[b, :Tb].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        vt = torch.from_numpy(v[b, :Tb].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0].numpy()
+        assert np.abs(out[b] - ref).max() < 1e-12
+        sc = torch.einsum("hd,htd->ht", qt[:, 0], kt) / math.sqrt(D)
+        assert np.abs(lse[b] - torch.logsumexp(sc, -1).numpy()).max() < 1e-12
+
+
+def test_v_bf16_equals_int2_v_mode_when_everything_is_in_the_windows():
+    # S + W >= T: both modes attend BF16 copies of the same rotated rows
+    rng = np.random.default_rng(32)
+    k = S.to_bf16_values(rng.standard_normal((2, 30, 2, 128)).astype(np.float32))
+    v = S.to_bf16_values(rng.standard_normal((2, 30, 2, 128)).astype(np.float32))
+    q = S.to_bf16_values(rng.standard_normal((2, 4, 128)).astype(np.float32))
+    rk, rv = S.qr_rotation(rng, 128).astype(np.float32), S.qr_rotation(rng, 128).astype(np.float32)
+    outs = []
+    for flags in (0, O.FLAG_V_BF16):
+        cfg = O.Config(1, 2, 4, 2, 128, 10, 20, 64, 0.96, 0.92, flags=flags)
+        cache = O.new_cache(cfg)
+        O.append(cfg, cache, 0, k, v, [0, 0], rk, rv)
+        outs.append(O.decode(cfg, cache, 0, q, [30, 17], rk, rv))
+    assert np.abs(outs[0][0] - outs[1][0]).max() < 1e-12
+    assert np.abs(outs[0][1] - outs[1][1]).max() < 1e-12
