@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--hadamard", action="store_true",
                     help="data-free in-quant Hadamard rotation instead of the calibrated R_K / R_V")
+    ap.add_argument("--v-bf16", action="store_true", help="K-only INT2: V kept BF16 at every position")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -59,8 +60,9 @@ def rotation_desc(args) -> str:
     return "in-quant Hadamard H_128 (data-free)" if getattr(args, "hadamard", False) else "calibrated R_K, R_V"
 
 
-def kv_bytes_per_bh(w, T: int) -> int:
-    """Algorithmic K+V bytes one decode step reads for one (sequence, KV head)."""
+def kv_bytes_per_bh(w, T: int, v_bf16: bool = False) -> int:
+    """Algorithmic K+V bytes one decode step reads for one (sequence, KV head)
+    (with V kept BF16, an INT2 position reads K codes + scale/zero and a BF16 V row)."""
     D = w.head_dim
     S, W = w.sink, w.recent
     if T <= S:
@@ -69,6 +71,8 @@ def kv_bytes_per_bh(w, T: int) -> int:
         tq = max(S, T - W)
         n_i2 = tq - S
         n_bf = S + (T - tq)
+    if v_bf16:
+        return n_i2 * (D // 4 + 4 * (D // 128) + 2 * D) + n_bf * 2 * 2 * D
     return n_i2 * 2 * (D // 4 + 4 * (D // 128)) + n_bf * 2 * 2 * D
 
 
@@ -165,7 +169,8 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # CPU oracle sample (test infrastructure, timed as the CPU baseline)
 # --------------------------------------------------------------------------
-def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False):
+def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
+                      v_bf16: bool = False):
     """Run inside a single-threaded child process: time the oracle's decode step
     (append of the current token + attention) for batch row 0 of the workload,
     restricted to its first `heads` KV heads (and their query heads)."""
@@ -177,7 +182,7 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadama
     T = w.context
     G = w.num_q_heads // w.num_kv_heads
     c = O.Config(1, 1, G * heads, heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip,
-                 flags=O.FLAG_HADAMARD if hadamard else 0)
+                 flags=(O.FLAG_HADAMARD if hadamard else 0) | (O.FLAG_V_BF16 if v_bf16 else 0))
     RK, RV = (None, None) if hadamard else S.rotations(w, 0)
     k, v = S.kv_rows(w, 0, T, batch=1)
     k, v = k[:, :, :heads], v[:, :, :heads]
@@ -194,12 +199,13 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadama
     print(json.dumps({"sec_per_step": statistics.mean(times), "steps": len(times)}))
 
 
-def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False):
+def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
+                   v_bf16: bool = False):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", "--workload", workload,
            "--steps", str(steps), "--warmup", str(warmup), "--sample-heads", str(heads)] + (
-               ["--hadamard"] if hadamard else [])
+               ["--hadamard"] if hadamard else []) + (["--v-bf16"] if v_bf16 else [])
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
@@ -217,7 +223,7 @@ def reference_arm(args):
     # about 75 ms of oracle work per KV head and step at T=16384: keep the run near two minutes
     heads = max(1, min(w.num_kv_heads, int(120.0 / (0.075 * (steps + args.warmup) * w.context / 16384))))
     t0 = time.time()
-    res = run_cpu_sample(args.workload, steps, args.warmup, heads, args.hadamard)
+    res = run_cpu_sample(args.workload, steps, args.warmup, heads, args.hadamard, args.v_bf16)
     sec = res["sec_per_step"]
     value = (heads / w.num_kv_heads) / sec  # the sample is heads/Hkv of one sequence's decode step
     sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}, {heads} of "
@@ -263,7 +269,8 @@ def ours(args):
 
     w = S.WORKLOADS[args.workload]
     L, Bsz, Hq, Hkv, D, T = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.context
-    flags = (K.FLAG_ABSORB_V if w.absorb_v else 0) | (K.FLAG_HADAMARD if args.hadamard else 0)
+    flags = ((K.FLAG_ABSORB_V if w.absorb_v else 0) | (K.FLAG_HADAMARD if args.hadamard else 0)
+             | (K.FLAG_V_BF16 if args.v_bf16 else 0))
     cfg = K.KVConfig(L, Bsz, Hq, Hkv, D, w.sink, w.recent, T, w.k_clip, w.v_clip, flags)
     lay = K.layout_query(cfg)
     stream = torch.cuda.current_stream()
@@ -386,7 +393,7 @@ def ours(args):
 
     if rank != 0:
         return
-    kv_bytes = kv_bytes_per_bh(w, T) * Bsz * Hkv * L
+    kv_bytes = kv_bytes_per_bh(w, T, args.v_bf16) * Bsz * Hkv * L
     tokens_per_s = whole_job_tokens_per_s(Bsz, world, ms)
     peak, peak_kind = measured_peaks()
     split_avg_ms = statistics.mean(split_ms)
@@ -394,7 +401,8 @@ def ours(args):
     step_gbs = kv_bytes / (ms / 1e3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv, hadamard=args.hadamard)
+        res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv, hadamard=args.hadamard,
+                             v_bf16=args.v_bf16)
         cpu = {"value": 1.0 / res["sec_per_step"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"oracle decode step (append + attention) for 1 of {Bsz} sequences of {args.workload}, "
                          f"T={T}, {res['steps']} timed steps, single thread"}
@@ -404,11 +412,14 @@ def ours(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(w), "step": "decode_step per layer: kv_append(1 token/seq) + attn_decode in one call",
                    "rotation": rotation_desc(args),
-                   "l2": "flushed between steps (512 MiB write)", "cache": "int2+bf16", "parallelism":
+                   "l2": "flushed between steps (512 MiB write)",
+                   "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16", "parallelism":
                        f"replica x{world}" if world > 1 else "single"},
         "kv_gbs": step_gbs, "kv_pct_hbm": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": split_kernel_traffic(args.workload), "kernel": "split_kernel (attn_decode)",
+                     # the committed counters were taken with calibrated rotations and INT2 V
+                     "traffic": None if (args.v_bf16 or args.hadamard) else split_kernel_traffic(args.workload),
+                     "kernel": "split_kernel (attn_decode)",
                      "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": kv_bytes // L},
         "e2e": {"value": world * Bsz / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -531,7 +542,7 @@ def ours_append(args):
 def main():
     args = parse()
     if args.cpu_sample_worker:
-        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard)
+        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard, args.v_bf16)
         return
     if args.impl == "reference":
         reference_arm(args)

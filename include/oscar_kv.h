@@ -69,6 +69,11 @@
  *     V: word 8j + g (g = 0..7); bit 2n (n = 0..15) = channel 128j + 8n + g.
  *   These orders let the decode kernel feed codes straight into tensor-core
  *   fragments.
+ *   K-only INT2 (OSCAR_FLAG_V_BF16) [model card, Run: a high-precision V cache
+ *   type keeps V high precision, at more memory]: the K role is as above; the
+ *   V role is instead
+ *   full  [B][Hkv][capacity][D] bf16  row p = position p, for every position,
+ *   and v_role_bytes = align256(B * Hkv * capacity * D * 2).
  *
  * Windows at decode time for a sequence of length T: sink = [0, min(S, T)),
  * ring = [max(S, T - W), T), INT2 = [S, max(S, T - W)).
@@ -103,8 +108,9 @@ enum {
   OSCAR_FLAG_ABSORB_V = 1, /* attn_decode returns o' (rotated basis); caller folds R_V^T into W_o */
   OSCAR_FLAG_IN_FP32 = 2,  /* k_new, v_new and q are float32 instead of bf16 */
   OSCAR_FLAG_OUT_FP32 = 4, /* attn_decode writes float32 instead of bf16 */
-  OSCAR_FLAG_HADAMARD = 8  /* rotate K, V, q and the output by the in-quant Hadamard H (above);
+  OSCAR_FLAG_HADAMARD = 8, /* rotate K, V, q and the output by the in-quant Hadamard H (above);
                               R_K and R_V are ignored and may be NULL */
+  OSCAR_FLAG_V_BF16 = 16   /* K-only INT2: V kept BF16 at every position (layout below) */
 };
 
 /* return codes */
@@ -114,7 +120,8 @@ typedef enum {
   OSCAR_ERR_CAPACITY = -2,    /* n_new or the seq-length hint exceeds capacity */
   OSCAR_ERR_WORKSPACE = -3,   /* workspace smaller than one split needs */
   OSCAR_ERR_LAUNCH = -4,      /* a CUDA launch or attribute call failed */
-  OSCAR_ERR_UNSUPPORTED = -5  /* head_dim not in {128, 256, 512}, group != 128, G > 8 */
+  OSCAR_ERR_UNSUPPORTED = -5  /* head_dim not in {128, 256, 512}, group != 128, G > 8, or a decode
+                                 whose B * Hkv * (S, W or, with OSCAR_FLAG_V_BF16, capacity) >= 2^31 */
 } oscar_status;
 
 /* bits OR-ed into *dev_status by the kernels */
@@ -144,12 +151,13 @@ typedef struct {
 typedef struct {
   uint64_t ncap;         /* INT2 rows per (sequence, KV head) */
   uint64_t sink_bytes, ring_bytes, codes_bytes, sz_bytes; /* one role of one layer */
-  uint64_t role_bytes;   /* sink + ring + codes + sz */
-  uint64_t layer_bytes;  /* 2 * role_bytes (K then V) */
+  uint64_t role_bytes;   /* K role: sink + ring + codes + sz */
+  uint64_t layer_bytes;  /* role_bytes + v_role_bytes (K then V) */
   uint64_t total_bytes;  /* num_layers * layer_bytes */
   uint64_t decode_workspace_bytes; /* attn_decode workspace with OSCAR_KV_MAX_SPLITS slots */
   int32_t max_splits;    /* OSCAR_KV_MAX_SPLITS */
   int32_t reserved;
+  uint64_t v_role_bytes; /* V role: role_bytes, or with OSCAR_FLAG_V_BF16 the BF16 rows */
 } oscar_kv_layout;
 
 /*

@@ -64,6 +64,11 @@ struct DecCfg {
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
   static constexpr int BF_BYTES = 2 * BOXES * BOX_BYTES;
   static constexpr int STAGE = ((I2_BYTES > BF_BYTES ? I2_BYTES : BF_BYTES) + 1023) / 1024 * 1024;
+  // K-only INT2 block (V kept BF16): 16 rows of K codes, their scale/zero,
+  // then the V rows as BF16 boxes (1 KB aligned for the 128-byte swizzle)
+  static constexpr int VB_SZ = kBfTok * ROWB;
+  static constexpr int VB_V = (kBfTok * ROWB + kBfTok * Dg * 4 + 1023) / 1024 * 1024;
+  static_assert(VB_V + BOXES * BOX_BYTES <= STAGE, "a K-only INT2 block fits a stage");
   // Each team owns NSTW private stages: it issues the bulk copies of its own
   // blocks into them and consumes them in order, so a stage's barrier phases
   // are produced and awaited by one team only.
@@ -93,6 +98,7 @@ struct DecCfg {
 // Per-(b, kv head) region sizes and the block list
 struct Regions {
   int T, n_sink, tq, n_int, n_ring;
+  int i2tok;            // tokens per INT2 block
   int ra, rlen1, nrb1;  // ring: first slot, positions before the slot wrap, their blocks
   int nsb, nib, nrb;
   int64_t cbf, ci2;
@@ -101,9 +107,12 @@ struct Regions {
 __host__ __device__ inline int imin(int x, int y) { return x < y ? x : y; }
 __host__ __device__ inline int imax(int x, int y) { return x > y ? x : y; }
 
-__host__ __device__ inline Regions make_regions(int T, int S, int W, int D) {
+// vb: V kept BF16 at every position; INT2 blocks then hold 16 tokens of INT2
+// K codes and BF16 V rows, and weigh like a BF16 block.
+__host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int vb) {
   Regions r;
   r.T = T;
+  r.i2tok = vb ? kBfTok : kI2Tok;
   if (T <= S) {
     r.n_sink = T; r.tq = T; r.n_int = 0; r.n_ring = 0;
   } else {
@@ -113,7 +122,7 @@ __host__ __device__ inline Regions make_regions(int T, int S, int W, int D) {
     r.n_ring = T - r.tq;
   }
   r.nsb = (r.n_sink + kBfTok - 1) / kBfTok;
-  r.nib = (r.n_int + kI2Tok - 1) / kI2Tok;
+  r.nib = (r.n_int + r.i2tok - 1) / r.i2tok;
   // ring positions [tq, T) sit in slots p mod W: cut them where the slots wrap
   // so that every block reads consecutive slots
   r.ra = r.n_ring > 0 ? r.tq % W : 0;
@@ -124,7 +133,7 @@ __host__ __device__ inline Regions make_regions(int T, int S, int W, int D) {
   // (a 128-token INT2 block takes ~1.7x a 16-token BF16 block for ~1.1x the
   // bytes: the codes are unpacked and the scale/zero algebra is extra work)
   r.cbf = int64_t(6) * D;
-  r.ci2 = int64_t(10) * D;
+  r.ci2 = vb ? r.cbf : int64_t(10) * D;
   return r;
 }
 
@@ -191,7 +200,8 @@ struct SegD {      // one segment: a unit's part of a CTA's slice
   int slot, nseg;  // partial slot of this CTA, CTAs sharing the unit
   // the unit's block list (the fields of Regions that block_of reads)
   int n_sink, n_int, n_ring, nsb, nib, ra, rlen1, nrb1;
-  int pad0, pad1;
+  int i2tok;       // tokens per INT2 block
+  int pad1;
 };
 
 // block_at on a segment's copy of its unit's block list
@@ -200,7 +210,7 @@ __device__ __forceinline__ Blk block_of(const SegD& r, int k) {
   if (k < r.nsb) {
     b.type = 0; b.first = k * kBfTok; b.count = min(kBfTok, r.n_sink - b.first);
   } else if (k < r.nsb + r.nib) {
-    b.type = 1; b.first = (k - r.nsb) * kI2Tok; b.count = min(kI2Tok, r.n_int - b.first);
+    b.type = 1; b.first = (k - r.nsb) * r.i2tok; b.count = min(r.i2tok, r.n_int - b.first);
   } else {
     const int kr = k - r.nsb - r.nib;
     b.type = 2;
@@ -213,6 +223,14 @@ __device__ __forceinline__ Blk block_of(const SegD& r, int k) {
     }
   }
   return b;
+}
+
+// Position of ring slot `slot` of a segment's unit: the ring holds positions
+// [tq, T) in slots p mod W, cut into the run from slot ra and the wrapped run
+// from slot 0.
+__device__ __forceinline__ int ring_pos(const SegD& r, int slot) {
+  const int tq = r.n_sink + r.n_int;
+  return slot >= r.ra ? tq + slot - r.ra : tq + r.rlen1 + slot;
 }
 
 // 2^e as a float, for -126 <= e <= 127
@@ -259,7 +277,7 @@ __device__ __forceinline__ int64_t div_small(int64_t x, int64_t d) {
 
 template <int D>
 __device__ __forceinline__ int64_t seq_cost(const DecodeArgs& a, const int* lens, int b) {
-  return b < a.g.B ? unit_cost(make_regions(seq_len_at(a, lens, b), a.g.S, a.g.W, D)) : 0;
+  return b < a.g.B ? unit_cost(make_regions(seq_len_at(a, lens, b), a.g.S, a.g.W, D, a.g.vb)) : 0;
 }
 
 template <int D>
@@ -348,7 +366,7 @@ __device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& 
     const int64_t uu = u + lane;
     const int b = int(uu) / g.Hkv, h = int(uu) % g.Hkv;
     const int T = uu < U ? seq_len_at(a, lens, b) : 0;
-    const Regions rg = make_regions(T, g.S, g.W, D);
+    const Regions rg = make_regions(T, g.S, g.W, D, g.vb);
     const int64_t cu = uu < U ? unit_cost(rg) : 0;
     int64_t incl = cu;
 #pragma unroll
@@ -365,7 +383,7 @@ __device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& 
       d.b = b; d.h = h;
       d.n_sink = rg.n_sink; d.n_int = rg.n_int; d.n_ring = rg.n_ring;
       d.nsb = rg.nsb; d.nib = rg.nib; d.ra = rg.ra; d.rlen1 = rg.rlen1; d.nrb1 = rg.nrb1;
-      d.pad0 = 0; d.pad1 = 0;
+      d.i2tok = rg.i2tok; d.pad1 = 0;
       d.kb = first_block_at(rg, max(lo, s0) - s0);
       d.ke = first_block_at(rg, min(hi, e0) - s0);
       if (pl.aligned) {
@@ -666,24 +684,36 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) {
         const int n4 = (bk.count + 3) & ~3;
         const uint32_t cb = n4 * C::ROWB, sb = n4 * C::Dg * 4;
-        mbar_arrive_expect_tx(full, 2 * cb + 2 * sb);
         const int64_t row = bh * g.ncap + bk.first;
-        bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
-        bulk_g2s(dst + kI2Tok * C::ROWB, vbase + codes_off + row * C::ROWB, cb, full);
-        bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
-        bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb, full);
+        if (g.vb) {
+          // K codes and scale/zero, and the BF16 V rows of the same positions
+          mbar_arrive_expect_tx(full, cb + sb + C::BOXES * C::BOX_BYTES);
+          bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
+          bulk_g2s(dst + C::VB_SZ, kbase + sz_off + row * C::Dg * 4, sb, full);
+          const int vrow = int(bh * g.cap + g.S + bk.first);
+#pragma unroll
+          for (int q = 0; q < C::BOXES; ++q) tma_load_2d(dst + C::VB_V + q * C::BOX_BYTES, &tvs, 64 * q, vrow, full);
+        } else {
+          mbar_arrive_expect_tx(full, 2 * cb + 2 * sb);
+          bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
+          bulk_g2s(dst + kI2Tok * C::ROWB, vbase + codes_off + row * C::ROWB, cb, full);
+          bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
+          bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb, full);
+        }
       }
     } else {
       // 16 rows of K and V as 64-column boxes, 128-byte swizzled by the TMA unit
+      // (with V kept BF16, V rows come from the position-indexed V map)
       if (lane == 0) {
         mbar_arrive_expect_tx(full, 2 * C::BOXES * C::BOX_BYTES);
         const CUtensorMap* mk = bk.type == 0 ? &tks : &tkr;
-        const CUtensorMap* mv = bk.type == 0 ? &tvs : &tvr;
+        const CUtensorMap* mv = (bk.type == 0 || g.vb) ? &tvs : &tvr;
         const int row0 = int(bk.type == 0 ? bh * g.S + bk.first : bh * g.W + bk.first);
+        const int vrow0 = g.vb ? int(bh * g.cap + (bk.type == 0 ? bk.first : ring_pos(sd, bk.first))) : row0;
 #pragma unroll
         for (int q = 0; q < C::BOXES; ++q) {
           tma_load_2d(dst + q * C::BOX_BYTES, mk, 64 * q, row0, full);
-          tma_load_2d(dst + (C::BOXES + q) * C::BOX_BYTES, mv, 64 * q, row0, full);
+          tma_load_2d(dst + (C::BOXES + q) * C::BOX_BYTES, mv, 64 * q, vrow0, full);
         }
       }
     }
@@ -700,6 +730,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (bk.type == 1) {
       const int p0 = g.S + bk.first;
       return p0 < st + n && max(st, g.S) < p0 + bk.count;
+    }
+    if (g.vb) {  // the V rows of a ring block sit at its positions
+      const int p0 = ring_pos(sx, bk.first);
+      if (p0 < st + n && st < p0 + bk.count) return true;
     }
     const int w0 = max(max(st, st + n - g.W), 0), wn = st + n - w0;  // ring positions written
     if (wn <= 0) return false;
@@ -882,7 +916,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const Blk bk = block_of(sd, sd.kb + team + j * C::NTEAMS);
         const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
-        const bool is_i2 = bk.type == 1;
+        // is_i2: K and V from INT2 codes (128-token block); kv16: K-only INT2
+        // block (V kept BF16): 16 tokens of INT2 K codes with BF16 V rows
+        const bool is_i2 = bk.type == 1 && !g.vb;
+        const bool kv16 = bk.type == 1 && g.vb;
         if (is_i2 != o_i2) {
           scale_o(is_i2 ? 1 : -1);
           o_i2 = is_i2;
@@ -953,6 +990,38 @@ __global__ void __launch_bounds__(kThreads, 2)
                 s[mt][nq][1] = fmaf(ksc[mt][1], (acc[i][nq][2] + acc[i][nq][3]) * qF[nq], kze[mt][1] * qsum[nq]);
               }
             }
+          }
+        } else if (kv16) {
+          // one m-tile: the INT2 scores of the 128-token path for tokens gq, gq + 8
+          const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + C::VB_SZ);
+          const uint2 w0 = *reinterpret_cast<const uint2*>(st + gq * C::ROWB + wt * 32 + cq * 8);
+          const uint2 w1 = *reinterpret_cast<const uint2*>(st + (gq + 8) * C::ROWB + wt * 32 + cq * 8);
+          float acc[NQT][4];
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nq][e] = 0.f;
+#pragma unroll
+          for (int wi = 0; wi < 2; ++wi) {
+            uint32_t r0[8], r1[8];
+            unpack16(wi ? w0.y : w0.x, r0);
+            unpack16(wi ? w1.y : w1.x, r1);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+              for (int nq = 0; nq < NQT; ++nq)
+                mma_f16(acc[nq], r0[2 * k4], r1[2 * k4], r0[2 * k4 + 1], r1[2 * k4 + 1], qf[4 * wi + k4][nq][0],
+                        qf[4 * wi + k4][nq][1]);
+          }
+          const uint32_t z0 = ksz[gq * C::Dg + wt], z1 = ksz[(gq + 8) * C::Dg + wt];
+          const float sc0 = __half2float(__ushort_as_half(z0 & 0xffff));
+          const float ze0 = __half2float(__ushort_as_half(z0 >> 16));
+          const float sc1 = __half2float(__ushort_as_half(z1 & 0xffff));
+          const float ze1 = __half2float(__ushort_as_half(z1 >> 16));
+#pragma unroll
+          for (int nq = 0; nq < NQT; ++nq) {
+            s[0][nq][0] = fmaf(sc0, (acc[nq][0] + acc[nq][1]) * qF[nq], ze0 * qsum[nq]);
+            s[0][nq][1] = fmaf(sc1, (acc[nq][2] + acc[nq][3]) * qF[nq], ze1 * qsum[nq]);
           }
         } else {
           const uint32_t kb_s = smem_u32(st);
@@ -1109,7 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             bw0[nq] = movmatrix_trans(split_bf16(p[0][nq][0]));
             bw1[nq] = movmatrix_trans(split_bf16(p[0][nq][1]));
           }
-          const uint32_t vb_s = smem_u32(st + C::BOXES * C::BOX_BYTES);
+          const uint32_t vb_s = smem_u32(st + (kv16 ? C::VB_V : C::BOXES * C::BOX_BYTES));
           const int mi = lane >> 3;
           const int tok = (lane & 7) + 8 * (mi >> 1);
           const bool partial = cnt < kBfTok;
@@ -1226,7 +1295,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           // any is used: a unit shared by many CTAs costs a few L2 round trips
           constexpr int D4 = D / 4;
           constexpr int IPT4 = C::HEADS * D4 / kThreads;
-          constexpr int SU = IPT4 >= 8 ? 2 : 16 / IPT4;
+          constexpr int SU = IPT4 >= 8 ? 1 : 16 / IPT4;
           static_assert(IPT4 * kThreads == C::HEADS * D4, "whole float4 chunks per thread");
           float4 acc[IPT4];
           float Mr[IPT4], Lr[IPT4];
@@ -1475,12 +1544,15 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   const uint8_t* kb = a.layer_base;
   const uint8_t* vb = a.layer_base + g.role_bytes;
   const uint64_t bh = uint64_t(g.B) * g.Hkv;
-  if (g.S > 0 && (!encode_rows_bf16(&maps[0], kb, bh * g.S, D, 64, kBfTok) ||
-                  !encode_rows_bf16(&maps[1], vb, bh * g.S, D, 64, kBfTok)))
-    return OSCAR_ERR_LAUNCH;
-  if (g.W > 0 && (!encode_rows_bf16(&maps[2], kb + g.sink_bytes, bh * g.W, D, 64, kBfTok) ||
-                  !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)))
-    return OSCAR_ERR_LAUNCH;
+  if (g.S > 0 && !encode_rows_bf16(&maps[0], kb, bh * g.S, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
+  if (g.W > 0 && !encode_rows_bf16(&maps[2], kb + g.sink_bytes, bh * g.W, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
+  if (g.vb) {
+    // V kept BF16: one map over its [B*Hkv*cap][D] rows, indexed by position
+    if (!encode_rows_bf16(&maps[1], vb, bh * uint64_t(g.cap), D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
+  } else {
+    if (g.S > 0 && !encode_rows_bf16(&maps[1], vb, bh * g.S, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
+    if (g.W > 0 && !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
+  }
   if (launch_pdl(split_kernel<D, NQT>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
                  maps[2], maps[3], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
@@ -1510,7 +1582,7 @@ int decode_grid(const Geom& g, int seq_len_hint, int num_splits) {
   // context of seq_len_hint implies (a CTA's fixed cost, ~10 us of set-up and
   // merge, runs in parallel with the others, so small problems spread wide)
   const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
-  const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D);
+  const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D, g.vb);
   const int64_t min_cost = int64_t(kNCW / g.Dg) * r.cbf;
   const int64_t by_work = std::max<int64_t>(1, unit_cost(r) * units / min_cost);
   return int(std::max<int64_t>(1, std::min(resident, by_work)));

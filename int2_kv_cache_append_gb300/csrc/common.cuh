@@ -19,6 +19,8 @@ struct Geom {
   int B, Hq, Hkv, D, G, Dg, S, W, cap;
   int64_t ncap;
   uint64_t sink_bytes, ring_bytes, codes_bytes, sz_bytes, role_bytes, layer_bytes;
+  int vb;                 // V kept BF16 at every position (K-only INT2)
+  uint64_t v_role_bytes;  // V role: role_bytes, or with vb [B][Hkv][cap][D] bf16
 };
 
 __host__ __device__ inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }

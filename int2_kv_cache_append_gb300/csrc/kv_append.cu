@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const AppendA
 //      OR their slots together.
 // Waits on the copies are bounded; on a timeout the CTA flags
 // OSCAR_DEV_TIMEOUT, waits (bounded) for its copies in flight and returns.
+// With V kept BF16 (K-only INT2) the V rows are stored as BF16 at their
+// positions instead of quantised.
 // With HAD (the in-quant Hadamard) steps 1 and 2 are replaced: each warp loads
 // its rows and transforms every 128-channel group in registers
 // (hadamard128_warp); no rotation matrix is read.
@@ -417,6 +419,12 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
     if (!finite && lane == 0) status_or(a.status, OSCAR_DEV_NONFINITE);
     const float tclip = __fmul_rn(ratio, amax);
 
+    if (role == 1 && g.vb) {  // K-only INT2: the V row is kept BF16 at its position
+      __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(role_base + (bh * g.cap + p) * (2 * D));
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) dv[lane + 32 * e] = __float2bfloat16_rn(v[e]);
+      continue;
+    }
     const bool to_sink = p < g.S;
     const bool to_ring = g.W > 0 && p >= newlen - g.W;
     if (to_sink || to_ring) {
@@ -547,7 +555,8 @@ int launch_append(const AppendArgs& a, cudaStream_t stream) {
       default: return OSCAR_ERR_UNSUPPORTED;
     }
   }
-  if (a.rows <= kSmallAppendRows) {
+  // K-only INT2 (V kept BF16) is written by the row-parallel kernel at every size
+  if (a.rows <= kSmallAppendRows || a.g.vb) {
     switch (a.g.D) {
       case 128: return launch_append_small<128>(a, stream);
       case 256: return launch_append_small<256>(a, stream);

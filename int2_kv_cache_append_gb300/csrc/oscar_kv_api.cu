@@ -15,7 +15,8 @@ int validate(const oscar_kv_config* c) {
     return OSCAR_ERR_INVALID;
   if (c->num_q_heads % c->num_kv_heads != 0) return OSCAR_ERR_INVALID;
   if (!(c->k_clip > 0.f && c->k_clip <= 1.f) || !(c->v_clip > 0.f && c->v_clip <= 1.f)) return OSCAR_ERR_INVALID;
-  if (c->flags & ~uint32_t(OSCAR_FLAG_ABSORB_V | OSCAR_FLAG_IN_FP32 | OSCAR_FLAG_OUT_FP32 | OSCAR_FLAG_HADAMARD))
+  if (c->flags & ~uint32_t(OSCAR_FLAG_ABSORB_V | OSCAR_FLAG_IN_FP32 | OSCAR_FLAG_OUT_FP32 | OSCAR_FLAG_HADAMARD |
+                           OSCAR_FLAG_V_BF16))
     return OSCAR_ERR_INVALID;
   if (c->group_size != OSCAR_KV_GROUP) return OSCAR_ERR_UNSUPPORTED;
   if (c->head_dim != 128 && c->head_dim != 256 && c->head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
@@ -42,7 +43,9 @@ Geom make_geom(const oscar_kv_config* c) {
   g.codes_bytes = oscar::align256(bh * uint64_t(g.ncap) * (g.D / 4));
   g.sz_bytes = oscar::align256(bh * uint64_t(g.ncap) * g.Dg * 4);
   g.role_bytes = g.sink_bytes + g.ring_bytes + g.codes_bytes + g.sz_bytes;
-  g.layer_bytes = 2 * g.role_bytes;
+  g.vb = (c->flags & OSCAR_FLAG_V_BF16) ? 1 : 0;
+  g.v_role_bytes = g.vb ? oscar::align256(bh * uint64_t(g.cap) * g.D * 2) : g.role_bytes;
+  g.layer_bytes = g.role_bytes + g.v_role_bytes;
   return g;
 }
 
@@ -104,6 +107,10 @@ int prep_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
     return OSCAR_ERR_INVALID;
   if (seq_len_hint > cfg->capacity) return OSCAR_ERR_CAPACITY;
   const Geom g = make_geom(cfg);
+  // the decode's TMA row coordinates are 32-bit: rows of each BF16 map must fit
+  const uint64_t bhk = uint64_t(g.B) * g.Hkv;
+  const uint64_t map_rows = bhk * uint64_t(g.vb ? (g.cap > g.S ? g.cap : g.S) : g.S);
+  if (map_rows >= (uint64_t(1) << 31) || bhk * uint64_t(g.W) >= (uint64_t(1) << 31)) return OSCAR_ERR_UNSUPPORTED;
   const int hint = seq_len_hint > 0 ? seq_len_hint : cfg->capacity;
   // partial slots per (sequence, query head): as many as the workspace holds,
   // up to OSCAR_KV_MAX_SPLITS; an explicit split count must fit in full
@@ -170,6 +177,7 @@ int kv_layout_query(const oscar_kv_config* cfg, oscar_kv_layout* out) {
   out->sz_bytes = g.sz_bytes;
   out->role_bytes = g.role_bytes;
   out->layer_bytes = g.layer_bytes;
+  out->v_role_bytes = g.v_role_bytes;
   out->total_bytes = g.layer_bytes * uint64_t(cfg->num_layers);
   out->decode_workspace_bytes = oscar::decode_workspace_bytes(g, OSCAR_KV_MAX_SPLITS);
   out->max_splits = OSCAR_KV_MAX_SPLITS;

@@ -19,6 +19,7 @@ FLAG_ABSORB_V = 1
 FLAG_IN_FP32 = 2
 FLAG_OUT_FP32 = 4
 FLAG_HADAMARD = 8  # rotate by the in-quant Hadamard; R_K / R_V may be None
+FLAG_V_BF16 = 16  # K-only INT2: V kept BF16 at every position
 
 DEV_OVER_CAPACITY = 1
 DEV_NONFINITE = 2
@@ -52,7 +53,7 @@ class _Layout(ctypes.Structure):
                 ("codes_bytes", ctypes.c_uint64), ("sz_bytes", ctypes.c_uint64), ("role_bytes", ctypes.c_uint64),
                 ("layer_bytes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
                 ("decode_workspace_bytes", ctypes.c_uint64), ("max_splits", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("v_role_bytes", ctypes.c_uint64)]
 
 
 @dataclass
