@@ -98,7 +98,6 @@ struct DecCfg {
 // Per-(b, kv head) region sizes and the block list
 struct Regions {
   int T, n_sink, tq, n_int, n_ring;
-  int i2tok;            // tokens per INT2 block
   int ra, rlen1, nrb1;  // ring: first slot, positions before the slot wrap, their blocks
   int nsb, nib, nrb;
   int64_t cbf, ci2;
@@ -112,7 +111,6 @@ __host__ __device__ inline int imax(int x, int y) { return x > y ? x : y; }
 __host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int vb) {
   Regions r;
   r.T = T;
-  r.i2tok = vb ? kBfTok : kI2Tok;
   if (T <= S) {
     r.n_sink = T; r.tq = T; r.n_int = 0; r.n_ring = 0;
   } else {
@@ -122,7 +120,8 @@ __host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int 
     r.n_ring = T - r.tq;
   }
   r.nsb = (r.n_sink + kBfTok - 1) / kBfTok;
-  r.nib = (r.n_int + r.i2tok - 1) / r.i2tok;
+  static_assert(kI2Tok == 128 && kBfTok == 16, "block counts below are shifts");
+  r.nib = vb ? (r.n_int + 15) >> 4 : (r.n_int + 127) >> 7;  // shifts: this runs in every plan pass
   // ring positions [tq, T) sit in slots p mod W: cut them where the slots wrap
   // so that every block reads consecutive slots
   r.ra = r.n_ring > 0 ? r.tq % W : 0;
@@ -200,17 +199,19 @@ struct SegD {      // one segment: a unit's part of a CTA's slice
   int slot, nseg;  // partial slot of this CTA, CTAs sharing the unit
   // the unit's block list (the fields of Regions that block_of reads)
   int n_sink, n_int, n_ring, nsb, nib, ra, rlen1, nrb1;
-  int i2tok;       // tokens per INT2 block
-  int pad1;
+  int pad0, pad1;
 };
 
-// block_at on a segment's copy of its unit's block list
+// block_at on a segment's copy of its unit's block list (VB: 16-token
+// INT2 blocks of the K-only INT2 cache)
+template <bool VB>
 __device__ __forceinline__ Blk block_of(const SegD& r, int k) {
+  constexpr int I2T = VB ? kBfTok : kI2Tok;
   Blk b;
   if (k < r.nsb) {
     b.type = 0; b.first = k * kBfTok; b.count = min(kBfTok, r.n_sink - b.first);
   } else if (k < r.nsb + r.nib) {
-    b.type = 1; b.first = (k - r.nsb) * r.i2tok; b.count = min(r.i2tok, r.n_int - b.first);
+    b.type = 1; b.first = (k - r.nsb) * I2T; b.count = min(I2T, r.n_int - b.first);
   } else {
     const int kr = k - r.nsb - r.nib;
     b.type = 2;
@@ -383,7 +384,7 @@ __device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& 
       d.b = b; d.h = h;
       d.n_sink = rg.n_sink; d.n_int = rg.n_int; d.n_ring = rg.n_ring;
       d.nsb = rg.nsb; d.nib = rg.nib; d.ra = rg.ra; d.rlen1 = rg.rlen1; d.nrb1 = rg.nrb1;
-      d.i2tok = rg.i2tok; d.pad1 = 0;
+      d.pad0 = 0; d.pad1 = 0;
       d.kb = first_block_at(rg, max(lo, s0) - s0);
       d.ke = first_block_at(rg, min(hi, e0) - s0);
       if (pl.aligned) {
@@ -609,7 +610,9 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
 // ---------------------------------------------------------------------------
 // split kernel
 // ---------------------------------------------------------------------------
-template <int D, int NQT>
+// VB: the cache keeps V as BF16 at every position (K-only INT2); a separate
+// instantiation, so the default kernel carries none of that block type's code
+template <int D, int NQT, bool VB>
 __global__ void __launch_bounds__(kThreads, 2)
     split_kernel(const __grid_constant__ CUtensorMap tks, const __grid_constant__ CUtensorMap tvs,
                  const __grid_constant__ CUtensorMap tkr, const __grid_constant__ CUtensorMap tvr,
@@ -676,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // calling warp (lane 0 arms the barrier with the byte count first).
   auto issue_block = [&](int si, int k, int stage) {
     const SegD& sd = seg[si];
-    const Blk bk = block_of(sd, k);
+    const Blk bk = block_of<VB>(sd, k);
     const int64_t bh = int64_t(sd.b) * g.Hkv + sd.h;
     const uint32_t full = smem_u32(&bars[stage]);
     const uint32_t dst = smem_u32(smem + C::OFF_STAGE + stage * C::STAGE);
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int n4 = (bk.count + 3) & ~3;
         const uint32_t cb = n4 * C::ROWB, sb = n4 * C::Dg * 4;
         const int64_t row = bh * g.ncap + bk.first;
-        if (g.vb) {
+        if constexpr (VB) {
           // K codes and scale/zero, and the BF16 V rows of the same positions
           mbar_arrive_expect_tx(full, cb + sb + C::BOXES * C::BOX_BYTES);
           bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
@@ -707,9 +710,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) {
         mbar_arrive_expect_tx(full, 2 * C::BOXES * C::BOX_BYTES);
         const CUtensorMap* mk = bk.type == 0 ? &tks : &tkr;
-        const CUtensorMap* mv = (bk.type == 0 || g.vb) ? &tvs : &tvr;
+        const CUtensorMap* mv = (bk.type == 0 || VB) ? &tvs : &tvr;
         const int row0 = int(bk.type == 0 ? bh * g.S + bk.first : bh * g.W + bk.first);
-        const int vrow0 = g.vb ? int(bh * g.cap + (bk.type == 0 ? bk.first : ring_pos(sd, bk.first))) : row0;
+        const int vrow0 = VB ? int(bh * g.cap + (bk.type == 0 ? bk.first : ring_pos(sd, bk.first))) : row0;
 #pragma unroll
         for (int q = 0; q < C::BOXES; ++q) {
           tma_load_2d(dst + q * C::BOX_BYTES, mk, 64 * q, row0, full);
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // append writes (sink positions and INT2 rows of [new_pos, new_pos + new_n),
   // ring slots of its last min(new_n, W) positions)?
   auto written = [&](const SegD& sx, int k) -> bool {
-    const Blk bk = block_of(sx, k);
+    const Blk bk = block_of<VB>(sx, k);
     const int st = a.new_pos[sx.b], n = a.new_n;
     if (n <= 0) return false;
     if (bk.type == 0) return bk.first < min(st + n, g.S) && st < bk.first + bk.count;
@@ -731,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int p0 = g.S + bk.first;
       return p0 < st + n && max(st, g.S) < p0 + bk.count;
     }
-    if (g.vb) {  // the V rows of a ring block sit at its positions
+    if constexpr (VB) {  // the V rows of a ring block sit at its positions
       const int p0 = ring_pos(sx, bk.first);
       if (p0 < st + n && st < p0 + bk.count) return true;
     }
@@ -914,12 +917,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (lane == 0) { abort_flag = 1; status_or(a.status, OSCAR_DEV_TIMEOUT); }
           break;
         }
-        const Blk bk = block_of(sd, sd.kb + team + j * C::NTEAMS);
+        const Blk bk = block_of<VB>(sd, sd.kb + team + j * C::NTEAMS);
         const uint8_t* st = smem + C::OFF_STAGE + stage * C::STAGE;
         // is_i2: K and V from INT2 codes (128-token block); kv16: K-only INT2
         // block (V kept BF16): 16 tokens of INT2 K codes with BF16 V rows
-        const bool is_i2 = bk.type == 1 && !g.vb;
-        const bool kv16 = bk.type == 1 && g.vb;
+        const bool is_i2 = bk.type == 1 && !VB;
+        const bool kv16 = VB && bk.type == 1;
         if (is_i2 != o_i2) {
           scale_o(is_i2 ? 1 : -1);
           o_i2 = is_i2;
@@ -1497,19 +1500,19 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 struct DevInfo {
   int sms = 0;
-  int occ[3][2] = {{0, 0}, {0, 0}, {0, 0}};
+  int occ[3][2][2] = {};  // [head_dim][G > 4][V kept BF16]
   bool ready = false;
 };
 DevInfo g_dev[64];
 
-template <int D, int NQT>
+template <int D, int NQT, bool VB>
 int prepare_split(int dev) {
   using C = DecCfg<D, NQT>;
-  if (cudaFuncSetAttribute(split_kernel<D, NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+  if (cudaFuncSetAttribute(split_kernel<D, NQT, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return -1;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<D, NQT>, kThreads, C::SMEM) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<D, NQT, VB>, kThreads, C::SMEM) !=
       cudaSuccess)
     return -1;
   return occ;
@@ -1519,11 +1522,15 @@ int dinfo_init(int dev) {
   DevInfo& di = g_dev[dev];
   if (di.ready) return 0;
   if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  const int o[6] = {prepare_split<128, 1>(dev), prepare_split<128, 2>(dev), prepare_split<256, 1>(dev),
-                    prepare_split<256, 2>(dev), prepare_split<512, 1>(dev), prepare_split<512, 2>(dev)};
-  for (int i = 0; i < 6; ++i) {
+  const int o[12] = {prepare_split<128, 1, false>(dev), prepare_split<128, 1, true>(dev),
+                     prepare_split<128, 2, false>(dev), prepare_split<128, 2, true>(dev),
+                     prepare_split<256, 1, false>(dev), prepare_split<256, 1, true>(dev),
+                     prepare_split<256, 2, false>(dev), prepare_split<256, 2, true>(dev),
+                     prepare_split<512, 1, false>(dev), prepare_split<512, 1, true>(dev),
+                     prepare_split<512, 2, false>(dev), prepare_split<512, 2, true>(dev)};
+  for (int i = 0; i < 12; ++i) {
     if (o[i] <= 0) return -1;
-    di.occ[i / 2][i % 2] = o[i];
+    di.occ[i / 4][(i / 2) % 2][i % 2] = o[i];
   }
   di.ready = true;
   return 0;
@@ -1531,7 +1538,7 @@ int dinfo_init(int dev) {
 
 int didx(int D) { return D == 128 ? 0 : (D == 256 ? 1 : 2); }
 
-template <int D, int NQT>
+template <int D, int NQT, bool VB>
 int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = DecCfg<D, NQT>;
   const Geom& g = a.g;
@@ -1553,7 +1560,7 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
     if (g.S > 0 && !encode_rows_bf16(&maps[1], vb, bh * g.S, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
     if (g.W > 0 && !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
   }
-  if (launch_pdl(split_kernel<D, NQT>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
+  if (launch_pdl(split_kernel<D, NQT, VB>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
                  maps[2], maps[3], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
@@ -1581,7 +1588,7 @@ int decode_grid(const Geom& g, int seq_len_hint, int num_splits) {
   // fewer, so that each team still gets about one block of the cache a
   // context of seq_len_hint implies (a CTA's fixed cost, ~10 us of set-up and
   // merge, runs in parallel with the others, so small problems spread wide)
-  const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0];
+  const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0][g.vb ? 1 : 0];
   const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D, g.vb);
   const int64_t min_cost = int64_t(kNCW / g.Dg) * r.cbf;
   const int64_t by_work = std::max<int64_t>(1, unit_cost(r) * units / min_cost);
@@ -1592,10 +1599,18 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || dinfo_init(dev) != 0) return OSCAR_ERR_LAUNCH;
   const bool big = a.g.G > 4;
+  if (a.g.vb) {
+    switch (a.g.D) {
+      case 128: return big ? launch_decode_d<128, 2, true>(a, stream) : launch_decode_d<128, 1, true>(a, stream);
+      case 256: return big ? launch_decode_d<256, 2, true>(a, stream) : launch_decode_d<256, 1, true>(a, stream);
+      case 512: return big ? launch_decode_d<512, 2, true>(a, stream) : launch_decode_d<512, 1, true>(a, stream);
+      default: return OSCAR_ERR_UNSUPPORTED;
+    }
+  }
   switch (a.g.D) {
-    case 128: return big ? launch_decode_d<128, 2>(a, stream) : launch_decode_d<128, 1>(a, stream);
-    case 256: return big ? launch_decode_d<256, 2>(a, stream) : launch_decode_d<256, 1>(a, stream);
-    case 512: return big ? launch_decode_d<512, 2>(a, stream) : launch_decode_d<512, 1>(a, stream);
+    case 128: return big ? launch_decode_d<128, 2, false>(a, stream) : launch_decode_d<128, 1, false>(a, stream);
+    case 256: return big ? launch_decode_d<256, 2, false>(a, stream) : launch_decode_d<256, 1, false>(a, stream);
+    case 512: return big ? launch_decode_d<512, 2, false>(a, stream) : launch_decode_d<512, 1, false>(a, stream);
     default: return OSCAR_ERR_UNSUPPORTED;
   }
 }
