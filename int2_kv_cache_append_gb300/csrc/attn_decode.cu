@@ -424,7 +424,8 @@ __device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& 
 // reading anything (q may be produced right before this call) and then at
 // once lets the split kernel launch, whose CTAs start their cache copies
 // while this kernel computes; the split kernel reads q' only after its own
-// wait for this grid's completion.
+// wait for this grid's completion.  In decode_step it computes while the
+// append runs and waits for the append only before exiting.
 // ---------------------------------------------------------------------------
 constexpr int kQrotThreads = 512;
 
@@ -443,12 +444,20 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
   const int c = threadIdx.x & 127, kp = threadIdx.x >> 7;
   const int col = chunk * 128 + c;
   const int64_t q0 = int64_t(bh) * G * D;  // first query head of this kv head
-  // in a fused step (decode_step) the split kernel may launch at once: it only
+  // In a fused step (decode_step) the split kernel may launch at once (it only
   // streams cache blocks the preceding append leaves untouched before waiting
-  // for this grid; otherwise it launches once everything before this call is done
-  if (a.fused) pdl_trigger();
-  pdl_wait();
-  if (!a.fused) pdl_trigger();
+  // for this grid), and this grid does not wait for the append before working:
+  // it reads only q, R_K and seq_lens, complete before the call's append began.
+  // It waits for the append just before exiting, so that its completion, which
+  // the split kernel waits for, still implies the append's.  Otherwise it waits
+  // first (q may be produced right before this call) and then lets the split
+  // kernel launch.
+  if (a.fused) {
+    pdl_trigger();
+  } else {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const int b = bh / a.g.Hkv;
   const int T = clamp_seq_len(a, b);
@@ -466,6 +475,7 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
         static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(0.f);
     }
     if (chunk == 0 && threadIdx.x < G && a.lse) a.lse[q0 / D + threadIdx.x] = -INFINITY;
+    if (a.fused) pdl_wait();
     return;
   }
 
@@ -605,6 +615,7 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
     }
     a.qbfrag[grp * (NQT * 1024) + e] = w;
   }
+  if (a.fused) pdl_wait();  // see above: completion implies the append's
 }
 
 // ---------------------------------------------------------------------------
