@@ -176,6 +176,49 @@ def hadamard_rotation(d: int) -> np.ndarray:
     return R
 
 
+def sylvester_hadamard(n: int) -> np.ndarray:
+    """Sylvester Hadamard matrix of order n (a power of two) divided by sqrt(n),
+    float64: H[i][k] = (-1)^popcount(i & k) / sqrt(n)."""
+    i = np.arange(n)
+    bits = np.bitwise_and.outer(i, i)
+    par = np.zeros_like(bits)
+    while bits.any():
+        par ^= bits & 1
+        bits >>= 1
+    return np.where(par == 1, -1.0, 1.0) / math.sqrt(n)
+
+
+def bit_reversal_index(n: int) -> np.ndarray:
+    """br[i] = i with its log2(n) bits reversed."""
+    b = int(round(math.log2(n)))
+    return np.array([int(format(i, f"0{b}b")[::-1], 2) if b else 0 for i in range(n)])
+
+
+def calibrate_rk(calib_q: np.ndarray) -> np.ndarray:
+    """K-side rotation fitted to a calibration set of query rows, float64 [D][D].
+
+    OSCAR-RotationZoo card [File format]: R_K = R H P_br, R the eigenvectors of
+    the query covariance, H a head-dim Hadamard, P_br the eigenvalue-sorted
+    bit-reversal permutation; hysenlabs article [How the offline rotation is
+    fit]: Q activations are captured offline and the rotation derived from
+    their covariance.  Read as: Sigma = Q^T Q (float64 over the rows); E = its
+    eigenvectors by descending eigenvalue (ties by index), each column signed so
+    that its largest-magnitude entry (the first, on ties) is positive;
+    H = sylvester_hadamard(D); P_br[i, br(i)] = 1, so column j of R_K is column
+    br(j) of E H.  The eigen-solver is the library one (numpy eigh).
+    """
+    q = np.asarray(calib_q, np.float64)
+    d = q.shape[1]
+    sigma = q.T @ q
+    w, e = np.linalg.eigh(sigma)
+    order = np.argsort(-w, kind="stable")
+    e = e[:, order]
+    piv = np.argmax(np.abs(e), axis=0)
+    e = e * np.where(e[piv, np.arange(d)] < 0, -1.0, 1.0)
+    eh = e @ sylvester_hadamard(d)
+    return eh[:, bit_reversal_index(d)]
+
+
 def rotations_of(cfg: "Config", R_K, R_V):
     """(R_K, R_V) a call uses: the given matrices, or the in-quant Hadamard for
     both when cfg.flags has FLAG_HADAMARD (the given ones are then ignored)."""

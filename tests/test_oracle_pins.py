@@ -589,3 +589,55 @@ def test_v_bf16_equals_int2_v_mode_when_everything_is_in_the_windows():
         outs.append(O.decode(cfg, cache, 0, q, [30, 17], rk, rv))
     assert np.abs(outs[0][0] - outs[1][0]).max() < 1e-12
     assert np.abs(outs[0][1] - outs[1][1]).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# calibration of R_K (NEXT row f4)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [2, 8, 128, 512])
+def test_sylvester_hadamard_matches_scipy(n):
+    L = pytest.importorskip("scipy.linalg")
+    assert np.abs(O.sylvester_hadamard(n) - L.hadamard(n) / math.sqrt(n)).max() < 1e-15
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_calibrate_rk_diagonal_closed_form(d):
+    # rows that are scaled unit vectors give a diagonal Sigma with distinct
+    # entries: E is the permutation sorting the channels by scale, so
+    # R[i][j] = (-1)^popcount(rank(i) & br(j)) / sqrt(d), written out by hand
+    rng = np.random.default_rng(41)
+    scale = rng.permutation(np.arange(1, d + 1)).astype(np.float64)
+    q = np.zeros((2 * d, d))
+    for i in range(d):
+        q[2 * i, i] = scale[i]
+        q[2 * i + 1, i] = -scale[i]
+    R = O.calibrate_rk(q)
+    order = sorted(range(d), key=lambda i: -scale[i])
+    rank = {ch: r for r, ch in enumerate(order)}
+    bits = d.bit_length() - 1
+    br = [int(format(j, f"0{bits}b")[::-1], 2) for j in range(d)]
+    for i in range(d):
+        for j in range(0, d, 7):
+            want = (-1.0) ** bin(rank[i] & br[j]).count("1") / math.sqrt(d)
+            assert abs(R[i, j] - want) < 1e-12
+
+
+def test_calibrate_rk_eigen_equation_order_and_signs():
+    # undo H P_br (scipy's Hadamard): the columns of E must satisfy Sigma e = lambda e,
+    # with lambda descending and each column's largest |entry| positive
+    L = pytest.importorskip("scipy.linalg")
+    d = 128
+    calib = S.activations(np.random.default_rng(42), (3000, d), [5, 40, 99], kind="t3")
+    R = O.calibrate_rk(calib)
+    bits = d.bit_length() - 1
+    P = np.zeros((d, d))
+    for i in range(d):
+        P[i, int(format(i, f"0{bits}b")[::-1], 2)] = 1.0
+    E = R @ P.T @ (L.hadamard(d) / math.sqrt(d)).T
+    sig = calib.astype(np.float64).T @ calib.astype(np.float64)
+    lam = np.einsum("ij,ij->j", E, sig @ E)
+    assert np.abs(sig @ E - E * lam).max() < 1e-9 * lam[0]
+    assert np.all(np.diff(lam) <= 1e-9 * lam[0])
+    assert np.abs(E.T @ E - np.eye(d)).max() < 1e-12
+    piv = np.argmax(np.abs(E), axis=0)
+    assert np.all(E[piv, np.arange(d)] > 0)
