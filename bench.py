@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--hadamard", action="store_true",
                     help="data-free in-quant Hadamard rotation instead of the calibrated R_K / R_V")
     ap.add_argument("--v-bf16", action="store_true", help="K-only INT2: V kept BF16 at every position")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="time the R_K calibration (Sigma, eigenvectors, H P_br) instead of the decode step")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -539,8 +541,59 @@ def ours_append(args):
     print(json.dumps(line), flush=True)
 
 
+def calibrate_arm(args):
+    """R_K calibration from 20,000 calibration tokens of the workload's shape
+    (every query head's row pooled): GPU time per calibration, with the oracle
+    (numpy float64 + LAPACK) timed on the same rows as the CPU baseline."""
+    import numpy as np
+    import torch
+
+    from int2_kv_cache_append_gb300 import build as B
+    from int2_kv_cache_append_gb300 import oscar_kv as K
+    from int2_kv_cache_append_gb300 import synth as S
+    B.build()
+    w = S.WORKLOADS[args.workload]
+    D = w.head_dim
+    rows = 20000 * w.num_q_heads
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7)
+    q = S.activations_torch(gen, (rows, D), S.outlier_channels(w.config_id, 0, D))
+    out = torch.empty((D, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.calibrate_workspace_bytes(D), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        K.calibrate_rk(q, out, ws, status=st)
+    steps = max(1, min(args.steps, 20))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        K.calibrate_rk(q, out, ws, status=st)
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    qn = q.cpu().numpy()
+    from oracle import oscar_oracle as O
+    t0 = time.perf_counter()
+    ref = O.calibrate_rk(qn)
+    cpu_s = time.perf_counter() - t0
+    line = {"metric": "R_K calibration time (Sigma = Q^T Q, eigenvectors, H P_br), 1 GB300", "value": ms,
+            "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": steps, "warmup": max(3, args.warmup),
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w), "rows": rows, "head_dim": D,
+                       "inputs": f"{rows * D * 4 / 1e6:.0f} MB of float32 rows (larger than L2)"},
+            "max_abs_diff_vs_oracle": float(np.abs(out.cpu().numpy().astype(np.float64) - ref).max()),
+            "dev_status": int(st.item()),
+            "cpu_baseline": {"value": cpu_s * 1e3, "unit": "ms", "kind": "oracle", "cores": os.cpu_count(),
+                             "sample": "the oracle (numpy float64 Q^T Q + LAPACK eigh) on the same rows"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.calibrate:
+        calibrate_arm(args)
+        return
     if args.cpu_sample_worker:
         cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard, args.v_bf16)
         return

@@ -130,7 +130,8 @@ enum {
   OSCAR_DEV_NONFINITE = 2,     /* a non-finite input row */
   OSCAR_DEV_FP16_RANGE = 4,    /* a scale, zero or scaled query component left the fp16 range */
   OSCAR_DEV_TIMEOUT = 8,       /* a pipeline wait gave up (the kernel returned early) */
-  OSCAR_DEV_EMPTY = 16         /* a sequence had seq_len < 1 (its output is zero) */
+  OSCAR_DEV_EMPTY = 16,        /* a sequence had seq_len < 1 (its output is zero) */
+  OSCAR_DEV_NOT_CONVERGED = 32 /* oscar_calibrate_rk: Jacobi reached its sweep limit */
 };
 
 typedef struct {
@@ -285,6 +286,35 @@ int attn_decode_static(const oscar_kv_config* cfg, const void* cache, int32_t la
  * of that call.  Pass NULL, NULL to stop.  The setting is per host thread.
  */
 int oscar_kv_set_profile_events(void* split_start, void* split_stop);
+
+/*
+ * oscar_calibrate_rk — the K-side rotation fitted to a calibration set of
+ * query rows ["OSCAR-RotationZoo" card, File format: R_K = R H P_br with R the
+ * eigenvectors of the query covariance, H a head-dim Hadamard and P_br the
+ * eigenvalue-sorted bit-reversal permutation; hysenlabs article, How the
+ * offline rotation is fit: activations captured offline, rotation derived
+ * from their covariance].  Offline work, not part of the decode path.
+ *   q          device [n_rows][head_dim] float32 query rows of one layer
+ *              (post-RoPE; every head's rows pooled), 16-byte aligned.
+ *   n_rows     1 .. 2^28.
+ *   R_K_out    device [head_dim][head_dim] float32, row-major, written:
+ *              Sigma = q^T q in float64; E = its eigenvectors (cyclic Jacobi
+ *              in float64) ordered by descending eigenvalue (ties by index),
+ *              each column signed so that its largest-magnitude entry (the
+ *              first, on ties) is positive; R_K = E H P_br with
+ *              H[i][k] = (-1)^popcount(i & k) / sqrt(D) and column j of R_K
+ *              = column br(j) of E H (br reverses the log2 D bits of j).
+ *   workspace  device, >= the size oscar_calibrate_workspace_query returns,
+ *              256-byte aligned; caller owned, contents undefined after.
+ * Launches three kernels on `stream`.  A Jacobi that reaches its sweep limit
+ * (40 sweeps) sets OSCAR_DEV_NOT_CONVERGED in *dev_status; the result is
+ * then the last iterate.  Errors: OSCAR_ERR_INVALID (null or misaligned
+ * pointer, n_rows out of range), OSCAR_ERR_UNSUPPORTED (head_dim),
+ * OSCAR_ERR_WORKSPACE, OSCAR_ERR_LAUNCH.
+ */
+int oscar_calibrate_workspace_query(int32_t head_dim, uint64_t* bytes);
+int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* R_K_out, void* workspace,
+                       uint64_t workspace_bytes, int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liboscar_kv.so")
-SOURCES = ["oscar_kv_api.cu", "kv_append.cu", "kv_append_tc.cu", "attn_decode.cu", "attn_decode_static.cu"]
+SOURCES = ["oscar_kv_api.cu", "kv_append.cu", "kv_append_tc.cu", "attn_decode.cu", "attn_decode_static.cu",
+           "calibrate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

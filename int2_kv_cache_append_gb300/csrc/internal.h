@@ -66,5 +66,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // CTAs of the split kernel: num_splits * B * Hkv, or (num_splits = 0) as many
 // as are resident at once, fewer when a context of seq_len_hint is short.
 int decode_grid(const Geom& g, int seq_len_hint, int num_splits);
+// R_K calibration (calibrate.cu)
+uint64_t calibrate_workspace_bytes(int D);
+int launch_calibrate(const float* q, int64_t n, int D, float* R, void* ws, int32_t* status, cudaStream_t stream);
 
 }  // namespace oscar

@@ -233,4 +233,21 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop) {
   return OSCAR_OK;
 }
 
+int oscar_calibrate_workspace_query(int32_t head_dim, uint64_t* bytes) {
+  if (!bytes) return OSCAR_ERR_INVALID;
+  if (head_dim != 128 && head_dim != 256 && head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
+  *bytes = oscar::calibrate_workspace_bytes(head_dim);
+  return OSCAR_OK;
+}
+
+int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* R_K_out, void* workspace,
+                       uint64_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (head_dim != 128 && head_dim != 256 && head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
+  if (!q || !R_K_out || !workspace || n_rows < 1 || n_rows > (int64_t(1) << 28)) return OSCAR_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(R_K_out, 16) || !aligned(workspace, 256)) return OSCAR_ERR_INVALID;
+  if (workspace_bytes < oscar::calibrate_workspace_bytes(head_dim)) return OSCAR_ERR_WORKSPACE;
+  return oscar::launch_calibrate(q, n_rows, head_dim, R_K_out, workspace, dev_status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

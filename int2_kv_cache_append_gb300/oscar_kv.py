@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LA
 
 # every symbol include/oscar_kv.h declares
 EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "decode_step", "attn_decode_static",
-           "oscar_kv_set_profile_events")
+           "oscar_kv_set_profile_events", "oscar_calibrate_workspace_query", "oscar_calibrate_rk")
 STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -179,3 +179,34 @@ def set_profile_events(start=None, stop=None) -> None:
     """Record torch.cuda.Event pair around the split kernel of later attn_decode calls (None, None stops)."""
     lib().oscar_kv_set_profile_events(None if start is None else ctypes.c_void_p(start.cuda_event),
                                       None if stop is None else ctypes.c_void_p(stop.cuda_event))
+
+
+def _calib_fns():
+    L = lib()
+    if not getattr(L, "_calib_ready", False):
+        L.oscar_calibrate_workspace_query.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_uint64)]
+        L.oscar_calibrate_workspace_query.restype = ctypes.c_int
+        L.oscar_calibrate_rk.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
+        L.oscar_calibrate_rk.restype = ctypes.c_int
+        L._calib_ready = True
+    return L
+
+
+def calibrate_workspace_bytes(head_dim: int) -> int:
+    n = ctypes.c_uint64(0)
+    rc = _calib_fns().oscar_calibrate_workspace_query(int(head_dim), ctypes.byref(n))
+    if rc != 0:
+        raise OscarError("oscar_calibrate_workspace_query", rc)
+    return int(n.value)
+
+
+def calibrate_rk(q, R_out, workspace, status=None, stream=None, check: bool = True) -> int:
+    """R_K fitted to the float32 query rows q [n][D] (see oscar_calibrate_rk); writes R_out [D][D]."""
+    n, d = int(q.shape[0]), int(q.shape[1])
+    rc = _calib_fns().oscar_calibrate_rk(_ptr(q), n, d, _ptr(R_out), _ptr(workspace),
+                                         int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                         _stream(stream))
+    if check and rc != 0:
+        raise OscarError("oscar_calibrate_rk", rc)
+    return rc

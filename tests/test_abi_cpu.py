@@ -117,3 +117,22 @@ def test_hadamard_flag_makes_rotations_optional(lib):
                            None, None) == -3
     assert lib.decode_step(ctypes.byref(had), big, 0, big, big, big, 1, big, big, 0, None, None, 0.0, 0, big,
                            None, big, 16, None, None) == -3
+
+
+def test_calibrate_entry_points_validate_before_launch(lib):
+    P = ctypes.c_void_p
+    big = P(1 << 20)  # never dereferenced: every call below stops in validation
+    n = ctypes.c_uint64(0)
+    assert lib.oscar_calibrate_workspace_query(96, ctypes.byref(n)) == -5
+    assert lib.oscar_calibrate_workspace_query(128, None) == -1
+    for d in (128, 256, 512):
+        assert lib.oscar_calibrate_workspace_query(d, ctypes.byref(n)) == 0
+        assert n.value == 3 * (-(-d * d * 8 // 256) * 256) + 256
+    f = lib.oscar_calibrate_rk
+    f.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, ctypes.c_uint64, P, P]
+    assert f(big, 1000, 96, big, big, 1 << 30, None, None) == -5          # head_dim
+    assert f(None, 1000, 128, big, big, 1 << 30, None, None) == -1        # null rows
+    assert f(big, 0, 128, big, big, 1 << 30, None, None) == -1            # no rows
+    assert f(big, (1 << 28) + 1, 128, big, big, 1 << 30, None, None) == -1
+    assert f(P((1 << 20) + 4), 1000, 128, big, big, 1 << 30, None, None) == -1  # misaligned
+    assert f(big, 1000, 128, big, big, 1000, None, None) == -3            # workspace too small

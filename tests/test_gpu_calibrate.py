@@ -1,0 +1,60 @@
+"""GPU parity of the R_K calibration (oscar_calibrate_rk) against the oracle.
+
+The calibration is unique once the eigenvalues are distinct (descending order,
+sign convention), so R_K is compared entry by entry: the GPU computes Sigma and
+the eigenvectors in float64 (Jacobi) and writes float32; the oracle uses
+float64 and numpy's eigensolver.  Tolerance 1e-5 on entries of magnitude about
+1/sqrt(D), from Jacobi's stopping rule (off-diagonal norm below 1e-13 of the
+Frobenius norm) over the smallest relative eigenvalue gap of these inputs,
+plus float32 rounding.  The diagonal case is exact up to rounding."""
+import numpy as np
+import pytest
+import torch
+
+from int2_kv_cache_append_gb300 import oscar_kv as K
+from int2_kv_cache_append_gb300 import synth as S
+from oracle import oscar_oracle as O
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int2_kv_cache_append_gb300 import build
+    build.build()
+
+
+def _gpu_calibrate(q: np.ndarray):
+    d = q.shape[1]
+    qt = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)).cuda()
+    out = torch.full((d, d), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.calibrate_workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    K.calibrate_rk(qt, out, ws, status=st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64), int(st.item())
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_calibrate_diagonal_case(d):
+    rng = np.random.default_rng(51)
+    scale = rng.permutation(np.arange(1, d + 1)).astype(np.float32)
+    q = np.zeros((2 * d, d), dtype=np.float32)
+    for i in range(d):
+        q[2 * i, i] = scale[i]
+        q[2 * i + 1, i] = -scale[i]
+    got, st = _gpu_calibrate(q)
+    assert st == 0
+    assert np.abs(got - O.calibrate_rk(q)).max() <= 1e-6
+
+
+@pytest.mark.parametrize("d,n", [(128, 4096), (256, 3000), (512, 2048)])
+def test_calibrate_matches_oracle(d, n):
+    rng = np.random.default_rng(d + n)
+    ch = rng.choice(d, max(1, round(0.02 * d)), replace=False)
+    q = S.activations(rng, (n, d), ch, kind="t3")
+    got, st = _gpu_calibrate(q)
+    assert st == 0
+    ref = O.calibrate_rk(q)
+    assert np.abs(got - ref).max() <= 1e-5, np.abs(got - ref).max()
+    assert np.abs(got @ got.T - np.eye(d)).max() <= 1e-5
