@@ -298,16 +298,17 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop);
  *              (post-RoPE; every head's rows pooled), 16-byte aligned.
  *   n_rows     1 .. 2^28.
  *   R_K_out    device [head_dim][head_dim] float32, row-major, written:
- *              Sigma = q^T q in float64; E = its eigenvectors (cyclic Jacobi
- *              in float64) ordered by descending eigenvalue (ties by index),
+ *              Sigma = q^T q in float64; E = its eigenvectors (one-sided
+ *              Jacobi in float64 on a cooperative grid) ordered by descending
+ *              eigenvalue (ties by index),
  *              each column signed so that its largest-magnitude entry (the
  *              first, on ties) is positive; R_K = E H P_br with
  *              H[i][k] = (-1)^popcount(i & k) / sqrt(D) and column j of R_K
  *              = column br(j) of E H (br reverses the log2 D bits of j).
  *   workspace  device, >= the size oscar_calibrate_workspace_query returns,
  *              256-byte aligned; caller owned, contents undefined after.
- * Launches three kernels on `stream`.  A Jacobi that reaches its sweep limit
- * (40 sweeps) sets OSCAR_DEV_NOT_CONVERGED in *dev_status; the result is
+ * Launches three kernels on `stream` (the second as a cooperative launch).
+ * A Jacobi that reaches its sweep limit (40 sweeps) sets OSCAR_DEV_NOT_CONVERGED in *dev_status; the result is
  * then the last iterate.  Errors: OSCAR_ERR_INVALID (null or misaligned
  * pointer, n_rows out of range), OSCAR_ERR_UNSUPPORTED (head_dim),
  * OSCAR_ERR_WORKSPACE, OSCAR_ERR_LAUNCH.

@@ -127,7 +127,7 @@ def test_calibrate_entry_points_validate_before_launch(lib):
     assert lib.oscar_calibrate_workspace_query(128, None) == -1
     for d in (128, 256, 512):
         assert lib.oscar_calibrate_workspace_query(d, ctypes.byref(n)) == 0
-        assert n.value == 3 * (-(-d * d * 8 // 256) * 256) + 256
+        assert n.value == 3 * (-(-d * d * 8 // 256) * 256) + (-(-d * 8 // 256) * 256) + 256
     f = lib.oscar_calibrate_rk
     f.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, ctypes.c_uint64, P, P]
     assert f(big, 1000, 96, big, big, 1 << 30, None, None) == -5          # head_dim
