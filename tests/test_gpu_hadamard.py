@@ -77,6 +77,7 @@ DEC_CASES = [
     (128, 2, 16, 2, 0, 100, [1500, 900], 0),               # S = 0, G = 8
     (128, 2, 4, 2, 64, 256, [200, 64], 0),                 # S + W >= T: all BF16
     (128, 1, 16, 8, 64, 256, [3000], K.FLAG_ABSORB_V),     # G = 2, output in the Hadamard basis
+    (128, 2, 8, 2, 32, 64, [800, 257], K.FLAG_IN_FP32),    # float32 q, k, v: qrot transforms float32 rows
     (256, 2, 8, 2, 8, 16, [400, 150], 0),
     (512, 1, 4, 2, 16, 64, [600], 0),
 ]
@@ -89,9 +90,11 @@ def test_hadamard_decode(case):
     rng = np.random.default_rng(D + B + Hq)
     ch = rng.choice(D, max(1, round(0.02 * D)), replace=False)
     T = max(seq_lens)
-    k = S.to_bf16_values(S.activations(rng, (B, T, Hkv, D), ch))
-    v = S.to_bf16_values(S.activations(rng, (B, T, Hkv, D), ch))
-    q = S.to_bf16_values(S.activations(rng, (B, Hq, D), ch))
+    k = S.activations(rng, (B, T, Hkv, D), ch)
+    v = S.activations(rng, (B, T, Hkv, D), ch)
+    q = S.activations(rng, (B, Hq, D), ch)
+    if not extra & K.FLAG_IN_FP32:
+        k, v, q = S.to_bf16_values(k), S.to_bf16_values(v), S.to_bf16_values(q)
     cache = O.new_cache(c)
     O.append(c, cache, 0, k, v, [0] * B, None, None)
     ref, ref_lse = O.decode(c, cache, 0, q, seq_lens, None, None, absorb_v=bool(extra & K.FLAG_ABSORB_V))
