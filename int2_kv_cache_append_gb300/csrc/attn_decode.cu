@@ -7,13 +7,17 @@
 // to use: V rotation absorbed into the output).
 //
 // Two kernels per call:
-//   qrot   q' = q R_K * sm_scale * log2(e) (float32) and per-group sums of q';
-//          zeroes the merge tickets and writes the output of empty sequences.
+//   qrot   q' = q R_K * sm_scale * log2(e) (float32; with the in-quant
+//          Hadamard a warp transform instead of R_K) written as the split
+//          kernel's ready mma fragments, with per-group sums of q'; zeroes the
+//          merge tickets and writes the output of empty sequences.
 //   split  a persistent grid of P CTAs (by default as many as are resident at
 //          once).  The block lists of all (sequence, KV head) units, in unit
-//          order, are concatenated and cut by bytes into P equal slices, one
-//          per CTA, so every CTA streams the same amount of cache and the
-//          grid ends in one wave.  A slice covers the tail of one unit, whole
+//          order, are concatenated and cut by time-weighted block costs into P
+//          equal slices, one per CTA, so every CTA has the same amount of work
+//          and the grid ends in one wave.  With V kept BF16 (K-only INT2, a
+//          separate instantiation) the INT2 part of a unit is cut into 16-token
+//          blocks of INT2 K codes with BF16 V rows.  A slice covers the tail of one unit, whole
 //          units and the head of another; each such unit part is a segment.
 //          Four warps form teams (one warp per 128-channel quant group); each
 //          team issues the bulk copies of its own blocks (cp.async.bulk for
@@ -33,8 +37,9 @@
 //          the end of a segment the CTA merges its teams and writes one partial
 //          (m, l, o') per head into the segment's slot; the last CTA of a unit
 //          to finish (an atomic ticket, never a wait) merges the unit's slots
-//          by log-sum-exp, applies o = o' R_V^T (skipped when absorbed) and
-//          stores the bf16/fp32 output and lse.
+//          by log-sum-exp in one online pass, applies o = o' R_V^T (o' H with
+//          the in-quant Hadamard; skipped when absorbed) and stores the
+//          bf16/fp32 output and lse.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
