@@ -20,6 +20,9 @@
 //
 // kv_append_rows_kernel, row-parallel, for appends of a few rows (a decode
 // step appends one token per sequence): 4 or 8 rows per CTA, described below.
+// It also takes every append of the in-quant Hadamard mode (rows transformed
+// in registers, no matrix) and of the K-only INT2 mode (V rows stored as BF16
+// at their positions).
 //
 // Both accumulate each rotated value with fp32 FMAs in increasing input-channel
 // order and run the same codec operations, so they write identical bytes.
