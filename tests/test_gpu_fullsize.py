@@ -4,7 +4,8 @@ configuration bench.py times (automatic split count, seq_len_hint = context).
 Inputs are drawn on the GPU with a seeded torch generator.  The GPU builds the
 whole cache with kv_append and decodes all sequences; the oracle rebuilds the
 cache of sampled (sequence, KV head) pairs from the same inputs (copied to the
-host) and decodes them.  With exact rotations (signed permutations) the GPU
+host) and decodes them.  Two tests run the bench's decode_step instead (the
+cache filled to T - 1 tokens, the call appending the last one and decoding).  With exact rotations (signed permutations) the GPU
 cache must equal the oracle's bit for bit on the sampled pairs, and the decode
 outputs must agree within the decode tolerances.  One test also runs the
 calibrated rotations and checks the sampled outputs against the oracle built
@@ -27,8 +28,9 @@ def _built():
     build.build()
 
 
-def _fill(w, cfg, cache, layer, RK, RV, T, seed):
-    """GPU-append T tokens per sequence; returns the bf16 K and V inputs kept on the device."""
+def _fill(w, cfg, cache, layer, RK, RV, T, seed, upto=None):
+    """Draw T tokens per sequence and GPU-append the first `upto` (all by default);
+    returns the bf16 K and V inputs kept on the device."""
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     ch = S.outlier_channels(w.config_id, layer, w.head_dim)
@@ -36,8 +38,9 @@ def _fill(w, cfg, cache, layer, RK, RV, T, seed):
     k = S.activations_torch(gen, shape, ch, dtype=torch.bfloat16)
     v = S.activations_torch(gen, shape, ch, dtype=torch.bfloat16)
     chunk = max(1, (1 << 26) // (w.batch * w.num_kv_heads * w.head_dim))
-    for p in range(0, T, chunk):
-        n = min(chunk, T - p)
+    upto = T if upto is None else upto
+    for p in range(0, upto, chunk):
+        n = min(chunk, upto - p)
         K.kv_append(cfg, cache, layer, k[:, p:p + n].contiguous(), v[:, p:p + n].contiguous(),
                     torch.full((w.batch,), p, dtype=torch.int32, device="cuda"), RK, RV)
     q = S.activations_torch(gen, (w.batch, w.num_q_heads, w.head_dim), ch, dtype=torch.bfloat16)
@@ -72,7 +75,10 @@ def _compare_cache_pair(w, gcache_np, ocfg, ocache, cfg_full, layer, b, h):
         assert np.array_equal(gv.sz[b, h, :n].view(np.uint16), ov.sz[0, 0].view(np.uint16))
 
 
-def _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32):
+def _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32, step_kv=None):
+    """attn_decode over T tokens, or with step_kv = (k, v) of the last token the
+    bench's decode_step: append that token at T - 1, then decode (re-appending
+    the same token writes the same bytes, so it may run twice)."""
     kc = K.KVConfig(**{**cfg.__dict__})
     kc.flags = (kc.flags & ~K.FLAG_OUT_FP32) | (K.FLAG_OUT_FP32 if out_fp32 else 0)
     lay = K.layout_query(kc)
@@ -81,13 +87,17 @@ def _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32):
     ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     seq = torch.full((w.batch,), T, dtype=torch.int32, device="cuda")
-    K.attn_decode(kc, cache, layer, q, seq, RK, RV, out, ws, lse=lse, seq_len_hint=T, status=st)
+    if step_kv is None:
+        K.attn_decode(kc, cache, layer, q, seq, RK, RV, out, ws, lse=lse, seq_len_hint=T, status=st)
+    else:
+        K.decode_step(kc, cache, layer, step_kv[0], step_kv[1], seq - 1, q, seq, RK, RV, out, ws, lse=lse,
+                      seq_len_hint=T, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
-def _run(wname, samples, layers=(0,), rot="perm", T=None, check_bytes=True):
+def _run(wname, samples, layers=(0,), rot="perm", T=None, check_bytes=True, fused=False):
     w = S.WORKLOADS[wname]
     T = T or w.context
     flags = K.FLAG_ABSORB_V if w.absorb_v else 0
@@ -100,9 +110,10 @@ def _run(wname, samples, layers=(0,), rot="perm", T=None, check_bytes=True):
     for layer in layers:
         RKn, RVn = S.rotations(w, layer, kind=rot)
         RK, RV = torch.from_numpy(RKn).cuda(), torch.from_numpy(RVn).cuda()
-        k, v, q = _fill(w, cfg, cache, layer, RK, RV, T, seed=4242 + layer)
-        o16, _ = _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32=False)
-        o32, l32 = _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32=True)
+        k, v, q = _fill(w, cfg, cache, layer, RK, RV, T, seed=4242 + layer, upto=T - 1 if fused else T)
+        step_kv = (k[:, T - 1:T].contiguous(), v[:, T - 1:T].contiguous()) if fused else None
+        o16, _ = _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32=False, step_kv=step_kv)
+        o32, l32 = _decode_all(w, cfg, cache, layer, q, T, RK, RV, out_fp32=True, step_kv=step_kv)
         gnp = cache.cpu().numpy() if check_bytes else None
         for b, h in samples:
             ocfg, ocache, ref, ref_lse = _oracle_pair(w, k, v, q, b, h, T, RKn, RVn)
@@ -121,6 +132,16 @@ def _run(wname, samples, layers=(0,), rot="perm", T=None, check_bytes=True):
 
 def test_full_qwen3_4b_layer():
     _run("qwen3-4b-layer", samples=[(0, 0), (3, 5), (7, 7)])
+
+
+def test_full_qwen3_4b_layer_decode_step():
+    # the bench's step: the cache holds T - 1 tokens, decode_step appends the
+    # last one and decodes over T
+    _run("qwen3-4b-layer", samples=[(0, 0), (4, 2), (7, 7)], fused=True)
+
+
+def test_full_qwen3_32b_decode_step():
+    _run("qwen3-32b-decode", samples=[(0, 0), (0, 7)], fused=True)
 
 
 def test_full_qwen3_4b_layer_calibrated_rotations():
