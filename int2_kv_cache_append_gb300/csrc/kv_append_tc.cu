@@ -301,19 +301,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (ring4) ring4[(32 * c + j) / 8] = q;
           }
         }
+        auto code_of = [&](float r) {
+          const float x = fminf(fmaxf(r, -tclip), tclip);
+          const int code = __float2int_rn(__fmul_rn(__fsub_rn(x, zf), inv));
+          return qok ? uint32_t(min(max(code, 0), 3)) : 0u;
+        };
+        // the role is uniform per CTA: one unrolled loop per code layout
+        if (role == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = fminf(fmaxf(v[j], -tclip), tclip);
-          int code = __float2int_rn(__fmul_rn(__fsub_rn(x, zf), inv));
-          code = qok ? min(max(code, 0), 3) : 0;
-          const int d = 32 * c + j;
-          if (role == 0) {
+          for (int j = 0; j < 32; ++j) {
+            const int d = 32 * c + j;
             const int kk = d >> 4, r16 = d & 15, hh = r16 >> 3, e = r16 & 7;
             const int word = 2 * (e >> 1) + (kk >> 2);
             const int bit = 2 * (2 * (kk & 3) + hh) + 16 * (e & 1);
-            words[word] |= uint32_t(code) << bit;
-          } else {
-            words[d & 7] |= uint32_t(code) << (2 * (d >> 3));
+            words[word] |= code_of(v[j]) << bit;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int d = 32 * c + j;
+            words[d & 7] |= code_of(v[j]) << (2 * (d >> 3));
           }
         }
       }
