@@ -12,11 +12,12 @@
 //   * A tiles of 128 rows are fetched with TMA tensor loads (cp.async.bulk.tensor,
 //     SWIZZLE_128B) into a 2-stage ring.
 //   * One thread of the producer warp issues 3 x 8 tcgen05.mma (M128 N128 K16,
-//     kind::f16, bf16 operands, fp32 accumulate) per tile into a double-buffered
-//     TMEM accumulator and signals completion with tcgen05.commit.
-//   * Eight epilogue warps in two groups (even and odd tiles, one TMEM
-//     accumulator each) read their 32 TMEM lanes (one row per thread) with
-//     tcgen05.ld and run the codec exactly as the CUDA-core kernel does, in two
+//     kind::f16, bf16 operands, fp32 accumulate) per tile into one of four TMEM
+//     accumulators and signals completion with tcgen05.commit.
+//   * Sixteen epilogue warps in four groups (tile 4k + g goes to group g, with
+//     accumulator g; four warps per SM sub-partition hide the codec's latency)
+//     read their 32 TMEM lanes (one row per thread) with tcgen05.ld and run the
+//     codec exactly as the CUDA-core kernel does, in two
 //     passes: row min/max (which give max|x| and, clamping being monotone, the
 //     clipped group min/max), then codes and BF16 copies.
 //
@@ -35,7 +36,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTileRows = 128;
-constexpr int kEpiWarps = 8;                 // two groups of four: even / odd tiles
+constexpr int kEpiWarps = 16;                // four groups of four: tiles 4k + group
 constexpr int kThreadsTc = (kEpiWarps + 1) * 32;
 constexpr uint32_t kKBlockBytes = kTileRows * 128;  // 128 rows x 64 bf16 (128 B), swizzled
 constexpr uint32_t kOperandBytes = 2 * kKBlockBytes; // K = 128 -> two K-blocks
@@ -43,7 +44,7 @@ constexpr uint32_t kOffB = 0;                          // 3 pieces of R^T
 constexpr uint32_t kOffA = 3 * kOperandBytes;          // 2 stages of A
 constexpr uint32_t kOffBar = kOffA + 2 * kOperandBytes;
 constexpr uint32_t kSmemTc = kOffBar + 128 + 1024;     // + alignment slack
-constexpr uint32_t kTmemCols = 256;                    // two 128-column fp32 accumulators
+constexpr uint32_t kTmemCols = 512;                    // four 128-column fp32 accumulators
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
@@ -112,8 +113,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t bar0 = base + kOffBar;
   auto full_a = [&](int s) { return bar0 + 8u * s; };
   auto empty_a = [&](int s) { return bar0 + 16u + 8u * s; };
-  auto acc_full = [&](int s) { return bar0 + 32u + 8u * s; };
-  auto acc_empty = [&](int s) { return bar0 + 48u + 8u * s; };
+  auto acc_full = [&](int s) { return bar0 + 32u + 8u * s; };   // s < 4
+  auto acc_empty = [&](int s) { return bar0 + 64u + 8u * s; };  // s < 4
 
   pdl_trigger();  // a dependent kernel may be scheduled now; it waits for our completion itself
   const int role = blockIdx.y;
@@ -127,8 +128,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(full_a(s), 1);
       mbar_init(empty_a(s), 1);
+    }
+    for (int s = 0; s < 4; ++s) {
       mbar_init(acc_full(s), 1);
-      mbar_init(acc_empty(s), kEpiWarps / 2);
+      mbar_init(acc_empty(s), kEpiWarps / 4);  // the four warps of the group that drains it
     }
     mbar_fence_init();
   }
@@ -172,8 +175,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {
       int it = 0;
       for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-        const int s = it & 1;
+        const int s = it & 1;  // A stage
         const uint32_t ph = (it >> 1) & 1;
+        const int sa = it & 3;  // TMEM accumulator
+        const uint32_t pa = (it >> 2) & 1;
         bool ok = true;
         if (it >= 2) ok = mbar_wait(empty_a(s), ph ^ 1);
         if (ok && !*((volatile int*)&abort_flag)) {
@@ -185,14 +190,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         } else {
           ok = false;
         }
-        if (ok && it >= 2) ok = mbar_wait(acc_empty(s), ph ^ 1);
+        if (ok && it >= 4) ok = mbar_wait(acc_empty(sa), pa ^ 1);
         if (!ok) {
           abort_flag = 1;
           status_or(a.status, OSCAR_DEV_TIMEOUT);
           break;
         }
         tc_fence_after();
-        const uint32_t dcol = tmem + uint32_t(s) * kD;
+        const uint32_t dcol = tmem + uint32_t(sa) * kD;
         const uint32_t a_base = sA + s * kOperandBytes;
 #pragma unroll
         for (int p = 0; p < 3; ++p) {
@@ -203,24 +208,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                       (p | k) != 0);
           }
         }
-        umma_commit(acc_full(s));
+        umma_commit(acc_full(sa));
         umma_commit(empty_a(s));
       }
       // drain: the last (up to two) commits must have landed before TMEM is freed
-      for (int j = (it >= 2 ? it - 2 : 0); j < it; ++j) mbar_wait(acc_full(j & 1), (j >> 1) & 1);
+      for (int j = (it >= 4 ? it - 4 : 0); j < it; ++j) mbar_wait(acc_full(j & 3), (j >> 2) & 1);
     }
   } else {
     // ------------------------------- epilogue --------------------------------
     const Geom& g = a.g;
     const float ratio = role ? a.v_clip : a.k_clip;
     uint8_t* role_base = a.layer_base + role * g.role_bytes;
-    const int grp = warp >> 2, quarter = warp & 3;  // tile parity handled, TMEM lane quarter
+    const int grp = warp >> 2, quarter = warp & 3;  // tile group (= accumulator), TMEM lane quarter
     int it = grp;
     for (int64_t tile = blockIdx.x + int64_t(grp) * gridDim.x; tile < ntiles;
-         tile += 2 * int64_t(gridDim.x), it += 2) {
-      const int s = it & 1;
+         tile += 4 * int64_t(gridDim.x), it += 4) {
+      const int s = it & 3;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(acc_full(s), (it >> 1) & 1);
+      if (lane == 0) ok = mbar_wait(acc_full(s), (it >> 2) & 1);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) { abort_flag = 1; status_or(a.status, OSCAR_DEV_TIMEOUT); }
