@@ -173,29 +173,34 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (warp == kEpiWarps) {
     // ------------------------- producer + MMA issuer -------------------------
     if (lane == 0) {
+      // this CTA's tiles j = 0, 1, ...: tile blockIdx.x + j * gridDim.x, A stage
+      // j & 1; the load of tile j + 1 is issued before waiting for tile j, into
+      // the stage the MMAs of tile j - 1 release
+      const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+      int loaded = 0;
+      auto load = [&](int j) -> bool {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(empty_a(s), ((j >> 1) & 1) ^ 1)) return false;
+        const int64_t tile = blockIdx.x + int64_t(j) * gridDim.x;
+        mbar_arrive_expect_tx(full_a(s), kOperandBytes);
+        const uint32_t dst = sA + s * kOperandBytes;
+        tma_load_2d(dst, tmap, 0, int(tile * kTileRows), full_a(s));
+        tma_load_2d(dst + kKBlockBytes, tmap, 64, int(tile * kTileRows), full_a(s));
+        ++loaded;
+        return true;
+      };
+      bool ok = my_tiles == 0 || load(0);
       int it = 0;
-      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      for (; ok && it < my_tiles; ++it) {
         const int s = it & 1;  // A stage
         const uint32_t ph = (it >> 1) & 1;
         const int sa = it & 3;  // TMEM accumulator
         const uint32_t pa = (it >> 2) & 1;
-        bool ok = true;
-        if (it >= 2) ok = mbar_wait(empty_a(s), ph ^ 1);
-        if (ok && !*((volatile int*)&abort_flag)) {
-          mbar_arrive_expect_tx(full_a(s), kOperandBytes);
-          const uint32_t dst = sA + s * kOperandBytes;
-          tma_load_2d(dst, tmap, 0, int(tile * kTileRows), full_a(s));
-          tma_load_2d(dst + kKBlockBytes, tmap, 64, int(tile * kTileRows), full_a(s));
-          ok = mbar_wait(full_a(s), ph);
-        } else {
-          ok = false;
-        }
+        if (*((volatile int*)&abort_flag)) ok = false;
+        if (ok && it + 1 < my_tiles) ok = load(it + 1);
+        if (ok) ok = mbar_wait(full_a(s), ph);
         if (ok && it >= 4) ok = mbar_wait(acc_empty(sa), pa ^ 1);
-        if (!ok) {
-          abort_flag = 1;
-          status_or(a.status, OSCAR_DEV_TIMEOUT);
-          break;
-        }
+        if (!ok) break;
         tc_fence_after();
         const uint32_t dcol = tmem + uint32_t(sa) * kD;
         const uint32_t a_base = sA + s * kOperandBytes;
@@ -211,7 +216,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         umma_commit(acc_full(sa));
         umma_commit(empty_a(s));
       }
-      // drain: the last (up to two) commits must have landed before TMEM is freed
+      if (!ok) {
+        abort_flag = 1;
+        status_or(a.status, OSCAR_DEV_TIMEOUT);
+        // loads issued for tiles not consumed (at most one ahead) must land
+        // before the CTA exits
+        for (int j = it; j < loaded; ++j) (void)mbar_wait(full_a(j & 1), (j >> 1) & 1);
+      }
+      // drain: the last (up to four) commits must have landed before TMEM is freed
       for (int j = (it >= 4 ? it - 4 : 0); j < it; ++j) mbar_wait(acc_full(j & 3), (j >> 2) & 1);
     }
   } else {
