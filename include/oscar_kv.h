@@ -9,10 +9,10 @@
  *  - kv_append: for every new token and KV head, rotate the post-RoPE key and
  *    value rows by the layer's orthogonal matrices, k' = k R_K, v' = v R_V
  *    ["OSCAR-LLAMACPP-Qwen3-4B-Thinking-2507-INT2-KV" model card, note under
- *    Files: in-graph post-RoPE orthogonal transform on K and V;
+ *    Files: K and V are rotated orthogonally after RoPE, inside the graph;
  *    "OSCAR-RotationZoo" card, File format: one head_dim x head_dim rotation
  *    per layer], clip the row to ratio * max|x| [model card, Run:
- *    LLAMA_KV_CLIP_RATIO, per-row outlier clip before quant; RotationZoo, How
+ *    LLAMA_KV_CLIP_RATIO, a clip of each row before it is quantised; RotationZoo, How
  *    to use: K clip 0.96, V clip 0.92], quantise each group of 128 channels
  *    along head_dim to 2-bit codes with an fp16 scale and zero [RotationZoo,
  *    Available rotations: group128 along head_dim; How to use:

@@ -3,7 +3,7 @@
 // write the BF16 sink / recent-window copies.
 //
 // Source: "OSCAR-LLAMACPP-Qwen3-4B-Thinking-2507-INT2-KV" model card (Files
-// note: post-RoPE orthogonal transform on K and V; Run: per-row clip ratio,
+// note: K and V are rotated orthogonally after RoPE; Run: per-row clip ratio,
 // high-precision sink/recent tokens) and "OSCAR-RotationZoo" (Available
 // rotations: group 128 along head_dim; How to use: K/V clip 0.96/0.92).
 //

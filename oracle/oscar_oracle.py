@@ -14,8 +14,8 @@ Sources (titles of the pages describing OSCAR; section in brackets):
 
 * OSCAR-LLAMACPP-Qwen3-4B-Thinking-2507-INT2-KV model card [Run]: per-row
   outlier clip before quantisation (clip ratio 0.96); first/last tokens kept
-  high-precision (sink 512 / recent 2048); [Files] note: the rotation is a
-  post-RoPE orthogonal transform applied to K and V.
+  high-precision (sink 512 / recent 2048); [Files] note: K and V are rotated
+  by an orthogonal matrix after RoPE.
 * OSCAR-LLAMACPP-Gemma-4-12B-it-INT2-KV card [Folders]: the rotation is applied
   to Q/K (and V); per-layer 512x512 rotations exist (head_dim 512).
 * OSCAR-RotationZoo card [Available rotations]: G is the INT2 quant group size
