@@ -49,7 +49,16 @@ Readings taken where the pages are silent (each listed in the design doc):
   and the output use that same matrix in place of R_K and R_V;
 * K-only INT2 (FLAG_V_BF16): V is kept high precision, the BF16 of the
   float32 rotated row for every position in a [B][Hkv][capacity][D] region;
-  K is stored as usual.
+  K is stored as usual;
+* Lloyd-Max levels (FLAG_LLOYD_MAX; hysenlabs article [Installing OSCAR and
+  running a first Qwen3-8B calibration]: the SGLANG_LLOYD_MAX switch; [Where
+  OSCAR loses]: LM_RATIO=1.16): the four levels of a group are
+  zero + unit * (0, rho, rho + 1, 2 rho + 1), rho = LM_RATIO being the ratio of
+  the outer to the inner gap between adjacent levels (the shape of the
+  four-level Lloyd-Max quantiser of a Gaussian), spread over the group's
+  min..max; rho is 1.16 at a resolution of 2^-8 (297/256) so that levels,
+  midpoints and the span 2 rho + 1 are exact binary fractions; the code is the
+  nearest level, a tie going to the lower one.
 
 The byte layout written by :func:`append` is the one the C header documents
 for the cache (regions, strides, code bit positions); it is implemented here
@@ -71,6 +80,10 @@ FLAG_IN_FP32 = 2
 FLAG_OUT_FP32 = 4
 FLAG_HADAMARD = 8
 FLAG_V_BF16 = 16
+FLAG_LLOYD_MAX = 32
+
+# Lloyd-Max level ratio: 1.16 rounded to a multiple of 2^-8
+LM_RATIO = 297 / 256
 
 
 # --------------------------------------------------------------------------
@@ -228,7 +241,16 @@ def rotations_of(cfg: "Config", R_K, R_V):
     return R_K, R_V
 
 
-def quantize_rows(r: np.ndarray, ratio: float):
+def lloyd_max_levels(rho: float = LM_RATIO) -> np.ndarray:
+    """The four Lloyd-Max levels in units of the group's step: 0, rho, rho+1, 2rho+1.
+
+    Adjacent gaps are rho, 1, rho: the outer gaps are rho times the inner one,
+    as in the four-level Lloyd-Max quantiser of a Gaussian (levels +-0.4528,
+    +-1.510 standard deviations, outer/inner gap 1.167)."""
+    return np.array([0.0, rho, rho + 1.0, 2.0 * rho + 1.0], dtype=np.float64)
+
+
+def quantize_rows(r: np.ndarray, ratio: float, lloyd_max: bool = False):
     """Clip then group-128 asymmetric INT2 quantisation of float32 rows.
 
     r: [N, D] float32 rotated rows.  Returns (codes [N, D] uint8 in 0..3,
@@ -236,10 +258,13 @@ def quantize_rows(r: np.ndarray, ratio: float):
 
     Steps, each a float32 round-to-nearest operation:
       a = max_j |r_j| ; t = ratio * a ; x = min(max(r, -t), t)
-      per group: mn = min x, mx = max x ; s32 = (mx - mn) / 3
+      per group: mn = min x, mx = max x ; s32 = (mx - mn) / span
       scale = fp16(s32) ; zero = fp16(mn)
       scale == 0      -> code 0
-      otherwise inv = 1 / scale ; code = clamp(rint((x - zero) * inv), 0, 3)
+      otherwise inv = 1 / scale ; y = (x - zero) * inv
+    Uniform levels (span 3): code = clamp(rint(y), 0, 3).
+    Lloyd-Max levels (span 2 rho + 1, levels lloyd_max_levels()): code = the
+    number of midpoints between adjacent levels that lie strictly below y.
     A non-finite scale or zero also yields code 0.
     """
     r = np.ascontiguousarray(r, dtype=np.float32)
@@ -251,7 +276,9 @@ def quantize_rows(r: np.ndarray, ratio: float):
     xg = x.reshape(n, ng, GROUP)
     mn = xg.min(axis=2)
     mx = xg.max(axis=2)
-    s32 = ((mx - mn) / np.float32(3.0)).astype(np.float32)
+    lev = lloyd_max_levels()
+    span = np.float32(lev[3]) if lloyd_max else np.float32(3.0)
+    s32 = ((mx - mn) / span).astype(np.float32)
     with np.errstate(over="ignore"):
         scale = s32.astype(np.float16)
         zero = mn.astype(np.float16)
@@ -262,18 +289,24 @@ def quantize_rows(r: np.ndarray, ratio: float):
         inv = np.where(ok, np.float32(1.0) / np.where(ok, sf, np.float32(1.0)), np.float32(0.0))
         inv = inv.astype(np.float32)
         y = ((xg - zf[:, :, None]).astype(np.float32) * inv[:, :, None]).astype(np.float32)
-        q = np.rint(y)
+        if lloyd_max:
+            mids = ((lev[:3] + lev[1:]) / 2).astype(np.float32)
+            q = sum((y > m).astype(np.float64) for m in mids)
+        else:
+            q = np.rint(y)
     q = np.where(ok[:, :, None], q, 0.0)
     codes = np.clip(q, 0, 3).astype(np.uint8).reshape(n, d)
     return codes, scale, zero
 
 
-def dequantize_rows(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
-    """x_hat = zero + scale * code, exact in float64 (fp16 inputs)."""
+def dequantize_rows(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray, lloyd_max: bool = False) -> np.ndarray:
+    """x_hat = zero + scale * level(code), exact in float64 (fp16 inputs);
+    level(c) = c, or lloyd_max_levels()[c] with Lloyd-Max levels."""
     n, d = codes.shape
     s = scale.astype(np.float64).repeat(GROUP, axis=1)
     z = zero.astype(np.float64).repeat(GROUP, axis=1)
-    return z + s * codes.astype(np.float64)
+    lev = lloyd_max_levels()[codes] if lloyd_max else codes.astype(np.float64)
+    return z + s * lev
 
 
 # --------------------------------------------------------------------------
@@ -381,7 +414,7 @@ def append(cfg: Config, cache: np.ndarray, layer: int, k_new: np.ndarray, v_new:
         view = CacheView(cfg, cache, layer, role)
         r = rotate_rows(np.asarray(x, np.float32).reshape(-1, D), R).reshape(B, n, H, D)
         rots.append(r)
-        codes, scale, zero = quantize_rows(r.reshape(-1, D), ratio)
+        codes, scale, zero = quantize_rows(r.reshape(-1, D), ratio, bool(cfg.flags & FLAG_LLOYD_MAX))
         packed = pack_codes(codes, role).reshape(B, n, H, D // 4)
         scale = scale.reshape(B, n, H, -1)
         zero = zero.reshape(B, n, H, -1)
@@ -433,7 +466,7 @@ def dequant_history(cfg: Config, cache: np.ndarray, layer: int, role: int, b: in
         codes = unpack_codes(view.codes[b, h, :n_int], D, role)
         sc = view.sz[b, h, :n_int, :, 0]
         ze = view.sz[b, h, :n_int, :, 1]
-        out[S:tq] = dequantize_rows(codes, sc, ze)
+        out[S:tq] = dequantize_rows(codes, sc, ze, bool(cfg.flags & FLAG_LLOYD_MAX))
     for p in range(tq, T):
         out[p] = bf16_bits_to_f32(view.ring[b, h, p % W])
     return out

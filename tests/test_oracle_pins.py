@@ -641,3 +641,166 @@ def test_calibrate_rk_eigen_equation_order_and_signs():
     assert np.abs(E.T @ E - np.eye(d)).max() < 1e-12
     piv = np.argmax(np.abs(E), axis=0)
     assert np.all(E[piv, np.arange(d)] > 0)
+
+
+# --------------------------------------------------------------------------
+# Lloyd-Max levels (FLAG_LLOYD_MAX)
+# --------------------------------------------------------------------------
+def test_lloyd_max_ratio_is_the_gaussian_lloyd_max_gap_ratio():
+    # Lloyd's iteration for four levels of N(0, 1) (centroid of each cell from the
+    # normal density, boundaries at the midpoints) converges to +-0.4528, +-1.5104;
+    # its outer gap over its inner gap is the ratio the pages set to 1.16, and the
+    # oracle's levels have gaps (rho, 1, rho) with rho that value
+    norm = pytest.importorskip("scipy.stats").norm
+    lv = np.array([-2.0, -0.5, 0.5, 2.0])
+    for _ in range(500):
+        b = np.concatenate([[-np.inf], (lv[:-1] + lv[1:]) / 2, [np.inf]])
+        lv = (norm.pdf(b[:-1]) - norm.pdf(b[1:])) / (norm.cdf(b[1:]) - norm.cdf(b[:-1]))
+    assert abs(lv[3] - 1.5104) < 1e-3 and abs(lv[2] - 0.4528) < 1e-3
+    gauss_ratio = (lv[3] - lv[2]) / (lv[2] - lv[1])
+    lev = O.lloyd_max_levels()
+    gaps = np.diff(lev)
+    assert lev[0] == 0.0 and gaps[1] == 1.0 and gaps[0] == gaps[2] == O.LM_RATIO
+    assert abs(O.LM_RATIO - GOLD["lm_ratio"]["value"]) <= 2.0 ** -9
+    assert abs(O.LM_RATIO - gauss_ratio) < 0.01
+    # every level, midpoint and the span are exact binary fractions (float32)
+    mids = (lev[:3] + lev[1:]) / 2
+    for v in [*lev, *mids]:
+        assert float(np.float32(v)) == v and Fraction(v).denominator <= 512
+
+
+def test_lloyd_max_codec_hand_example():
+    # group 0 spans 0 .. 2 rho + 1 = 850/256, so the unit is exactly 1 and the zero
+    # 0: level midpoints 297/512, 850/512, 1403/512 split the codes; a value on a
+    # midpoint takes the lower level, its float32 neighbours fall either side
+    rho = Fraction(297, 256)
+    up = lambda v: float(np.nextafter(np.float32(v), np.float32(10)))
+    dn = lambda v: float(np.nextafter(np.float32(v), np.float32(-10)))
+    m1, m2, m3 = 297 / 512, 850 / 512, 1403 / 512
+    vals = [0.0, 850 / 256,
+            dn(m1), m1, up(m1),
+            297 / 256, dn(m2), m2, up(m2),
+            553 / 256, dn(m3), m3, up(m3)]
+    r = _row(vals)
+    codes, sc, ze = O.quantize_rows(r, 1.0, lloyd_max=True)
+    assert float(sc[0, 0]) == 1.0 and float(ze[0, 0]) == 0.0
+    assert list(codes[0, :13]) == [0, 3, 0, 0, 1, 1, 1, 1, 2, 2, 2, 2, 3]
+    assert (codes[0, 13:] == 0).all()
+    xh = O.dequantize_rows(codes, sc, ze, lloyd_max=True)
+    assert [Fraction(v) for v in xh[0, [0, 5, 9, 1]]] == [0, rho, rho + 1, 2 * rho + 1]
+
+
+def _lm_lattice_rows(rng, shape):
+    # per 128-group x = z + u * level(c) with u, z multiples of 2^-6 (u <= 4,
+    # |z| <= 8), codes 0 and 3 present: every x and the span are exact in float32,
+    # the unit and zero exact in fp16, so the codec (clip ratio 1) returns x exactly
+    lev = O.lloyd_max_levels()
+    x = np.empty(shape, dtype=np.float32)
+    D = shape[-1]
+    for idx in np.ndindex(*shape[:-1]):
+        for j in range(D // 128):
+            u = rng.integers(1, 257) / 64.0
+            z = -rng.integers(0, 513) / 64.0
+            c = rng.integers(0, 4, 128)
+            c[0], c[1] = 0, 3
+            x[idx][128 * j:128 * (j + 1)] = z + u * lev[c]
+    return x
+
+
+def test_lloyd_max_lattice_rows_round_trip_exactly():
+    rng = np.random.default_rng(13)
+    for d in (128, 256, 512):
+        r = _lm_lattice_rows(rng, (40, d))
+        codes, sc, ze = O.quantize_rows(r, 1.0, lloyd_max=True)
+        xh = O.dequantize_rows(codes, sc, ze, lloyd_max=True)
+        assert np.array_equal(xh, r.astype(np.float64))
+        # the uniform codec does not reproduce these rows
+        cu, su, zu = O.quantize_rows(r, 1.0)
+        assert not np.array_equal(O.dequantize_rows(cu, su, zu), r.astype(np.float64))
+
+
+def test_lloyd_max_codes_are_nearest_levels_and_error_bound():
+    rng = np.random.default_rng(14)
+    n, d = 300, 256
+    r = S.activations(rng, (n, d), [3, 100, 200], kind="t3")
+    lev = O.lloyd_max_levels()
+    rho = O.LM_RATIO
+    for ratio in (1.0, 0.96, 0.92):
+        codes, sc, ze = O.quantize_rows(r, ratio, lloyd_max=True)
+        t = (np.float32(ratio) * np.abs(r).max(axis=1))[:, None]
+        x = np.clip(r, -t, t).astype(np.float64).reshape(n, 2, 128)
+        u = sc.astype(np.float64)[:, :, None]
+        z = ze.astype(np.float64)[:, :, None]
+        # brute force: distance to each of the four levels, in float64
+        dist = np.abs(x[..., None] - (z[..., None] + u[..., None] * lev))
+        best = dist.min(-1)
+        mine = np.take_along_axis(dist, codes.reshape(n, 2, 128)[..., None].astype(np.int64), -1)[..., 0]
+        # the codec decides in float32: a different choice only within rounding of a tie
+        assert np.all(mine - best <= 1e-5 * u)
+        assert np.mean(mine == best) > 0.999
+        # error bound: half the outer gap plus the fp16 rounding of unit and zero
+        mn, mx = x.min(2), x.max(2)
+        s32 = (mx - mn) / (2 * rho + 1)
+        slack = (sc.astype(np.float64) * rho / 2 + (2 * rho + 1) * np.abs(sc.astype(np.float64) - s32)
+                 + np.abs(ze.astype(np.float64) - mn) + 1e-6 * np.abs(mx))
+        xh = O.dequantize_rows(codes, sc, ze, lloyd_max=True).reshape(n, 2, 128)
+        assert (np.abs(xh - x).max(2) <= slack).all()
+
+
+def test_lloyd_max_lowers_squared_error_on_gaussian_rows():
+    # levels shaped like the Gaussian Lloyd-Max quantiser fit Gaussian rows better
+    # than evenly spaced ones over the same min..max; the inverse shape (wide
+    # middle gap) does worse, so this fixes which gap rho multiplies
+    rng = np.random.default_rng(15)
+    r = rng.standard_normal((2000, 128)).astype(np.float32)
+    cu, su, zu = O.quantize_rows(r, 1.0)
+    cl, sl, zl = O.quantize_rows(r, 1.0, lloyd_max=True)
+    mse_u = np.mean((O.dequantize_rows(cu, su, zu) - r) ** 2)
+    mse_l = np.mean((O.dequantize_rows(cl, sl, zl, lloyd_max=True) - r) ** 2)
+    assert mse_l < 0.95 * mse_u
+    # inverse shape, brute-force nearest level over the same span
+    inv = np.array([0.0, 1.0, 1.0 + O.LM_RATIO, 2.0 + O.LM_RATIO]) * (2 * O.LM_RATIO + 1) / (2 + O.LM_RATIO)
+    g = r.reshape(-1, 128).astype(np.float64)
+    mn, mx = g.min(1, keepdims=True), g.max(1, keepdims=True)
+    levels = mn[..., None] + (mx - mn)[..., None] / (2 * O.LM_RATIO + 1) * inv
+    mse_inv = np.mean(np.min((g[..., None] - levels) ** 2, -1))
+    assert mse_inv > mse_u
+
+
+def test_lloyd_max_constant_group_and_flag_layout():
+    r = np.full((1, 128), -0.75, np.float32)
+    codes, sc, ze = O.quantize_rows(r, 1.0, lloyd_max=True)
+    assert float(sc[0, 0]) == 0.0 and float(ze[0, 0]) == -0.75 and (codes == 0).all()
+    # the flag changes the meaning of the codes, not the bytes' layout
+    a = O.layout(O.Config(2, 3, 8, 2, 256, 16, 32, 500))
+    b = O.layout(O.Config(2, 3, 8, 2, 256, 16, 32, 500, flags=O.FLAG_LLOYD_MAX))
+    assert a == b
+
+
+def test_lloyd_max_decode_equals_library_sdpa_on_exact_rows():
+    # S = W = 0: every position is INT2; on Lloyd-Max lattice rows (R = I, clip 1)
+    # both K and V are stored exactly, so the decode is plain attention over (K, V)
+    B, H, G, D, T = 2, 2, 4, 128, 50
+    cfg = O.Config(1, B, H * G, H, D, 0, 0, 64, 1.0, 1.0, flags=O.FLAG_LLOYD_MAX)
+    rng = np.random.default_rng(32)
+    k = _lm_lattice_rows(rng, (B, T, H, D))
+    v = _lm_lattice_rows(rng, (B, T, H, D))
+    q = S.to_bf16_values(rng.standard_normal((B, H * G, D)).astype(np.float32))
+    I = np.eye(D, dtype=np.float32)
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, v, [0, 0], I, I)
+    lens = [T, 31]
+    out, lse = O.decode(cfg, cache, 0, q, lens, I, I)
+    for b in range(B):
+        Tb = lens[b]
+        qt = torch.from_numpy(q[b].astype(np.float64))[:, None, :]
+        kt = torch.from_numpy(k[b, :Tb].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        vt = torch.from_numpy(v[b, :Tb].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0].numpy()
+        assert np.abs(out[b] - ref).max() < 1e-11 * max(1.0, np.abs(ref).max())
+        sc_ = torch.einsum("hd,htd->ht", qt[:, 0], kt) / math.sqrt(D)
+        assert np.abs(lse[b] - torch.logsumexp(sc_, -1).numpy()).max() < 1e-11
+    # the same cache read with uniform levels is a different (wrong) answer
+    plain = O.Config(1, B, H * G, H, D, 0, 0, 64, 1.0, 1.0)
+    out_u, _ = O.decode(plain, cache, 0, q, lens, I, I)
+    assert np.abs(out_u - out).max() > 1e-2
