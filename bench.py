@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--hadamard", action="store_true",
                     help="data-free in-quant Hadamard rotation instead of the calibrated R_K / R_V")
     ap.add_argument("--v-bf16", action="store_true", help="K-only INT2: V kept BF16 at every position")
+    ap.add_argument("--lloyd-max", action="store_true",
+                    help="INT2 codes index the Lloyd-Max levels (0, rho, rho + 1, 2 rho + 1) instead of evenly spaced ones")
     ap.add_argument("--calibrate", action="store_true",
                     help="time the R_K calibration (Sigma, eigenvectors, H P_br) instead of the decode step")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
@@ -172,7 +174,7 @@ class ClockSampler:
 # CPU oracle sample (test infrastructure, timed as the CPU baseline)
 # --------------------------------------------------------------------------
 def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
-                      v_bf16: bool = False):
+                      v_bf16: bool = False, lloyd_max: bool = False):
     """Run inside a single-threaded child process: time the oracle's decode step
     (append of the current token + attention) for batch row 0 of the workload,
     restricted to its first `heads` KV heads (and their query heads)."""
@@ -184,7 +186,8 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadama
     T = w.context
     G = w.num_q_heads // w.num_kv_heads
     c = O.Config(1, 1, G * heads, heads, w.head_dim, w.sink, w.recent, T, w.k_clip, w.v_clip,
-                 flags=(O.FLAG_HADAMARD if hadamard else 0) | (O.FLAG_V_BF16 if v_bf16 else 0))
+                 flags=(O.FLAG_HADAMARD if hadamard else 0) | (O.FLAG_V_BF16 if v_bf16 else 0)
+                 | (O.FLAG_LLOYD_MAX if lloyd_max else 0))
     RK, RV = (None, None) if hadamard else S.rotations(w, 0)
     k, v = S.kv_rows(w, 0, T, batch=1)
     k, v = k[:, :, :heads], v[:, :, :heads]
@@ -202,12 +205,13 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadama
 
 
 def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
-                   v_bf16: bool = False):
+                   v_bf16: bool = False, lloyd_max: bool = False):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", "--workload", workload,
            "--steps", str(steps), "--warmup", str(warmup), "--sample-heads", str(heads)] + (
-               ["--hadamard"] if hadamard else []) + (["--v-bf16"] if v_bf16 else [])
+               ["--hadamard"] if hadamard else []) + (["--v-bf16"] if v_bf16 else []) + (
+               ["--lloyd-max"] if lloyd_max else [])
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
@@ -225,7 +229,7 @@ def reference_arm(args):
     # about 75 ms of oracle work per KV head and step at T=16384: keep the run near two minutes
     heads = max(1, min(w.num_kv_heads, int(120.0 / (0.075 * (steps + args.warmup) * w.context / 16384))))
     t0 = time.time()
-    res = run_cpu_sample(args.workload, steps, args.warmup, heads, args.hadamard, args.v_bf16)
+    res = run_cpu_sample(args.workload, steps, args.warmup, heads, args.hadamard, args.v_bf16, args.lloyd_max)
     sec = res["sec_per_step"]
     value = (heads / w.num_kv_heads) / sec  # the sample is heads/Hkv of one sequence's decode step
     sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}, {heads} of "
@@ -272,7 +276,7 @@ def ours(args):
     w = S.WORKLOADS[args.workload]
     L, Bsz, Hq, Hkv, D, T = w.num_layers, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.context
     flags = ((K.FLAG_ABSORB_V if w.absorb_v else 0) | (K.FLAG_HADAMARD if args.hadamard else 0)
-             | (K.FLAG_V_BF16 if args.v_bf16 else 0))
+             | (K.FLAG_V_BF16 if args.v_bf16 else 0) | (K.FLAG_LLOYD_MAX if args.lloyd_max else 0))
     cfg = K.KVConfig(L, Bsz, Hq, Hkv, D, w.sink, w.recent, T, w.k_clip, w.v_clip, flags)
     lay = K.layout_query(cfg)
     stream = torch.cuda.current_stream()
@@ -404,7 +408,7 @@ def ours(args):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv, hadamard=args.hadamard,
-                             v_bf16=args.v_bf16)
+                             v_bf16=args.v_bf16, lloyd_max=args.lloyd_max)
         cpu = {"value": 1.0 / res["sec_per_step"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"oracle decode step (append + attention) for 1 of {Bsz} sequences of {args.workload}, "
                          f"T={T}, {res['steps']} timed steps, single thread"}
@@ -415,12 +419,15 @@ def ours(args):
         "config": {"workload": workload_desc(w), "step": "decode_step per layer: kv_append(1 token/seq) + attn_decode in one call",
                    "rotation": rotation_desc(args),
                    "l2": "flushed between steps (512 MiB write)",
-                   "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16", "parallelism":
+                   "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16",
+                   "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 297/256" if args.lloyd_max else "uniform",
+                   "parallelism":
                        f"replica x{world}" if world > 1 else "single"},
         "kv_gbs": step_gbs, "kv_pct_hbm": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     # the committed counters were taken with calibrated rotations and INT2 V
-                     "traffic": None if (args.v_bf16 or args.hadamard) else split_kernel_traffic(args.workload),
+                     # the committed counters were taken with calibrated rotations, INT2 V, uniform levels
+                     "traffic": None if (args.v_bf16 or args.hadamard or args.lloyd_max)
+                     else split_kernel_traffic(args.workload),
                      "kernel": "split_kernel (attn_decode)",
                      "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": kv_bytes // L},
@@ -595,7 +602,8 @@ def main():
         calibrate_arm(args)
         return
     if args.cpu_sample_worker:
-        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard, args.v_bf16)
+        cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard, args.v_bf16,
+                          args.lloyd_max)
         return
     if args.impl == "reference":
         reference_arm(args)

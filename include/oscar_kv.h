@@ -50,6 +50,16 @@
  *   clamp(rint_half_even((x - z) * fl(1/s)), 0, 3);
  *   every step is a float32 round-to-nearest operation without FMA.
  *   Dequantised value: z + s * code.
+ * Lloyd-Max levels (OSCAR_FLAG_LLOYD_MAX) [hysenlabs article, Installing
+ * OSCAR and running a first Qwen3-8B calibration: an SGLANG_LLOYD_MAX switch;
+ * Where OSCAR loses: results quoted at LM_RATIO=1.16]: the four levels of a
+ * group are unevenly spaced like the four-level Lloyd-Max quantiser of a
+ * Gaussian, level(c) = (0, rho, rho + 1, 2 rho + 1)[c], with rho = 297/256
+ * (1.16 at a resolution of 2^-8; the outer gaps are rho times the inner one).
+ * The quantiser is as above except s = fp16((mx - mn) / (2 rho + 1)) and, with
+ * y = (x - z) * fl(1/s), code = [y > rho/2] + [y > rho + 1/2] + [y > 3rho/2 + 1]
+ * (the nearest level; on a midpoint, the lower one).  Dequantised value:
+ * z + s * level(code).  The bytes' layout does not change.
  *
  * Cache layout (bytes; every region starts on a 256-byte boundary; the cache
  * base pointer must be 256-byte aligned).  For layer l and role r (0 = K,
@@ -110,7 +120,8 @@ enum {
   OSCAR_FLAG_OUT_FP32 = 4, /* attn_decode writes float32 instead of bf16 */
   OSCAR_FLAG_HADAMARD = 8, /* rotate K, V, q and the output by the in-quant Hadamard H (above);
                               R_K and R_V are ignored and may be NULL */
-  OSCAR_FLAG_V_BF16 = 16   /* K-only INT2: V kept BF16 at every position (layout below) */
+  OSCAR_FLAG_V_BF16 = 16,  /* K-only INT2: V kept BF16 at every position (layout below) */
+  OSCAR_FLAG_LLOYD_MAX = 32 /* INT2 codes index Lloyd-Max levels instead of evenly spaced ones (above) */
 };
 
 /* return codes */

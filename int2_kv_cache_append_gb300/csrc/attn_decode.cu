@@ -626,9 +626,11 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
 // ---------------------------------------------------------------------------
 // split kernel
 // ---------------------------------------------------------------------------
-// VB: the cache keeps V as BF16 at every position (K-only INT2); a separate
-// instantiation, so the default kernel carries none of that block type's code
-template <int D, int NQT, bool VB>
+// VB: the cache keeps V as BF16 at every position (K-only INT2); LM: INT2
+// codes index the Lloyd-Max levels, level(c) = rho * c + kLmHi * (2 c1), so each
+// INT2 product runs a second time over the codes' high bits.  Separate
+// instantiations: the default kernel carries none of either mode's code.
+template <int D, int NQT, bool VB, bool LM>
 __global__ void __launch_bounds__(kThreads, 2)
     split_kernel(const __grid_constant__ CUtensorMap tks, const __grid_constant__ CUtensorMap tvs,
                  const __grid_constant__ CUtensorMap tkr, const __grid_constant__ CUtensorMap tvr,
@@ -994,6 +996,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                             qf[kk][nq][0], qf[kk][nq][1]);
               }
             }
+            // Lloyd-Max levels: the same products over the codes' high bits
+            float acch[MG][NQT][4];
+            if constexpr (LM) {
+#pragma unroll
+              for (int i = 0; i < MG; ++i)
+#pragma unroll
+                for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) acch[i][nq][e] = 0.f;
+#pragma unroll
+              for (int wi = 0; wi < 2; ++wi) {
+                uint32_t r[MG][2][8];
+#pragma unroll
+                for (int i = 0; i < MG; ++i) {
+                  unpack16_hi(wi ? w[i][0].y : w[i][0].x, r[i][0]);
+                  unpack16_hi(wi ? w[i][1].y : w[i][1].x, r[i][1]);
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                  const int kk = 4 * wi + k4;
+#pragma unroll
+                  for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+                    for (int i = 0; i < MG; ++i)
+                      mma_f16(acch[i][nq], r[i][0][2 * k4], r[i][1][2 * k4], r[i][0][2 * k4 + 1],
+                              r[i][1][2 * k4 + 1], qf[kk][nq][0], qf[kk][nq][1]);
+                }
+              }
+            }
 #pragma unroll
             for (int i = 0; i < MG; ++i) {
               const int mt = m0 + i;
@@ -1005,8 +1036,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               kze[mt][1] = __half2float(__ushort_as_half(z1 >> 16));
 #pragma unroll
               for (int nq = 0; nq < NQT; ++nq) {
-                s[mt][nq][0] = fmaf(ksc[mt][0], (acc[i][nq][0] + acc[i][nq][1]) * qF[nq], kze[mt][0] * qsum[nq]);
-                s[mt][nq][1] = fmaf(ksc[mt][1], (acc[i][nq][2] + acc[i][nq][3]) * qF[nq], kze[mt][1] * qsum[nq]);
+                if constexpr (LM) {
+                  const float d0 = fmaf(kLmRho, acc[i][nq][0] + acc[i][nq][1], kLmHi * (acch[i][nq][0] + acch[i][nq][1]));
+                  const float d1 = fmaf(kLmRho, acc[i][nq][2] + acc[i][nq][3], kLmHi * (acch[i][nq][2] + acch[i][nq][3]));
+                  s[mt][nq][0] = fmaf(ksc[mt][0], d0 * qF[nq], kze[mt][0] * qsum[nq]);
+                  s[mt][nq][1] = fmaf(ksc[mt][1], d1 * qF[nq], kze[mt][1] * qsum[nq]);
+                } else {
+                  s[mt][nq][0] = fmaf(ksc[mt][0], (acc[i][nq][0] + acc[i][nq][1]) * qF[nq], kze[mt][0] * qsum[nq]);
+                  s[mt][nq][1] = fmaf(ksc[mt][1], (acc[i][nq][2] + acc[i][nq][3]) * qF[nq], kze[mt][1] * qsum[nq]);
+                }
               }
             }
           }
@@ -1032,6 +1070,25 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mma_f16(acc[nq], r0[2 * k4], r1[2 * k4], r0[2 * k4 + 1], r1[2 * k4 + 1], qf[4 * wi + k4][nq][0],
                         qf[4 * wi + k4][nq][1]);
           }
+          float acch[NQT][4];
+          if constexpr (LM) {  // Lloyd-Max levels: the products over the codes' high bits
+#pragma unroll
+            for (int nq = 0; nq < NQT; ++nq)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acch[nq][e] = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 2; ++wi) {
+              uint32_t r0[8], r1[8];
+              unpack16_hi(wi ? w0.y : w0.x, r0);
+              unpack16_hi(wi ? w1.y : w1.x, r1);
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4)
+#pragma unroll
+                for (int nq = 0; nq < NQT; ++nq)
+                  mma_f16(acch[nq], r0[2 * k4], r1[2 * k4], r0[2 * k4 + 1], r1[2 * k4 + 1], qf[4 * wi + k4][nq][0],
+                          qf[4 * wi + k4][nq][1]);
+            }
+          }
           const uint32_t z0 = ksz[gq * C::Dg + wt], z1 = ksz[(gq + 8) * C::Dg + wt];
           const float sc0 = __half2float(__ushort_as_half(z0 & 0xffff));
           const float ze0 = __half2float(__ushort_as_half(z0 >> 16));
@@ -1039,8 +1096,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float ze1 = __half2float(__ushort_as_half(z1 >> 16));
 #pragma unroll
           for (int nq = 0; nq < NQT; ++nq) {
-            s[0][nq][0] = fmaf(sc0, (acc[nq][0] + acc[nq][1]) * qF[nq], ze0 * qsum[nq]);
-            s[0][nq][1] = fmaf(sc1, (acc[nq][2] + acc[nq][3]) * qF[nq], ze1 * qsum[nq]);
+            if constexpr (LM) {
+              const float d0 = fmaf(kLmRho, acc[nq][0] + acc[nq][1], kLmHi * (acch[nq][0] + acch[nq][1]));
+              const float d1 = fmaf(kLmRho, acc[nq][2] + acc[nq][3], kLmHi * (acch[nq][2] + acch[nq][3]));
+              s[0][nq][0] = fmaf(sc0, d0 * qF[nq], ze0 * qsum[nq]);
+              s[0][nq][1] = fmaf(sc1, d1 * qF[nq], ze1 * qsum[nq]);
+            } else {
+              s[0][nq][0] = fmaf(sc0, (acc[nq][0] + acc[nq][1]) * qF[nq], ze0 * qsum[nq]);
+              s[0][nq][1] = fmaf(sc1, (acc[nq][2] + acc[nq][3]) * qF[nq], ze1 * qsum[nq]);
+            }
           }
         } else {
           const uint32_t kb_s = smem_u32(st);
@@ -1153,6 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int ks = 0; ks < MT_MAX; ++ks) {
             uint32_t bw0[NQT], bw1[NQT];
+            uint32_t bh0[NQT], bh1[NQT];  // Lloyd-Max levels: the high-bit pass's operands
             // V scale/zero of this lane's two tokens (group wt)
             const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + 2 * kI2Tok * C::ROWB) + kI2Tok * C::Dg;
             const int t0 = 16 * ks + gq, t1 = t0 + 8;
@@ -1167,8 +1232,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               const float w0 = v0 ? p[ks][nq][0] * vs0 : 0.f;
               const float w1 = v1 ? p[ks][nq][1] * vs1 : 0.f;
               zeta[nq] += (v0 ? p[ks][nq][0] * vz0 : 0.f) + (v1 ? p[ks][nq][1] * vz1 : 0.f);
-              bw0[nq] = movmatrix_trans(split_f16(w0));
-              bw1[nq] = movmatrix_trans(split_f16(w1));
+              if constexpr (LM) {
+                bw0[nq] = movmatrix_trans(split_f16(w0 * kLmRho));
+                bw1[nq] = movmatrix_trans(split_f16(w1 * kLmRho));
+                bh0[nq] = movmatrix_trans(split_f16(w0 * kLmHi));
+                bh1[nq] = movmatrix_trans(split_f16(w1 * kLmHi));
+              } else {
+                bw0[nq] = movmatrix_trans(split_f16(w0));
+                bw1[nq] = movmatrix_trans(split_f16(w1));
+              }
             }
             // codes of word (wt, gq) for tokens 2cq, 2cq+1, 2cq+8, 2cq+9 of this k-step
             const int ta = 16 * ks + 2 * cq;
@@ -1187,6 +1259,21 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int nq = 0; nq < NQT; ++nq)
                   mma_f16(o[mtd][nq], rx[2 * m4], rx[2 * m4 + 1], ry[2 * m4], ry[2 * m4 + 1], bw0[nq], bw1[nq]);
+              }
+            }
+            if constexpr (LM) {  // + kLmHi * sum of p * scale * (2 c1): the codes' high bits
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint32_t rx[8], ry[8];
+                unpack16_v_hi(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
+                unpack16_v_hi(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+#pragma unroll
+                for (int m4 = 0; m4 < 4; ++m4) {
+                  const int mtd = 4 * hh + m4;
+#pragma unroll
+                  for (int nq = 0; nq < NQT; ++nq)
+                    mma_f16(o[mtd][nq], rx[2 * m4], rx[2 * m4 + 1], ry[2 * m4], ry[2 * m4 + 1], bh0[nq], bh1[nq]);
+                }
               }
             }
           }
@@ -1516,45 +1603,49 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 struct DevInfo {
   int sms = 0;
-  int occ[3][2][2] = {};  // [head_dim][G > 4][V kept BF16]
+  int occ[3][2][2][2] = {};  // [head_dim][G > 4][V kept BF16][Lloyd-Max levels]
   bool ready = false;
 };
 DevInfo g_dev[64];
 
-template <int D, int NQT, bool VB>
+template <int D, int NQT, bool VB, bool LM>
 int prepare_split(int dev) {
   using C = DecCfg<D, NQT>;
-  if (cudaFuncSetAttribute(split_kernel<D, NQT, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+  if (cudaFuncSetAttribute(split_kernel<D, NQT, VB, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return -1;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<D, NQT, VB>, kThreads, C::SMEM) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<D, NQT, VB, LM>, kThreads, C::SMEM) !=
       cudaSuccess)
     return -1;
   return occ;
+}
+
+int didx(int D) { return D == 128 ? 0 : (D == 256 ? 1 : 2); }
+
+template <int D>
+bool prepare_d(int dev, DevInfo& di) {
+  const int o[8] = {prepare_split<D, 1, false, false>(dev), prepare_split<D, 1, true, false>(dev),
+                    prepare_split<D, 2, false, false>(dev), prepare_split<D, 2, true, false>(dev),
+                    prepare_split<D, 1, false, true>(dev),  prepare_split<D, 1, true, true>(dev),
+                    prepare_split<D, 2, false, true>(dev),  prepare_split<D, 2, true, true>(dev)};
+  for (int k = 0; k < 8; ++k) {
+    if (o[k] <= 0) return false;
+    di.occ[didx(D)][(k / 2) % 2][k % 2][k / 4] = o[k];
+  }
+  return true;
 }
 
 int dinfo_init(int dev) {
   DevInfo& di = g_dev[dev];
   if (di.ready) return 0;
   if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  const int o[12] = {prepare_split<128, 1, false>(dev), prepare_split<128, 1, true>(dev),
-                     prepare_split<128, 2, false>(dev), prepare_split<128, 2, true>(dev),
-                     prepare_split<256, 1, false>(dev), prepare_split<256, 1, true>(dev),
-                     prepare_split<256, 2, false>(dev), prepare_split<256, 2, true>(dev),
-                     prepare_split<512, 1, false>(dev), prepare_split<512, 1, true>(dev),
-                     prepare_split<512, 2, false>(dev), prepare_split<512, 2, true>(dev)};
-  for (int i = 0; i < 12; ++i) {
-    if (o[i] <= 0) return -1;
-    di.occ[i / 4][(i / 2) % 2][i % 2] = o[i];
-  }
+  if (!prepare_d<128>(dev, di) || !prepare_d<256>(dev, di) || !prepare_d<512>(dev, di)) return -1;
   di.ready = true;
   return 0;
 }
 
-int didx(int D) { return D == 128 ? 0 : (D == 256 ? 1 : 2); }
-
-template <int D, int NQT, bool VB>
+template <int D, int NQT, bool VB, bool LM>
 int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   using C = DecCfg<D, NQT>;
   const Geom& g = a.g;
@@ -1576,7 +1667,7 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
     if (g.S > 0 && !encode_rows_bf16(&maps[1], vb, bh * g.S, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
     if (g.W > 0 && !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
   }
-  if (launch_pdl(split_kernel<D, NQT, VB>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
+  if (launch_pdl(split_kernel<D, NQT, VB, LM>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
                  maps[2], maps[3], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
@@ -1604,31 +1695,29 @@ int decode_grid(const Geom& g, int seq_len_hint, int num_splits) {
   // fewer, so that each team still gets about one block of the cache a
   // context of seq_len_hint implies (a CTA's fixed cost, ~10 us of set-up and
   // merge, runs in parallel with the others, so small problems spread wide)
-  const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0][g.vb ? 1 : 0];
+  const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0][g.vb ? 1 : 0][g.lm ? 1 : 0];
   const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D, g.vb);
   const int64_t min_cost = int64_t(kNCW / g.Dg) * r.cbf;
   const int64_t by_work = std::max<int64_t>(1, unit_cost(r) * units / min_cost);
   return int(std::max<int64_t>(1, std::min(resident, by_work)));
 }
 
+template <bool VB, bool LM>
+int launch_decode_mode(const DecodeArgs& a, cudaStream_t stream) {
+  const bool big = a.g.G > 4;
+  switch (a.g.D) {
+    case 128: return big ? launch_decode_d<128, 2, VB, LM>(a, stream) : launch_decode_d<128, 1, VB, LM>(a, stream);
+    case 256: return big ? launch_decode_d<256, 2, VB, LM>(a, stream) : launch_decode_d<256, 1, VB, LM>(a, stream);
+    case 512: return big ? launch_decode_d<512, 2, VB, LM>(a, stream) : launch_decode_d<512, 1, VB, LM>(a, stream);
+    default: return OSCAR_ERR_UNSUPPORTED;
+  }
+}
+
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64 || dinfo_init(dev) != 0) return OSCAR_ERR_LAUNCH;
-  const bool big = a.g.G > 4;
-  if (a.g.vb) {
-    switch (a.g.D) {
-      case 128: return big ? launch_decode_d<128, 2, true>(a, stream) : launch_decode_d<128, 1, true>(a, stream);
-      case 256: return big ? launch_decode_d<256, 2, true>(a, stream) : launch_decode_d<256, 1, true>(a, stream);
-      case 512: return big ? launch_decode_d<512, 2, true>(a, stream) : launch_decode_d<512, 1, true>(a, stream);
-      default: return OSCAR_ERR_UNSUPPORTED;
-    }
-  }
-  switch (a.g.D) {
-    case 128: return big ? launch_decode_d<128, 2, false>(a, stream) : launch_decode_d<128, 1, false>(a, stream);
-    case 256: return big ? launch_decode_d<256, 2, false>(a, stream) : launch_decode_d<256, 1, false>(a, stream);
-    case 512: return big ? launch_decode_d<512, 2, false>(a, stream) : launch_decode_d<512, 1, false>(a, stream);
-    default: return OSCAR_ERR_UNSUPPORTED;
-  }
+  if (a.g.vb) return a.g.lm ? launch_decode_mode<true, true>(a, stream) : launch_decode_mode<true, false>(a, stream);
+  return a.g.lm ? launch_decode_mode<false, true>(a, stream) : launch_decode_mode<false, false>(a, stream);
 }
 
 }  // namespace oscar

@@ -20,6 +20,7 @@ struct Geom {
   int64_t ncap;
   uint64_t sink_bytes, ring_bytes, codes_bytes, sz_bytes, role_bytes, layer_bytes;
   int vb;                 // V kept BF16 at every position (K-only INT2)
+  int lm;                 // INT2 codes index the Lloyd-Max levels (fills the padding before v_role_bytes)
   uint64_t v_role_bytes;  // V role: role_bytes, or with vb [B][Hkv][cap][D] bf16
 };
 
@@ -91,6 +92,53 @@ __device__ __forceinline__ void unpack16_v(uint32_t w, uint32_t (&r)[8]) {
 
 // log2 of the value unpack16_v gives a code of register p, per unit of code
 __device__ __forceinline__ constexpr int unpack_v_exp(int p) { return (p == 0 || p == 5) ? 0 : 2 * unpack_k(p) - 24; }
+
+// Lloyd-Max levels: level(c) = (0, rho, rho + 1, 2 rho + 1)[c] with rho = 297/256
+// (1.16 to 2^-8), so the span, the midpoints and the level algebra below are
+// exact binary fractions.  Writing c = c0 + 2 c1, level(c) = rho * c + (1 - rho) * c1
+// = rho * c + kLmHi * (2 c1): the decode multiplies the code sum by rho and adds
+// kLmHi times the same sum over the codes' high bits (unpack16_hi).
+constexpr float kLmRho = 1.16015625f;
+constexpr float kLmSpan = 3.3203125f;    // 2 rho + 1: the group's range in level units
+constexpr float kLmHi = -0.080078125f;   // (1 - rho) / 2
+constexpr float kLmMid0 = 0.580078125f;  // rho / 2
+constexpr float kLmMid1 = 1.66015625f;   // rho + 1/2
+constexpr float kLmMid2 = 2.740234375f;  // 3 rho / 2 + 1
+
+// nearest Lloyd-Max level of y = (x - zero) / unit; on a midpoint the lower one
+__device__ __forceinline__ int lm_code(float y) { return (y > kLmMid0) + (y > kLmMid1) + (y > kLmMid2); }
+
+// As unpack16, keeping only the high bit of each code: register p holds
+// 2 * c1 * 4^k(p) * 2^-24 where unpack16 holds c * 4^k(p) * 2^-24.
+__device__ __forceinline__ void unpack16_hi(uint32_t w, uint32_t (&r)[8]) {
+  r[0] = w & 0x00020002u;
+  r[1] = w & 0x00080008u;
+  r[2] = w & 0x00200020u;
+  r[3] = w & 0x00800080u;
+  r[4] = w & 0x02000200u;
+  const uint32_t w2 = w >> 10;
+  r[5] = w2 & 0x00020002u;
+  r[6] = w2 & 0x00080008u;
+  r[7] = w2 & 0x00200020u;
+}
+
+// As unpack16_v for the high bits: registers 0 and 5 hold 2 * c1 as exact fp16
+// integers, the others 2 * c1 at the code's subnormal position.
+__device__ __forceinline__ void unpack16_v_hi(uint32_t w, uint32_t (&r)[8]) {
+  const uint32_t M = 0x64006400u;
+  uint32_t t0, t5;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t0) : "r"(w), "r"(0x00020002u), "r"(M));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(M));
+  r[1] = w & 0x00080008u;
+  r[2] = w & 0x00200020u;
+  r[3] = w & 0x00800080u;
+  r[4] = w & 0x02000200u;
+  const uint32_t w2 = w >> 10;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t5) : "r"(w2), "r"(0x00020002u), "r"(M));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[5]) : "r"(t5), "r"(M));
+  r[6] = w2 & 0x00080008u;
+  r[7] = w2 & 0x00200020u;
+}
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -21,8 +21,9 @@
 // kv_append_rows_kernel, row-parallel, for appends of a few rows (a decode
 // step appends one token per sequence): 4 or 8 rows per CTA, described below.
 // It also takes every append of the in-quant Hadamard mode (rows transformed
-// in registers, no matrix) and of the K-only INT2 mode (V rows stored as BF16
-// at their positions).
+// in registers, no matrix), of the K-only INT2 mode (V rows stored as BF16
+// at their positions) and of the Lloyd-Max levels (span 2 rho + 1, codes by
+// comparison with the level midpoints, lm_code).
 //
 // Both accumulate each rotated value with fp32 FMAs in increasing input-channel
 // order and run the same codec operations, so they write identical bytes.
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       }
-      const float s32 = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      const float s32 = __fdiv_rn(__fsub_rn(mx, mn), g.lm ? kLmSpan : 3.0f);
       const __half sh = __float2half_rn(s32);
       const __half zh = __float2half_rn(mn);
       const float sf = __half2float(sh), zf = __half2float(zh);
@@ -488,8 +489,9 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
     for (int k = 0; k < C::SPL; ++k) {
       const int s = part * C::SPL + k;
       const float x = fminf(fmaxf(y[my_j * kGroup + slot_channel(role, my_w, s)], -tclip), tclip);
-      int c = __float2int_rn(__fmul_rn(__fsub_rn(x, my_zf), my_inv));
-      c = my_ok ? min(max(c, 0), 3) : 0;
+      const float yq = __fmul_rn(__fsub_rn(x, my_zf), my_inv);
+      int c = g.lm ? lm_code(yq) : min(max(__float2int_rn(yq), 0), 3);
+      c = my_ok ? c : 0;
       word |= uint32_t(c) << (2 * s);
     }
 #pragma unroll
@@ -558,8 +560,9 @@ int launch_append(const AppendArgs& a, cudaStream_t stream) {
       default: return OSCAR_ERR_UNSUPPORTED;
     }
   }
-  // K-only INT2 (V kept BF16) is written by the row-parallel kernel at every size
-  if (a.rows <= kSmallAppendRows || a.g.vb) {
+  // K-only INT2 (V kept BF16) and Lloyd-Max levels are written by the
+  // row-parallel kernel at every size
+  if (a.rows <= kSmallAppendRows || a.g.vb || a.g.lm) {
     switch (a.g.D) {
       case 128: return launch_append_small<128>(a, stream);
       case 256: return launch_append_small<256>(a, stream);

@@ -16,7 +16,7 @@ int validate(const oscar_kv_config* c) {
   if (c->num_q_heads % c->num_kv_heads != 0) return OSCAR_ERR_INVALID;
   if (!(c->k_clip > 0.f && c->k_clip <= 1.f) || !(c->v_clip > 0.f && c->v_clip <= 1.f)) return OSCAR_ERR_INVALID;
   if (c->flags & ~uint32_t(OSCAR_FLAG_ABSORB_V | OSCAR_FLAG_IN_FP32 | OSCAR_FLAG_OUT_FP32 | OSCAR_FLAG_HADAMARD |
-                           OSCAR_FLAG_V_BF16))
+                           OSCAR_FLAG_V_BF16 | OSCAR_FLAG_LLOYD_MAX))
     return OSCAR_ERR_INVALID;
   if (c->group_size != OSCAR_KV_GROUP) return OSCAR_ERR_UNSUPPORTED;
   if (c->head_dim != 128 && c->head_dim != 256 && c->head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
@@ -44,6 +44,7 @@ Geom make_geom(const oscar_kv_config* c) {
   g.sz_bytes = oscar::align256(bh * uint64_t(g.ncap) * g.Dg * 4);
   g.role_bytes = g.sink_bytes + g.ring_bytes + g.codes_bytes + g.sz_bytes;
   g.vb = (c->flags & OSCAR_FLAG_V_BF16) ? 1 : 0;
+  g.lm = (c->flags & OSCAR_FLAG_LLOYD_MAX) ? 1 : 0;
   g.v_role_bytes = g.vb ? oscar::align256(bh * uint64_t(g.cap) * g.D * 2) : g.role_bytes;
   g.layer_bytes = g.role_bytes + g.v_role_bytes;
   return g;

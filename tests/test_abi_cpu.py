@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
 @pytest.mark.parametrize("shape", [
     (1, 1, 4, 1, 128, 64, 256, 1024), (2, 3, 8, 2, 256, 5, 7, 100), (36, 32, 32, 8, 128, 64, 256, 32768),
     (1, 4, 16, 8, 512, 512, 2048, 65536), (1, 2, 2, 2, 128, 0, 0, 1), (1, 1, 8, 1, 128, 300, 0, 200)])
-@pytest.mark.parametrize("flags", [0, K.FLAG_V_BF16])
+@pytest.mark.parametrize("flags", [0, K.FLAG_V_BF16, K.FLAG_LLOYD_MAX, K.FLAG_LLOYD_MAX | K.FLAG_V_BF16])
 def test_layout_matches_oracle(lib, shape, flags):
     L, B, Hq, Hkv, D, S, W, cap = shape
     got = K.layout_query(K.KVConfig(L, B, Hq, Hkv, D, S, W, cap, flags=flags))

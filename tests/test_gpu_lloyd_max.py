@@ -1,0 +1,171 @@
+"""GPU parity of the Lloyd-Max INT2 levels (OSCAR_FLAG_LLOYD_MAX).
+
+Append: with exact rotations (signed permutations) every rotated value is exact
+on both sides, so the cache must equal the oracle's byte for byte (codes by the
+midpoint rule, unit and zero, BF16 windows), for every append size (the flag
+always takes the row-parallel kernel) and with V kept BF16 as well.  Decode:
+outputs against the oracle on identical cache bytes, with the tolerances of the
+evenly-spaced decode tests; the decode reads each INT2 product twice (all code
+bits, then the high bits), which these cases reach for every head_dim, both
+query-head tilings and both V storage forms.  decode_step with the flag is
+bit-identical to kv_append followed by attn_decode."""
+import numpy as np
+import pytest
+import torch
+
+from int2_kv_cache_append_gb300 import oscar_kv as K
+from int2_kv_cache_append_gb300 import synth as S
+from oracle import oscar_oracle as O
+from tests.gpu_helpers import bf16_round64, gpu_append, gpu_decode, new_cache, rel_l2
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int2_kv_cache_append_gb300 import build
+    build.build()
+
+
+def _inputs(seed, B, n, H, D, fp32=False):
+    rng = np.random.default_rng(seed)
+    ch = rng.choice(D, size=max(1, D // 50), replace=False)
+    k = S.activations(rng, (B, n, H, D), ch)
+    v = S.activations(rng, (B, n, H, D), ch)
+    if not fp32:
+        k, v = S.to_bf16_values(k), S.to_bf16_values(v)
+    return k, v
+
+
+APPEND_CASES = [
+    # D, B, Hkv, S, W, cap, chunks (n per call), start offsets per sequence, extra flags
+    (128, 2, 2, 16, 32, 256, [40, 1, 7, 64], [0, 3], 0),
+    (128, 2, 4, 16, 64, 1400, [700, 1, 50], [0, 2], 0),        # > 1024 rows per role in one call
+    (128, 2, 2, 8, 16, 300, [120, 1, 33], [0, 5], K.FLAG_V_BF16),
+    (256, 2, 2, 5, 9, 200, [33, 17, 2], [1, 0], 0),
+    (512, 2, 2, 8, 16, 160, [50, 31, 1], [0, 7], 0),
+]
+
+
+@pytest.mark.parametrize("case", APPEND_CASES)
+@pytest.mark.parametrize("fp32", [False, True])
+def test_lloyd_max_append_exact_chain_bitwise(case, fp32):
+    D, B, H, S_, W, cap, chunks, offs, extra = case
+    c = O.Config(2, B, 2 * H, H, D, S_, W, cap, 0.96, 0.92,
+                 flags=K.FLAG_LLOYD_MAX | extra | (K.FLAG_IN_FP32 if fp32 else 0))
+    rng = np.random.default_rng(D + B + 11)
+    RK = S.signed_permutation(rng, D).astype(np.float32)
+    RV = S.signed_permutation(rng, D).astype(np.float32)
+    ocache, gcache = O.new_cache(c), new_cache(c)
+    pos = list(offs)
+    for i, n in enumerate(chunks):
+        k, v = _inputs(700 + i, B, n, H, D, fp32)
+        O.append(c, ocache, 1, k, v, pos, RK, RV)
+        gpu_append(c, gcache, 1, k, v, pos, RK, RV)
+        pos = [p + n for p in pos]
+    got = gcache.cpu().numpy()
+    diff = np.nonzero(got != ocache)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+    # the levels matter: the evenly spaced codec writes different bytes
+    plain = O.Config(2, B, 2 * H, H, D, S_, W, cap, 0.96, 0.92, flags=extra)
+    pcache = O.new_cache(plain)
+    pos = list(offs)
+    for i, n in enumerate(chunks):
+        k, v = _inputs(700 + i, B, n, H, D, fp32)
+        O.append(plain, pcache, 1, k, v, pos, RK, RV)
+        pos = [p + n for p in pos]
+    assert np.count_nonzero(pcache != ocache) > 0
+
+
+DEC_CASES = [
+    # D, B, Hq, Hkv, S, W, seq_lens, extra flags
+    (128, 1, 4, 1, 64, 256, [1024], 0),
+    (128, 2, 8, 2, 16, 32, [700, 333], 0),                    # ragged
+    (128, 2, 16, 2, 0, 100, [1500, 900], 0),                  # S = 0, G = 8 (two query tiles)
+    (128, 1, 8, 8, 512, 0, [2000], 0),                        # W = 0, G = 1
+    (128, 3, 6, 3, 20, 40, [30, 19, 1], 0),                   # T <= S, T = 1
+    (128, 1, 16, 8, 64, 256, [3000], K.FLAG_ABSORB_V),        # G = 2, absorbed V
+    (128, 2, 8, 2, 16, 64, [900, 500], K.FLAG_HADAMARD),      # with the in-quant Hadamard
+    (128, 2, 8, 2, 16, 64, [900, 500], K.FLAG_V_BF16),        # Lloyd-Max K, BF16 V
+    (128, 2, 32, 4, 16, 64, [1200, 700], K.FLAG_V_BF16),      # ... G = 8
+    (256, 2, 8, 2, 8, 16, [400, 150], 0),
+    (512, 1, 4, 2, 16, 64, [600], 0),
+    (512, 1, 16, 2, 16, 64, [700], 0),                        # D = 512, G = 8
+]
+
+
+@pytest.mark.parametrize("case", DEC_CASES)
+def test_lloyd_max_decode(case):
+    D, B, Hq, Hkv, S_, W, seq_lens, extra = case
+    c = O.Config(1, B, Hq, Hkv, D, S_, W, max(seq_lens), 0.96, 0.92, flags=K.FLAG_LLOYD_MAX | extra)
+    rng = np.random.default_rng(D + B + Hq + 5)
+    ch = rng.choice(D, max(1, round(0.02 * D)), replace=False)
+    T = max(seq_lens)
+    k = S.to_bf16_values(S.activations(rng, (B, T, Hkv, D), ch))
+    v = S.to_bf16_values(S.activations(rng, (B, T, Hkv, D), ch))
+    q = S.to_bf16_values(S.activations(rng, (B, Hq, D), ch))
+    if extra & K.FLAG_HADAMARD:
+        RK = RV = None
+    else:
+        RK, RV = S.qr_rotation(rng, D).astype(np.float32), S.qr_rotation(rng, D).astype(np.float32)
+    cache = O.new_cache(c)
+    O.append(c, cache, 0, k, v, [0] * B, RK, RV)
+    # both sides decode the same bytes (shorter lengths read the same ring slots)
+    ref, ref_lse = O.decode(c, cache, 0, q, seq_lens, RK, RV, absorb_v=bool(extra & K.FLAG_ABSORB_V))
+    gc = torch.from_numpy(cache).cuda()
+    o16, lse = gpu_decode(c, gc, 0, q, seq_lens, RK, RV, out_fp32=False)
+    o32, lse32 = gpu_decode(c, gc, 0, q, seq_lens, RK, RV, out_fp32=True)
+    r16, r32 = rel_l2(o16, bf16_round64(ref)), rel_l2(o32, ref)
+    m32 = float(np.abs(o32 - ref).max())
+    dl = float(np.max(np.abs(lse - ref_lse) - 1e-5 * np.abs(ref_lse)))
+    assert r16 <= 1e-3, f"bf16 rel-L2 {r16}"
+    assert m32 <= 5e-3 and r32 <= 2e-4, f"fp32 max-abs {m32} rel-L2 {r32}"
+    assert dl <= 1e-4, f"lse {dl}"
+    assert np.array_equal(lse, lse32)
+
+
+@pytest.mark.parametrize("case", [(128, 3, 16, 4, 16, 64, 1200, [500, 63, 1000], 1, 0),
+                                  (128, 2, 8, 2, 8, 16, 600, [100, 300], 40, 0),       # append longer than the ring
+                                  (128, 2, 32, 8, 64, 256, 4096, [4000, 777], 1, K.FLAG_V_BF16),
+                                  (256, 2, 8, 4, 16, 32, 700, [650, 90], 3, 0)])
+def test_lloyd_max_decode_step_equals_append_then_decode(case):
+    D, B, Hq, Hkv, S_, W, cap, pre, n, extra = case
+    kc = K.KVConfig(1, B, Hq, Hkv, D, S_, W, cap, 0.96, 0.92, K.FLAG_OUT_FP32 | K.FLAG_LLOYD_MAX | extra)
+    lay = K.layout_query(kc)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4000 + D + n)
+    ch = np.array([5, 77])
+    rand = lambda shape: S.activations_torch(gen, shape, ch, dtype=torch.bfloat16)
+    rng = np.random.default_rng(D + n + 1)
+    rk = torch.from_numpy(S.qr_rotation(rng, D).astype(np.float32)).cuda()
+    rv = torch.from_numpy(S.qr_rotation(rng, D).astype(np.float32)).cuda()
+    cache = torch.zeros(lay["total_bytes"], dtype=torch.uint8, device="cuda")
+    T0 = max(pre)
+    K.kv_append(kc, cache, 0, rand((B, T0, Hkv, D)), rand((B, T0, Hkv, D)),
+                torch.zeros(B, dtype=torch.int32, device="cuda"), rk, rv)
+    k_new, v_new, q = rand((B, n, Hkv, D)), rand((B, n, Hkv, D)), rand((B, Hq, D))
+    start = torch.tensor(pre, dtype=torch.int32, device="cuda")
+    seq = start + n
+    results = []
+    for fused in (False, True):
+        c = cache.clone()
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+        ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            K.decode_step(kc, c, 0, k_new, v_new, start, q, seq, rk, rv, out, ws, lse=lse, seq_len_hint=cap,
+                          status=st)
+        else:
+            K.kv_append(kc, c, 0, k_new, v_new, start, rk, rv, status=st)
+            K.attn_decode(kc, c, 0, q, seq, rk, rv, out, ws, lse=lse, seq_len_hint=cap, status=st)
+        torch.cuda.synchronize()
+        results.append((c.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy(), int(st.item())))
+    (c0, o0, l0, s0), (c1, o1, l1, s1) = results
+    assert s0 == s1 == 0
+    assert np.array_equal(c0, c1)
+    assert np.isfinite(o0).all()
+    dif = np.argwhere((o0.view(np.uint32) != o1.view(np.uint32)).any(axis=2))
+    assert dif.size == 0, (f"outputs differ at (b, head) {dif[:12].tolist()} of {len(dif)}, "
+                           f"max |diff| {np.abs(o0 - o1).max():.3e}")
+    assert np.array_equal(l0.view(np.uint32), l1.view(np.uint32)), f"lse max |diff| {np.abs(l0 - l1).max():.3e}"
