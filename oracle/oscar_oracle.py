@@ -58,7 +58,11 @@ Readings taken where the pages are silent (each listed in the design doc):
   four-level Lloyd-Max quantiser of a Gaussian), spread over the group's
   min..max; rho is 1.16 at a resolution of 2^-8 (297/256) so that levels,
   midpoints and the span 2 rho + 1 are exact binary fractions; the code is the
-  nearest level, a tie going to the lower one.
+  nearest level, a tie going to the lower one;
+* R_V calibration (RotationZoo [File format]: the V rotation is built on a
+  score-weighted V covariance): the printed V^T diag(K^T (Q^T Q) K) V read
+  with K holding keys as columns, so each key row is weighted by its score
+  energy w_t = k_t Q^T Q k_t^T; R_V = E H P_br as for R_K.
 
 The byte layout written by :func:`append` is the one the C header documents
 for the cache (regions, strides, code bit positions); it is implemented here
@@ -207,22 +211,16 @@ def bit_reversal_index(n: int) -> np.ndarray:
     return np.array([int(format(i, f"0{b}b")[::-1], 2) if b else 0 for i in range(n)])
 
 
-def calibrate_rk(calib_q: np.ndarray) -> np.ndarray:
-    """K-side rotation fitted to a calibration set of query rows, float64 [D][D].
+def rotation_from_covariance(sigma: np.ndarray) -> np.ndarray:
+    """R = E H P_br for a symmetric positive semi-definite covariance, float64 [D][D].
 
-    OSCAR-RotationZoo card [File format]: R_K = R H P_br, R the eigenvectors of
-    the query covariance, H a head-dim Hadamard, P_br the eigenvalue-sorted
-    bit-reversal permutation; hysenlabs article [How the offline rotation is
-    fit]: Q activations are captured offline and the rotation derived from
-    their covariance.  Read as: Sigma = Q^T Q (float64 over the rows); E = its
-    eigenvectors by descending eigenvalue (ties by index), each column signed so
-    that its largest-magnitude entry (the first, on ties) is positive;
-    H = sylvester_hadamard(D); P_br[i, br(i)] = 1, so column j of R_K is column
-    br(j) of E H.  The eigen-solver is the library one (numpy eigh).
+    E = the eigenvectors of sigma by descending eigenvalue (ties by index), each
+    column signed so that its largest-magnitude entry (the first, on ties) is
+    positive; H = sylvester_hadamard(D); P_br[i, br(i)] = 1, so column j of R
+    is column br(j) of E H.  The eigen-solver is the library one (numpy eigh).
     """
-    q = np.asarray(calib_q, np.float64)
-    d = q.shape[1]
-    sigma = q.T @ q
+    sigma = np.asarray(sigma, np.float64)
+    d = sigma.shape[0]
     w, e = np.linalg.eigh(sigma)
     order = np.argsort(-w, kind="stable")
     e = e[:, order]
@@ -230,6 +228,46 @@ def calibrate_rk(calib_q: np.ndarray) -> np.ndarray:
     e = e * np.where(e[piv, np.arange(d)] < 0, -1.0, 1.0)
     eh = e @ sylvester_hadamard(d)
     return eh[:, bit_reversal_index(d)]
+
+
+def calibrate_rk(calib_q: np.ndarray) -> np.ndarray:
+    """K-side rotation fitted to a calibration set of query rows, float64 [D][D].
+
+    OSCAR-RotationZoo card [File format]: R_K = R H P_br, R the eigenvectors of
+    the query covariance, H a head-dim Hadamard, P_br the eigenvalue-sorted
+    bit-reversal permutation; hysenlabs article [How the offline rotation is
+    fit]: Q activations are captured offline and the rotation derived from
+    their covariance.  Read as: Sigma = Q^T Q (float64 over the rows), then
+    rotation_from_covariance(Sigma).
+    """
+    q = np.asarray(calib_q, np.float64)
+    return rotation_from_covariance(q.T @ q)
+
+
+def score_energy(calib_q: np.ndarray, calib_k: np.ndarray) -> np.ndarray:
+    """w_t = k_t (Q^T Q) k_t^T for every key row: the sum over the calibration
+    queries of the squared logit q_n . k_t, float64 [n_kv]."""
+    q = np.asarray(calib_q, np.float64)
+    k = np.asarray(calib_k, np.float64)
+    sigma_q = q.T @ q
+    return np.einsum("ti,ij,tj->t", k, sigma_q, k)
+
+
+def calibrate_rv(calib_q: np.ndarray, calib_k: np.ndarray, calib_v: np.ndarray) -> np.ndarray:
+    """V-side rotation fitted to the score-weighted V covariance, float64 [D][D].
+
+    OSCAR-RotationZoo card [File format]: the V rotation file is built on
+    Sigma_V = V^T diag(K^T (Q^T Q) K) V, with the same R H P_br construction as
+    the K side.  The printed product composes when K holds the keys as columns
+    (D x n_kv) and Q and V hold rows: K^T Q^T Q K = S^T S with S = Q K the
+    logits of every calibration query against every key, whose diagonal is each
+    key's score energy w_t (score_energy).  Read as: Sigma_V = sum_t w_t v_t^T v_t
+    over the key/value rows of one layer (row t of calib_k and of calib_v are
+    the same token and KV head), then rotation_from_covariance(Sigma_V).
+    """
+    v = np.asarray(calib_v, np.float64)
+    w = score_energy(calib_q, calib_k)
+    return rotation_from_covariance((v * w[:, None]).T @ v)
 
 
 def rotations_of(cfg: "Config", R_K, R_V):

@@ -804,3 +804,88 @@ def test_lloyd_max_decode_equals_library_sdpa_on_exact_rows():
     plain = O.Config(1, B, H * G, H, D, 0, 0, 64, 1.0, 1.0)
     out_u, _ = O.decode(plain, cache, 0, q, lens, I, I)
     assert np.abs(out_u - out).max() > 1e-2
+
+
+# --------------------------------------------------------------------------
+# R_V calibration: score-weighted V covariance
+# --------------------------------------------------------------------------
+def test_score_energy_is_the_sum_of_squared_logits():
+    # brute force over every (query, key) logit in plain Python
+    rng = np.random.default_rng(61)
+    q = rng.standard_normal((7, 16))
+    k = rng.standard_normal((5, 16))
+    w = O.score_energy(q, k)
+    for t in range(5):
+        tot = 0.0
+        for n in range(7):
+            tot += sum(float(q[n, i]) * float(k[t, i]) for i in range(16)) ** 2
+        assert abs(w[t] - tot) <= 1e-12 * tot
+
+
+def _rank_hadamard_bitrev(rank, d):
+    # R[i, j] = H[rank(i), br(j)] for E = the permutation sending channel i to column rank(i)
+    bits = d.bit_length() - 1
+    br = [int(format(j, f"0{bits}b")[::-1], 2) for j in range(d)]
+    return np.array([[(-1.0) ** bin(int(rank[i]) & br[j]).count("1") / math.sqrt(d) for j in range(d)]
+                     for i in range(d)])
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_calibrate_rv_diagonal_closed_form_weights_decide_the_order(d):
+    # channel i: value rows +-a_i e_i with key e_i; queries sigma_j e_j.  Every
+    # weight of channel i is sigma_i^2, so Sigma_V = diag(2 sigma_i^2 a_i^2).  The
+    # magnitudes a_i grow with i (the unweighted V covariance ranks channels by
+    # i); sigma_i a_i = perm(i) + 1 ranks them by perm instead
+    rng = np.random.default_rng(62 + d)
+    perm = rng.permutation(d)
+    a = 1.0 + np.arange(d) / d
+    sig = (perm + 1.0) / a
+    Q = np.diag(sig)
+    K = np.repeat(np.eye(d), 2, axis=0)
+    V = np.repeat(np.diag(a), 2, axis=0) * np.tile([1.0, -1.0], d)[:, None]
+    R = O.calibrate_rv(Q, K, V)
+    rank = np.empty(d, int)
+    rank[np.argsort(-perm, kind="stable")] = np.arange(d)
+    assert np.abs(R - _rank_hadamard_bitrev(rank, d)).max() < 1e-12
+    # without the weights the order would follow a_i
+    assert np.abs(O.calibrate_rk(V) - _rank_hadamard_bitrev(np.arange(d)[::-1], d)).max() < 1e-12
+
+
+def test_calibrate_rv_reduces_to_the_v_covariance_for_isotropic_queries():
+    # Q^T Q = 9 I and unit-norm keys give every key the weight 9: R_V is then the
+    # fit of V's own covariance
+    d = 128
+    rng = np.random.default_rng(63)
+    Q = 3.0 * np.eye(d)
+    K = rng.standard_normal((900, d))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    V = S.activations(rng, (900, d), [4, 50, 100], kind="t3")
+    assert np.abs(O.calibrate_rv(Q, K, V) - O.calibrate_rk(V)).max() < 1e-9
+
+
+def test_calibrate_rv_eigen_equation_on_token_by_token_covariance():
+    # Sigma_V summed one token at a time from the explicit logit matrix; undoing
+    # H P_br (scipy's Hadamard) leaves its eigenvectors, descending and signed
+    L = pytest.importorskip("scipy.linalg")
+    d = 128
+    rng = np.random.default_rng(64)
+    ch = [5, 40, 99]
+    Q = S.activations(rng, (500, d), ch, kind="t3").astype(np.float64)
+    K = S.activations(rng, (400, d), ch, kind="t3").astype(np.float64)
+    V = S.activations(rng, (400, d), ch, kind="t3").astype(np.float64)
+    logits = Q @ K.T
+    sig = np.zeros((d, d))
+    for t in range(K.shape[0]):
+        sig += float(np.sum(logits[:, t] ** 2)) * np.outer(V[t], V[t])
+    R = O.calibrate_rv(Q, K, V)
+    bits = d.bit_length() - 1
+    P = np.zeros((d, d))
+    for i in range(d):
+        P[i, int(format(i, f"0{bits}b")[::-1], 2)] = 1.0
+    E = R @ P.T @ (L.hadamard(d) / math.sqrt(d)).T
+    lam = np.einsum("ij,ij->j", E, sig @ E)
+    assert np.abs(sig @ E - E * lam).max() < 1e-9 * lam[0]
+    assert np.all(np.diff(lam) <= 1e-9 * lam[0])
+    assert np.abs(E.T @ E - np.eye(d)).max() < 1e-12
+    piv = np.argmax(np.abs(E), axis=0)
+    assert np.all(E[piv, np.arange(d)] > 0)
