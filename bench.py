@@ -549,9 +549,10 @@ def ours_append(args):
 
 
 def calibrate_arm(args):
-    """R_K calibration from 20,000 calibration tokens of the workload's shape
-    (every query head's row pooled): GPU time per calibration, with the oracle
-    (numpy float64 + LAPACK) timed on the same rows as the CPU baseline."""
+    """R_K and R_V calibration from 20,000 calibration tokens of the workload's
+    shape (every query head's row pooled for Q, every KV head's for K and V):
+    GPU time per calibration, with the oracle (numpy float64 + LAPACK) timed on
+    the same rows as the CPU baseline."""
     import numpy as np
     import torch
 
@@ -562,28 +563,42 @@ def calibrate_arm(args):
     w = S.WORKLOADS[args.workload]
     D = w.head_dim
     rows = 20000 * w.num_q_heads
+    kv_rows = 20000 * w.num_kv_heads
     gen = torch.Generator(device="cuda")
     gen.manual_seed(7)
-    q = S.activations_torch(gen, (rows, D), S.outlier_channels(w.config_id, 0, D))
+    ch = S.outlier_channels(w.config_id, 0, D)
+    q = S.activations_torch(gen, (rows, D), ch)
+    k = S.activations_torch(gen, (kv_rows, D), ch)
+    v = S.activations_torch(gen, (kv_rows, D), ch)
     out = torch.empty((D, D), dtype=torch.float32, device="cuda")
+    out_v = torch.empty((D, D), dtype=torch.float32, device="cuda")
     ws = torch.empty(K.calibrate_workspace_bytes(D), dtype=torch.uint8, device="cuda")
+    ws_v = torch.empty(K.calibrate_rv_workspace_bytes(D, kv_rows), dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for _ in range(max(3, args.warmup)):
-        K.calibrate_rk(q, out, ws, status=st)
     steps = max(1, min(args.steps, 20))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    torch.cuda.synchronize()
-    for a, b in ev:
-        a.record()
-        K.calibrate_rk(q, out, ws, status=st)
-        b.record()
-    torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-    qn = q.cpu().numpy()
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    ms = timed(lambda: K.calibrate_rk(q, out, ws, status=st))
+    ms_v = timed(lambda: K.calibrate_rv(q, k, v, out_v, ws_v, status=st))
+    qn, kn, vn = q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy()
     from oracle import oscar_oracle as O
     t0 = time.perf_counter()
     ref = O.calibrate_rk(qn)
     cpu_s = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    ref_v = O.calibrate_rv(qn, kn, vn)
+    cpu_v = time.perf_counter() - t0
     line = {"metric": "R_K calibration time (Sigma = Q^T Q, eigenvectors, H P_br), 1 GB300", "value": ms,
             "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": steps, "warmup": max(3, args.warmup),
             "dtype": "f64", "data": "synthetic",
@@ -592,7 +607,13 @@ def calibrate_arm(args):
             "max_abs_diff_vs_oracle": float(np.abs(out.cpu().numpy().astype(np.float64) - ref).max()),
             "dev_status": int(st.item()),
             "cpu_baseline": {"value": cpu_s * 1e3, "unit": "ms", "kind": "oracle", "cores": os.cpu_count(),
-                             "sample": "the oracle (numpy float64 Q^T Q + LAPACK eigh) on the same rows"}}
+                             "sample": "the oracle (numpy float64 Q^T Q + LAPACK eigh) on the same rows"},
+            "rv": {"metric": "R_V calibration time (score-weighted Sigma_V, eigenvectors, H P_br)", "value": ms_v,
+                   "unit": "ms", "q_rows": rows, "kv_rows": kv_rows,
+                   "max_abs_diff_vs_oracle": float(np.abs(out_v.cpu().numpy().astype(np.float64) - ref_v).max()),
+                   "cpu_baseline": {"value": cpu_v * 1e3, "unit": "ms", "kind": "oracle", "cores": os.cpu_count(),
+                                    "sample": "the oracle (numpy float64 weights, Sigma_V + LAPACK eigh) on the "
+                                              "same rows"}}}
     print(json.dumps(line), flush=True)
 
 

@@ -142,7 +142,7 @@ enum {
   OSCAR_DEV_FP16_RANGE = 4,    /* a scale, zero or scaled query component left the fp16 range */
   OSCAR_DEV_TIMEOUT = 8,       /* a pipeline wait gave up (the kernel returned early) */
   OSCAR_DEV_EMPTY = 16,        /* a sequence had seq_len < 1 (its output is zero) */
-  OSCAR_DEV_NOT_CONVERGED = 32 /* oscar_calibrate_rk: Jacobi reached its sweep limit */
+  OSCAR_DEV_NOT_CONVERGED = 32 /* oscar_calibrate_rk / _rv: Jacobi reached its sweep limit */
 };
 
 typedef struct {
@@ -327,6 +327,35 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop);
 int oscar_calibrate_workspace_query(int32_t head_dim, uint64_t* bytes);
 int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* R_K_out, void* workspace,
                        uint64_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * oscar_calibrate_rv — the V-side rotation fitted to the score-weighted V
+ * covariance ["OSCAR-RotationZoo" card, File format: the V rotation is built
+ * on V^T diag(K^T (Q^T Q) K) V with the same R H P_br construction].  The
+ * printed product composes when K holds the keys as columns: K^T Q^T Q K is
+ * then S^T S for the logits S of every calibration query against every key,
+ * and its diagonal is each key's score energy.  Offline work.
+ *   q          device [n_q_rows][head_dim] float32 query rows of one layer
+ *              (post-RoPE, every head's rows pooled), 16-byte aligned.
+ *   k, v       device [n_kv_rows][head_dim] float32 key and value rows of the
+ *              same layer (row t of k and of v: one token of one KV head),
+ *              16-byte aligned.
+ *   n_q_rows, n_kv_rows  1 .. 2^28.
+ *   R_V_out    device [head_dim][head_dim] float32, row-major, written:
+ *              Sigma_Q = q^T q and w_t = k_t Sigma_Q k_t^T in float64,
+ *              Sigma_V = sum_t w_t v_t^T v_t in float64, then E, its sign
+ *              convention, H and P_br exactly as oscar_calibrate_rk does for
+ *              Sigma.
+ *   workspace  device, >= the size oscar_calibrate_rv_workspace_query returns
+ *              (it grows with n_kv_rows), 256-byte aligned; caller owned,
+ *              contents undefined after.
+ * Launches six kernels on `stream` (the fifth as a cooperative launch).  Sweep
+ * limit, status bits and errors as oscar_calibrate_rk.
+ */
+int oscar_calibrate_rv_workspace_query(int32_t head_dim, int64_t n_kv_rows, uint64_t* bytes);
+int oscar_calibrate_rv(const float* q, int64_t n_q_rows, const float* k, const float* v, int64_t n_kv_rows,
+                       int32_t head_dim, float* R_V_out, void* workspace, uint64_t workspace_bytes,
+                       int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,20 +1,28 @@
-// Calibration of the K-side rotation from query activations:
-// Sigma = Q^T Q in float64, its eigenvectors by one-sided Jacobi in float64,
-// sorted by descending eigenvalue with a sign convention, then
-// R_K = E H_D P_br.
+// Calibration of the rotations from activations:
+//   K side: Sigma = Q^T Q in float64, its eigenvectors by one-sided Jacobi in
+//   float64, sorted by descending eigenvalue with a sign convention, then
+//   R_K = E H_D P_br;
+//   V side: the same from Sigma_V = sum_t w_t v_t^T v_t, each key/value row
+//   weighted by its score energy w_t = k_t Q^T Q k_t^T (the sum over the
+//   calibration queries of the squared logit q . k_t).
 //
 // Source: "OSCAR-RotationZoo" model card (File format: R_K = R H P_br with R
 // the eigenvectors of the query covariance, H a head-dim Hadamard and P_br the
-// eigenvalue-sorted bit-reversal permutation) and the hysenlabs article on
-// OSCAR (How the offline rotation is fit: Q/K/V activations are captured
-// offline and the rotation is derived from their covariance).
+// eigenvalue-sorted bit-reversal permutation; the V rotation built on the
+// score-weighted V covariance V^T diag(K^T (Q^T Q) K) V, read with K holding
+// the keys as columns) and the hysenlabs article on OSCAR (How the offline
+// rotation is fit: Q/K/V activations are captured offline and the rotation is
+// derived from their covariance).
 //
-// Offline work, not on the decode path.  Three kernels on the caller's stream:
-//   cov_kernel       Sigma += Q^T Q: CTA (i, j, c) accumulates the 64 x 64
-//                    tile (i, j) of Sigma over row chunk c in float64 (a product
-//                    of two float32 values is exact in float64; each thread a
-//                    4 x 4 register block) and adds it into Sigma with float64
-//                    atomics;
+// Offline work, not on the decode path.  Kernels on the caller's stream:
+//   cov_kernel       Sigma += X^T diag(w) X: CTA (i, j, c) accumulates the
+//                    64 x 64 tile (i, j) of Sigma over row chunk c in float64
+//                    (a product of two float32 values is exact in float64; a
+//                    row weight adds one rounding; each thread a 4 x 4 register
+//                    block) and adds it into Sigma with float64 atomics;
+//   weight_kernel    (V side) w_t = k_t Sigma_Q k_t^T: thread j of a CTA of D
+//                    threads forms column j of k Sigma_Q for 16 key rows, the
+//                    CTA reduces each row's dot product with k;
 //   jacobi_kernel    cooperative grid, one CTA per column pair: one-sided
 //                    Jacobi on Sigma (below);
 //   finalize_kernel  one CTA, one thread per eigenpair / row: rank the
@@ -37,10 +45,11 @@ constexpr int64_t kCovChunk = 4096;   // rows per CTA
 constexpr int kMaxSweeps = 40;
 constexpr int kPairThreads = 256;
 
-// Sigma tile (ti, tj) += Q^T Q over one chunk of rows; thread (ty, tx) owns a
-// 4 x 4 block of the 64 x 64 tile; rows are staged as float64 (exact).
+// Sigma tile (ti, tj) += X^T diag(w) X over one chunk of rows (w NULL: all
+// weights 1); thread (ty, tx) owns a 4 x 4 block of the 64 x 64 tile; rows are
+// staged as float64 (exact), the first operand times its row's weight.
 __global__ void __launch_bounds__(256) cov_kernel(const float* __restrict__ q, int64_t n, int D,
-                                                  double* __restrict__ sigma) {
+                                                  const double* __restrict__ wrow, double* __restrict__ sigma) {
   __shared__ double sa[kCovRows][kCovTile], sb[kCovRows][kCovTile];
   const int ti = blockIdx.x, tj = blockIdx.y;
   const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
@@ -56,7 +65,7 @@ __global__ void __launch_bounds__(256) cov_kernel(const float* __restrict__ q, i
       const int rr = idx / kCovTile, cc = idx % kCovTile;
       const int64_t row = row0 + rr;
       const bool in = row < row_hi;
-      sa[rr][cc] = in ? double(q[row * D + ti * kCovTile + cc]) : 0.0;
+      sa[rr][cc] = in ? double(q[row * D + ti * kCovTile + cc]) * (wrow ? wrow[row] : 1.0) : 0.0;
       sb[rr][cc] = in ? double(q[row * D + tj * kCovTile + cc]) : 0.0;
     }
     __syncthreads();
@@ -80,6 +89,41 @@ __global__ void __launch_bounds__(256) cov_kernel(const float* __restrict__ q, i
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       atomicAdd(&sigma[int64_t(ti * kCovTile + ty * 4 + i) * D + tj * kCovTile + tx * 4 + j], acc[i][j]);
+}
+
+constexpr int kWTok = 16;  // key rows per weight_kernel CTA
+
+// w[t] = k_t Sigma_Q k_t^T for kWTok key rows; blockDim.x == D (Sigma_Q is
+// symmetric, so thread j reads column j as row j's transpose: coalesced).
+__global__ void __launch_bounds__(512) weight_kernel(const float* __restrict__ k, int64_t n, int D,
+                                                     const double* __restrict__ sq, double* __restrict__ w) {
+  __shared__ float ks[kWTok][512];
+  __shared__ double red[kWTok][16];
+  const int j = threadIdx.x;
+  const int64_t t0 = int64_t(blockIdx.x) * kWTok;
+  for (int r = 0; r < kWTok; ++r) ks[r][j] = t0 + r < n ? k[(t0 + r) * D + j] : 0.f;
+  __syncthreads();
+  double y[kWTok];
+#pragma unroll
+  for (int r = 0; r < kWTok; ++r) y[r] = 0.0;
+  for (int i = 0; i < D; ++i) {
+    const double sij = sq[int64_t(i) * D + j];
+#pragma unroll
+    for (int r = 0; r < kWTok; ++r) y[r] = fma(double(ks[r][i]), sij, y[r]);
+  }
+  const int warp = j >> 5, lane = j & 31, nw = D >> 5;
+#pragma unroll
+  for (int r = 0; r < kWTok; ++r) {
+    double v = y[r] * double(ks[r][j]);
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[r][warp] = v;
+  }
+  __syncthreads();
+  if (j < kWTok && t0 + j < n) {
+    double tot = 0.0;
+    for (int q = 0; q < nw; ++q) tot += red[j][q];
+    w[t0 + j] = tot;
+  }
 }
 
 // Sum of v over the block (every thread gets it); red has blockDim / 32 slots.
@@ -235,23 +279,44 @@ __global__ void finalize_kernel(const double* __restrict__ A, const double* __re
   }
 }
 
-}  // namespace
+// Workspace: A (Sigma, then Sigma V by columns), V, E (on the V side first
+// Sigma_Q), the eigenvalues, the sweep maxima and info; then (V side) the row
+// weights.
+struct CalibWs {
+  double *A, *V, *E, *lam;
+  unsigned long long* sweep_max;
+  int32_t* info;
+  double* w;
+};
 
-uint64_t calibrate_workspace_bytes(int D) { return 3 * align256(uint64_t(D) * D * 8) + align256(uint64_t(D) * 8) + 256; }
-
-int launch_calibrate(const float* q, int64_t n, int D, float* R, void* ws, int32_t* status, cudaStream_t stream) {
-  uint8_t* w = static_cast<uint8_t*>(ws);
+CalibWs calib_ws(void* ws, int D) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
   const uint64_t mat = align256(uint64_t(D) * D * 8);
-  double* A = reinterpret_cast<double*>(w);  // Sigma, then Sigma V (columns)
-  double* V = reinterpret_cast<double*>(w + mat);
-  double* E = reinterpret_cast<double*>(w + 2 * mat);
-  double* lam = reinterpret_cast<double*>(w + 3 * mat);
-  unsigned long long* sweep_max = reinterpret_cast<unsigned long long*>(w + 3 * mat + align256(uint64_t(D) * 8));
-  int32_t* info = reinterpret_cast<int32_t*>(sweep_max + 2);
-  if (cudaMemsetAsync(A, 0, size_t(D) * D * 8, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  CalibWs c;
+  c.A = reinterpret_cast<double*>(b);
+  c.V = reinterpret_cast<double*>(b + mat);
+  c.E = reinterpret_cast<double*>(b + 2 * mat);
+  c.lam = reinterpret_cast<double*>(b + 3 * mat);
+  c.sweep_max = reinterpret_cast<unsigned long long*>(b + 3 * mat + align256(uint64_t(D) * 8));
+  c.info = reinterpret_cast<int32_t*>(c.sweep_max + 2);
+  c.w = reinterpret_cast<double*>(b + calibrate_workspace_bytes(D));
+  return c;
+}
+
+// Sigma (zeroed here) += X^T diag(w) X over the n rows of x
+int launch_cov(const float* x, int64_t n, int D, const double* w, double* sigma, cudaStream_t stream) {
+  if (cudaMemsetAsync(sigma, 0, size_t(D) * D * 8, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   const int64_t chunks = (n + kCovChunk - 1) / kCovChunk;
-  cov_kernel<<<dim3(D / kCovTile, D / kCovTile, unsigned(chunks)), 256, 0, stream>>>(q, n, D, A);
-  if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  cov_kernel<<<dim3(D / kCovTile, D / kCovTile, unsigned(chunks)), 256, 0, stream>>>(x, n, D, w, sigma);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
+}
+
+// R = E H_D P_br from the covariance in c.A (overwritten)
+int launch_fit(CalibWs& c, int D, float* R, int32_t* status, cudaStream_t stream) {
+  double* A = c.A;
+  double* V = c.V;
+  unsigned long long* sweep_max = c.sweep_max;
+  int32_t* info = c.info;
   // one CTA per column pair, as many as can be resident together
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -262,8 +327,35 @@ int launch_calibrate(const float* q, int64_t n, int D, float* R, void* ws, int32
   if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(jacobi_kernel), dim3(grid), dim3(kPairThreads), args, 0,
                                   stream) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
-  finalize_kernel<<<1, D, 0, stream>>>(A, V, lam, E, R, D);
+  finalize_kernel<<<1, D, 0, stream>>>(A, V, c.lam, c.E, R, D);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
+}
+
+}  // namespace
+
+uint64_t calibrate_workspace_bytes(int D) { return 3 * align256(uint64_t(D) * D * 8) + align256(uint64_t(D) * 8) + 256; }
+
+uint64_t calibrate_rv_workspace_bytes(int D, int64_t n_kv) {
+  return calibrate_workspace_bytes(D) + align256(uint64_t(n_kv) * 8);
+}
+
+int launch_calibrate(const float* q, int64_t n, int D, float* R, void* ws, int32_t* status, cudaStream_t stream) {
+  CalibWs c = calib_ws(ws, D);
+  const int rc = launch_cov(q, n, D, nullptr, c.A, stream);
+  if (rc != OSCAR_OK) return rc;
+  return launch_fit(c, D, R, status, stream);
+}
+
+int launch_calibrate_rv(const float* q, int64_t nq, const float* k, const float* v, int64_t nkv, int D, float* R,
+                        void* ws, int32_t* status, cudaStream_t stream) {
+  CalibWs c = calib_ws(ws, D);
+  int rc = launch_cov(q, nq, D, nullptr, c.E, stream);  // Sigma_Q (E is free until the fit's last kernel)
+  if (rc != OSCAR_OK) return rc;
+  weight_kernel<<<unsigned((nkv + kWTok - 1) / kWTok), D, 0, stream>>>(k, nkv, D, c.E, c.w);
+  if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_LAUNCH;
+  rc = launch_cov(v, nkv, D, c.w, c.A, stream);
+  if (rc != OSCAR_OK) return rc;
+  return launch_fit(c, D, R, status, stream);
 }
 
 }  // namespace oscar

@@ -69,5 +69,9 @@ int decode_grid(const Geom& g, int seq_len_hint, int num_splits);
 // R_K calibration (calibrate.cu)
 uint64_t calibrate_workspace_bytes(int D);
 int launch_calibrate(const float* q, int64_t n, int D, float* R, void* ws, int32_t* status, cudaStream_t stream);
+// R_V calibration from the score-weighted V covariance (calibrate.cu)
+uint64_t calibrate_rv_workspace_bytes(int D, int64_t n_kv);
+int launch_calibrate_rv(const float* q, int64_t nq, const float* k, const float* v, int64_t nkv, int D, float* R,
+                        void* ws, int32_t* status, cudaStream_t stream);
 
 }  // namespace oscar

@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LA
 
 # every symbol include/oscar_kv.h declares
 EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "decode_step", "attn_decode_static",
-           "oscar_kv_set_profile_events", "oscar_calibrate_workspace_query", "oscar_calibrate_rk")
+           "oscar_kv_set_profile_events", "oscar_calibrate_workspace_query", "oscar_calibrate_rk",
+           "oscar_calibrate_rv_workspace_query", "oscar_calibrate_rv")
 STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -190,6 +191,12 @@ def _calib_fns():
         L.oscar_calibrate_rk.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
         L.oscar_calibrate_rk.restype = ctypes.c_int
+        L.oscar_calibrate_rv_workspace_query.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)]
+        L.oscar_calibrate_rv_workspace_query.restype = ctypes.c_int
+        L.oscar_calibrate_rv.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
+        L.oscar_calibrate_rv.restype = ctypes.c_int
         L._calib_ready = True
     return L
 
@@ -210,4 +217,27 @@ def calibrate_rk(q, R_out, workspace, status=None, stream=None, check: bool = Tr
                                          _stream(stream))
     if check and rc != 0:
         raise OscarError("oscar_calibrate_rk", rc)
+    return rc
+
+
+def calibrate_rv_workspace_bytes(head_dim: int, n_kv_rows: int) -> int:
+    n = ctypes.c_uint64(0)
+    rc = _calib_fns().oscar_calibrate_rv_workspace_query(int(head_dim), int(n_kv_rows), ctypes.byref(n))
+    if rc != 0:
+        raise OscarError("oscar_calibrate_rv_workspace_query", rc)
+    return int(n.value)
+
+
+def calibrate_rv(q, k, v, R_out, workspace, status=None, stream=None, check: bool = True) -> int:
+    """R_V fitted to the score-weighted covariance of the float32 value rows v [n][D],
+    each weighted by k_t q^T q k_t^T (see oscar_calibrate_rv); writes R_out [D][D]."""
+    nq, d = int(q.shape[0]), int(q.shape[1])
+    nkv = int(k.shape[0])
+    if tuple(k.shape) != tuple(v.shape) or int(k.shape[1]) != d:
+        raise ValueError("k and v must both be [n_kv][head_dim] with the head_dim of q")
+    rc = _calib_fns().oscar_calibrate_rv(_ptr(q), nq, _ptr(k), _ptr(v), nkv, d, _ptr(R_out), _ptr(workspace),
+                                         int(workspace.numel() * workspace.element_size()), _ptr(status),
+                                         _stream(stream))
+    if check and rc != 0:
+        raise OscarError("oscar_calibrate_rv", rc)
     return rc

@@ -250,7 +250,7 @@ def score_energy(calib_q: np.ndarray, calib_k: np.ndarray) -> np.ndarray:
     q = np.asarray(calib_q, np.float64)
     k = np.asarray(calib_k, np.float64)
     sigma_q = q.T @ q
-    return np.einsum("ti,ij,tj->t", k, sigma_q, k)
+    return np.sum((k @ sigma_q) * k, axis=1)
 
 
 def calibrate_rv(calib_q: np.ndarray, calib_k: np.ndarray, calib_v: np.ndarray) -> np.ndarray:

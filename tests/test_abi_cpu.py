@@ -136,3 +136,32 @@ def test_calibrate_entry_points_validate_before_launch(lib):
     assert f(big, (1 << 28) + 1, 128, big, big, 1 << 30, None, None) == -1
     assert f(P((1 << 20) + 4), 1000, 128, big, big, 1 << 30, None, None) == -1  # misaligned
     assert f(big, 1000, 128, big, big, 1000, None, None) == -3            # workspace too small
+
+
+def test_calibrate_rv_entry_points_validate_before_launch(lib):
+    P = ctypes.c_void_p
+    big = P(1 << 20)  # never dereferenced: every call below stops in validation
+    n = ctypes.c_uint64(0)
+    q = lib.oscar_calibrate_rv_workspace_query
+    q.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)]
+    assert q(96, 100, ctypes.byref(n)) == -5
+    assert q(128, 0, ctypes.byref(n)) == -1
+    assert q(128, 100, None) == -1
+    a = lambda x: -(-x // 256) * 256
+    for d in (128, 256, 512):
+        for rows in (1, 1000, 160000):
+            assert q(d, rows, ctypes.byref(n)) == 0
+            # the R_K workspace followed by one float64 weight per key row
+            assert n.value == 3 * a(d * d * 8) + a(d * 8) + 256 + a(rows * 8)
+    f = lib.oscar_calibrate_rv
+    f.argtypes = [P, ctypes.c_int64, P, P, ctypes.c_int64, ctypes.c_int32, P, P, ctypes.c_uint64, P, P]
+    ok = dict(q=big, nq=1000, k=big, v=big, nkv=500, d=128, r=big, ws=big, wsb=1 << 30)
+    call = lambda **kw: f(*({**ok, **kw}.values()), None, None)
+    assert call(d=96) == -5                                   # head_dim
+    for name in ("q", "k", "v", "r", "ws"):
+        assert call(**{name: None}) == -1                     # null pointer
+    assert call(nq=0) == -1 and call(nkv=0) == -1             # no rows
+    assert call(nkv=(1 << 28) + 1) == -1
+    assert call(k=P((1 << 20) + 4)) == -1                     # misaligned
+    assert call(ws=P((1 << 20) + 128)) == -1                  # workspace not 256-aligned
+    assert call(wsb=3 * a(128 * 128 * 8) + a(128 * 8) + 256) == -3   # no room for the weights

@@ -1,4 +1,4 @@
-"""GPU parity of the R_K calibration (oscar_calibrate_rk) against the oracle.
+"""GPU parity of the R_K and R_V calibrations (oscar_calibrate_rk, _rv) against the oracle.
 
 The calibration is unique once the eigenvalues are distinct (descending order,
 sign convention), so R_K is compared entry by entry: the GPU computes Sigma and
@@ -6,7 +6,9 @@ the eigenvectors in float64 (Jacobi) and writes float32; the oracle uses
 float64 and numpy's eigensolver.  Tolerance 1e-5 on entries of magnitude about
 1/sqrt(D), from Jacobi's stopping rule (off-diagonal norm below 1e-13 of the
 Frobenius norm) over the smallest relative eigenvalue gap of these inputs,
-plus float32 rounding.  The diagonal case is exact up to rounding."""
+plus float32 rounding.  The diagonal case is exact up to rounding.  R_V uses the
+same fit on the score-weighted V covariance; the smallest relative eigenvalue
+gaps of its inputs here (3e-7 .. 5e-6) are those of the R_K inputs."""
 import numpy as np
 import pytest
 import torch
@@ -56,5 +58,46 @@ def test_calibrate_matches_oracle(d, n):
     got, st = _gpu_calibrate(q)
     assert st == 0
     ref = O.calibrate_rk(q)
+    assert np.abs(got - ref).max() <= 1e-5, np.abs(got - ref).max()
+    assert np.abs(got @ got.T - np.eye(d)).max() <= 1e-5
+
+
+def _gpu_calibrate_rv(q, k, v):
+    d = q.shape[1]
+    qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda() for x in (q, k, v))
+    out = torch.full((d, d), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.calibrate_rv_workspace_bytes(d, k.shape[0]), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    K.calibrate_rv(qt, kt, vt, out, ws, status=st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64), int(st.item())
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_calibrate_rv_diagonal_case(d):
+    # channel i: values +-a_i e_i with key e_i, queries sig_j e_j: Sigma_V is
+    # diagonal and the weights, not the value magnitudes, set the order
+    rng = np.random.default_rng(70 + d)
+    perm = rng.permutation(d)
+    a = (1.0 + np.arange(d) / d).astype(np.float32)
+    sig = ((perm + 1.0) / a).astype(np.float32)
+    q = np.diag(sig)
+    k = np.repeat(np.eye(d, dtype=np.float32), 2, axis=0)
+    v = np.repeat(np.diag(a), 2, axis=0) * np.tile(np.float32([1.0, -1.0]), d)[:, None]
+    got, st = _gpu_calibrate_rv(q, k, v)
+    assert st == 0
+    assert np.abs(got - O.calibrate_rv(q, k, v)).max() <= 1e-6
+
+
+@pytest.mark.parametrize("d,nq,nkv", [(128, 4096, 3000), (256, 3000, 2500), (512, 2048, 2100)])
+def test_calibrate_rv_matches_oracle(d, nq, nkv):
+    rng = np.random.default_rng(d + nq + nkv)
+    ch = rng.choice(d, max(1, round(0.02 * d)), replace=False)
+    q = S.activations(rng, (nq, d), ch, kind="t3")
+    k = S.activations(rng, (nkv, d), ch, kind="t3")
+    v = S.activations(rng, (nkv, d), ch, kind="t3")
+    got, st = _gpu_calibrate_rv(q, k, v)
+    assert st == 0
+    ref = O.calibrate_rv(q, k, v)
     assert np.abs(got - ref).max() <= 1e-5, np.abs(got - ref).max()
     assert np.abs(got @ got.T - np.eye(d)).max() <= 1e-5
