@@ -1494,31 +1494,50 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) store(i, j * kGroup + lane + 32 * e, x[e]);
           }
-        } else if (a.absorb_v) {
-          // o' itself (the caller folds R_V^T into its output projection)
-          for (int r = threadIdx.x; r < D; r += 32 * kNCW)
+        } else if (a.absorb_v || (rv_smem && rv_ok)) {
+          // o = o' R_V^T (or o' when absorbed): one thread per output channel r
+          const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
+          for (int r = threadIdx.x; r < D; r += 32 * kNCW) {
+            float res[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) res[i] = 0.f;
+            if (a.absorb_v) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (i < Gh) res[i] = ob[i * D + r];
+            } else {
+              // 16-byte loads in a skewed walk over j: thread r reads chunk
+              // (j4 + r) % (D / 4) of row r and of each o' row, so the eight
+              // threads of a quarter warp touch eight different chunks
+#pragma unroll 4
+              for (int j4 = 0; j4 < D / 4; ++j4) {
+                const int jc = ((j4 + r) & (D / 4 - 1)) * 4;
+                const float4 rv = *reinterpret_cast<const float4*>(rvs + r * D + jc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  if (i < Gh) {
+                    const float4 ov = *reinterpret_cast<const float4*>(ob + i * D + jc);
+                    res[i] = fmaf(rv.x, ov.x, fmaf(rv.y, ov.y, fmaf(rv.z, ov.z, fmaf(rv.w, ov.w, res[i]))));
+                  }
+                }
+              }
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              if (i < Gh) store(i, r, ob[i * D + r]);
+              if (i < Gh) store(i, r, res[i]);
+          }
         } else {
-          // o = o' R_V^T: warp w takes rows w, w + 4, ... of R_V; lane l reads
-          // columns 4l .. 4l + 3 (+ 128 per step) and the warp reduces, so every
-          // load is coalesced (and conflict-free from shared memory).  The rows
-          // come from the stage area when they were prefetched there, else
-          // through L2; the arithmetic and its order are the same either way, so
-          // the output does not depend on which CTA of the unit merges it
-          const bool from_smem = rv_smem && rv_ok;
-          const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
+          // rows of R_V from L2: warp w takes rows w, w + 4, ...; lane l reads
+          // columns 4l .. 4l + 3 (+ 128 per step), so every load is coalesced
 #pragma unroll 4
           for (int r = warp; r < D; r += kNCW) {
             const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);
-            const float4* rs4 = reinterpret_cast<const float4*>(rvs + r * D);
             float res[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) res[i] = 0.f;
 #pragma unroll
             for (int j4 = lane; j4 < D / 4; j4 += 32) {
-              const float4 rv = from_smem ? rs4[j4] : __ldg(rv4 + j4);
+              const float4 rv = __ldg(rv4 + j4);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 if (i < Gh) {

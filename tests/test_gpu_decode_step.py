@@ -1,7 +1,9 @@
 """decode_step (append + decode in one call) against kv_append followed by
-attn_decode: the same kernels on the same data, so outputs, lse, cache bytes
-and status words must be identical bit for bit, whatever blocks the fused call
-streams before the append completes.  Cases cover one and several new tokens,
+attn_decode: the same kernels on the same data, so lse, cache bytes and status
+words must be identical bit for bit, whatever blocks the fused call streams
+before the append completes, and outputs equal up to the rounding of the V
+un-rotation, whose summation order depends on the CTA that merges a unit
+(assert_same_decode).  Cases cover one and several new tokens,
 ring wrap, appends longer than the ring, new positions inside the sink, G = 8
 and D = 256.  The oracle agreement of the sequential calls is covered by the
 decode and append parity tests."""
@@ -11,6 +13,7 @@ import torch
 
 from int2_kv_cache_append_gb300 import oscar_kv as K
 from int2_kv_cache_append_gb300 import synth as S
+from tests.gpu_helpers import assert_same_decode
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
 
@@ -74,7 +77,4 @@ def test_decode_step_equals_append_then_decode(case):
     assert s0 == s1 == 0
     assert np.array_equal(c0, c1)
     assert np.isfinite(o0).all()
-    dif = np.argwhere((o0.view(np.uint32) != o1.view(np.uint32)).any(axis=2))
-    assert dif.size == 0, (f"outputs differ at (b, head) {dif[:12].tolist()} of {len(dif)}, "
-                           f"max |diff| {np.abs(o0 - o1).max():.3e}")
-    assert np.array_equal(l0.view(np.uint32), l1.view(np.uint32)), f"lse max |diff| {np.abs(l0 - l1).max():.3e}"
+    assert_same_decode(o0, o1, l0, l1)
