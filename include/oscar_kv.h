@@ -19,11 +19,12 @@
  *    --kv-cache-dtype int2 --kv-cache-quant-group-size 128], and keep the
  *    first `sink` and the last `recent` tokens as BF16 [model card, Run:
  *    LLAMA_KV_HP_SINK / LLAMA_KV_HP_RECENT; hysenlabs article, What OSCAR
- *    compresses: INT2 bulk with a small BF16 sink and recent window].
+ *    compresses: the bulk of the cache INT2, BF16 only for the first and the
+ *    latest tokens].
  *
  *  - attn_decode: one decode step of attention over that mixed cache without
  *    a separate dequantise pass [hysenlabs article, How the offline rotation
- *    is fit: fused mixed-precision flash attention]: the query is rotated by
+ *    is fit: one fused attention kernel over the mixed cache]: the query is rotated by
  *    R_K (the same rotation as K, so q'.k' = q.k) ["OSCAR-LLAMACPP-Gemma-4-
  *    12B-it-INT2-KV" card, Folders: applied to Q/K (and V)], softmax over all
  *    cached positions, and the value rotation is undone once at the output,

@@ -8,9 +8,9 @@
 //
 // Source: "OSCAR-RotationZoo" model card (File format: R_K = R H P_br with R
 // the eigenvectors of the query covariance, H a head-dim Hadamard and P_br the
-// eigenvalue-sorted bit-reversal permutation; the V rotation built on the
-// score-weighted V covariance V^T diag(K^T (Q^T Q) K) V, read with K holding
-// the keys as columns) and the hysenlabs article on OSCAR (How the offline
+// eigenvalue-sorted bit-reversal permutation; for V, the covariance of the
+// value rows weighted by attention scores, printed as V^T diag(K^T (Q^T Q) K) V
+// and read with K holding the keys as columns) and the hysenlabs article on OSCAR (How the offline
 // rotation is fit: Q/K/V activations are captured offline and the rotation is
 // derived from their covariance).
 //

@@ -24,8 +24,8 @@ Sources (titles of the pages describing OSCAR; section in brackets):
   quant group size 128; [File format]: one head_dim x head_dim rotation per
   layer, shared by the heads of the layer.
 * hysenlabs article on FutureMLS-Lab/OSCAR [What OSCAR compresses]: bulk of the
-  cache INT2, small BF16 sink and recent window; [How the offline rotation is
-  fit]: clipping thresholds bound the values before they are rounded; fused
+  cache INT2, BF16 only for the first and the latest tokens; [How the offline rotation is
+  fit]: the fit also yields clip limits applied ahead of rounding; fused
   mixed INT2+BF16 flash attention instead of dequantise-then-attend.
 
 Readings taken where the pages are silent (each listed in the design doc):
@@ -59,8 +59,8 @@ Readings taken where the pages are silent (each listed in the design doc):
   min..max; rho is 1.16 at a resolution of 2^-8 (297/256) so that levels,
   midpoints and the span 2 rho + 1 are exact binary fractions; the code is the
   nearest level, a tie going to the lower one;
-* R_V calibration (RotationZoo [File format]: the V rotation is built on a
-  score-weighted V covariance): the printed V^T diag(K^T (Q^T Q) K) V read
+* R_V calibration (RotationZoo [File format]: the V rotation comes from a
+  covariance of the values weighted by scores): the printed V^T diag(K^T (Q^T Q) K) V read
   with K holding keys as columns, so each key row is weighted by its score
   energy w_t = k_t Q^T Q k_t^T; R_V = E H P_br as for R_K.
 
@@ -254,7 +254,7 @@ def score_energy(calib_q: np.ndarray, calib_k: np.ndarray) -> np.ndarray:
 
 
 def calibrate_rv(calib_q: np.ndarray, calib_k: np.ndarray, calib_v: np.ndarray) -> np.ndarray:
-    """V-side rotation fitted to the score-weighted V covariance, float64 [D][D].
+    """V-side rotation fitted to the value covariance weighted by score energy, float64 [D][D].
 
     OSCAR-RotationZoo card [File format]: the V rotation file is built on
     Sigma_V = V^T diag(K^T (Q^T Q) K) V, with the same R H P_br construction as

@@ -7,7 +7,7 @@ float64 and numpy's eigensolver.  Tolerance 1e-5 on entries of magnitude about
 1/sqrt(D), from Jacobi's stopping rule (off-diagonal norm below 1e-13 of the
 Frobenius norm) over the smallest relative eigenvalue gap of these inputs,
 plus float32 rounding.  The diagonal case is exact up to rounding.  R_V uses the
-same fit on the score-weighted V covariance; the smallest relative eigenvalue
+same fit on the value covariance weighted by score energy; the smallest relative eigenvalue
 gaps of its inputs here (3e-7 .. 5e-6) are those of the R_K inputs."""
 import numpy as np
 import pytest
