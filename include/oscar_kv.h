@@ -113,6 +113,7 @@ extern "C" {
 
 #define OSCAR_KV_GROUP 128       /* quant group along head_dim */
 #define OSCAR_KV_MAX_SPLITS 64   /* upper bound on decode partial slots per query head */
+#define OSCAR_KV_CALIB_MAX_ROWS 268431360LL /* calibration rows per call: 65535 chunks of 4096 */
 
 /* config flags */
 enum {
@@ -308,7 +309,7 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop);
  * from their covariance].  Offline work, not part of the decode path.
  *   q          device [n_rows][head_dim] float32 query rows of one layer
  *              (post-RoPE; every head's rows pooled), 16-byte aligned.
- *   n_rows     1 .. 2^28.
+ *   n_rows     1 .. OSCAR_KV_CALIB_MAX_ROWS.
  *   R_K_out    device [head_dim][head_dim] float32, row-major, written:
  *              Sigma = q^T q in float64; E = its eigenvectors (one-sided
  *              Jacobi in float64 on a cooperative grid) ordered by descending
@@ -341,7 +342,7 @@ int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* 
  *   k, v       device [n_kv_rows][head_dim] float32 key and value rows of the
  *              same layer (row t of k and of v: one token of one KV head),
  *              16-byte aligned.
- *   n_q_rows, n_kv_rows  1 .. 2^28.
+ *   n_q_rows, n_kv_rows  1 .. OSCAR_KV_CALIB_MAX_ROWS.
  *   R_V_out    device [head_dim][head_dim] float32, row-major, written:
  *              Sigma_Q = q^T q and w_t = k_t Sigma_Q k_t^T in float64,
  *              Sigma_V = sum_t w_t v_t^T v_t in float64, then E, its sign

@@ -42,6 +42,8 @@ namespace {
 constexpr int kCovTile = 64;          // Sigma tile per CTA
 constexpr int kCovRows = 32;          // rows staged per step
 constexpr int64_t kCovChunk = 4096;   // rows per CTA
+// the row chunks are the grid's z dimension (at most 65535)
+static_assert(OSCAR_KV_CALIB_MAX_ROWS == 65535 * kCovChunk, "calibration row limit");
 constexpr int kMaxSweeps = 40;
 constexpr int kPairThreads = 256;
 

@@ -244,7 +244,7 @@ int oscar_calibrate_workspace_query(int32_t head_dim, uint64_t* bytes) {
 int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* R_K_out, void* workspace,
                        uint64_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (head_dim != 128 && head_dim != 256 && head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
-  if (!q || !R_K_out || !workspace || n_rows < 1 || n_rows > (int64_t(1) << 28)) return OSCAR_ERR_INVALID;
+  if (!q || !R_K_out || !workspace || n_rows < 1 || n_rows > OSCAR_KV_CALIB_MAX_ROWS) return OSCAR_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(R_K_out, 16) || !aligned(workspace, 256)) return OSCAR_ERR_INVALID;
   if (workspace_bytes < oscar::calibrate_workspace_bytes(head_dim)) return OSCAR_ERR_WORKSPACE;
   return oscar::launch_calibrate(q, n_rows, head_dim, R_K_out, workspace, dev_status,
@@ -252,7 +252,7 @@ int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* 
 }
 
 int oscar_calibrate_rv_workspace_query(int32_t head_dim, int64_t n_kv_rows, uint64_t* bytes) {
-  if (!bytes || n_kv_rows < 1 || n_kv_rows > (int64_t(1) << 28)) return OSCAR_ERR_INVALID;
+  if (!bytes || n_kv_rows < 1 || n_kv_rows > OSCAR_KV_CALIB_MAX_ROWS) return OSCAR_ERR_INVALID;
   if (head_dim != 128 && head_dim != 256 && head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
   *bytes = oscar::calibrate_rv_workspace_bytes(head_dim, n_kv_rows);
   return OSCAR_OK;
@@ -263,7 +263,7 @@ int oscar_calibrate_rv(const float* q, int64_t n_q_rows, const float* k, const f
                        int32_t* dev_status, void* stream) {
   if (head_dim != 128 && head_dim != 256 && head_dim != 512) return OSCAR_ERR_UNSUPPORTED;
   if (!q || !k || !v || !R_V_out || !workspace) return OSCAR_ERR_INVALID;
-  if (n_q_rows < 1 || n_q_rows > (int64_t(1) << 28) || n_kv_rows < 1 || n_kv_rows > (int64_t(1) << 28))
+  if (n_q_rows < 1 || n_q_rows > OSCAR_KV_CALIB_MAX_ROWS || n_kv_rows < 1 || n_kv_rows > OSCAR_KV_CALIB_MAX_ROWS)
     return OSCAR_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(R_V_out, 16) || !aligned(workspace, 256))
     return OSCAR_ERR_INVALID;

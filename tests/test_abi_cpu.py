@@ -133,7 +133,7 @@ def test_calibrate_entry_points_validate_before_launch(lib):
     assert f(big, 1000, 96, big, big, 1 << 30, None, None) == -5          # head_dim
     assert f(None, 1000, 128, big, big, 1 << 30, None, None) == -1        # null rows
     assert f(big, 0, 128, big, big, 1 << 30, None, None) == -1            # no rows
-    assert f(big, (1 << 28) + 1, 128, big, big, 1 << 30, None, None) == -1
+    assert f(big, 65535 * 4096 + 1, 128, big, big, 1 << 30, None, None) == -1  # more row chunks than grid z
     assert f(P((1 << 20) + 4), 1000, 128, big, big, 1 << 30, None, None) == -1  # misaligned
     assert f(big, 1000, 128, big, big, 1000, None, None) == -3            # workspace too small
 
@@ -161,7 +161,7 @@ def test_calibrate_rv_entry_points_validate_before_launch(lib):
     for name in ("q", "k", "v", "r", "ws"):
         assert call(**{name: None}) == -1                     # null pointer
     assert call(nq=0) == -1 and call(nkv=0) == -1             # no rows
-    assert call(nkv=(1 << 28) + 1) == -1
+    assert call(nkv=65535 * 4096 + 1) == -1 and call(nq=65535 * 4096 + 1) == -1  # grid z holds 65535 chunks
     assert call(k=P((1 << 20) + 4)) == -1                     # misaligned
     assert call(ws=P((1 << 20) + 128)) == -1                  # workspace not 256-aligned
     assert call(wsb=3 * a(128 * 128 * 8) + a(128 * 8) + 256) == -3   # no room for the weights
