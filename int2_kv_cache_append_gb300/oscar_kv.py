@@ -110,7 +110,16 @@ def lib():
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor argument (None -> NULL).  The library's kernels
+    read it as a dense array in device memory, so a host tensor or a strided view
+    is refused here instead of reaching the GPU."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"oscar_kv: expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError("oscar_kv: expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):

@@ -165,3 +165,15 @@ def test_calibrate_rv_entry_points_validate_before_launch(lib):
     assert call(k=P((1 << 20) + 4)) == -1                     # misaligned
     assert call(ws=P((1 << 20) + 128)) == -1                  # workspace not 256-aligned
     assert call(wsb=3 * a(128 * 128 * 8) + a(128 * 8) + 256) == -3   # no room for the weights
+
+
+def test_binding_refuses_host_tensors(lib):
+    # the kernels would dereference a host address on the GPU: refused before the call
+    import torch
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        K._ptr(torch.zeros(4))
+    assert K._ptr(None) is None
+    cfg = K.KVConfig(1, 1, 4, 1, 128, 4, 8, 64)
+    with pytest.raises(ValueError):
+        K.kv_append(cfg, torch.zeros(64, dtype=torch.uint8), 0, torch.zeros(1, 1, 1, 128), torch.zeros(1, 1, 1, 128),
+                    torch.zeros(1, dtype=torch.int32), torch.eye(128), torch.eye(128))
