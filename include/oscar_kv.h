@@ -224,7 +224,11 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  *              cut into equal slices of work, one per CTA, so a CTA can cover
  *              the tail of one unit and the head of the next.
  *   out        device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_OUT_FP32);
- *              o = o' R_V^T, or o' with OSCAR_FLAG_ABSORB_V.
+ *              o = o' R_V^T, or o' with OSCAR_FLAG_ABSORB_V.  At head_dim 128 the
+ *              last bits of o may differ between calls: the CTA that finishes
+ *              a sequence's KV head last merges it and applies R_V^T in one of
+ *              two summation orders (R_V from shared memory or from L2); lse
+ *              and o' do not depend on it.
  *   lse        device float32 [B][Hq] or NULL: natural-log log-sum-exp of the
  *              scaled scores.
  *   workspace  device scratch of workspace_bytes (see kv_layout_query); it
@@ -247,7 +251,8 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
  * decode step of a serving loop (append the current token of every sequence,
  * then attend over the whole context).  Same computation and results as the
  * two calls made in sequence with the same arguments (kv_append of k_new,
- * v_new at start_pos; attn_decode over seq_lens); the pages' append (Qwen3-4B
+ * v_new at start_pos; attn_decode over seq_lens; `out` up to the last bits, as
+ * between any two attn_decode calls); the pages' append (Qwen3-4B
  * card, Run; RotationZoo, How to use) and fused attention (hysenlabs article,
  * How the offline rotation is fit) back to back.
  * Because the call knows which cache locations the append writes (the sink
