@@ -356,7 +356,8 @@ int oscar_calibrate_rk(const float* q, int64_t n_rows, int32_t head_dim, float* 
  *   workspace  device, >= the size oscar_calibrate_rv_workspace_query returns
  *              (it grows with n_kv_rows), 256-byte aligned; caller owned,
  *              contents undefined after.
- * Launches six kernels on `stream` (the fifth as a cooperative launch).  Sweep
+ * Launches five kernels on `stream` (the fourth as a cooperative launch) and
+ * two memsets.  Sweep
  * limit, status bits and errors as oscar_calibrate_rk.
  */
 int oscar_calibrate_rv_workspace_query(int32_t head_dim, int64_t n_kv_rows, uint64_t* bytes);
