@@ -239,6 +239,8 @@ def reference_arm(args):
             "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_desc(w), "rotation": rotation_desc(args),
+                       "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16",
+                       "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 297/256" if args.lloyd_max else "uniform",
                        "sample": f"{heads} of {w.num_kv_heads} KV heads of one sequence per step"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
