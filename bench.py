@@ -455,6 +455,9 @@ def ours_append(args):
     from int2_kv_cache_append_gb300 import oscar_kv as K
     from int2_kv_cache_append_gb300 import synth as S
 
+    if args.hadamard or args.v_bf16 or args.lloyd_max:
+        raise SystemExit("bench.py: --hadamard, --v-bf16 and --lloyd-max select decode modes; the append "
+                         "workload measures the tensor-core append of the default mode only")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
