@@ -240,7 +240,7 @@ def reference_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_desc(w), "rotation": rotation_desc(args),
                        "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16",
-                       "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 297/256" if args.lloyd_max else "uniform",
+                       "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 1.16 (float32)" if args.lloyd_max else "uniform",
                        "sample": f"{heads} of {w.num_kv_heads} KV heads of one sequence per step"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -422,7 +422,7 @@ def ours(args):
                    "rotation": rotation_desc(args),
                    "l2": "flushed between steps (512 MiB write)",
                    "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16",
-                   "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 297/256" if args.lloyd_max else "uniform",
+                   "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 1.16 (float32)" if args.lloyd_max else "uniform",
                    "parallelism":
                        f"replica x{world}" if world > 1 else "single"},
         "kv_gbs": step_gbs, "kv_pct_hbm": step_gbs / peak,

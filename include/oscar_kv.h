@@ -55,11 +55,13 @@
  * OSCAR and running a first Qwen3-8B calibration: an SGLANG_LLOYD_MAX switch;
  * Where OSCAR loses: results quoted at LM_RATIO=1.16]: the four levels of a
  * group are unevenly spaced like the four-level Lloyd-Max quantiser of a
- * Gaussian, level(c) = (0, rho, rho + 1, 2 rho + 1)[c], with rho = 297/256
- * (1.16 at a resolution of 2^-8; the outer gaps are rho times the inner one).
- * The quantiser is as above except s = fp16((mx - mn) / (2 rho + 1)) and, with
- * y = (x - z) * fl(1/s), code = [y > rho/2] + [y > rho + 1/2] + [y > 3rho/2 + 1]
- * (the nearest level; on a midpoint, the lower one).  Dequantised value:
+ * Gaussian, level(c) = (0, rho, rho + 1, 2 rho + 1)[c], with rho = 1.16
+ * rounded to float32 (the outer gaps are rho times the inner one).
+ * The quantiser is as above except s = fp16((mx - mn) / span) with the float32
+ * span = 2 rho + 1 (exact) and, with y = (x - z) * fl(1/s),
+ * code = [y > m0] + [y > m1] + [y > m2] for the float32 midpoints m0 = rho/2,
+ * m1 = rho + 1/2 (both exact) and m2 = fl(span - m0) (the float32 nearest to
+ * 3rho/2 + 1): the nearest level; on a midpoint, the lower one.  Dequantised value:
  * z + s * level(code).  The bytes' layout does not change.
  *
  * Cache layout (bytes; every region starts on a 256-byte boundary; the cache

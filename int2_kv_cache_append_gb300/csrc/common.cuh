@@ -93,17 +93,22 @@ __device__ __forceinline__ void unpack16_v(uint32_t w, uint32_t (&r)[8]) {
 // log2 of the value unpack16_v gives a code of register p, per unit of code
 __device__ __forceinline__ constexpr int unpack_v_exp(int p) { return (p == 0 || p == 5) ? 0 : 2 * unpack_k(p) - 24; }
 
-// Lloyd-Max levels: level(c) = (0, rho, rho + 1, 2 rho + 1)[c] with rho = 297/256
-// (1.16 to 2^-8), so the span, the midpoints and the level algebra below are
-// exact binary fractions.  Writing c = c0 + 2 c1, level(c) = rho * c + (1 - rho) * c1
-// = rho * c + kLmHi * (2 c1): the decode multiplies the code sum by rho and adds
-// kLmHi times the same sum over the codes' high bits (unpack16_hi).
-constexpr float kLmRho = 1.16015625f;
-constexpr float kLmSpan = 3.3203125f;    // 2 rho + 1: the group's range in level units
-constexpr float kLmHi = -0.080078125f;   // (1 - rho) / 2
-constexpr float kLmMid0 = 0.580078125f;  // rho / 2
-constexpr float kLmMid1 = 1.66015625f;   // rho + 1/2
-constexpr float kLmMid2 = 2.740234375f;  // 3 rho / 2 + 1
+// Lloyd-Max levels: level(c) = (0, rho, rho + 1, 2 rho + 1)[c] with rho = 1.16
+// (LM_RATIO as printed, rounded to float32).  Writing c = c0 + 2 c1,
+// level(c) = rho * c + (1 - rho) * c1 = rho * c + kLmHi * (2 c1): the decode
+// multiplies the code sum by rho and adds kLmHi times the same sum over the
+// codes' high bits (unpack16_hi).  The codec's span and level midpoints are
+// float32, each the single rounding of an exact value (so any evaluation of
+// these constant expressions at float or higher precision gives the same bits):
+//   span = 2 rho + 1 (exact), m0 = rho / 2 (exact), m1 = rho + 1/2 (exact),
+//   m2 = span - m0 = the float32 nearest to 3 rho / 2 + 1;
+// kLmHi = (1 - rho) / 2 is exact as well (Sterbenz).
+constexpr float kLmRho = 1.16f;
+constexpr float kLmSpan = 2.0f * kLmRho + 1.0f;      // the group's range in level units
+constexpr float kLmHi = (1.0f - kLmRho) * 0.5f;
+constexpr float kLmMid0 = kLmRho * 0.5f;
+constexpr float kLmMid1 = kLmRho + 0.5f;
+constexpr float kLmMid2 = kLmSpan - kLmMid0;
 
 // nearest Lloyd-Max level of y = (x - zero) / unit; on a midpoint the lower one
 __device__ __forceinline__ int lm_code(float y) { return (y > kLmMid0) + (y > kLmMid1) + (y > kLmMid2); }

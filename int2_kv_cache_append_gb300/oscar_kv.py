@@ -20,7 +20,7 @@ FLAG_IN_FP32 = 2
 FLAG_OUT_FP32 = 4
 FLAG_HADAMARD = 8  # rotate by the in-quant Hadamard; R_K / R_V may be None
 FLAG_V_BF16 = 16  # K-only INT2: V kept BF16 at every position
-FLAG_LLOYD_MAX = 32  # INT2 codes index Lloyd-Max levels (0, rho, rho + 1, 2 rho + 1), rho = 297/256
+FLAG_LLOYD_MAX = 32  # INT2 codes index Lloyd-Max levels (0, rho, rho + 1, 2 rho + 1), rho = 1.16 (float32)
 
 DEV_OVER_CAPACITY = 1
 DEV_NONFINITE = 2

@@ -28,7 +28,7 @@ Sources (titles of the pages describing OSCAR; section in brackets):
   fit]: the fit also yields clip limits applied ahead of rounding; fused
   mixed INT2+BF16 flash attention instead of dequantise-then-attend.
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 
 * quantiser: asymmetric per group of 128 along head_dim, scale=(max-min)/3,
   zero=min, both stored as IEEE fp16 (round-to-nearest-even);
@@ -56,9 +56,10 @@ Readings taken where the pages are silent (each listed in the design doc):
   zero + unit * (0, rho, rho + 1, 2 rho + 1), rho = LM_RATIO being the ratio of
   the outer to the inner gap between adjacent levels (the shape of the
   four-level Lloyd-Max quantiser of a Gaussian), spread over the group's
-  min..max; rho is 1.16 at a resolution of 2^-8 (297/256) so that levels,
-  midpoints and the span 2 rho + 1 are exact binary fractions; the code is the
-  nearest level, a tie going to the lower one;
+  min..max; rho is the printed 1.16 rounded to float32, the span 2 rho + 1 and
+  the midpoints rho / 2, rho + 1/2 (both exact) and 3 rho / 2 + 1 (computed as
+  span - rho / 2, one rounding) are float32; the code is the number of
+  midpoints strictly below y: the nearest level, a tie going to the lower one;
 * R_V calibration (RotationZoo [File format]: the V rotation comes from a
   covariance of the values weighted by scores): the printed V^T diag(K^T (Q^T Q) K) V read
   with K holding keys as columns, so each key row is weighted by its score
@@ -86,8 +87,24 @@ FLAG_HADAMARD = 8
 FLAG_V_BF16 = 16
 FLAG_LLOYD_MAX = 32
 
-# Lloyd-Max level ratio: 1.16 rounded to a multiple of 2^-8
-LM_RATIO = 297 / 256
+# Lloyd-Max level ratio LM_RATIO = 1.16 as printed, rounded once to float32
+LM_RATIO = float(np.float32(1.16))
+
+
+def lloyd_max_thresholds():
+    """(span, (m0, m1, m2)) of the Lloyd-Max codec as float32, each one
+    IEEE round-to-nearest operation on rho = float32(LM_RATIO), in this order:
+      span = 2 * rho + 1        (exact: 2 rho and 1 share the step of [2, 4))
+      m0   = rho * 0.5          (exact)
+      m1   = rho + 0.5          (exact: both are multiples of rho's step)
+      m2   = span - m0          (the float32 nearest to 3 rho / 2 + 1)
+    m0, m1, m2 are the midpoints between adjacent levels (0, rho, rho + 1, 2 rho + 1)."""
+    rho = np.float32(LM_RATIO)
+    span = np.float32(np.float32(2.0) * rho) + np.float32(1.0)
+    m0 = np.float32(rho * np.float32(0.5))
+    m1 = np.float32(rho + np.float32(0.5))
+    m2 = np.float32(span - m0)
+    return np.float32(span), (m0, m1, m2)
 
 
 # --------------------------------------------------------------------------
@@ -301,8 +318,9 @@ def quantize_rows(r: np.ndarray, ratio: float, lloyd_max: bool = False):
       scale == 0      -> code 0
       otherwise inv = 1 / scale ; y = (x - zero) * inv
     Uniform levels (span 3): code = clamp(rint(y), 0, 3).
-    Lloyd-Max levels (span 2 rho + 1, levels lloyd_max_levels()): code = the
-    number of midpoints between adjacent levels that lie strictly below y.
+    Lloyd-Max levels (span 2 rho + 1, levels lloyd_max_levels(), float32
+    span and midpoints from lloyd_max_thresholds()): code = the number of
+    midpoints between adjacent levels that lie strictly below y.
     A non-finite scale or zero also yields code 0.
     """
     r = np.ascontiguousarray(r, dtype=np.float32)
@@ -314,8 +332,8 @@ def quantize_rows(r: np.ndarray, ratio: float, lloyd_max: bool = False):
     xg = x.reshape(n, ng, GROUP)
     mn = xg.min(axis=2)
     mx = xg.max(axis=2)
-    lev = lloyd_max_levels()
-    span = np.float32(lev[3]) if lloyd_max else np.float32(3.0)
+    lm_span, lm_mids = lloyd_max_thresholds()
+    span = lm_span if lloyd_max else np.float32(3.0)
     s32 = ((mx - mn) / span).astype(np.float32)
     with np.errstate(over="ignore"):
         scale = s32.astype(np.float16)
@@ -328,8 +346,7 @@ def quantize_rows(r: np.ndarray, ratio: float, lloyd_max: bool = False):
         inv = inv.astype(np.float32)
         y = ((xg - zf[:, :, None]).astype(np.float32) * inv[:, :, None]).astype(np.float32)
         if lloyd_max:
-            mids = ((lev[:3] + lev[1:]) / 2).astype(np.float32)
-            q = sum((y > m).astype(np.float64) for m in mids)
+            q = sum((y > m).astype(np.float64) for m in lm_mids)
         else:
             q = np.rint(y)
     q = np.where(ok[:, :, None], q, 0.0)

@@ -345,6 +345,108 @@ def test_all_bf16_window_equals_library_sdpa():
     assert np.abs(lse - torch.logsumexp(sc, dim=-1).numpy()).max() < 1e-12
 
 
+def _signed_permutation(rng, d):
+    # a random permutation matrix with random signs (orthogonal, not symmetric):
+    # every product with it is exact in every float format
+    P = np.zeros((d, d), np.float32)
+    P[np.arange(d), rng.permutation(d)] = rng.choice([-1.0, 1.0], d)
+    assert not np.array_equal(P, P.T)
+    return P
+
+
+def _symmetric_lattice_rotated_rows(rng, shape):
+    # rows in the rotated basis: per 128-group values in {-3s/2, -s/2, s/2, 3s/2}
+    # (s a power of two, both extremes present): exact in bf16 and fp16, and the
+    # codec (clip ratio 1) returns them exactly (scale s, zero -3s/2, codes 0..3)
+    x = np.empty(shape, dtype=np.float32)
+    D = shape[-1]
+    for idx in np.ndindex(*shape[:-1]):
+        for j in range(D // 128):
+            s = float(rng.choice([0.25, 0.5, 1.0, 2.0]))
+            c = rng.integers(0, 4, 128)
+            c[0], c[1] = 0, 3
+            x[idx][128 * j:128 * (j + 1)] = s * (c - 1.5)
+    return x
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_rotated_cache_decode_equals_sdpa_on_unrotated_rows(D):
+    # Gemma card [Folders]: the rotation applies to Q/K (and V); so q'.k' = q.k and
+    # the output is un-rotated.  With signed-permutation R_K, R_V (exact) and rows
+    # whose rotated images are exact in every storage form (BF16 windows and the
+    # INT2 region alike, clip ratio 1), append + decode through the rotations must
+    # equal plain attention over the UNROTATED K and V.
+    B, H, G, T = 2, 2, 2, 40
+    cfg = O.Config(1, B, H * G, H, D, 4, 6, 64, 1.0, 1.0)
+    rng = np.random.default_rng(71 + D)
+    RK, RV = _signed_permutation(rng, D), _signed_permutation(rng, D)
+    rk = _symmetric_lattice_rotated_rows(rng, (B, T, H, D))
+    rv = _symmetric_lattice_rotated_rows(rng, (B, T, H, D))
+    k = (rk.astype(np.float64) @ RK.T.astype(np.float64)).astype(np.float32)  # k R_K = rk exactly
+    v = (rv.astype(np.float64) @ RV.T.astype(np.float64)).astype(np.float32)
+    q = S.to_bf16_values(rng.standard_normal((B, H * G, D)).astype(np.float32))
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, v, [0, 0], RK, RV)
+    lens = [T, 23]
+    for absorb in (False, True):
+        out, lse = O.decode(cfg, cache, 0, q, lens, RK, RV, absorb_v=absorb)
+        for b in range(B):
+            Tb = lens[b]
+            if b == 1:  # the ring holds the last W appended positions: only T is fully windowed
+                continue
+            qt = torch.from_numpy(q[b].astype(np.float64))[:, None, :]
+            kt = torch.from_numpy(k[b, :Tb].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+            vt = torch.from_numpy(v[b, :Tb].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0].numpy()
+            if absorb:  # the rotated basis: o' = o R_V
+                ref = ref @ RV.astype(np.float64)
+            assert np.abs(out[b] - ref).max() < 1e-12 * max(1.0, np.abs(ref).max())
+            sc = torch.einsum("hd,htd->ht", qt[:, 0], kt) / math.sqrt(D)
+            assert np.abs(lse[b] - torch.logsumexp(sc, -1).numpy()).max() < 1e-12
+
+
+def test_qr_rotated_bf16_windows_equal_sdpa_on_unrotated_rows_within_bf16_rounding():
+    # S + W >= T, calibrated-like (QR) rotations: the cache holds BF16(k R_K) and
+    # BF16(v R_V); decode must equal attention over the unrotated K and V up to
+    # the BF16 rounding of the rotated rows.  Bound, with u = 2^-9 (BF16 unit
+    # roundoff) and eps = max_t |score perturbation| <= sm_scale |q| u |k_t|:
+    #   |out - ref| <= (e^{2 eps} - 1) (max_t |v_t - c| + u max_t |v_t|_2) + u max_t |v_t|_2,
+    #   |lse - ref| <= eps,
+    # c any per-channel constant (the weight changes sum to zero): the midrange
+    B, H, G, D, T = 2, 2, 3, 128, 30
+    cfg = O.Config(1, B, H * G, H, D, 10, 24, 64, 0.96, 0.92)
+    rng = np.random.default_rng(77)
+    RK, RV = S.qr_rotation(rng, D).astype(np.float32), S.qr_rotation(rng, D).astype(np.float32)
+    k = S.to_bf16_values(rng.standard_normal((B, T, H, D)).astype(np.float32))
+    # V rows with a common offset: a wrong un-rotation moves the output by about the offset
+    v = S.to_bf16_values(rng.standard_normal((B, T, H, D)).astype(np.float32) + np.float32(2.0))
+    q = S.to_bf16_values(rng.standard_normal((B, H * G, D)).astype(np.float32) * np.float32(0.5))
+    cache = O.new_cache(cfg)
+    O.append(cfg, cache, 0, k, v, [0, 0], RK, RV)
+    out, lse = O.decode(cfg, cache, 0, q, [T, T], RK, RV)
+    u = 2.0 ** -9 * (1 + 2.0 ** -14)  # BF16 rounding, plus the float32 rounding of the rotated row
+    for b in range(B):
+        qt = torch.from_numpy(q[b].astype(np.float64))[:, None, :]
+        kt = torch.from_numpy(k[b].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        vt = torch.from_numpy(v[b].astype(np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[:, 0].numpy()
+        sc = torch.einsum("hd,htd->ht", qt[:, 0], kt) / math.sqrt(D)
+        qn = np.linalg.norm(q[b].astype(np.float64), axis=1)                      # [Hq]
+        kn = np.linalg.norm(k[b].astype(np.float64), axis=2)                      # [T, H]
+        vn = np.linalg.norm(v[b].astype(np.float64), axis=2)
+        for i in range(H * G):
+            h = i // G
+            eps = qn[i] * u * kn[:, h].max() / math.sqrt(D)
+            vh = v[b, :, h].astype(np.float64)
+            c = (vh.max(0) + vh.min(0)) / 2
+            bound = (math.exp(2 * eps) - 1) * (np.abs(vh - c).max() + u * vn[:, h].max()) + u * vn[:, h].max()
+            err = np.abs(out[b, i] - ref[i]).max()
+            assert err <= bound, (b, i, err, bound)
+            assert abs(lse[b, i] - float(torch.logsumexp(sc[i], -1))) <= eps
+        # the bound is small against the output (a transposed rotation moves it by ~2)
+        assert bound < 0.25 * np.abs(ref).min()
+
+
 def test_uniform_attention_window_boundaries_closed_form():
     # K = 0 -> uniform attention; V rows constant p+1 per token.  BF16 tokens keep
     # p+1; INT2 tokens hold the constant-row codec value fp16(fl32(ratio*(p+1))).
@@ -661,26 +763,40 @@ def test_lloyd_max_ratio_is_the_gaussian_lloyd_max_gap_ratio():
     lev = O.lloyd_max_levels()
     gaps = np.diff(lev)
     assert lev[0] == 0.0 and gaps[1] == 1.0 and gaps[0] == gaps[2] == O.LM_RATIO
-    assert abs(O.LM_RATIO - GOLD["lm_ratio"]["value"]) <= 2.0 ** -9
+    # the ratio is the printed one, rounded once to float32
+    assert O.LM_RATIO == float(np.float32(GOLD["lm_ratio"]["value"]))
     assert abs(O.LM_RATIO - gauss_ratio) < 0.01
-    # every level, midpoint and the span are exact binary fractions (float32)
-    mids = (lev[:3] + lev[1:]) / 2
-    for v in [*lev, *mids]:
-        assert float(np.float32(v)) == v and Fraction(v).denominator <= 512
+    # span and midpoints: float32 roundings of the exact values of the levels
+    # (the span and the first two midpoints are exact, the third one rounding)
+    span, mids = O.lloyd_max_thresholds()
+    rho = Fraction(O.LM_RATIO)
+    assert Fraction(float(span)) == 2 * rho + 1
+    exact_mids = [rho / 2, rho + Fraction(1, 2), 3 * rho / 2 + 1]
+    assert Fraction(float(mids[0])) == exact_mids[0] and Fraction(float(mids[1])) == exact_mids[1]
+    assert float(mids[2]) == float(np.float32(float(exact_mids[2])))
+    ulp = Fraction(float(np.spacing(np.float32(mids[2]))))
+    assert abs(Fraction(float(mids[2])) - exact_mids[2]) <= ulp / 2
 
 
 def test_lloyd_max_codec_hand_example():
-    # group 0 spans 0 .. 2 rho + 1 = 850/256, so the unit is exactly 1 and the zero
-    # 0: level midpoints 297/512, 850/512, 1403/512 split the codes; a value on a
-    # midpoint takes the lower level, its float32 neighbours fall either side
-    rho = Fraction(297, 256)
+    # group 0 spans 0 .. 2 rho + 1 (exact in float32), so the unit is exactly 1 and
+    # the zero 0 and y = x: the float32 level midpoints rho/2, rho + 1/2 and
+    # RN(3 rho/2 + 1) split the codes; a value on a midpoint takes the lower
+    # level, its float32 neighbours fall either side
+    rho32 = np.float32(O.LM_RATIO)
+    rho = Fraction(O.LM_RATIO)
+    span = float(np.float32(2) * rho32 + np.float32(1))
+    assert Fraction(span) == 2 * rho + 1
     up = lambda v: float(np.nextafter(np.float32(v), np.float32(10)))
     dn = lambda v: float(np.nextafter(np.float32(v), np.float32(-10)))
-    m1, m2, m3 = 297 / 512, 850 / 512, 1403 / 512
-    vals = [0.0, 850 / 256,
+    m1 = float(rho32 * np.float32(0.5))
+    m2 = float(rho32 + np.float32(0.5))
+    m3 = float(np.float32(span) - np.float32(m1))
+    lev2 = float(np.float32(float(rho + 1)))  # rho + 1 needs 25 bits: its float32 neighbour
+    vals = [0.0, span,
             dn(m1), m1, up(m1),
-            297 / 256, dn(m2), m2, up(m2),
-            553 / 256, dn(m3), m3, up(m3)]
+            float(rho32), dn(m2), m2, up(m2),
+            lev2, dn(m3), m3, up(m3)]
     r = _row(vals)
     codes, sc, ze = O.quantize_rows(r, 1.0, lloyd_max=True)
     assert float(sc[0, 0]) == 1.0 and float(ze[0, 0]) == 0.0
@@ -691,19 +807,23 @@ def test_lloyd_max_codec_hand_example():
 
 
 def _lm_lattice_rows(rng, shape):
-    # per 128-group x = z + u * level(c) with u, z multiples of 2^-6 (u <= 4,
-    # |z| <= 8), codes 0 and 3 present: every x and the span are exact in float32,
-    # the unit and zero exact in fp16, so the codec (clip ratio 1) returns x exactly
+    # per 128-group x = u * (level(c) - k) with u = 2^e (e in -6..2) and k in 1..3,
+    # codes 0 and 3 present: level - k is rho - k, rho + 1 - k, 2 rho + 1 - k or
+    # -k, each exact in float32 (24 significant bits of rho, shifted), and so is the
+    # span u (2 rho + 1); the unit u and zero -u k are exact in fp16, so the codec
+    # (clip ratio 1) returns x exactly although x - zero = u (rho + 1) is not
     lev = O.lloyd_max_levels()
     x = np.empty(shape, dtype=np.float32)
     D = shape[-1]
     for idx in np.ndindex(*shape[:-1]):
         for j in range(D // 128):
-            u = rng.integers(1, 257) / 64.0
-            z = -rng.integers(0, 513) / 64.0
+            u = 2.0 ** int(rng.integers(-6, 3))
+            kz = int(rng.integers(1, 4))
             c = rng.integers(0, 4, 128)
             c[0], c[1] = 0, 3
-            x[idx][128 * j:128 * (j + 1)] = z + u * lev[c]
+            vals = u * (lev[c] - kz)
+            assert np.array_equal(vals.astype(np.float32).astype(np.float64), vals)
+            x[idx][128 * j:128 * (j + 1)] = vals
     return x
 
 
