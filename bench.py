@@ -30,7 +30,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "INT2+BF16 KV decode-attn tokens/s and KV GB/s (% of HBM peak), 1 GB300"
-DEFAULT_WORKLOAD = "qwen3-4b-layer"
+APPEND_METRIC = "INT2 KV append tokens/s (rotate + clip + INT2 pack), 1 GB300"
+DEFAULT_WORKLOAD = "qwen3-8b-36L"
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -51,6 +52,7 @@ def parse():
                     help="time the R_K calibration (Sigma, eigenvectors, H P_br) instead of the decode step")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--sample-heads", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--append-pairs", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -204,45 +206,149 @@ def cpu_sample_worker(workload: str, steps: int, warmup: int, heads: int, hadama
     print(json.dumps({"sec_per_step": statistics.mean(times), "steps": len(times)}))
 
 
-def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
-                   v_bf16: bool = False, lloyd_max: bool = False):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
+def cpu_append_worker(workload: str, pairs: int):
+    """Run inside a single-threaded child process: time the oracle's append of
+    the workload's new tokens for `pairs` (sequence, KV head) pairs."""
+    import numpy as np
+    from int2_kv_cache_append_gb300 import synth as S
+    from oracle import oscar_oracle as O
+
+    w = S.WORKLOADS[workload]
+    c = O.Config(1, 1, w.num_q_heads // w.num_kv_heads, 1, w.head_dim, w.sink, w.recent, w.context, w.k_clip,
+                 w.v_clip)
+    RK, RV = S.rotations(w, 0)
+    k, v = S.kv_rows(w, 0, w.append_tokens, batch=1)
+    cache = O.new_cache(c)
+    t0 = time.perf_counter()
+    for i in range(pairs):
+        h = i % w.num_kv_heads
+        O.append(c, cache, 0, k[:, :, h:h + 1], v[:, :, h:h + 1], [w.context - w.append_tokens], RK, RV)
+    print(json.dumps({"sec": time.perf_counter() - t0, "pairs": pairs}))
+
+
+def _sample_cmd(workload: str, steps: int, warmup: int, heads: int, hadamard=False, v_bf16=False, lloyd_max=False,
+                append_pairs: int = 0):
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample-worker", "--workload", workload,
            "--steps", str(steps), "--warmup", str(warmup), "--sample-heads", str(heads)] + (
                ["--hadamard"] if hadamard else []) + (["--v-bf16"] if v_bf16 else []) + (
                ["--lloyd-max"] if lloyd_max else [])
-    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
+    if append_pairs:
+        cmd += ["--append-pairs", str(append_pairs)]
+    return cmd
+
+
+_SAMPLE_ENV = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                   CUDA_VISIBLE_DEVICES="")
+
+
+def run_cpu_sample(workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
+                   v_bf16: bool = False, lloyd_max: bool = False, append_pairs: int = 0):
+    """One single-threaded oracle sample in a child process."""
+    cmd = _sample_cmd(workload, steps, warmup, heads, hadamard, v_bf16, lloyd_max, append_pairs)
+    r = subprocess.run(cmd, env=_SAMPLE_ENV, capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("cpu sample failed: " + r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def run_cpu_samples_parallel(n: int, workload: str, steps: int, warmup: int, heads: int, hadamard: bool = False,
+                             v_bf16: bool = False, lloyd_max: bool = False, append_pairs: int = 0):
+    """n single-threaded oracle samples at once, one child process per host core."""
+    cmd = _sample_cmd(workload, steps, warmup, heads, hadamard, v_bf16, lloyd_max, append_pairs)
+    procs = [subprocess.Popen(cmd, env=_SAMPLE_ENV, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+             for _ in range(n)]
+    res = []
+    for p in procs:
+        out, err = p.communicate(timeout=1800)
+        if p.returncode != 0:
+            raise RuntimeError("cpu sample failed: " + err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    return res
+
+
+def cpu_baseline_decode(w, args, L: int):
+    """The oracle's decode step (append of the current token + attention over T)
+    for one sequence and one layer, every KV head, timed on one host thread and
+    on every host core at once (one process per core): tokens/s of the whole
+    workload = sequences per second / layers."""
+    Hkv = w.num_kv_heads
+    ncores = os.cpu_count() or 1
+    one = run_cpu_sample(w.name, steps=2, warmup=1, heads=Hkv, hadamard=args.hadamard, v_bf16=args.v_bf16,
+                         lloyd_max=args.lloyd_max)
+    allc = run_cpu_samples_parallel(ncores, w.name, steps=2, warmup=1, heads=Hkv, hadamard=args.hadamard,
+                                    v_bf16=args.v_bf16, lloyd_max=args.lloyd_max)
+    single = 1.0 / (one["sec_per_step"] * L)
+    total = sum(1.0 / (r["sec_per_step"] * L) for r in allc)
+    return {"value": total, "unit": "tokens/s", "cores": ncores, "kind": "oracle",
+            "single_thread_value": single,
+            "sample": (f"oracle (numpy; codec float32, attention float64) decode step of one sequence and one "
+                       f"layer of {w.name} (append of the current token, then attention over T={w.context} for "
+                       f"all {Hkv} KV heads), {one['steps']} timed steps after 1 warm-up; single thread, and one "
+                       f"single-threaded process per host core at once ({ncores}); tokens/s = sequences per "
+                       f"second / {L} layers")}
+
+
+def cpu_baseline_append(w):
+    """The oracle's append of the workload in full (every sequence and KV head),
+    on one host thread and split over every host core (one process each)."""
+    pairs = w.batch * w.num_kv_heads
+    ncores = os.cpu_count() or 1
+    one = run_cpu_sample(w.name, 0, 0, 0, append_pairs=pairs)
+    per = max(1, -(-pairs // ncores))
+    allc = run_cpu_samples_parallel(min(ncores, pairs), w.name, 0, 0, 0, append_pairs=per)
+    tok_per_pair = w.append_tokens / w.num_kv_heads  # a token spans every KV head
+    single = pairs * tok_per_pair / one["sec"]
+    total = sum(r["pairs"] * tok_per_pair / r["sec"] for r in allc)
+    return {"value": total, "unit": "tokens/s", "cores": ncores, "kind": "oracle", "single_thread_value": single,
+            "sample": (f"oracle append (rotate in float64, codec float32, windows) of all {w.batch} x "
+                       f"{w.num_kv_heads} (sequence, KV head) pairs of {w.append_tokens} new tokens on one thread; "
+                       f"all cores: {min(ncores, pairs)} single-threaded processes with {per} pairs each")}
+
+
 def reference_arm(args):
-    """The oracle as the reference implementation, timed on this host's cores."""
+    """The oracle as the reference implementation, timed on every host core at
+    once (one single-threaded process per core, each running the same bounded
+    sample; the rates add up)."""
     from int2_kv_cache_append_gb300 import synth as S
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = S.WORKLOADS[args.workload]
     steps = max(1, args.steps)
-    # about 75 ms of oracle work per KV head and step at T=16384: keep the run near two minutes
-    heads = max(1, min(w.num_kv_heads, int(120.0 / (0.075 * (steps + args.warmup) * w.context / 16384))))
+    ncores = os.cpu_count() or 1
     t0 = time.time()
-    res = run_cpu_sample(args.workload, steps, args.warmup, heads, args.hadamard, args.v_bf16, args.lloyd_max)
-    sec = res["sec_per_step"]
-    value = (heads / w.num_kv_heads) / sec  # the sample is heads/Hkv of one sequence's decode step
-    sample = (f"oracle (numpy, fp64 attention) on batch row 0 of {args.workload}, {heads} of "
-              f"{w.num_kv_heads} KV heads: append of the current token + decode over T={w.context}; "
-              f"single thread; tokens/s scaled by the fraction of a sequence sampled")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "rotation": rotation_desc(args),
+    if w.append_tokens > 0:
+        # one (sequence, KV head) pair of the append per step
+        res = run_cpu_samples_parallel(ncores, args.workload, 0, 0, 0, append_pairs=steps)
+        tok_per_pair = w.append_tokens / w.num_kv_heads
+        value = sum(r["pairs"] * tok_per_pair / r["sec"] for r in res)
+        ms = statistics.mean(r["sec"] / r["pairs"] for r in res) * 1e3
+        sample = (f"oracle append of {w.append_tokens} new tokens for one (sequence, KV head) pair of "
+                  f"{args.workload} per step, {steps} steps, one single-threaded process per host core "
+                  f"({ncores}); tokens/s = pairs x {w.append_tokens} / {w.num_kv_heads} KV heads / s")
+        sample_desc = "one (sequence, KV head) append per step"
+    else:
+        # about 75 ms of oracle work per KV head and step at T = 16384: keep the run near two minutes
+        heads = max(1, min(w.num_kv_heads, int(120.0 / (0.075 * (steps + args.warmup) * w.context / 16384))))
+        res = run_cpu_samples_parallel(ncores, args.workload, steps, args.warmup, heads, args.hadamard,
+                                       args.v_bf16, args.lloyd_max)
+        # a sample step is heads / Hkv of one sequence's decode step in one of L layers
+        value = sum((heads / w.num_kv_heads) / r["sec_per_step"] / w.num_layers for r in res)
+        ms = statistics.mean(r["sec_per_step"] for r in res) * 1e3
+        sample = (f"oracle (numpy; codec float32, attention float64) on batch row 0 of {args.workload}, {heads} "
+                  f"of {w.num_kv_heads} KV heads of one layer per step: append of the current token + decode over "
+                  f"T={w.context}; one single-threaded process per host core ({ncores}); tokens/s scaled by the "
+                  f"fraction of a token's work ({heads}/{w.num_kv_heads} heads, 1/{w.num_layers} layers) sampled")
+        sample_desc = f"{heads} of {w.num_kv_heads} KV heads of one sequence and layer per step"
+    line = {"impl": "reference", "metric": METRIC if w.append_tokens == 0 else APPEND_METRIC, "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w) + (f" append{w.append_tokens}" if w.append_tokens else ""),
+                       "rotation": rotation_desc(args),
                        "cache": "int2 K + bf16 V" if args.v_bf16 else "int2+bf16",
                        "levels": "Lloyd-Max (0, rho, rho+1, 2rho+1), rho = 1.16 (float32)" if args.lloyd_max else "uniform",
-                       "sample": f"{heads} of {w.num_kv_heads} KV heads of one sequence per step"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+                       "sample": sample_desc},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ncores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.time() - t0}
     print(json.dumps(line), flush=True)
@@ -364,8 +470,10 @@ def ours(args):
     # library's stream right around the split kernel (an event between two
     # kernels stops the second from launching early, so this pass is kept out
     # of the step timing above)
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_)]
     for i in range(K_):
         flush.zero_()
+        pev[i][0].record(stream)
         for layer in range(L):
             RK, RV = rots[layer]
             ks, ke = kev[i * L + layer]
@@ -373,8 +481,12 @@ def ours(args):
             K.decode_step(cfg, cache, layer, k1, v1, start, q, seq, RK, RV, out, ws, lse=lse, seq_len_hint=T,
                           status=status)
             K.set_profile_events(None, None)
+        pev[i][1].record(stream)
     torch.cuda.synchronize()
     split_ms = [a.elapsed_time(b) for a, b in kev]
+    # the split kernels' share of the very steps they were timed in
+    prof_step_ms = statistics.mean(a.elapsed_time(b) for a, b in pev)
+    split_share = sum(split_ms) / sum(a.elapsed_time(b) for a, b in pev)
     clocks.stop()
 
     # ---- end-to-end through the public API with host buffers
@@ -409,11 +521,7 @@ def ours(args):
     step_gbs = kv_bytes / (ms / 1e3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        res = run_cpu_sample(args.workload, steps=3, warmup=1, heads=Hkv, hadamard=args.hadamard,
-                             v_bf16=args.v_bf16, lloyd_max=args.lloyd_max)
-        cpu = {"value": 1.0 / res["sec_per_step"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"oracle decode step (append + attention) for 1 of {Bsz} sequences of {args.workload}, "
-                         f"T={T}, {res['steps']} timed steps, single thread"}
+        cpu = cpu_baseline_decode(w, args, L)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": K_,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -432,6 +540,10 @@ def ours(args):
                      else split_kernel_traffic(args.workload),
                      "kernel": "split_kernel (attn_decode)",
                      "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
+                     # kernel_ms comes from a second pass of the same steps with events
+                     # recorded around each split launch; that pass's own step time and
+                     # the split kernels' share of it:
+                     "kernel_pass_ms_per_step": prof_step_ms, "kernel_share_of_step": split_share,
                      "algorithmic_bytes_per_launch": kv_bytes // L},
         "e2e": {"value": world * Bsz / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -535,7 +647,7 @@ def ours_append(args):
     gbs = hbm_bytes / (ms / 1e3) / 1e9
     tfs = flops / (ms / 1e3) / 1e12
     line = {
-        "metric": "INT2 KV append tokens/s (rotate + clip + INT2 pack), 1 GB300", "value": tokens / (ms / 1e3),
+        "metric": APPEND_METRIC, "value": tokens / (ms / 1e3),
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w) + f" append{n}", "l2": "flushed between steps (512 MiB write)"},
@@ -547,7 +659,8 @@ def ours_append(args):
                      "algorithmic_bytes_per_launch": hbm_bytes, "algorithmic_flops_per_launch": flops},
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * k.numel() * k.element_size(), "d2h_bytes_per_step": 4},
-        "gpu_launches": args.steps, "clocks": clocks.summary(), "cpu_baseline": None,
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "cpu_baseline": None if (args.no_cpu_baseline or world > 1) else cpu_baseline_append(w),
         "dev_status": int(status.item()),
     }
     print(json.dumps(line), flush=True)
@@ -626,6 +739,9 @@ def main():
     args = parse()
     if args.calibrate:
         calibrate_arm(args)
+        return
+    if args.cpu_sample_worker and args.append_pairs:
+        cpu_append_worker(args.workload, args.append_pairs)
         return
     if args.cpu_sample_worker:
         cpu_sample_worker(args.workload, args.steps, args.warmup, args.sample_heads, args.hadamard, args.v_bf16,

@@ -54,13 +54,7 @@ extern "C" int attn_decode_static(const oscar_kv_config* cfg, const void* cache,
   const int v = kv_layout_query(cfg, &lay);
   if (v != OSCAR_OK) return v;
   // the smallest decode (one split) must fit in the fixed array
-  const uint64_t bq = uint64_t(cfg->batch) * cfg->num_q_heads;
-  const uint64_t units = uint64_t(cfg->batch) * cfg->num_kv_heads;
-  const uint64_t D = uint64_t(cfg->head_dim), Dg = D / OSCAR_KV_GROUP;
-  const uint64_t nqt = cfg->num_q_heads / cfg->num_kv_heads > 4 ? 2 : 1;
-  const uint64_t one_split = oscar::align256(units * Dg * nqt * 2048) + oscar::align256(units * Dg * nqt * 4096) +
-                             oscar::align256(bq * Dg * 4) + oscar::align256(bq * Dg * 4) +
-                             oscar::align256(bq * D * 4) + oscar::align256(bq * 2 * 4) + oscar::align256(units * 4);
+  const uint64_t one_split = oscar::decode_workspace_bytes(oscar::geom_of(cfg), 1);
   if (one_split > OSCAR_KV_STATIC_SCRATCH_BYTES) return OSCAR_ERR_WORKSPACE;
   int err = OSCAR_OK;
   void* ws = scratch_for_current_device(&err);

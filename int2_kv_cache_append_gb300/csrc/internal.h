@@ -55,6 +55,8 @@ struct DecodeArgs {
 };
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns);
+// cache geometry of a validated configuration
+Geom geom_of(const oscar_kv_config* c);
 // optional events recorded around the split kernel (per host thread)
 extern thread_local cudaEvent_t g_prof_start, g_prof_stop;
 int launch_append(const AppendArgs& a, cudaStream_t stream);

@@ -50,6 +50,13 @@ Geom make_geom(const oscar_kv_config* c) {
   return g;
 }
 
+}  // namespace
+
+namespace oscar {
+Geom geom_of(const oscar_kv_config* c) { return make_geom(c); }
+}  // namespace oscar
+
+namespace {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace

@@ -122,6 +122,66 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check(t, name: str, dtypes, shape=None, min_bytes=None, optional: bool = False):
+    """Refuse, before anything reaches the GPU, a tensor whose dtype, shape or
+    size does not match what the library will read or write through it."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"oscar_kv: {name} is required")
+    if t.dtype not in dtypes:
+        raise ValueError(f"oscar_kv: {name} must be {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"oscar_kv: {name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if min_bytes is not None and t.numel() * t.element_size() < min_bytes:
+        raise ValueError(f"oscar_kv: {name} holds {t.numel() * t.element_size()} bytes, needs {min_bytes}")
+
+
+def _dt():
+    import torch
+    return torch
+
+
+def _check_cache(cfg: "KVConfig", cache):
+    torch = _dt()
+    _check(cache, "cache", (torch.uint8,), min_bytes=layout_query(cfg)["total_bytes"])
+
+
+def _check_rot(cfg: "KVConfig", R, name: str):
+    torch = _dt()
+    # with the in-quant Hadamard the matrices are not read (None allowed)
+    _check(R, name, (torch.float32,), min_bytes=cfg.head_dim * cfg.head_dim * 4,
+           optional=bool(cfg.flags & FLAG_HADAMARD))
+
+
+def _in_dtypes(cfg: "KVConfig"):
+    torch = _dt()
+    return (torch.float32,) if cfg.flags & FLAG_IN_FP32 else (torch.bfloat16,)
+
+
+def _check_decode_io(cfg: "KVConfig", q, seq_lens, out, lse, status):
+    torch = _dt()
+    B, Hq, D = cfg.batch, cfg.num_q_heads, cfg.head_dim
+    _check(q, "q", _in_dtypes(cfg), shape=(B, Hq, D))
+    _check(seq_lens, "seq_lens", (torch.int32,), shape=(B,))
+    _check(out, "out", (torch.float32,) if cfg.flags & FLAG_OUT_FP32 else (torch.bfloat16,), shape=(B, Hq, D))
+    _check(lse, "lse", (torch.float32,), min_bytes=B * Hq * 4, optional=True)
+    _check(status, "status", (torch.int32,), min_bytes=4, optional=True)
+
+
+def _check_append_io(cfg: "KVConfig", k_new, v_new, start_pos, debug_rot, status):
+    torch = _dt()
+    B, H, D = cfg.batch, cfg.num_kv_heads, cfg.head_dim
+    if k_new is None or k_new.dim() != 4:
+        raise ValueError("oscar_kv: k_new must be [batch][n_new][num_kv_heads][head_dim]")
+    n = int(k_new.shape[1])
+    _check(k_new, "k_new", _in_dtypes(cfg), shape=(B, n, H, D))
+    _check(v_new, "v_new", _in_dtypes(cfg), shape=(B, n, H, D))
+    _check(start_pos, "start_pos", (torch.int32,), shape=(B,))
+    _check(debug_rot, "debug_rot", (torch.float32,), min_bytes=B * n * H * 2 * D * 4, optional=True)
+    _check(status, "status", (torch.int32,), min_bytes=4, optional=True)
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -141,6 +201,10 @@ def layout_query(cfg: KVConfig) -> dict:
 
 def kv_append(cfg: KVConfig, cache, layer: int, k_new, v_new, start_pos, R_K, R_V, debug_rot=None,
               status=None, stream=None, check: bool = True) -> int:
+    _check_append_io(cfg, k_new, v_new, start_pos, debug_rot, status)
+    _check_cache(cfg, cache)
+    _check_rot(cfg, R_K, "R_K")
+    _check_rot(cfg, R_V, "R_V")
     rc = lib().kv_append(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(k_new), _ptr(v_new), _ptr(start_pos),
                          int(k_new.shape[1]), _ptr(R_K), _ptr(R_V), _ptr(debug_rot), _ptr(status), _stream(stream))
     if check and rc != 0:
@@ -151,6 +215,11 @@ def kv_append(cfg: KVConfig, cache, layer: int, k_new, v_new, start_pos, R_K, R_
 def attn_decode(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, out, workspace, lse=None,
                 seq_len_hint: int = 0, sm_scale: float = 0.0, num_splits: int = 0, status=None, stream=None,
                 check: bool = True) -> int:
+    _check_decode_io(cfg, q, seq_lens, out, lse, status)
+    _check_cache(cfg, cache)
+    _check_rot(cfg, R_K, "R_K")
+    _check_rot(cfg, R_V, "R_V")
+    _check(workspace, "workspace", (_dt().uint8,))
     rc = lib().attn_decode(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(q), _ptr(seq_lens), int(seq_len_hint),
                            _ptr(R_K), _ptr(R_V), float(sm_scale), int(num_splits), _ptr(out), _ptr(lse),
                            _ptr(workspace), int(workspace.numel() * workspace.element_size()), _ptr(status),
@@ -164,6 +233,12 @@ def decode_step(cfg: KVConfig, cache, layer: int, k_new, v_new, start_pos, q, se
                 lse=None, seq_len_hint: int = 0, sm_scale: float = 0.0, num_splits: int = 0, status=None,
                 stream=None, check: bool = True) -> int:
     """kv_append of k_new/v_new ([B][n][Hkv][D]) at start_pos, then attn_decode, in one call."""
+    _check_append_io(cfg, k_new, v_new, start_pos, None, status)
+    _check_decode_io(cfg, q, seq_lens, out, lse, status)
+    _check_cache(cfg, cache)
+    _check_rot(cfg, R_K, "R_K")
+    _check_rot(cfg, R_V, "R_V")
+    _check(workspace, "workspace", (_dt().uint8,))
     n_new = int(k_new.shape[1])
     rc = lib().decode_step(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(k_new), _ptr(v_new), _ptr(start_pos),
                            n_new, _ptr(q), _ptr(seq_lens), int(seq_len_hint), _ptr(R_K), _ptr(R_V), float(sm_scale),
@@ -178,6 +253,10 @@ def attn_decode_static(cfg: KVConfig, cache, layer: int, q, seq_lens, R_K, R_V, 
                        seq_len_hint: int = 0, sm_scale: float = 0.0, num_splits: int = 0, status=None, stream=None,
                        check: bool = True) -> int:
     """attn_decode with the library's fixed scratch array (no workspace argument)."""
+    _check_decode_io(cfg, q, seq_lens, out, lse, status)
+    _check_cache(cfg, cache)
+    _check_rot(cfg, R_K, "R_K")
+    _check_rot(cfg, R_V, "R_V")
     rc = lib().attn_decode_static(ctypes.byref(cfg.c()), _ptr(cache), layer, _ptr(q), _ptr(seq_lens),
                                   int(seq_len_hint), _ptr(R_K), _ptr(R_V), float(sm_scale), int(num_splits),
                                   _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
@@ -220,7 +299,14 @@ def calibrate_workspace_bytes(head_dim: int) -> int:
 
 def calibrate_rk(q, R_out, workspace, status=None, stream=None, check: bool = True) -> int:
     """R_K fitted to the float32 query rows q [n][D] (see oscar_calibrate_rk); writes R_out [D][D]."""
+    torch = _dt()
+    if q is None or q.dim() != 2:
+        raise ValueError("oscar_kv: q must be [n_rows][head_dim] float32")
     n, d = int(q.shape[0]), int(q.shape[1])
+    _check(q, "q", (torch.float32,))
+    _check(R_out, "R_out", (torch.float32,), shape=(d, d))
+    _check(workspace, "workspace", (torch.uint8,))
+    _check(status, "status", (torch.int32,), min_bytes=4, optional=True)
     rc = _calib_fns().oscar_calibrate_rk(_ptr(q), n, d, _ptr(R_out), _ptr(workspace),
                                          int(workspace.numel() * workspace.element_size()), _ptr(status),
                                          _stream(stream))
@@ -240,10 +326,18 @@ def calibrate_rv_workspace_bytes(head_dim: int, n_kv_rows: int) -> int:
 def calibrate_rv(q, k, v, R_out, workspace, status=None, stream=None, check: bool = True) -> int:
     """R_V fitted to the score-weighted covariance of the float32 value rows v [n][D],
     each weighted by k_t q^T q k_t^T (see oscar_calibrate_rv); writes R_out [D][D]."""
+    torch = _dt()
+    if q is None or q.dim() != 2 or k is None or k.dim() != 2:
+        raise ValueError("oscar_kv: q and k must be [n_rows][head_dim] float32")
     nq, d = int(q.shape[0]), int(q.shape[1])
     nkv = int(k.shape[0])
-    if tuple(k.shape) != tuple(v.shape) or int(k.shape[1]) != d:
+    if v is None or tuple(k.shape) != tuple(v.shape) or int(k.shape[1]) != d:
         raise ValueError("k and v must both be [n_kv][head_dim] with the head_dim of q")
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, name, (torch.float32,))
+    _check(R_out, "R_out", (torch.float32,), shape=(d, d))
+    _check(workspace, "workspace", (torch.uint8,))
+    _check(status, "status", (torch.int32,), min_bytes=4, optional=True)
     rc = _calib_fns().oscar_calibrate_rv(_ptr(q), nq, _ptr(k), _ptr(v), nkv, d, _ptr(R_out), _ptr(workspace),
                                          int(workspace.numel() * workspace.element_size()), _ptr(status),
                                          _stream(stream))

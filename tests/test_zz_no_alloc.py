@@ -66,13 +66,24 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 
 
 def test_static_scratch_rejects_oversized_decode():
-    # B * Hq = 65536 heads of D = 128: one split alone needs > 64 MiB of scratch
+    import ctypes
+    # B * Hq = 65536 heads of D = 128: one split alone needs > 64 MiB of scratch.
+    # Every pointer is NULL: the size check comes first, so a regression in it
+    # fails on the host instead of launching on buffers that do not exist.
     kc = K.KVConfig(1, 1024, 64, 8, 128, 0, 0, 64)
     assert K.STATIC_SCRATCH_BYTES == 16 << 20
-    dummy = torch.empty(256, dtype=torch.uint8, device="cuda")
-    rc = K.attn_decode_static(kc, dummy, 0, dummy, dummy, dummy, dummy, dummy, dummy, check=False)
+    rc = K.lib().attn_decode_static(ctypes.byref(kc.c()), None, 0, None, None, 0, None, None, 0.0, 0, None, None,
+                                    None, None)
     assert rc == -3
-    # an explicit split count that does not fit is rejected too
+    # an explicit split count that does not fit is rejected too; the buffers
+    # are the sizes this configuration needs, so a regression that launched
+    # anyway would still stay inside them
     kc = K.KVConfig(1, 64, 32, 8, 128, 0, 0, 64)
-    rc = K.attn_decode_static(kc, dummy, 0, dummy, dummy, dummy, dummy, dummy, dummy, num_splits=64, check=False)
+    lay = K.layout_query(kc)
+    cache = torch.zeros(lay["total_bytes"], dtype=torch.uint8, device="cuda")
+    q = torch.zeros((64, 32, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((64, 32, 128), dtype=torch.bfloat16, device="cuda")
+    seq = torch.full((64,), 64, dtype=torch.int32, device="cuda")
+    eye = torch.eye(128, dtype=torch.float32, device="cuda")
+    rc = K.attn_decode_static(kc, cache, 0, q, seq, eye, eye, out, num_splits=64, check=False)
     assert rc == -3
