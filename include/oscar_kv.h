@@ -308,6 +308,22 @@ int attn_decode_static(const oscar_kv_config* cfg, const void* cache, int32_t la
 int oscar_kv_set_profile_events(void* split_start, void* split_stop);
 
 /*
+ * oscar_kv_set_wait_test — test hook for the device-timeout path (no
+ * counterpart on the pages).  Every wait of the split-attention kernel on one
+ * of its shared-memory barriers is bounded; when the bound runs out the kernel
+ * ORs OSCAR_DEV_TIMEOUT into *dev_status, waits (bounded again) for the copies
+ * it issued, skips the rest of its work and returns, leaving the context
+ * usable.  For attn_decode / decode_step calls made later from the calling host
+ * thread this hook sets that bound to wait_ns (0 = the default, about 2 s) and
+ * makes the first copy issued by CTA 0 expect `extra_bytes` more than its copies
+ * deliver, so that its barrier never completes and the bounded wait runs out;
+ * every copy still completes.  (0, 0) restores normal operation.  A decode run
+ * with extra_bytes > 0 leaves at least one output unit unwritten.  Returns
+ * OSCAR_ERR_INVALID for wait_ns > 10 s or extra_bytes outside [0, 2^20].
+ */
+int oscar_kv_set_wait_test(uint64_t wait_ns, int32_t extra_bytes);
+
+/*
  * oscar_calibrate_rk — the K-side rotation fitted to a calibration set of
  * query rows ["OSCAR-RotationZoo" card, File format: R_K = R H P_br with R the
  * eigenvectors of the query covariance, H a head-dim Hadamard and P_br the

@@ -701,6 +701,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t bh = int64_t(sd.b) * g.Hkv + sd.h;
     const uint32_t full = smem_u32(&bars[stage]);
     const uint32_t dst = smem_u32(smem + C::OFF_STAGE + stage * C::STAGE);
+    // test hook: CTA 0's first block expects bytes no copy delivers, so its
+    // wait runs out (every copy issued still completes)
+    const uint32_t extra = (a.wait_poison > 0 && blockIdx.x == 0 && issued == 0 && team == 0) ? a.wait_poison : 0;
     if (bk.type == 1) {
       if (lane == 0) {
         const int n4 = (bk.count + 3) & ~3;
@@ -708,14 +711,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int64_t row = bh * g.ncap + bk.first;
         if constexpr (VB) {
           // K codes and scale/zero, and the BF16 V rows of the same positions
-          mbar_arrive_expect_tx(full, cb + sb + C::BOXES * C::BOX_BYTES);
+          mbar_arrive_expect_tx(full, cb + sb + C::BOXES * C::BOX_BYTES + extra);
           bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
           bulk_g2s(dst + C::VB_SZ, kbase + sz_off + row * C::Dg * 4, sb, full);
           const int vrow = int(bh * g.cap + g.S + bk.first);
 #pragma unroll
           for (int q = 0; q < C::BOXES; ++q) tma_load_2d(dst + C::VB_V + q * C::BOX_BYTES, &tvs, 64 * q, vrow, full);
         } else {
-          mbar_arrive_expect_tx(full, 2 * cb + 2 * sb);
+          mbar_arrive_expect_tx(full, 2 * cb + 2 * sb + extra);
           bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
           bulk_g2s(dst + kI2Tok * C::ROWB, vbase + codes_off + row * C::ROWB, cb, full);
           bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
@@ -726,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // 16 rows of K and V as 64-column boxes, 128-byte swizzled by the TMA unit
       // (with V kept BF16, V rows come from the position-indexed V map)
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, 2 * C::BOXES * C::BOX_BYTES);
+        mbar_arrive_expect_tx(full, 2 * C::BOXES * C::BOX_BYTES + extra);
         const CUtensorMap* mk = bk.type == 0 ? &tks : &tkr;
         const CUtensorMap* mv = (bk.type == 0 || VB) ? &tvs : &tvr;
         const int row0 = int(bk.type == 0 ? bh * g.S + bk.first : bh * g.W + bk.first);
@@ -812,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     ++qb_issued;
   };
   auto qb_wait = [&]() {  // thread 0 waits; a CTA barrier must follow before others read
-    if (threadIdx.x == 0 && !mbar_wait(qb_bar, qb_waited & 1)) {
+    if (threadIdx.x == 0 && !mbar_wait(qb_bar, qb_waited & 1, a.wait_ns)) {
       abort_flag = 1;
       status_or(a.status, OSCAR_DEV_TIMEOUT);
     }
@@ -927,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int j = 0; j < nmine; ++j) {
         const int stage = my_stage(consumed);
         int ok = 1;
-        if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (consumed / C::NSTW) & 1);
+        if (lane == 0) ok = mbar_wait(smem_u32(&bars[stage]), (consumed / C::NSTW) & 1, a.wait_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         // the warps of a team must take the same decision: they meet at team barriers below
         if constexpr (C::TS > 1) ok = team_all(ok, 1 + team, 32 * C::TS);
@@ -1472,7 +1475,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         asm volatile("bar.sync 15, %0;" ::"r"(32 * kNCW) : "memory");
         bool rv_ok = true;
         if (rv_smem) {
-          rv_ok = mbar_wait(rv_bar, 0);
+          rv_ok = mbar_wait(rv_bar, 0, a.wait_ns);
           if (!rv_ok && threadIdx.x == 0) status_or(a.status, OSCAR_DEV_TIMEOUT);
         }
         auto store = [&](int i, int r, float v) {
@@ -1575,12 +1578,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // after an early exit, wait (bounded) for copies still landing in our stages
   // and in the shared q' image
+  // (each wait is bounded and none is skipped: a stage whose barrier never
+  // completes does not stop the wait for the copies of the later ones)
   if (wt == 0 && lane == 0)
-    for (int jj = consumed; jj < issued; ++jj)
-      if (!mbar_wait(smem_u32(&bars[my_stage(jj)]), (jj / C::NSTW) & 1)) break;
+    for (int jj = consumed; jj < issued; ++jj) (void)mbar_wait(smem_u32(&bars[my_stage(jj)]), (jj / C::NSTW) & 1, a.wait_ns);
   if (threadIdx.x == 0)
-    for (; qb_waited < qb_issued; ++qb_waited)
-      if (!mbar_wait(qb_bar, qb_waited & 1)) break;
+    for (; qb_waited < qb_issued; ++qb_waited) (void)mbar_wait(qb_bar, qb_waited & 1, a.wait_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -1677,6 +1680,8 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
 }  // namespace
 
 thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+thread_local uint64_t g_test_wait_ns = 0;
+thread_local int g_test_wait_poison = 0;
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns) {
   const uint64_t bq = uint64_t(g.B) * g.Hq, units = uint64_t(g.B) * g.Hkv;

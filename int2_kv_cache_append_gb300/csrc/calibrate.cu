@@ -190,7 +190,12 @@ __global__ void __launch_bounds__(kPairThreads) jacobi_kernel(double* __restrict
         be = block_sum(be, red);
         ga = block_sum(ga, red);
         const double nrm = sqrt(al * be);
-        if (ga != 0.0 && nrm > 0.0) {
+        if (!isfinite(al) || !isfinite(be) || !isfinite(ga)) {
+          // a non-finite covariance (non-finite calibration rows): flag it and
+          // let the sweep count run out instead of reporting convergence
+          if (tid == 0) status_or(status, OSCAR_DEV_NONFINITE);
+          worst = INFINITY;
+        } else if (ga != 0.0 && nrm > 0.0) {
           worst = fmax(worst, fabs(ga) / nrm);
           const double zeta = (be - al) / (2.0 * ga);
           const double az = fabs(zeta);
@@ -236,14 +241,19 @@ __global__ void __launch_bounds__(kPairThreads) jacobi_kernel(double* __restrict
 // ties, positive), then each row of E times H_D (in-place butterflies, 1/sqrt D)
 // and column j of R from column br(j).
 __global__ void finalize_kernel(const double* __restrict__ A, const double* __restrict__ V,
-                                double* __restrict__ lam, double* __restrict__ E, float* __restrict__ R, int D) {
+                                double* __restrict__ lam, double* __restrict__ E, float* __restrict__ R, int D,
+                                int32_t* status) {
   const int i = threadIdx.x;
   double n2 = 0.0;
   for (int r = 0; r < D; ++r) {
     const double a = A[int64_t(i) * D + r];
     n2 += a * a;
   }
-  lam[i] = sqrt(n2);
+  // a non-finite eigenvalue is flagged and ranks last (as -inf), so the ranks
+  // stay a permutation (ties by index) and every column of E is written
+  const double l0 = sqrt(n2);
+  if (!isfinite(l0)) status_or(status, OSCAR_DEV_NONFINITE);
+  lam[i] = isfinite(l0) ? l0 : -INFINITY;
   __syncthreads();
   const double li = lam[i];
   int rank = 0;
@@ -329,7 +339,7 @@ int launch_fit(CalibWs& c, int D, float* R, int32_t* status, cudaStream_t stream
   if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(jacobi_kernel), dim3(grid), dim3(kPairThreads), args, 0,
                                   stream) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
-  finalize_kernel<<<1, D, 0, stream>>>(A, V, c.lam, c.E, R, D);
+  finalize_kernel<<<1, D, 0, stream>>>(A, V, c.lam, c.E, R, D, status);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
 }
 

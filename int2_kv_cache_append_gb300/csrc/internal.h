@@ -52,6 +52,8 @@ struct DecodeArgs {
   float qscale;    // sm_scale * log2(e)
   int in_fp32, out_fp32, absorb_v;
   int hadamard;    // q and the output use the in-quant Hadamard (R_K, R_V unused)
+  uint64_t wait_ns;  // limit of every barrier wait in the split kernel (test hook; ~2 s by default)
+  int wait_poison;   // test hook: extra bytes CTA 0 expects on its first copy (0 normally)
 };
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns);
@@ -59,6 +61,9 @@ uint64_t decode_workspace_bytes(const Geom& g, int ns);
 Geom geom_of(const oscar_kv_config* c);
 // optional events recorded around the split kernel (per host thread)
 extern thread_local cudaEvent_t g_prof_start, g_prof_stop;
+// timeout-path test hook (per host thread): wait limit and extra expected bytes
+extern thread_local uint64_t g_test_wait_ns;
+extern thread_local int g_test_wait_poison;
 int launch_append(const AppendArgs& a, cudaStream_t stream);
 int launch_append_tc(const AppendArgs& a, cudaStream_t stream);  // D = 128, bf16 inputs
 // 2-D tiled TMA map of a row-major bf16 matrix [rows][cols], 128-byte swizzle

@@ -165,6 +165,8 @@ int prep_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
   a.new_pos = nullptr;
   a.new_n = 0;
   a.fused = 0;
+  a.wait_ns = oscar::g_test_wait_ns > 0 ? oscar::g_test_wait_ns : 2000000000ull;
+  a.wait_poison = oscar::g_test_wait_poison;
   return OSCAR_OK;
 }
 
@@ -241,6 +243,12 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop) {
   return OSCAR_OK;
 }
 
+int oscar_kv_set_wait_test(uint64_t wait_ns, int32_t extra_bytes) {
+  if (wait_ns > 10000000000ull || extra_bytes < 0 || extra_bytes > (1 << 20)) return OSCAR_ERR_INVALID;
+  oscar::g_test_wait_ns = wait_ns;
+  oscar::g_test_wait_poison = extra_bytes;
+  return OSCAR_OK;
+}
 int oscar_calibrate_workspace_query(int32_t head_dim, uint64_t* bytes) {
   if (!bytes) return OSCAR_ERR_INVALID;
   if (head_dim != 128 && head_dim != 256 && head_dim != 512) return OSCAR_ERR_UNSUPPORTED;

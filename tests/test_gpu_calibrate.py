@@ -2,13 +2,18 @@
 
 The calibration is unique once the eigenvalues are distinct (descending order,
 sign convention), so R_K is compared entry by entry: the GPU computes Sigma and
-the eigenvectors in float64 (Jacobi) and writes float32; the oracle uses
-float64 and numpy's eigensolver.  Tolerance 1e-5 on entries of magnitude about
-1/sqrt(D), from Jacobi's stopping rule (off-diagonal norm below 1e-13 of the
-Frobenius norm) over the smallest relative eigenvalue gap of these inputs,
-plus float32 rounding.  The diagonal case is exact up to rounding.  R_V uses the
-same fit on the value covariance weighted by score energy; the smallest relative eigenvalue
-gaps of its inputs here (3e-7 .. 5e-6) are those of the R_K inputs."""
+the eigenvectors in float64 (one-sided Jacobi) and writes float32; the oracle
+uses float64 and numpy's eigensolver.  Tolerance 1e-5 on entries of magnitude
+about 1/sqrt(D): the Jacobi stops after the sweep in which the largest |cosine|
+between two rotated columns of Sigma V is at most 1e-15 (or after 40 sweeps,
+which sets OSCAR_DEV_NOT_CONVERGED); a residual cosine c between columns i and j
+turns the eigenvector pair by about c / delta_ij, delta_ij their relative
+eigenvalue gap, so with the smallest relative gaps of these inputs
+(3e-7 .. 5e-6) the eigenvector error is below 1e-8, far inside the tolerance,
+to which float32 rounding of R (6e-8 relative) adds little.  The diagonal case
+is exact up to rounding.  R_V uses the same fit on the value covariance weighted
+by score energy; its inputs here have gaps in the same range.  A non-finite
+calibration row is flagged (OSCAR_DEV_NONFINITE) instead of passing silently."""
 import numpy as np
 import pytest
 import torch
@@ -101,3 +106,25 @@ def test_calibrate_rv_matches_oracle(d, nq, nkv):
     ref = O.calibrate_rv(q, k, v)
     assert np.abs(got - ref).max() <= 1e-5, np.abs(got - ref).max()
     assert np.abs(got @ got.T - np.eye(d)).max() <= 1e-5
+
+
+@pytest.mark.parametrize("d", [128, 512])
+def test_calibrate_nonfinite_row_is_flagged(d):
+    rng = np.random.default_rng(d + 5)
+    q = rng.standard_normal((2000, d)).astype(np.float32)
+    q[17, 3] = np.nan
+    qt = torch.from_numpy(q).cuda()
+    out = torch.empty((d, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.calibrate_workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    K.calibrate_rk(qt, out, ws, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & K.DEV_NONFINITE
+    # the same rows without the NaN calibrate cleanly
+    q[17, 3] = 0.5
+    st.zero_()
+    K.calibrate_rk(torch.from_numpy(q).cuda(), out, ws, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    R = out.cpu().numpy().astype(np.float64)
+    assert np.abs(R @ R.T - np.eye(d)).max() < 1e-5
