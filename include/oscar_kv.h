@@ -226,11 +226,11 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  *              cut into equal slices of work, one per CTA, so a CTA can cover
  *              the tail of one unit and the head of the next.
  *   out        device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_OUT_FP32);
- *              o = o' R_V^T, or o' with OSCAR_FLAG_ABSORB_V.  At head_dim 128 the
- *              last bits of o may differ between calls: the CTA that finishes
- *              a sequence's KV head last merges it and applies R_V^T in one of
- *              two summation orders (R_V from shared memory or from L2); lse
- *              and o' do not depend on it.
+ *              o = o' R_V^T, or o' with OSCAR_FLAG_ABSORB_V.  Repeated calls on
+ *              the same inputs give the same bits: the CTA that merges a
+ *              sequence's KV head (the last of its CTAs to finish) may change
+ *              from call to call, but the merge and the un-rotation do the
+ *              same arithmetic in the same order in every CTA.
  *   lse        device float32 [B][Hq] or NULL: natural-log log-sum-exp of the
  *              scaled scores.
  *   workspace  device scratch of workspace_bytes (see kv_layout_query); it

@@ -1497,9 +1497,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) store(i, j * kGroup + lane + 32 * e, x[e]);
           }
-        } else if (a.absorb_v || (rv_smem && rv_ok)) {
-          // o = o' R_V^T (or o' when absorbed): one thread per output channel r
-          const float* rvs = reinterpret_cast<const float*>(smem + C::OFF_STAGE);
+        } else if (a.absorb_v || D == 128) {
+          // o = o' R_V^T (or o' when absorbed): one thread per output channel r.
+          // At head_dim 128, R_V comes from the stage area when it was
+          // prefetched there, else from L2, through the same arithmetic in the
+          // same order, so the output does not depend on which CTA merges.
+          const float* rvs = (rv_smem && rv_ok) ? reinterpret_cast<const float*>(smem + C::OFF_STAGE) : nullptr;
           for (int r = threadIdx.x; r < D; r += 32 * kNCW) {
             float res[8];
 #pragma unroll
@@ -1512,14 +1515,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               // 16-byte loads in a skewed walk over j: thread r reads chunk
               // (j4 + r) % (D / 4) of row r and of each o' row, so the eight
               // threads of a quarter warp touch eight different chunks
+              const float4* rv4 = reinterpret_cast<const float4*>(rvs ? rvs + r * D : a.R_V + int64_t(r) * D);
 #pragma unroll 4
               for (int j4 = 0; j4 < D / 4; ++j4) {
-                const int jc = ((j4 + r) & (D / 4 - 1)) * 4;
-                const float4 rv = *reinterpret_cast<const float4*>(rvs + r * D + jc);
+                const int jq = (j4 + r) & (D / 4 - 1);
+                const float4 rv = rvs ? rv4[jq] : __ldg(rv4 + jq);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   if (i < Gh) {
-                    const float4 ov = *reinterpret_cast<const float4*>(ob + i * D + jc);
+                    const float4 ov = *reinterpret_cast<const float4*>(ob + i * D + 4 * jq);
                     res[i] = fmaf(rv.x, ov.x, fmaf(rv.y, ov.y, fmaf(rv.z, ov.z, fmaf(rv.w, ov.w, res[i]))));
                   }
                 }
@@ -1530,8 +1534,9 @@ __global__ void __launch_bounds__(kThreads, 2)
               if (i < Gh) store(i, r, res[i]);
           }
         } else {
-          // rows of R_V from L2: warp w takes rows w, w + 4, ...; lane l reads
-          // columns 4l .. 4l + 3 (+ 128 per step), so every load is coalesced
+          // head_dim 256 / 512 (R_V is never prefetched): rows of R_V from L2,
+          // warp w takes rows w, w + 4, ...; lane l reads columns 4l .. 4l + 3
+          // (+ 128 per step), so every load is coalesced
 #pragma unroll 4
           for (int r = warp; r < D; r += kNCW) {
             const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);

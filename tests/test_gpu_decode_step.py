@@ -1,8 +1,7 @@
 """decode_step (append + decode in one call) against kv_append followed by
-attn_decode: the same kernels on the same data, so lse, cache bytes and status
-words must be identical bit for bit, whatever blocks the fused call streams
-before the append completes, and outputs equal up to the rounding of the V
-un-rotation, whose summation order depends on the CTA that merges a unit
+attn_decode: the same kernels on the same data, so outputs, lse, cache bytes and
+status words must be identical bit for bit, whatever blocks the fused call
+streams before the append completes and whichever CTA merges a unit
 (assert_same_decode).  Cases cover one and several new tokens,
 ring wrap, appends longer than the ring, new positions inside the sink, G = 8
 and D = 256.  The oracle agreement of the sequential calls is covered by the

@@ -1,10 +1,10 @@
-"""Repeated attn_decode calls on the same inputs: lse identical bit for bit, and
-outputs equal up to the rounding of the V un-rotation (assert_same_decode),
-although the CTA that merges a unit's partial results (the last of the unit's
-CTAs to finish) changes from call to call.  Each case shares every unit among
-several CTAs and reaches both sources of R_V at the merge: rows prefetched into
-shared memory (head_dim 128, a merging CTA with no copy in flight) and rows read
-through L2."""
+"""Repeated attn_decode calls on the same inputs: outputs and lse identical bit
+for bit (assert_same_decode), although the CTA that merges a unit's partial
+results (the last of the unit's CTAs to finish) changes from call to call.
+Each case shares every unit among several CTAs and reaches both sources of R_V
+at the merge: rows prefetched into shared memory (head_dim 128, a merging CTA
+with no copy in flight) and rows read through L2; the un-rotation does the same
+arithmetic in the same order from either."""
 import numpy as np
 import pytest
 import torch
