@@ -113,7 +113,7 @@ __host__ __device__ inline int imax(int x, int y) { return x > y ? x : y; }
 
 // vb: V kept BF16 at every position; INT2 blocks then hold 16 tokens of INT2
 // K codes and BF16 V rows, and weigh like a BF16 block.
-__host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int vb) {
+__host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int vb, int lm = 0) {
   Regions r;
   r.T = T;
   if (T <= S) {
@@ -135,9 +135,12 @@ __host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int 
   r.nrb = r.nrb1 + (r.n_ring - r.rlen1 + kBfTok - 1) / kBfTok;
   // work weights of one block, in proportion to its measured processing time
   // (a 128-token INT2 block takes ~1.7x a 16-token BF16 block for ~1.1x the
-  // bytes: the codes are unpacked and the scale/zero algebra is extra work)
+  // bytes: the codes are unpacked and the scale/zero algebra is extra work;
+  // with Lloyd-Max levels every INT2 product runs a second time over the
+  // codes' high bits, ~1.7x again: split kernel 61.4 -> 85.5 us on the
+  // qwen3-4b layer, whose weighted cost is 53 % INT2)
   r.cbf = int64_t(6) * D;
-  r.ci2 = vb ? r.cbf : int64_t(10) * D;
+  r.ci2 = vb ? r.cbf : int64_t(lm ? 17 : 10) * D;
   return r;
 }
 
@@ -281,17 +284,17 @@ __device__ __forceinline__ int64_t div_small(int64_t x, int64_t d) {
   return q;
 }
 
-template <int D, bool VB>
+template <int D, bool VB, bool LM>
 __device__ __forceinline__ int64_t seq_cost(const DecodeArgs& a, const int* lens, int b) {
-  return b < a.g.B ? unit_cost(make_regions(seq_len_at(a, lens, b), a.g.S, a.g.W, D, VB)) : 0;
+  return b < a.g.B ? unit_cost(make_regions(seq_len_at(a, lens, b), a.g.S, a.g.W, D, VB, LM)) : 0;
 }
 
-template <int D, bool VB>
+template <int D, bool VB, bool LM>
 __device__ Plan make_plan(const DecodeArgs& a, const int* lens, int lane) {
   const Geom& g = a.g;
   int64_t W = 0, cmax = 0;
   for (int b0 = 0; b0 < g.B; b0 += 32) {
-    int64_t sm = seq_cost<D, VB>(a, lens, b0 + lane), mx = sm;
+    int64_t sm = seq_cost<D, VB, LM>(a, lens, b0 + lane), mx = sm;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       sm += __shfl_xor_sync(0xffffffffu, sm, o);
@@ -315,29 +318,29 @@ __device__ Plan make_plan(const DecodeArgs& a, const int* lens, int lane) {
 }
 
 // Start cost of unit k (k <= B * Hkv).
-template <int D, bool VB>
+template <int D, bool VB, bool LM>
 __device__ int64_t unit_start(const DecodeArgs& a, const int* lens, int lane, int64_t k) {
   const int Hkv = a.g.Hkv;
   const int bk = int(k) / Hkv, hk = int(k) % Hkv;  // k <= B * Hkv < 2^31
   int64_t base = 0;
   for (int b0 = 0; b0 < bk; b0 += 32) {
-    int64_t c = b0 + lane < bk ? seq_cost<D, VB>(a, lens, b0 + lane) * Hkv : 0;
+    int64_t c = b0 + lane < bk ? seq_cost<D, VB, LM>(a, lens, b0 + lane) * Hkv : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     base += c;
   }
-  return base + (hk > 0 ? hk * seq_cost<D, VB>(a, lens, bk) : 0);
+  return base + (hk > 0 ? hk * seq_cost<D, VB, LM>(a, lens, bk) : 0);
 }
 
 // Unit holding cost x (0 <= x < W) and its start cost.
-template <int D, bool VB>
+template <int D, bool VB, bool LM>
 __device__ void locate(const DecodeArgs& a, const int* lens, int lane, int64_t x, int& u, int64_t& us) {
   const int Hkv = a.g.Hkv;
   int64_t base = 0;
   u = 0;
   us = 0;
   for (int b0 = 0; b0 < a.g.B; b0 += 32) {
-    const int64_t per = seq_cost<D, VB>(a, lens, b0 + lane);
+    const int64_t per = seq_cost<D, VB, LM>(a, lens, b0 + lane);
     int64_t incl = per * Hkv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -362,7 +365,7 @@ __device__ void locate(const DecodeArgs& a, const int* lens, int lane, int64_t x
 // start cost us (warp-wide; lane 0's results are the ones used).  Lists at most
 // kMaxSeg segments; returns their number and leaves (u, us) at the first unit
 // not listed.
-template <int D, bool VB>
+template <int D, bool VB, bool LM>
 __device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& pl, int c, int64_t lo, int64_t hi,
                               int& u, int64_t& us, SegD* seg, int lane) {
   const Geom& g = a.g;
@@ -372,7 +375,7 @@ __device__ int build_segments(const DecodeArgs& a, const int* lens, const Plan& 
     const int64_t uu = u + lane;
     const int b = int(uu) / g.Hkv, h = int(uu) % g.Hkv;
     const int T = uu < U ? seq_len_at(a, lens, b) : 0;
-    const Regions rg = make_regions(T, g.S, g.W, D, VB);
+    const Regions rg = make_regions(T, g.S, g.W, D, VB, LM);
     const int64_t cu = uu < U ? unit_cost(rg) : 0;
     int64_t incl = cu;
 #pragma unroll
@@ -651,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 
   // ---- this CTA's slice [lo, hi) of the concatenated unit costs
-  const Plan pl = make_plan<D, VB>(a, lens, lane);
+  const Plan pl = make_plan<D, VB, LM>(a, lens, lane);
   const int c = blockIdx.x;
   if (pl.W == 0 || c >= pl.P) return;
   int64_t lo, hi, us_next = 0;
@@ -659,14 +662,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (pl.aligned) {
     const int64_t U = int64_t(g.B) * g.Hkv;
     const int64_t k0 = div_floor(int64_t(c) * U + pl.P - 1, pl.P), k1 = div_floor(int64_t(c + 1) * U + pl.P - 1, pl.P);
-    lo = unit_start<D, VB>(a, lens, lane, k0);
-    hi = unit_start<D, VB>(a, lens, lane, k1);
+    lo = unit_start<D, VB, LM>(a, lens, lane, k0);
+    hi = unit_start<D, VB, LM>(a, lens, lane, k1);
     u_next = int(k0);
     us_next = lo;
   } else {
     lo = div_floor(int64_t(c) * pl.W + pl.P - 1, pl.P);
     hi = div_floor(int64_t(c + 1) * pl.W + pl.P - 1, pl.P);
-    if (lo < hi) locate<D, VB>(a, lens, lane, lo, u_next, us_next);
+    if (lo < hi) locate<D, VB, LM>(a, lens, lane, lo, u_next, us_next);
   }
   if (lo >= hi) return;
 
@@ -836,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (;;) {
     // ---- segment table of the next window (warp 0), then start streaming
     if (warp == 0) {
-      const int n = build_segments<D, VB>(a, lens, pl, c, lo, hi, u_next, us_next, seg, lane);
+      const int n = build_segments<D, VB, LM>(a, lens, pl, c, lo, hi, u_next, us_next, seg, lane);
       if (lane == 0) {
         win_n = n;
         win_more = us_next < hi && u_next < int64_t(g.B) * g.Hkv;
@@ -1706,7 +1709,7 @@ int decode_grid(const Geom& g, int seq_len_hint, int num_splits) {
   // context of seq_len_hint implies (a CTA's fixed cost, ~10 us of set-up and
   // merge, runs in parallel with the others, so small problems spread wide)
   const int64_t resident = int64_t(di.sms) * di.occ[didx(g.D)][g.G > 4 ? 1 : 0][g.vb ? 1 : 0][g.lm ? 1 : 0];
-  const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D, g.vb);
+  const Regions r = make_regions(seq_len_hint, g.S, g.W, g.D, g.vb, g.lm);
   const int64_t min_cost = int64_t(kNCW / g.Dg) * r.cbf;
   const int64_t by_work = std::max<int64_t>(1, unit_cost(r) * units / min_cost);
   return int(std::max<int64_t>(1, std::min(resident, by_work)));

@@ -141,28 +141,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // B operand: piece p holds B_p[n][k] with R[k][n] = B_0 + B_1 + B_2 (bf16)
-  {
-    // all 160 threads; float4 loads along rows of R (coalesced, many in flight)
-    const float4* R4 = reinterpret_cast<const float4*>(R);
-#pragma unroll 4
-    for (int idx = threadIdx.x; idx < kD * kD / 4; idx += kThreadsTc) {
-      const float4 x4 = __ldg(R4 + idx);
-      const int k = (idx * 4) / kD, n0 = (idx * 4) % kD;
-      const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+  // B operand: piece p holds B_p[n][k] with R[k][n] = B_0 + B_1 + B_2 (bf16).
+  // Each thread builds one 16-byte chunk of each piece: 8 consecutive k of row
+  // n.  Consecutive threads take consecutive n, so every load of R is a
+  // coalesced row segment and the chunk stores of a warp spread over all banks
+  // (the 128-byte swizzle puts rows n and n + 1 .. n + 7 in different chunks).
+  for (int cidx = threadIdx.x; cidx < kD * (kD / 8); cidx += kThreadsTc) {
+    const int n = cidx % kD, k0 = (cidx / kD) * 8;
+    uint32_t ph[4], pm[4], pl[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = xs[e];
-        const __nv_bfloat16 h = __float2bfloat16_rn(x);
-        const float r1 = x - __bfloat162float(h);
-        const __nv_bfloat16 m = __float2bfloat16_rn(r1);
-        const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
-        const uint32_t off = sw128_offset(n0 + e, k);
-        *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 0 * kOperandBytes + off) = h;
-        *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 1 * kOperandBytes + off) = m;
-        *reinterpret_cast<__nv_bfloat16*>(smem + kOffB + 2 * kOperandBytes + off) = l;
-      }
+    for (int e = 0; e < 8; e += 2) {
+      uint32_t p0[3], p1[3];
+      split3_bf16(__ldg(R + (k0 + e) * kD + n), p0);
+      split3_bf16(__ldg(R + (k0 + e + 1) * kD + n), p1);
+      ph[e / 2] = p0[0] | (p1[0] << 16);
+      pm[e / 2] = p0[1] | (p1[1] << 16);
+      pl[e / 2] = p0[2] | (p1[2] << 16);
     }
+    const uint32_t off = sw128_offset(n, k0);
+    *reinterpret_cast<uint4*>(smem + kOffB + 0 * kOperandBytes + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    *reinterpret_cast<uint4*>(smem + kOffB + 1 * kOperandBytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+    *reinterpret_cast<uint4*>(smem + kOffB + 2 * kOperandBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make generic smem writes visible to the MMA
   tc_fence_before();
@@ -249,9 +248,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const bool valid = row < a.rows;
       float v[32];
 
-      // pass 1: raw row min / max (NaN-propagating, so a NaN row shows as non-finite)
+      // pass 1: raw row min / max (NaN-propagating, so a NaN row shows as non-finite).
+      // The loops over the four 32-column chunks stay rolled: sixteen warps run
+      // this code and it must fit the instruction cache.
       float rmn = INFINITY, rmx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(taddr + 32 * c, v);
 #pragma unroll
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       uint32_t words[8];
 #pragma unroll
       for (int w = 0; w < 8; ++w) words[w] = 0;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(taddr + 32 * c, v);
         if (dbg) {
@@ -323,22 +324,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const int code = __float2int_rn(__fmul_rn(__fsub_rn(x, zf), inv));
           return qok ? uint32_t(min(max(code, 0), 3)) : 0u;
         };
-        // the role is uniform per CTA: one unrolled loop per code layout
+        // the role is uniform per CTA: one loop per code layout.  Channel
+        // d = 32 c + j; the chunk's codes are gathered with shifts that do not
+        // depend on c, then moved into place.
         if (role == 0) {
+          // K: word 2 (e >> 1) + (c >> 1), bit 8 (c & 1) + 4 (j >> 4) + 2 hh + 16 (e & 1)
+          // with e = j & 7, hh = (j >> 3) & 1 (the header's K layout for d)
+          uint32_t wl[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int d = 32 * c + j;
-            const int kk = d >> 4, r16 = d & 15, hh = r16 >> 3, e = r16 & 7;
-            const int word = 2 * (e >> 1) + (kk >> 2);
-            const int bit = 2 * (2 * (kk & 3) + hh) + 16 * (e & 1);
-            words[word] |= code_of(v[j]) << bit;
+            const int e = j & 7, hh = (j >> 3) & 1;
+            wl[e >> 1] |= code_of(v[j]) << (4 * (j >> 4) + 2 * hh + 16 * (e & 1));
+          }
+          const int sh = 8 * (c & 1);
+          const bool hi = (c >> 1) != 0;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t x = wl[m] << sh;
+            words[2 * m] |= hi ? 0u : x;
+            words[2 * m + 1] |= hi ? x : 0u;
           }
         } else {
+          // V: word d & 7 = j & 7, bit 2 (d >> 3) = 8 c + 2 (j >> 3)
+          uint32_t wl[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int d = 32 * c + j;
-            words[d & 7] |= code_of(v[j]) << (2 * (d >> 3));
-          }
+          for (int j = 0; j < 32; ++j) wl[j & 7] |= code_of(v[j]) << (2 * (j >> 3));
+#pragma unroll
+          for (int m = 0; m < 8; ++m) words[m] |= wl[m] << (8 * c);
         }
       }
       if (in_cache && p >= g.S) {
