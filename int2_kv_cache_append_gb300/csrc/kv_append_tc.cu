@@ -45,6 +45,7 @@ constexpr uint32_t kOffA = 3 * kOperandBytes;          // 2 stages of A
 constexpr uint32_t kOffBar = kOffA + 2 * kOperandBytes;
 constexpr uint32_t kSmemTc = kOffBar + 128 + 1024;     // + alignment slack
 constexpr uint32_t kTmemCols = 512;                    // four 128-column fp32 accumulators
+constexpr int kSposCache = 256;                        // start positions staged in shared memory
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ int spos[kSposCache];  // start positions of the first kSposCache sequences
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     *reinterpret_cast<uint4*>(smem + kOffB + 1 * kOperandBytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
     *reinterpret_cast<uint4*>(smem + kOffB + 2 * kOperandBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
+  for (int i = threadIdx.x; i < a.g.B && i < kSposCache; i += kThreadsTc) spos[i] = a.start_pos[i];
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make generic smem writes visible to the MMA
   tc_fence_before();
   __syncthreads();
@@ -281,8 +284,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int64_t bt = row / g.Hkv;
         const int t = int(bt % a.n_new);
         b = int(bt / a.n_new);
-        p = a.start_pos[b] + t;
-        newlen = a.start_pos[b] + a.n_new;
+        const int sp = b < kSposCache ? spos[b] : a.start_pos[b];
+        p = sp + t;
+        newlen = sp + a.n_new;
         bh = int64_t(b) * g.Hkv + h;
         if (!finite) status_or(a.status, OSCAR_DEV_NONFINITE);
         if (!rng_ok) status_or(a.status, OSCAR_DEV_FP16_RANGE);
@@ -319,10 +323,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (ring4) ring4[(32 * c + j) / 8] = q;
           }
         }
+        // code = clamp(rint((clamp(r, -t, t) - z) * inv), 0, 3) as the codec
+        // defines it, evaluated without the clamp of r and without a qok
+        // select: (1) where r > t, the group's max was clipped to t, so
+        // (t - z) * inv rounds to 3 and, every step being monotone, r gives a
+        // code >= 3 as well; symmetrically below -t, and a group with no
+        // clipped value has no r beyond t; (2) inv = 0 when !qok, so the
+        // product is 0 (or NaN for a non-finite zero, which cvt.rni turns into 0).
         auto code_of = [&](float r) {
-          const float x = fminf(fmaxf(r, -tclip), tclip);
-          const int code = __float2int_rn(__fmul_rn(__fsub_rn(x, zf), inv));
-          return qok ? uint32_t(min(max(code, 0), 3)) : 0u;
+          const uint32_t code = __float2uint_rn(__fmul_rn(__fsub_rn(r, zf), inv));  // saturates below 0
+          return min(code, 3u);
         };
         // the role is uniform per CTA: one loop per code layout.  Channel
         // d = 32 c + j; the chunk's codes are gathered with shifts that do not
