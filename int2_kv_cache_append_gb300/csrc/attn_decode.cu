@@ -64,6 +64,10 @@ struct DecCfg {
   static constexpr int TS = Dg;              // warps per team (one quant group each)
   static constexpr int NTEAMS = kNCW / TS;
   static constexpr int ROWB = D / 4;         // code bytes per token
+  // INT2 code rows of 64 or 128 bytes arrive as swizzled TMA boxes: plain
+  // rows put the 8 token rows of a code load in the same banks (4- to 8-way
+  // conflicts); 32-byte rows (head_dim 128) have none worth a second map
+  static constexpr bool SWZ = D >= 256;
   static constexpr int BOXES = D / 64;       // 16-row x 64-column TMA boxes per BF16 matrix
   static constexpr int BOX_BYTES = kBfTok * 128;
   static constexpr int I2_BYTES = kI2Tok * (2 * ROWB + 2 * Dg * 4);
@@ -633,10 +637,19 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
 // codes index the Lloyd-Max levels, level(c) = rho * c + kLmHi * (2 c1), so each
 // INT2 product runs a second time over the codes' high bits.  Separate
 // instantiations: the default kernel carries none of either mode's code.
+// XOR applied by the TMA swizzle (32, 64 or 128 bytes, the code row size
+// ROWB) to the 16-byte chunk index of token row t of a stage's code matrix:
+// address bits 7.. of the row start, masked to the chunk-index bits.
+template <int ROWB>
+__device__ __forceinline__ uint32_t code_chunk_xor(int t) {
+  return (uint32_t(t * ROWB) >> 7) & uint32_t(ROWB / 16 - 1);
+}
+
 template <int D, int NQT, bool VB, bool LM>
 __global__ void __launch_bounds__(kThreads, 2)
     split_kernel(const __grid_constant__ CUtensorMap tks, const __grid_constant__ CUtensorMap tvs,
                  const __grid_constant__ CUtensorMap tkr, const __grid_constant__ CUtensorMap tvr,
+                 const __grid_constant__ CUtensorMap tkc, const __grid_constant__ CUtensorMap tvc,
                  const DecodeArgs a) {
   using C = DecCfg<D, NQT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -690,6 +703,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int team = warp / C::TS, wt = warp % C::TS;  // wt = quant group handled
   const int gq = lane >> 2, cq = lane & 3;
+  // Columns of this lane's INT2 code loads in a 128-token stage: K bytes
+  // 32 wt + 8 cq of rows 16 m + gq (+ 8), V word 8 wt + gq of rows
+  // 16 k + 2 cq + {0, 1} (+ 8).  In the swizzled stage (head_dim >= 256) the
+  // 16-byte chunk c of token row t sits at chunk c ^ code_chunk_xor(t), an XOR
+  // that depends only on t mod 8, which the lane fixes.
+  const int kcol = C::SWZ ? int(((uint32_t(2 * wt + (cq >> 1)) ^ code_chunk_xor<C::ROWB>(gq)) << 4) |
+                                uint32_t(8 * (cq & 1)))
+                          : wt * 32 + cq * 8;
+  const int vcol0 = C::SWZ ? int(((uint32_t(2 * wt + (gq >> 2)) ^ code_chunk_xor<C::ROWB>(2 * cq)) << 2) |
+                                 uint32_t(gq & 3))
+                           : wt * 8 + gq;
+  const int vcol1 = C::SWZ ? int(((uint32_t(2 * wt + (gq >> 2)) ^ code_chunk_xor<C::ROWB>(2 * cq + 1)) << 2) |
+                                 uint32_t(gq & 3))
+                           : wt * 8 + gq;
   const int Gh = g.G;
   auto my_stage = [&](int j) { return team * C::NSTW + j % C::NSTW; };
   int issued = 0, consumed = 0;  // blocks of this team issued / consumed so far
@@ -720,6 +747,14 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int vrow = int(bh * g.cap + g.S + bk.first);
 #pragma unroll
           for (int q = 0; q < C::BOXES; ++q) tma_load_2d(dst + C::VB_V + q * C::BOX_BYTES, &tvs, 64 * q, vrow, full);
+        } else if constexpr (C::SWZ) {
+          // K and V codes as 128-row TMA boxes, swizzled by the row size (see
+          // code_chunk_xor); rows past the unit's last token are not used
+          mbar_arrive_expect_tx(full, 2 * kI2Tok * C::ROWB + 2 * sb + extra);
+          tma_load_2d(dst, &tkc, 0, int(row), full);
+          tma_load_2d(dst + kI2Tok * C::ROWB, &tvc, 0, int(row), full);
+          bulk_g2s(dst + 2 * kI2Tok * C::ROWB, kbase + sz_off + row * C::Dg * 4, sb, full);
+          bulk_g2s(dst + 2 * kI2Tok * C::ROWB + kI2Tok * C::Dg * 4, vbase + sz_off + row * C::Dg * 4, sb, full);
         } else {
           mbar_arrive_expect_tx(full, 2 * cb + 2 * sb + extra);
           bulk_g2s(dst, kbase + codes_off + row * C::ROWB, cb, full);
@@ -973,8 +1008,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int i = 0; i < MG; ++i) {
               const int t0 = 16 * (m0 + i) + gq;
-              w[i][0] = *reinterpret_cast<const uint2*>(kc + (tb + t0) * C::ROWB + wt * 32 + cq * 8);
-              w[i][1] = *reinterpret_cast<const uint2*>(kc + (tb + t0 + 8) * C::ROWB + wt * 32 + cq * 8);
+              w[i][0] = *reinterpret_cast<const uint2*>(kc + (tb + t0) * C::ROWB + kcol);
+              w[i][1] = *reinterpret_cast<const uint2*>(kc + (tb + t0 + 8) * C::ROWB + kcol);
             }
             float acc[MG][NQT][4];
 #pragma unroll
@@ -1250,10 +1285,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             // codes of word (wt, gq) for tokens 2cq, 2cq+1, 2cq+8, 2cq+9 of this k-step
             const int ta = 16 * ks + 2 * cq;
-            const uint32_t wa = vc[(tb + ta + 0) * (C::ROWB / 4) + wt * 8 + gq];
-            const uint32_t wb = vc[(tb + ta + 1) * (C::ROWB / 4) + wt * 8 + gq];
-            const uint32_t wc = vc[(tb + ta + 8) * (C::ROWB / 4) + wt * 8 + gq];
-            const uint32_t wd = vc[(tb + ta + 9) * (C::ROWB / 4) + wt * 8 + gq];
+            const uint32_t wa = vc[(tb + ta + 0) * (C::ROWB / 4) + vcol0];
+            const uint32_t wb = vc[(tb + ta + 1) * (C::ROWB / 4) + vcol1];
+            const uint32_t wc = vc[(tb + ta + 8) * (C::ROWB / 4) + vcol0];
+            const uint32_t wd = vc[(tb + ta + 9) * (C::ROWB / 4) + vcol1];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               uint32_t rx[8], ry[8];
@@ -1678,8 +1713,19 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
     if (g.S > 0 && !encode_rows_bf16(&maps[1], vb, bh * g.S, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
     if (g.W > 0 && !encode_rows_bf16(&maps[3], vb + g.sink_bytes, bh * g.W, D, 64, kBfTok)) return OSCAR_ERR_LAUNCH;
   }
+  // INT2 code rows [B*Hkv*ncap][D/4] per role, 128-row swizzled boxes (unused with V kept BF16)
+  CUtensorMap cmaps[2];
+  std::memset(cmaps, 0, sizeof(cmaps));
+  const uint64_t crows = bh * uint64_t(g.ncap);
+  if (C::SWZ && !g.vb && crows > 0) {
+    if (crows >= (uint64_t(1) << 31)) return OSCAR_ERR_LAUNCH;  // 32-bit TMA row coordinates
+    const uint64_t codes_off = g.sink_bytes + g.ring_bytes;
+    if (!encode_code_rows(&cmaps[0], kb + codes_off, crows, C::ROWB, kI2Tok) ||
+        !encode_code_rows(&cmaps[1], vb + codes_off, crows, C::ROWB, kI2Tok))
+      return OSCAR_ERR_LAUNCH;
+  }
   if (launch_pdl(split_kernel<D, NQT, VB, LM>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
-                 maps[2], maps[3], a) != cudaSuccess)
+                 maps[2], maps[3], cmaps[0], cmaps[1], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   return OSCAR_OK;

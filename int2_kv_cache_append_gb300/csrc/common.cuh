@@ -26,6 +26,26 @@ struct Geom {
 
 __host__ __device__ inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
+// Division of 32-bit unsigned integers by a divisor d (1 <= d <= 2^31) fixed
+// for a launch, as a multiply-high, an add and a shift: with l = ceil(log2 d)
+// and m = floor(2^32 (2^l - d) / d) + 1, floor(x / d) = (mulhi(x, m) + x) >> l
+// for every 32-bit x (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994, section 4).
+struct FastDiv {
+  uint32_t mul, shift;
+};
+inline FastDiv fastdiv_make(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  FastDiv f;
+  f.shift = l;
+  f.mul = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  return f;
+}
+__device__ __forceinline__ uint32_t fastdiv(uint32_t x, const FastDiv& f) {
+  return uint32_t((uint64_t(__umulhi(x, f.mul)) + x) >> f.shift);
+}
+
 // ---------------------------------------------------------------------------
 // small PTX wrappers
 // ---------------------------------------------------------------------------
@@ -192,6 +212,32 @@ __device__ __forceinline__ float fmin_nan(float a, float b) {
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float d;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+// three-operand forms (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (r0 - z, r1 - z) * inv as one packed subtract and one packed multiply; each
+// element is rounded as __fmul_rn(__fsub_rn(r, z), inv) rounds it.  zz and ii
+// hold z and inv in both halves.
+__device__ __forceinline__ void sub_mul_x2(float r0, float r1, uint64_t zz, uint64_t ii, float& y0, float& y1) {
+  uint64_t x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(r0), "f"(r1));
+  asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(zz));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(ii));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(x));
+}
+__device__ __forceinline__ uint64_t splat_x2(float x) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(x));
   return d;
 }
 

@@ -25,6 +25,7 @@ struct AppendArgs {
   float k_clip, v_clip;
   int in_fp32;
   int hadamard;          // rotate by the in-quant Hadamard (R_K, R_V unused)
+  FastDiv div_hkv, div_n_new;  // set by the tensor-core launcher (rows < 2^31)
 };
 
 struct DecodeArgs {
@@ -69,6 +70,10 @@ int launch_append_tc(const AppendArgs& a, cudaStream_t stream);  // D = 128, bf1
 // 2-D tiled TMA map of a row-major bf16 matrix [rows][cols], 128-byte swizzle
 bool encode_rows_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_cols,
                       uint32_t box_rows);
+// 2-D tiled TMA map of INT2 code rows [rows][rowb] (uint8; rowb = 32, 64 or
+// 128), box [box_rows][rowb], swizzled by the row size: 16-byte chunk c of
+// row t lands at chunk c ^ ((t * rowb / 128) mod (rowb / 16))
+bool encode_code_rows(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t rowb, uint32_t box_rows);
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // CTAs of the split kernel: num_splits * B * Hkv, or (num_splits = 0) as many
 // as are resident at once, fewer when a context of seq_len_hint is short.

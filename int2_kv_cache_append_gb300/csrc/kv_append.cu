@@ -570,7 +570,7 @@ int launch_append(const AppendArgs& a, cudaStream_t stream) {
       default: return OSCAR_ERR_UNSUPPORTED;
     }
   }
-  if (a.g.D == 128 && !a.in_fp32) return launch_append_tc(a, stream);
+  if (a.g.D == 128 && !a.in_fp32 && a.rows < (int64_t(1) << 31)) return launch_append_tc(a, stream);
   switch (a.g.D) {
     case 128: return launch_append_d<128>(a, stream);
     case 256: return launch_append_d<256>(a, stream);

@@ -10,7 +10,8 @@
 //     The pieces are written to shared memory transposed (N x K, K-major) in the
 //     128-byte swizzled layout the MMA descriptors expect.
 //   * A tiles of 128 rows are fetched with TMA tensor loads (cp.async.bulk.tensor,
-//     SWIZZLE_128B) into a 2-stage ring.
+//     SWIZZLE_128B) into a 4-stage ring: up to three tiles (96 KB) in flight per
+//     SM, what a 1-2 us loaded DRAM latency asks for at the full HBM rate.
 //   * One thread of the producer warp issues 3 x 8 tcgen05.mma (M128 N128 K16,
 //     kind::f16, bf16 operands, fp32 accumulate) per tile into one of four TMEM
 //     accumulators and signals completion with tcgen05.commit.
@@ -41,8 +42,9 @@ constexpr int kThreadsTc = (kEpiWarps + 1) * 32;
 constexpr uint32_t kKBlockBytes = kTileRows * 128;  // 128 rows x 64 bf16 (128 B), swizzled
 constexpr uint32_t kOperandBytes = 2 * kKBlockBytes; // K = 128 -> two K-blocks
 constexpr uint32_t kOffB = 0;                          // 3 pieces of R^T
-constexpr uint32_t kOffA = 3 * kOperandBytes;          // 2 stages of A
-constexpr uint32_t kOffBar = kOffA + 2 * kOperandBytes;
+constexpr int kStagesA = 4;                            // A ring depth
+constexpr uint32_t kOffA = 3 * kOperandBytes;          // kStagesA stages of A
+constexpr uint32_t kOffBar = kOffA + kStagesA * kOperandBytes;
 constexpr uint32_t kSmemTc = kOffBar + 128 + 1024;     // + alignment slack
 constexpr uint32_t kTmemCols = 512;                    // four 128-column fp32 accumulators
 constexpr int kSposCache = 256;                        // start positions staged in shared memory
@@ -75,19 +77,35 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// tcgen05.ld of 32 consecutive fp32 columns of the thread's TMEM lane, without
+// the wait; tmem_wait32 waits for all of the thread's loads and carries the
+// registers, so nothing reads them before they have landed.
+__device__ __forceinline__ void tmem_ld32_start(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// 64 consecutive fp32 columns of the thread's TMEM lane; the wait carries the
+// registers so nothing reads them before the load has landed.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -113,10 +131,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sB = base + kOffB, sA = base + kOffA;
   const uint32_t bar0 = base + kOffBar;
-  auto full_a = [&](int s) { return bar0 + 8u * s; };
-  auto empty_a = [&](int s) { return bar0 + 16u + 8u * s; };
-  auto acc_full = [&](int s) { return bar0 + 32u + 8u * s; };   // s < 4
-  auto acc_empty = [&](int s) { return bar0 + 64u + 8u * s; };  // s < 4
+  auto full_a = [&](int s) { return bar0 + 8u * s; };          // s < kStagesA
+  auto empty_a = [&](int s) { return bar0 + 32u + 8u * s; };    // s < kStagesA
+  auto acc_full = [&](int s) { return bar0 + 64u + 8u * s; };   // s < 4
+  auto acc_empty = [&](int s) { return bar0 + 96u + 8u * s; };  // s < 4
 
   pdl_trigger();  // a dependent kernel may be scheduled now; it waits for our completion itself
   const int role = blockIdx.y;
@@ -127,7 +145,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStagesA; ++s) {
       mbar_init(full_a(s), 1);
       mbar_init(empty_a(s), 1);
     }
@@ -176,13 +194,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------- producer + MMA issuer -------------------------
     if (lane == 0) {
       // this CTA's tiles j = 0, 1, ...: tile blockIdx.x + j * gridDim.x, A stage
-      // j & 1; the load of tile j + 1 is issued before waiting for tile j, into
-      // the stage the MMAs of tile j - 1 release
+      // j % kStagesA.  The loads run kStagesA - 1 tiles ahead; the refill of a
+      // stage is issued right after the MMAs of the next tile, so the wait for
+      // the MMAs that release it never leaves the tensor pipe without work.
       const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
       int loaded = 0;
       auto load = [&](int j) -> bool {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(empty_a(s), ((j >> 1) & 1) ^ 1)) return false;
+        const int s = j % kStagesA;
+        if (j >= kStagesA && !mbar_wait(empty_a(s), ((j / kStagesA) & 1) ^ 1)) return false;
         const int64_t tile = blockIdx.x + int64_t(j) * gridDim.x;
         mbar_arrive_expect_tx(full_a(s), kOperandBytes);
         const uint32_t dst = sA + s * kOperandBytes;
@@ -191,15 +210,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         ++loaded;
         return true;
       };
-      bool ok = my_tiles == 0 || load(0);
+      bool ok = true;
+      for (int j = 0; ok && j < kStagesA - 1 && j < my_tiles; ++j) ok = load(j);
       int it = 0;
       for (; ok && it < my_tiles; ++it) {
-        const int s = it & 1;  // A stage
-        const uint32_t ph = (it >> 1) & 1;
+        const int s = it % kStagesA;  // A stage
+        const uint32_t ph = (it / kStagesA) & 1;
         const int sa = it & 3;  // TMEM accumulator
         const uint32_t pa = (it >> 2) & 1;
         if (*((volatile int*)&abort_flag)) ok = false;
-        if (ok && it + 1 < my_tiles) ok = load(it + 1);
         if (ok) ok = mbar_wait(full_a(s), ph);
         if (ok && it >= 4) ok = mbar_wait(acc_empty(sa), pa ^ 1);
         if (!ok) break;
@@ -217,13 +236,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         umma_commit(acc_full(sa));
         umma_commit(empty_a(s));
+        // refill the stage of tile it - 1 (its MMAs precede the ones just issued)
+        if (it + kStagesA - 1 < my_tiles) ok = load(it + kStagesA - 1);
       }
       if (!ok) {
         abort_flag = 1;
         status_or(a.status, OSCAR_DEV_TIMEOUT);
-        // loads issued for tiles not consumed (at most one ahead) must land
-        // before the CTA exits
-        for (int j = it; j < loaded; ++j) (void)mbar_wait(full_a(j & 1), (j >> 1) & 1);
+        // loads issued for tiles not consumed (up to kStagesA - 1 ahead) must
+        // land before the CTA exits
+        for (int j = it; j < loaded; ++j) (void)mbar_wait(full_a(j % kStagesA), (j / kStagesA) & 1);
       }
       // drain: the last (up to four) commits must have landed before TMEM is freed
       for (int j = (it >= 4 ? it - 4 : 0); j < it; ++j) mbar_wait(acc_full(j & 3), (j >> 2) & 1);
@@ -249,20 +270,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t taddr = tmem + (uint32_t(32 * quarter) << 16) + uint32_t(s) * kD;
       const int64_t row = tile * kTileRows + 32 * quarter + lane;
       const bool valid = row < a.rows;
-      float v[32];
 
       // pass 1: raw row min / max (NaN-propagating, so a NaN row shows as non-finite).
       // The loops over the four 32-column chunks stay rolled: sixteen warps run
       // this code and it must fit the instruction cache.
+      // Two 64-column loads, each reduced in two independent chains.
       float rmn = INFINITY, rmx = -INFINITY;
+      {
+        float rmn1 = INFINITY, rmx1 = -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(taddr + 32 * c, v);
+        for (int c = 0; c < 2; ++c) {
+          float w[64];
+          tmem_ld64(taddr + 64 * c, w);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          rmn = fmin_nan(rmn, v[j]);
-          rmx = fmax_nan(rmx, v[j]);
+          for (int j = 0; j < 64; j += 4) {
+            rmn = fmin3_nan(rmn, w[j], w[j + 1]);
+            rmx = fmax3_nan(rmx, w[j], w[j + 1]);
+            rmn1 = fmin3_nan(rmn1, w[j + 2], w[j + 3]);
+            rmx1 = fmax3_nan(rmx1, w[j + 2], w[j + 3]);
+          }
         }
+        rmn = fmin_nan(rmn, rmn1);
+        rmx = fmax_nan(rmx, rmx1);
       }
       const bool finite = isfinite(rmn) && isfinite(rmx);
       const float amax = fmaxf(fabsf(rmn), fabsf(rmx));          // max_j |r_j|
@@ -276,14 +305,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const bool rng_ok = isfinite(sf) && isfinite(zf);
       const bool qok = rng_ok && sf != 0.f;
       const float inv = qok ? __frcp_rn(sf) : 0.f;
+      const uint64_t zz = splat_x2(zf), ii = splat_x2(inv);
 
       int b = 0, p = -1, newlen = 0;
       int64_t bh = 0;
       if (valid) {
-        const int h = int(row % g.Hkv);
-        const int64_t bt = row / g.Hkv;
-        const int t = int(bt % a.n_new);
-        b = int(bt / a.n_new);
+        // row = (b n_new + t) Hkv + h, below 2^31 on this path
+        const uint32_t r32 = uint32_t(row);
+        const uint32_t bt = fastdiv(r32, a.div_hkv);
+        const int h = int(r32 - bt * uint32_t(g.Hkv));
+        const uint32_t bq = fastdiv(bt, a.div_n_new);
+        const int t = int(bt - bq * uint32_t(a.n_new));
+        b = int(bq);
         const int sp = b < kSposCache ? spos[b] : a.start_pos[b];
         p = sp + t;
         newlen = sp + a.n_new;
@@ -304,9 +337,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       uint32_t words[8];
 #pragma unroll
       for (int w = 0; w < 8; ++w) words[w] = 0;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(taddr + 32 * c, v);
+      // one 32-column chunk c of the row, raw TMEM words in r
+      auto chunk = [&](const uint32_t (&r)[32], const int c) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
         if (dbg) {
 #pragma unroll
           for (int j = 0; j < 32; j += 4) dbg[(32 * c + j) / 4] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -330,13 +365,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // code >= 3 as well; symmetrically below -t, and a group with no
         // clipped value has no r beyond t; (2) inv = 0 when !qok, so the
         // product is 0 (or NaN for a non-finite zero, which cvt.rni turns into 0).
-        auto code_of = [&](float r) {
-          const uint32_t code = __float2uint_rn(__fmul_rn(__fsub_rn(r, zf), inv));  // saturates below 0
-          return min(code, 3u);
+        // Channels go in pairs through one packed subtract and multiply.
+        float cf[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) sub_mul_x2(v[j], v[j + 1], zz, ii, cf[j], cf[j + 1]);
+        auto code_of = [&](int j) {
+          return min(__float2uint_rn(cf[j]), 3u);  // the conversion saturates below 0
         };
         // the role is uniform per CTA: one loop per code layout.  Channel
         // d = 32 c + j; the chunk's codes are gathered with shifts that do not
-        // depend on c, then moved into place.
+        // depend on c, then moved into place.  Codes occupy disjoint bit
+        // pairs, so they are combined with additions (shift-and-add is one
+        // instruction).
         if (role == 0) {
           // K: word 2 (e >> 1) + (c >> 1), bit 8 (c & 1) + 4 (j >> 4) + 2 hh + 16 (e & 1)
           // with e = j & 7, hh = (j >> 3) & 1 (the header's K layout for d)
@@ -344,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int e = j & 7, hh = (j >> 3) & 1;
-            wl[e >> 1] |= code_of(v[j]) << (4 * (j >> 4) + 2 * hh + 16 * (e & 1));
+            wl[e >> 1] += code_of(j) << (4 * (j >> 4) + 2 * hh + 16 * (e & 1));
           }
           const int sh = 8 * (c & 1);
           const bool hi = (c >> 1) != 0;
@@ -358,10 +398,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           // V: word d & 7 = j & 7, bit 2 (d >> 3) = 8 c + 2 (j >> 3)
           uint32_t wl[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-          for (int j = 0; j < 32; ++j) wl[j & 7] |= code_of(v[j]) << (2 * (j >> 3));
+          for (int j = 0; j < 32; ++j) wl[j & 7] += code_of(j) << (2 * (j >> 3));
 #pragma unroll
           for (int m = 0; m < 8; ++m) words[m] |= wl[m] << (8 * c);
         }
+      };
+      uint32_t ra[32];
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32_start(taddr + 32 * c, ra);
+        tmem_wait32(ra);
+        chunk(ra, c);
       }
       if (in_cache && p >= g.S) {
         const int64_t irow = bh * g.ncap + (p - g.S);
@@ -416,6 +463,22 @@ bool encode_rows_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t c
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_code_rows(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t rowb, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rows == 0) return false;
+  const CUtensorMapSwizzle sw = rowb == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
+                                : rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_128B;
+  if (rowb != 32 && rowb != 64 && rowb != 128) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(rowb), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(rowb)};
+  const cuuint32_t box[2] = {rowb, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 bool make_rows_map(CUtensorMap* m, const void* ptr, int64_t rows) {
@@ -436,11 +499,15 @@ int launch_append_tc(const AppendArgs& a, cudaStream_t stream) {
       return OSCAR_ERR_LAUNCH;
     attr_set[dev] = 1;
   }
+  if (a.rows >= (int64_t(1) << 31)) return OSCAR_ERR_LAUNCH;  // 32-bit row indices and TMA coordinates
   CUtensorMap mk, mv;
   if (!make_rows_map(&mk, a.k_new, a.rows) || !make_rows_map(&mv, a.v_new, a.rows)) return OSCAR_ERR_LAUNCH;
   const int64_t ntiles = (a.rows + kTileRows - 1) / kTileRows;
   const int per_role = int(std::min<int64_t>(ntiles, std::max(1, sms[dev] / 2)));
-  kv_append_tc_kernel<<<dim3(per_role, 2, 1), kThreadsTc, kSmemTc, stream>>>(mk, mv, a);
+  AppendArgs ka = a;
+  ka.div_hkv = fastdiv_make(uint32_t(a.g.Hkv));
+  ka.div_n_new = fastdiv_make(uint32_t(a.n_new));
+  kv_append_tc_kernel<<<dim3(per_role, 2, 1), kThreadsTc, kSmemTc, stream>>>(mk, mv, ka);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
 }
 
