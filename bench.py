@@ -554,7 +554,8 @@ def ours(args):
                      # the committed counters were taken with calibrated rotations, INT2 V, uniform levels
                      "traffic": None if (args.v_bf16 or args.hadamard or args.lloyd_max)
                      else split_kernel_traffic(args.workload),
-                     "kernel": "split_kernel (attn_decode)",
+                     "kernel": "split_kernel (attn_decode)" if D == 128 or w.absorb_v or args.hadamard
+                     else "split_kernel + unrot_kernel (attn_decode)",
                      "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
                      # kernel_ms comes from a second pass of the same steps with events
                      # recorded around each split launch; that pass's own step time and
@@ -563,7 +564,8 @@ def ours(args):
                      "algorithmic_bytes_per_launch": kv_bytes // L},
         "e2e": {"value": world * Bsz / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * L * K_,
+        # append, qrot, split (+ unrot at head_dim 256/512 with V un-rotated)
+        "gpu_launches": (3 + int(D >= 256 and not w.absorb_v and not args.hadamard)) * L * K_,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "dev_status": st,

@@ -239,9 +239,11 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  *              explicit num_splits must fit in full).
  * Launches two kernels on `stream`: query rotation (which writes q' as the
  * split kernel's MMA fragments), then split attention whose last CTA per
- * (sequence, KV head) merges that unit's partials and un-rotates V.
- * Both use programmatic dependent launch; the first waits for all prior work
- * on the stream before reading q.  Concurrent calls must not share a workspace.
+ * (sequence, KV head) merges that unit's partials and un-rotates V; at
+ * head_dim 256 and 512 with V neither absorbed nor Hadamard-rotated a third
+ * kernel applies R_V^T to every merged output instead.  All use programmatic
+ * dependent launch; the first waits for all prior work on the stream before
+ * reading q.  Concurrent calls must not share a workspace.
  */
 int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, const void* q,
                 const int32_t* seq_lens, int32_t seq_len_hint, const float* R_K, const float* R_V,
@@ -265,7 +267,8 @@ int attn_decode(const oscar_kv_config* cfg, const void* cache, int32_t layer, co
  * made (they are read before the append completes); q may still be produced
  * by the kernel preceding the call.  Arguments, errors and the workspace are
  * those of kv_append and attn_decode; everything is validated before
- * anything is launched.  Launches three kernels on `stream`.
+ * anything is launched.  Launches the append kernel and attn_decode's kernels
+ * on `stream`.
  */
 int decode_step(const oscar_kv_config* cfg, void* cache, int32_t layer, const void* k_new, const void* v_new,
                 const int32_t* start_pos, int32_t n_new, const void* q, const int32_t* seq_lens,

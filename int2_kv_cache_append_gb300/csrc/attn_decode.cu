@@ -6,7 +6,7 @@
 // card (Folders: the rotation applies to Q/K and V); "OSCAR-RotationZoo" (How
 // to use: V rotation absorbed into the output).
 //
-// Two kernels per call:
+// Two kernels per call (three at head_dim 256/512 with V un-rotated, see unrot):
 //   qrot   q' = q R_K * sm_scale * log2(e) (float32; with the in-quant
 //          Hadamard a warp transform instead of R_K) written as the split
 //          kernel's ready mma fragments, with per-group sums of q'; zeroes the
@@ -40,6 +40,9 @@
 //          by log-sum-exp in one online pass, applies o = o' R_V^T (o' H with
 //          the in-quant Hadamard; skipped when absorbed) and stores the
 //          bf16/fp32 output and lse.
+//   unrot  head_dim 256 / 512, V un-rotated by R_V: o = o' R_V^T for every
+//          (sequence, query head) at once, from the merged o' the split
+//          kernel leaves in workspace slot 0.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -1572,36 +1575,14 @@ __global__ void __launch_bounds__(kThreads, 2)
               if (i < Gh) store(i, r, res[i]);
           }
         } else {
-          // head_dim 256 / 512 (R_V is never prefetched): rows of R_V from L2,
-          // warp w takes rows w, w + 4, ...; lane l reads columns 4l .. 4l + 3
-          // (+ 128 per step), so every load is coalesced
-#pragma unroll 4
-          for (int r = warp; r < D; r += kNCW) {
-            const float4* rv4 = reinterpret_cast<const float4*>(a.R_V + int64_t(r) * D);
-            float res[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) res[i] = 0.f;
-#pragma unroll
-            for (int j4 = lane; j4 < D / 4; j4 += 32) {
-              const float4 rv = __ldg(rv4 + j4);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (i < Gh) {
-                  const float4 ov = reinterpret_cast<const float4*>(ob + i * D)[j4];
-                  res[i] = fmaf(rv.x, ov.x, fmaf(rv.y, ov.y, fmaf(rv.z, ov.z, fmaf(rv.w, ov.w, res[i]))));
-                }
-              }
-            }
-            float mine = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (i < Gh) {
-#pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) res[i] += __shfl_xor_sync(0xffffffffu, res[i], o2);
-                if (lane == i) mine = res[i];
-              }
-            }
-            if (lane < Gh) store(lane, r, mine);
+          // head_dim 256 / 512: o' goes to the unit's workspace slot 0 (every
+          // slot has been read) and unrot_kernel applies R_V^T for all units
+          // at once, spread over the GPU (here one CTA per unit would read all
+          // of R_V through L2, one row round trip at a time)
+          for (int e = threadIdx.x; e < Gh * (D / 4); e += kThreads) {
+            const int i = e / (D / 4), j4 = e % (D / 4);
+            const int64_t si = (int64_t(b) * g.Hq + head0 + i) * a.ns;
+            __stcg(reinterpret_cast<float4*>(a.ws_acc + si * D) + j4, reinterpret_cast<const float4*>(ob + i * D)[j4]);
           }
         }
         if (threadIdx.x < Gh && a.lse) {
@@ -1632,6 +1613,77 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---------------------------------------------------------------------------
 // host launch
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// o = o' R_V^T at head_dim 256 / 512 (V not absorbed, no in-quant Hadamard):
+// the split kernel leaves the merged o' of every (sequence, query head) in its
+// workspace slot 0.  CTA (x, y) holds rows [16 x, 16 x + 16) of R_V in shared
+// memory; each warp takes one (sequence, head) vector at a time, lane l
+// multiplies its float4 chunks l, l + 32, ... of o' with the 16 rows, and a
+// halving butterfly leaves the sum of output r0 + (l >> 1) in lanes l.
+// Empty sequences keep the output qrot wrote.
+// ---------------------------------------------------------------------------
+constexpr int kUnrotRows = 16;
+// unrot_kernel runs after the split kernel (the decode's fourth launch)
+inline bool unrot_launched(int D, const DecodeArgs& a) { return D >= 256 && !a.absorb_v && !a.hadamard; }
+constexpr int kUnrotThreads = 256;
+
+template <int W, int SH>
+__device__ __forceinline__ void butterfly_half(float (&res)[kUnrotRows], int lane) {
+  const bool up = (lane & SH) != 0;
+#pragma unroll
+  for (int i = 0; i < W; ++i) {
+    const float send = up ? res[i] : res[i + W];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, SH);
+    res[i] = (up ? res[i + W] : res[i]) + recv;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kUnrotThreads, 1) unrot_kernel(const DecodeArgs a) {
+  __shared__ __align__(16) float rv[kUnrotRows][D];
+  pdl_wait();  // the split kernel's merges are complete
+  const int r0 = blockIdx.x * kUnrotRows;
+  const float4* src = reinterpret_cast<const float4*>(a.R_V + int64_t(r0) * D);
+  for (int e = threadIdx.x; e < kUnrotRows * D / 4; e += kUnrotThreads)
+    reinterpret_cast<float4*>(&rv[0][0])[e] = __ldg(src + e);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = a.g.B * a.g.Hq;
+  constexpr int C4 = D / 128;  // float4 chunks of o' per lane
+  for (int vi = blockIdx.y * (kUnrotThreads / 32) + warp; vi < nvec; vi += gridDim.y * (kUnrotThreads / 32)) {
+    if (clamp_seq_len(a, vi / a.g.Hq) == 0) continue;
+    const float4* op = reinterpret_cast<const float4*>(a.ws_acc + int64_t(vi) * a.ns * D);
+    float4 o[C4];
+#pragma unroll
+    for (int k = 0; k < C4; ++k) o[k] = __ldcg(op + lane + 32 * k);
+    float res[kUnrotRows];
+#pragma unroll
+    for (int rr = 0; rr < kUnrotRows; ++rr) {
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < C4; ++k) {
+        const float4 r4 = reinterpret_cast<const float4*>(&rv[rr][0])[lane + 32 * k];
+        acc = fmaf(r4.x, o[k].x, fmaf(r4.y, o[k].y, fmaf(r4.z, o[k].z, fmaf(r4.w, o[k].w, acc))));
+      }
+      res[rr] = acc;
+    }
+    // halving butterfly: after the step over lane bit s, a lane keeps the half
+    // of its values that its bit s selects, summed with its partner's
+    butterfly_half<8, 16>(res, lane);
+    butterfly_half<4, 8>(res, lane);
+    butterfly_half<2, 4>(res, lane);
+    butterfly_half<1, 2>(res, lane);
+    res[0] += __shfl_xor_sync(0xffffffffu, res[0], 1);
+    if ((lane & 1) == 0) {
+      const int64_t oi = int64_t(vi) * D + r0 + (lane >> 1);
+      if (a.out_fp32)
+        static_cast<float*>(a.out)[oi] = res[0];
+      else
+        static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(res[0]);
+    }
+  }
+}
+
 template <typename K, typename... Args>
 cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args&... args) {
   cudaLaunchConfig_t cfg = {};
@@ -1727,6 +1779,13 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   if (launch_pdl(split_kernel<D, NQT, VB, LM>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
                  maps[2], maps[3], cmaps[0], cmaps[1], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
+  if (unrot_launched(D, a)) {
+    const int nvec = g.B * g.Hq, wpc = kUnrotThreads / 32;
+    const int gy = std::max(1, std::min((nvec + wpc - 1) / wpc, 8));
+    if (launch_pdl(unrot_kernel<D>, dim3(D / kUnrotRows, unsigned(gy)), dim3(kUnrotThreads), 0, stream, a) !=
+        cudaSuccess)
+      return OSCAR_ERR_LAUNCH;
+  }
   if (prof && cudaEventRecord(g_prof_stop, stream) != cudaSuccess) return OSCAR_ERR_LAUNCH;
   return OSCAR_OK;
 }

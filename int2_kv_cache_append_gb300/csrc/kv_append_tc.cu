@@ -10,11 +10,15 @@
 //     The pieces are written to shared memory transposed (N x K, K-major) in the
 //     128-byte swizzled layout the MMA descriptors expect.
 //   * A tiles of 128 rows are fetched with TMA tensor loads (cp.async.bulk.tensor,
-//     SWIZZLE_128B) into a 4-stage ring: up to three tiles (96 KB) in flight per
-//     SM, what a 1-2 us loaded DRAM latency asks for at the full HBM rate.
-//   * One thread of the producer warp issues 3 x 8 tcgen05.mma (M128 N128 K16,
+//     SWIZZLE_128B) into a 4-stage ring by a loader warp of their own, which
+//     refills a stage as soon as the MMAs reading it complete; it starts while
+//     the other warps build R's pieces.
+//   * One thread of the MMA warp issues 3 x 8 tcgen05.mma (M128 N128 K16,
 //     kind::f16, bf16 operands, fp32 accumulate) per tile into one of four TMEM
-//     accumulators and signals completion with tcgen05.commit.
+//     accumulators and signals completion with tcgen05.commit.  It waits only
+//     for its tile's data and accumulator: the tensor pipe, ~1 us per tile for
+//     the three pieces, is what bounds this kernel, so no other wait may sit
+//     between two tiles' MMAs.
 //   * Sixteen epilogue warps in four groups (tile 4k + g goes to group g, with
 //     accumulator g; four warps per SM sub-partition hide the codec's latency)
 //     read their 32 TMEM lanes (one row per thread) with tcgen05.ld and run the
@@ -38,7 +42,10 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTileRows = 128;
 constexpr int kEpiWarps = 16;                // four groups of four: tiles 4k + group
-constexpr int kThreadsTc = (kEpiWarps + 1) * 32;
+constexpr int kMmaWarp = kEpiWarps;          // one thread issues the MMAs
+constexpr int kLoadWarp = kEpiWarps + 1;     // one thread issues the TMA loads
+constexpr int kThreadsTc = (kEpiWarps + 2) * 32;
+constexpr int kComputeThreads = (kEpiWarps + 1) * 32;  // every warp but the loader
 constexpr uint32_t kKBlockBytes = kTileRows * 128;  // 128 rows x 64 bf16 (128 B), swizzled
 constexpr uint32_t kOperandBytes = 2 * kKBlockBytes; // K = 128 -> two K-blocks
 constexpr uint32_t kOffB = 0;                          // 3 pieces of R^T
@@ -161,12 +168,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  tc_fence_before();
+  __syncthreads();  // barriers initialised: the loader starts while the others build B
+
+  // this CTA's tiles j = 0, 1, ...: tile blockIdx.x + j * gridDim.x, A stage j % kStagesA
+  const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  if (warp == kLoadWarp) {
+    // ------------------------------ TMA loader -------------------------------
+    // Refills a stage as soon as the MMAs of the tile in it have completed, up
+    // to kStagesA tiles ahead of the MMA issuer.
+    if (lane == 0) {
+      int loaded = 0;
+      bool ok = true;
+      for (int j = 0; j < my_tiles; ++j) {
+        const int s = j % kStagesA;
+        if (j >= kStagesA) ok = mbar_wait(empty_a(s), ((j / kStagesA) & 1) ^ 1);
+        if (!ok || *((volatile int*)&abort_flag)) break;
+        const int64_t tile = blockIdx.x + int64_t(j) * gridDim.x;
+        mbar_arrive_expect_tx(full_a(s), kOperandBytes);
+        const uint32_t dst = sA + s * kOperandBytes;
+        tma_load_2d(dst, tmap, 0, int(tile * kTileRows), full_a(s));
+        tma_load_2d(dst + kKBlockBytes, tmap, 64, int(tile * kTileRows), full_a(s));
+        ++loaded;
+      }
+      if (!ok) {
+        abort_flag = 1;
+        status_or(a.status, OSCAR_DEV_TIMEOUT);
+      }
+      // every copy issued lands before the CTA exits (tiles before the last
+      // kStagesA were consumed: their stages were refilled)
+      for (int j = (loaded > kStagesA ? loaded - kStagesA : 0); j < loaded; ++j)
+        (void)mbar_wait(full_a(j % kStagesA), (j / kStagesA) & 1);
+    }
+    return;  // the barriers below are named ones that leave the loader out
+  }
   // B operand: piece p holds B_p[n][k] with R[k][n] = B_0 + B_1 + B_2 (bf16).
   // Each thread builds one 16-byte chunk of each piece: 8 consecutive k of row
   // n.  Consecutive threads take consecutive n, so every load of R is a
   // coalesced row segment and the chunk stores of a warp spread over all banks
   // (the 128-byte swizzle puts rows n and n + 1 .. n + 7 in different chunks).
-  for (int cidx = threadIdx.x; cidx < kD * (kD / 8); cidx += kThreadsTc) {
+  for (int cidx = threadIdx.x; cidx < kD * (kD / 8); cidx += kComputeThreads) {
     const int n = cidx % kD, k0 = (cidx / kD) * 8;
     uint32_t ph[4], pm[4], pl[4];
 #pragma unroll
@@ -183,37 +224,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     *reinterpret_cast<uint4*>(smem + kOffB + 1 * kOperandBytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
     *reinterpret_cast<uint4*>(smem + kOffB + 2 * kOperandBytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
   }
-  for (int i = threadIdx.x; i < a.g.B && i < kSposCache; i += kThreadsTc) spos[i] = a.start_pos[i];
+  for (int i = threadIdx.x; i < a.g.B && i < kSposCache; i += kComputeThreads) spos[i] = a.start_pos[i];
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // make generic smem writes visible to the MMA
   tc_fence_before();
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"r"(kComputeThreads) : "memory");  // B and spos ready (not the loader)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == kEpiWarps) {
-    // ------------------------- producer + MMA issuer -------------------------
+  if (warp == kMmaWarp) {
+    // ------------------------------ MMA issuer -------------------------------
     if (lane == 0) {
-      // this CTA's tiles j = 0, 1, ...: tile blockIdx.x + j * gridDim.x, A stage
-      // j % kStagesA.  The loads run kStagesA - 1 tiles ahead; the refill of a
-      // stage is issued right after the MMAs of the next tile, so the wait for
-      // the MMAs that release it never leaves the tensor pipe without work.
-      const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-      int loaded = 0;
-      auto load = [&](int j) -> bool {
-        const int s = j % kStagesA;
-        if (j >= kStagesA && !mbar_wait(empty_a(s), ((j / kStagesA) & 1) ^ 1)) return false;
-        const int64_t tile = blockIdx.x + int64_t(j) * gridDim.x;
-        mbar_arrive_expect_tx(full_a(s), kOperandBytes);
-        const uint32_t dst = sA + s * kOperandBytes;
-        tma_load_2d(dst, tmap, 0, int(tile * kTileRows), full_a(s));
-        tma_load_2d(dst + kKBlockBytes, tmap, 64, int(tile * kTileRows), full_a(s));
-        ++loaded;
-        return true;
-      };
       bool ok = true;
-      for (int j = 0; ok && j < kStagesA - 1 && j < my_tiles; ++j) ok = load(j);
       int it = 0;
-      for (; ok && it < my_tiles; ++it) {
+      for (; it < my_tiles; ++it) {
         const int s = it % kStagesA;  // A stage
         const uint32_t ph = (it / kStagesA) & 1;
         const int sa = it & 3;  // TMEM accumulator
@@ -236,15 +259,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         umma_commit(acc_full(sa));
         umma_commit(empty_a(s));
-        // refill the stage of tile it - 1 (its MMAs precede the ones just issued)
-        if (it + kStagesA - 1 < my_tiles) ok = load(it + kStagesA - 1);
       }
       if (!ok) {
         abort_flag = 1;
         status_or(a.status, OSCAR_DEV_TIMEOUT);
-        // loads issued for tiles not consumed (up to kStagesA - 1 ahead) must
-        // land before the CTA exits
-        for (int j = it; j < loaded; ++j) (void)mbar_wait(full_a(j % kStagesA), (j / kStagesA) & 1);
       }
       // drain: the last (up to four) commits must have landed before TMEM is freed
       for (int j = (it >= 4 ? it - 4 : 0); j < it; ++j) mbar_wait(acc_full(j & 3), (j >> 2) & 1);
@@ -424,10 +442,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"r"(kComputeThreads) : "memory");  // every MMA and TMEM load is done
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_slot), "r"(kTmemCols)
+                 : "memory");
   }
 }
 
