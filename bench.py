@@ -403,6 +403,7 @@ def ours(args):
              | (K.FLAG_V_BF16 if args.v_bf16 else 0) | (K.FLAG_LLOYD_MAX if args.lloyd_max else 0))
     cfg = K.KVConfig(L, Bsz, Hq, Hkv, D, w.sink, w.recent, T, w.k_clip, w.v_clip, flags)
     lay = K.layout_query(cfg)
+    decode_kernels = K.decode_kernels(cfg)
     stream = torch.cuda.current_stream()
 
     # ---- setup (untimed): rotations, cache pre-fill of T-1 tokens per sequence
@@ -554,8 +555,8 @@ def ours(args):
                      # the committed counters were taken with calibrated rotations, INT2 V, uniform levels
                      "traffic": None if (args.v_bf16 or args.hadamard or args.lloyd_max)
                      else split_kernel_traffic(args.workload),
-                     "kernel": "split_kernel (attn_decode)" if D == 128 or w.absorb_v or args.hadamard
-                     else "split_kernel + unrot_kernel (attn_decode)",
+                     "kernel": "split_kernel" + ("" if decode_kernels == 2 else " + unrot_kernel")
+                               + " (attn_decode)",
                      "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
                      # kernel_ms comes from a second pass of the same steps with events
                      # recorded around each split launch; that pass's own step time and
@@ -564,8 +565,8 @@ def ours(args):
                      "algorithmic_bytes_per_launch": kv_bytes // L},
         "e2e": {"value": world * Bsz / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        # append, qrot, split (+ unrot at head_dim 256/512 with V un-rotated)
-        "gpu_launches": (3 + int(D >= 256 and not w.absorb_v and not args.hadamard)) * L * K_,
+        # the append + attn_decode's kernels (qrot, split, and unrot where used)
+        "gpu_launches": (1 + decode_kernels) * L * K_,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "dev_status": st,

@@ -304,11 +304,23 @@ int attn_decode_static(const oscar_kv_config* cfg, const void* cache, int32_t la
  * While both events are non-NULL (cudaEvent_t passed as void*), every
  * attn_decode call made from the calling host thread records `split_start` on
  * its stream immediately before launching the split-attention kernel and
- * `split_stop` immediately after it, so that cudaEventElapsedTime gives that
- * kernel's device time.  Recording between kernels removes the launch overlap
+ * `split_stop` immediately after it and the un-rotation kernel that may
+ * follow it (see oscar_kv_decode_kernels), so that cudaEventElapsedTime gives
+ * the device time of the attention proper.  Recording between kernels removes the launch overlap
  * of that call.  Pass NULL, NULL to stop.  The setting is per host thread.
  */
 int oscar_kv_set_profile_events(void* split_start, void* split_stop);
+
+/*
+ * oscar_kv_decode_kernels — how many kernels one attn_decode call with this
+ * configuration launches (no counterpart on the pages; for launch accounting
+ * and graph planning): query rotation and split attention, plus an
+ * un-rotation kernel at head_dim 256 / 512 with V neither absorbed nor
+ * Hadamard-rotated.  decode_step launches one kernel more (the append).
+ * Needs no device.  Returns 2 or 3, or OSCAR_ERR_INVALID for an invalid
+ * configuration.
+ */
+int oscar_kv_decode_kernels(const oscar_kv_config* cfg);
 
 /*
  * oscar_kv_set_wait_test — test hook for the device-timeout path (no

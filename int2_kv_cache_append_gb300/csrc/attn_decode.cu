@@ -1641,12 +1641,24 @@ __device__ __forceinline__ void butterfly_half(float (&res)[kUnrotRows], int lan
 template <int D>
 __global__ void __launch_bounds__(kUnrotThreads, 1) unrot_kernel(const DecodeArgs a) {
   __shared__ __align__(16) float rv[kUnrotRows][D];
-  pdl_wait();  // the split kernel's merges are complete
+  __shared__ __align__(8) uint64_t rv_bar;
+  __shared__ int rv_ok;
   const int r0 = blockIdx.x * kUnrotRows;
-  const float4* src = reinterpret_cast<const float4*>(a.R_V + int64_t(r0) * D);
-  for (int e = threadIdx.x; e < kUnrotRows * D / 4; e += kUnrotThreads)
-    reinterpret_cast<float4*>(&rv[0][0])[e] = __ldg(src + e);
+  // R_V's rows arrive with one bulk copy, issued before the wait for the split
+  // kernel (they do not depend on it)
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&rv_bar), 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(smem_u32(&rv_bar), kUnrotRows * D * 4);
+    bulk_g2s(smem_u32(&rv[0][0]), a.R_V + int64_t(r0) * D, kUnrotRows * D * 4, smem_u32(&rv_bar));
+  }
+  pdl_wait();  // the split kernel's merges are complete
+  if (threadIdx.x == 0) {
+    rv_ok = mbar_wait(smem_u32(&rv_bar), 0, a.wait_ns);
+    if (!rv_ok) status_or(a.status, OSCAR_DEV_TIMEOUT);
+  }
   __syncthreads();
+  if (!rv_ok) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = a.g.B * a.g.Hq;
   constexpr int C4 = D / 128;  // float4 chunks of o' per lane
@@ -1795,6 +1807,10 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
 thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 thread_local uint64_t g_test_wait_ns = 0;
 thread_local int g_test_wait_poison = 0;
+
+int decode_kernel_count(const Geom& g, bool absorb_v, bool hadamard) {
+  return 2 + (g.D >= 256 && !absorb_v && !hadamard ? 1 : 0);
+}
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns) {
   const uint64_t bq = uint64_t(g.B) * g.Hq, units = uint64_t(g.B) * g.Hkv;

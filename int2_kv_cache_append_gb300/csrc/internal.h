@@ -58,6 +58,8 @@ struct DecodeArgs {
 };
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns);
+// kernels one attn_decode launches
+int decode_kernel_count(const Geom& g, bool absorb_v, bool hadamard);
 // cache geometry of a validated configuration
 Geom geom_of(const oscar_kv_config* c);
 // optional events recorded around the split kernel (per host thread)

@@ -243,6 +243,13 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop) {
   return OSCAR_OK;
 }
 
+int oscar_kv_decode_kernels(const oscar_kv_config* cfg) {
+  const int v = validate(cfg);
+  if (v != OSCAR_OK) return v;
+  return oscar::decode_kernel_count(make_geom(cfg), (cfg->flags & OSCAR_FLAG_ABSORB_V) != 0,
+                                    (cfg->flags & OSCAR_FLAG_HADAMARD) != 0);
+}
+
 int oscar_kv_set_wait_test(uint64_t wait_ns, int32_t extra_bytes) {
   if (wait_ns > 10000000000ull || extra_bytes < 0 || extra_bytes > (1 << 20)) return OSCAR_ERR_INVALID;
   oscar::g_test_wait_ns = wait_ns;

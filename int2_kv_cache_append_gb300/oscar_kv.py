@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "WORKSPACE", -4: "LA
 
 # every symbol include/oscar_kv.h declares
 EXPORTS = ("kv_layout_query", "kv_append", "attn_decode", "decode_step", "attn_decode_static",
-           "oscar_kv_set_profile_events", "oscar_kv_set_wait_test", "oscar_calibrate_workspace_query",
+           "oscar_kv_set_profile_events", "oscar_kv_set_wait_test", "oscar_kv_decode_kernels",
+           "oscar_calibrate_workspace_query",
            "oscar_calibrate_rk",
            "oscar_calibrate_rv_workspace_query", "oscar_calibrate_rv")
 STATIC_SCRATCH_BYTES = 16 << 20
@@ -108,6 +109,8 @@ def lib():
         L.oscar_kv_set_profile_events.restype = ctypes.c_int
         L.oscar_kv_set_wait_test.argtypes = [ctypes.c_uint64, ctypes.c_int32]
         L.oscar_kv_set_wait_test.restype = ctypes.c_int
+        L.oscar_kv_decode_kernels.argtypes = [ctypes.POINTER(_Config)]
+        L.oscar_kv_decode_kernels.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -272,6 +275,14 @@ def set_profile_events(start=None, stop=None) -> None:
     """Record torch.cuda.Event pair around the split kernel of later attn_decode calls (None, None stops)."""
     lib().oscar_kv_set_profile_events(None if start is None else ctypes.c_void_p(start.cuda_event),
                                       None if stop is None else ctypes.c_void_p(stop.cuda_event))
+
+
+def decode_kernels(cfg: KVConfig) -> int:
+    """Kernels one attn_decode call launches (see oscar_kv_decode_kernels)."""
+    rc = lib().oscar_kv_decode_kernels(ctypes.byref(cfg.c()))
+    if rc < 0:
+        raise OscarError("oscar_kv_decode_kernels", rc)
+    return rc
 
 
 def set_wait_test(wait_ns: int = 0, extra_bytes: int = 0) -> None:

@@ -86,3 +86,15 @@ def test_calibration_refuses_mismatched_tensors():
     with pytest.raises(ValueError, match="oscar_kv"):
         K.calibrate_rv(torch.zeros(10, 128), torch.zeros(5, 128), torch.zeros(5, 128),
                        torch.zeros(128, 128, dtype=torch.float64), ws)
+
+
+def test_decode_kernel_count():
+    # query rotation + split attention, and the un-rotation kernel only at
+    # head_dim 256 / 512 with V neither absorbed nor Hadamard-rotated
+    assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 128, 4, 8, 64)) == 2
+    assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 256, 4, 8, 64)) == 3
+    assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 512, 4, 8, 64)) == 3
+    assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 512, 4, 8, 64, flags=K.FLAG_ABSORB_V)) == 2
+    assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 512, 4, 8, 64, flags=K.FLAG_HADAMARD)) == 2
+    with pytest.raises(K.OscarError):
+        K.decode_kernels(K.KVConfig(1, 2, 8, 3, 128, 4, 8, 64))  # 8 query heads over 3 KV heads

@@ -236,3 +236,18 @@ def test_decode_many_units_per_cta():
         ref, ref_lse = O.decode(oc, ocache, 0, q[b:b + 1].float().cpu().numpy(), [int(lens[b])], RK, RV)
         assert np.abs(o0[b] - ref[0]).max() <= 5e-3 and rel_l2(o0[b], ref[0]) <= 2e-4, b
         assert np.max(np.abs(l0[b] - ref_lse[0]) - 1e-5 * np.abs(ref_lse[0])) <= 1e-4, b
+
+
+@pytest.mark.parametrize("D,flags", [(128, 0), (128, K.FLAG_ABSORB_V), (256, 0), (512, 0), (512, K.FLAG_ABSORB_V)])
+@pytest.mark.parametrize("splits", [4, 16])
+def test_decode_merge_paths(D, flags, splits):
+    # With num_splits = n every (sequence, KV head) is shared by n CTAs whose
+    # last merges the n partials; at head_dim 256 / 512 with V un-rotated it
+    # leaves o' in workspace slot 0 and unrot_kernel applies R_V^T.  The result
+    # must meet the oracle, and the kernel count must say whether unrot ran.
+    c = O.Config(1, 2, 8, 2, D, 16, 64, 2600, 0.96, 0.92, flags=flags)
+    lens = [2500, 1300]
+    cache, q, RK, RV = _build(c, lens, seed=D + splits + flags)
+    _check(c, cache, q, lens, RK, RV, num_splits=splits)
+    from tests.gpu_helpers import kcfg
+    assert K.decode_kernels(kcfg(c)) == 2 + (D >= 256 and not flags & K.FLAG_ABSORB_V)

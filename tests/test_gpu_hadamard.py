@@ -149,3 +149,26 @@ def test_hadamard_decode_step_equals_append_then_decode(case):
     assert np.array_equal(c0, c1)
     assert np.isfinite(o0).all()
     assert_same_decode(o0, o1, l0, l1)
+
+
+@pytest.mark.parametrize("D", [128, 512])
+@pytest.mark.parametrize("splits", [4, 16])
+def test_hadamard_decode_merge_paths(D, splits):
+    # the last CTA's merge applies H whether 4 or 16 CTAs share a unit
+    B, Hq, Hkv, T = 2, 8, 2, 1900
+    c = O.Config(1, B, Hq, Hkv, D, 16, 64, T, 0.96, 0.92, flags=K.FLAG_HADAMARD)
+    rng = np.random.default_rng(D + splits)
+    ch = rng.choice(D, max(1, round(0.02 * D)), replace=False)
+    k = S.to_bf16_values(S.activations(rng, (B, T, Hkv, D), ch))
+    v = S.to_bf16_values(S.activations(rng, (B, T, Hkv, D), ch))
+    q = S.to_bf16_values(S.activations(rng, (B, Hq, D), ch))
+    lens = [T, 1100]
+    cache = O.new_cache(c)
+    O.append(c, cache, 0, k, v, [0] * B, None, None)
+    ref, ref_lse = O.decode(c, cache, 0, q, lens, None, None)
+    gc = torch.from_numpy(cache).cuda()
+    o32, lse32 = gpu_decode(c, gc, 0, q, lens, None, None, out_fp32=True, num_splits=splits)
+    r32, m32 = rel_l2(o32, ref), float(np.abs(o32 - ref).max())
+    dl = float(np.max(np.abs(lse32 - ref_lse) - 1e-5 * np.abs(ref_lse)))
+    assert m32 <= 5e-3 and r32 <= 2e-4, f"fp32 max-abs {m32} rel-L2 {r32}"
+    assert dl <= 1e-4, f"lse {dl}"
