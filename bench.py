@@ -119,24 +119,29 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# DRAM bytes (read + write) per split-kernel launch from ncu captures of the
-# default mode (profiles/split_kernel_<workload>.md), with the attn_decode.cu
-# source they were taken on: reported only while the source is unchanged.
-# The 36-layer workload was captured with --layers 1; every layer's launch
-# reads the same bytes.
+# DRAM bytes (read + write) per launch of the dominant kernel from ncu captures
+# (profiles/<kernel>_<workload>.md), with the source file and its hash at
+# capture: reported only while that source is unchanged.  The split-kernel
+# entries are for the default mode; the 36-layer workload was captured with
+# --layers 1 (every layer's launch reads the same bytes); at head_dim 512 the
+# figure is the split kernel's alone (unrot_kernel reads R_V and the merged
+# outputs, a few MB from L2).
 MEASURED_TRAFFIC = {
-    "qwen3-8b-36L": ("019231160ba45cdf", 647623168),
-    "hd512": ("019231160ba45cdf", 754315264),
-    "qwen3-32b-decode": ("019231160ba45cdf", 78270208),
+    "qwen3-8b-36L": ("attn_decode.cu", "a66eff6947186d2c", 647630080),
+    "hd512": ("attn_decode.cu", "a66eff6947186d2c", 753272832),
+    "qwen3-32b-decode": ("attn_decode.cu", "a66eff6947186d2c", 78338560),
+    "qwen3-32b-append": ("kv_append_tc.cu", "da55696891866101", 143004928),
 }
 
 
-def split_kernel_traffic(workload: str):
-    """ncu DRAM bytes per split-kernel launch, or None if not measured on the current source."""
-    src = os.path.join(ROOT, "int2_kv_cache_append_gb300", "csrc", "attn_decode.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+def measured_traffic(workload: str):
+    """ncu DRAM bytes per launch of the dominant kernel, or None if not measured on the current source."""
     entry = MEASURED_TRAFFIC.get(workload)
-    return entry[1] if entry and entry[0] == sha else None
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "int2_kv_cache_append_gb300", "csrc", entry[0])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return entry[2] if entry[1] == sha else None
 
 
 class ClockSampler:
@@ -554,7 +559,7 @@ def ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      # the committed counters were taken with calibrated rotations, INT2 V, uniform levels
                      "traffic": None if (args.v_bf16 or args.hadamard or args.lloyd_max)
-                     else split_kernel_traffic(args.workload),
+                     else measured_traffic(args.workload),
                      "kernel": "split_kernel" + ("" if decode_kernels == 2 else " + unrot_kernel")
                                + " (attn_decode)",
                      "kernel_ms": split_avg_ms, "peak_kind": peak_kind,
@@ -672,7 +677,8 @@ def ours_append(args):
         "config": {"workload": workload_desc(w) + f" append{n}", "l2": "flushed between steps (512 MiB write)"},
         "roofline": {"bound": "hbm" if gbs / peaks["hbm_gbs"] >= tfs / peaks["bf16_tflops"] else "tensor",
                      "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                     "traffic": None, "kernel": "kv_append_tc_kernel",
+                     "traffic": measured_traffic(args.workload) if args.workload == "qwen3-32b-append" else None,
+                     "kernel": "kv_append_tc_kernel",
                      "tensor_tflops_algorithmic": tfs, "tensor_frac_algorithmic": tfs / peaks["bf16_tflops"],
                      "tensor_frac_issued_3piece": 3 * tfs / peaks["bf16_tflops"],
                      "algorithmic_bytes_per_launch": hbm_bytes, "algorithmic_flops_per_launch": flops},
