@@ -10,7 +10,7 @@
 // Two CUDA-core kernels (the tensor-core kernel for large head_dim-128 bf16
 // appends is in kv_append_tc.cu):
 //
-// kv_append_kernel, tiled: one CTA of 128 threads handles RPC = 128*128/D rows
+// kv_append_kernel, tiled: one CTA of 128 threads handles RPC = 64*128/D rows
 // of one role (K or V):
 //   1. stage the input rows in shared memory as float32;
 //   2. rotate: each row's D outputs are split over 128/RPC threads, each
@@ -41,7 +41,9 @@ constexpr int64_t kSmallAppendRows = 1024;
 
 template <int D>
 struct AppendCfg {
-  static constexpr int RPC = kAppendThreads * 128 / D;  // rows per CTA
+  // rows per CTA: 64 KB of shared memory for inputs and rotated rows, so that
+  // three CTAs share an SM (the rotation is fp32 FMA work that needs the warps)
+  static constexpr int RPC = kAppendThreads * 64 / D;
   static constexpr int TPR = kAppendThreads / RPC;      // threads per row while rotating
   static constexpr int LD = D + 1;                      // padded smem row (conflict-free)
   static constexpr int SMEM = 2 * RPC * LD * 4;
@@ -245,6 +247,9 @@ template <int D, int RPC>
 struct RowsCfg {
   static constexpr int CH_ROWS = (65536 / (D * 4)) < D ? 65536 / (D * 4) : D;  // rows of R per chunk
   static constexpr int NCH = D / CH_ROWS;
+  // two stages: deeper staging (six 32 KB chunks, one CTA per SM) made the
+  // head_dim-512 decode step slower, its CTAs keeping the attention kernel,
+  // launched early, off their SMs
   static constexpr int NSTG = NCH > 1 ? 2 : 1;
   static constexpr uint32_t CH_BYTES = uint32_t(CH_ROWS) * D * 4;
   static constexpr int CPT = D / 128;  // output columns per thread
@@ -257,6 +262,7 @@ struct RowsCfg {
   static constexpr int LPW = 32 / NW;          // lanes per word
   static constexpr int SPL = 16 / LPW;         // 2-bit slots per lane
   static_assert(RPC % 4 == 0, "rows per CTA must be a multiple of the warp count");
+  static_assert(SMEM <= 227 * 1024, "dynamic shared memory of one CTA");
 };
 
 // Steps 1 and 2 with a rotation matrix R: stream R into shared memory, stage
