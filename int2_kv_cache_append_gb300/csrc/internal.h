@@ -72,6 +72,9 @@ int launch_append_tc(const AppendArgs& a, cudaStream_t stream);  // D = 128, bf1
 // 2-D tiled TMA map of a row-major bf16 matrix [rows][cols], 128-byte swizzle
 bool encode_rows_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t cols, uint32_t box_cols,
                       uint32_t box_rows);
+// 2-D tiled TMA map of a row-major float32 matrix [rows][cols], no swizzle
+bool encode_f32_tiles(CUtensorMap* m, const float* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                      uint32_t box_rows);
 // 2-D tiled TMA map of INT2 code rows [rows][rowb] (uint8; rowb = 32, 64 or
 // 128), box [box_rows][rowb], swizzled by the row size: 16-byte chunk c of
 // row t lands at chunk c ^ ((t * rowb / 128) mod (rowb / 16))

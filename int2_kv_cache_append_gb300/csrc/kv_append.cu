@@ -507,6 +507,292 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
   }
 }
 
+// ---------------------------------------------------------------------------
+// Row-parallel append at head_dim 256 / 512, sliced by quant group.  A CTA of
+// the row-parallel kernel above streams all of R through shared memory (1 MB
+// at head_dim 512) for a handful of rows, so a decode step's append waits on
+// that stream.  Here a thread-block cluster of D/128 CTAs shares RPC rows:
+// CTA q computes output channels [128 q, 128 q + 128) — one quant group — and
+// streams only that column slice of R (TMA tensor loads of 64 x 128 fp32
+// boxes, 32 KB each).  The row's max |y| (the clip threshold) is the one value
+// the group needs from the others: each CTA posts its slice's maximum in
+// shared memory and reads the others' through distributed shared memory
+// between two cluster barriers.  The rotated values are the same fp32 sums
+// in the same order as in the kernels above and the codec takes the same
+// operations, so the bytes written are identical.  Every CTA reaches both
+// cluster barriers, also after a timed-out copy.
+// ---------------------------------------------------------------------------
+template <int D, int RPC>
+struct SliceCfg {
+  static constexpr int SL = D / kGroup;        // CTAs per cluster
+  static constexpr int CH_ROWS = 64;           // rows of R's slice per chunk
+  static constexpr int NCH = D / CH_ROWS;
+  static constexpr int NSTG = 2;
+  static constexpr uint32_t CH_BYTES = uint32_t(CH_ROWS) * kGroup * 4;
+  static constexpr uint32_t OFF_X = NSTG * CH_BYTES;                  // [D][RPC] inputs, transposed
+  static constexpr uint32_t OFF_Y = OFF_X + uint32_t(D) * RPC * 4;     // [RPC][128] rotated slice
+  static constexpr uint32_t OFF_M = OFF_Y + uint32_t(RPC) * kGroup * 4;  // [RPC] slice max |y|, [RPC] finite
+  static constexpr uint32_t OFF_BAR = (OFF_M + 2 * RPC * 4 + 7) & ~7u;
+  static constexpr uint32_t SMEM = OFF_BAR + 8 * NSTG;
+  static_assert(RPC % 4 == 0, "rows per CTA must be a multiple of the warp count");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <int D, int RPC>
+__global__ void __launch_bounds__(kAppendThreads)
+    kv_append_slices_kernel(const __grid_constant__ CUtensorMap tmRK, const __grid_constant__ CUtensorMap tmRV,
+                            const AppendArgs a) {
+  using C = SliceCfg<D, RPC>;
+  extern __shared__ __align__(128) unsigned char sm[];
+  float* Rs = reinterpret_cast<float*>(sm);                    // [NSTG][CH_ROWS][128]
+  float* xs = reinterpret_cast<float*>(sm + C::OFF_X);         // [D][RPC]
+  float* ys = reinterpret_cast<float*>(sm + C::OFF_Y);         // [RPC][128]
+  uint32_t* ms = reinterpret_cast<uint32_t*>(sm + C::OFF_M);   // [RPC] max |y| bits, [RPC] finite
+  const uint32_t bar0 = smem_u32(sm + C::OFF_BAR);
+
+  pdl_trigger();
+  const int role = blockIdx.y;
+  const int q = int(cluster_rank());                  // quant group of this CTA
+  const int64_t row0 = int64_t(blockIdx.x / C::SL) * RPC;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const CUtensorMap* tmR = role ? &tmRV : &tmRK;
+  const int col0 = q * kGroup;
+
+  // 1. R's column slice, one 64-row box per chunk (thread 0)
+  auto issue_chunk = [&](int ch, int s) {
+    mbar_arrive_expect_tx(bar0 + 8 * s, C::CH_BYTES);
+    tma_load_2d(smem_u32(Rs) + s * C::CH_BYTES, tmR, col0, ch * C::CH_ROWS, bar0 + 8 * s);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < C::NSTG; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int s = 0; s < C::NSTG && s < C::NCH; ++s) issue_chunk(s, s);
+  // inputs, 8 channels per load, stored transposed; rows past the end are zero
+  for (int idx = tid; idx < RPC * (D / 8); idx += kAppendThreads) {
+    const int r = idx / (D / 8), i0 = (idx % (D / 8)) * 8;
+    const int64_t row = row0 + r;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+    if (row < a.rows) {
+      if (a.in_fp32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(role ? a.v_new : a.k_new) +
+                                                            row * D + i0);
+        const float4 u0 = src[0], u1 = src[1];
+        v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
+        v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
+      } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(role ? a.v_new : a.k_new) + row * D + i0);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] = __uint_as_float(w[e] << 16);
+          v[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xs[(i0 + e) * RPC + r] = v[e];
+  }
+  __syncthreads();
+
+  // 2. column col0 + tid of every row, fp32 FMAs in increasing input channel
+  float acc[RPC];
+#pragma unroll
+  for (int r = 0; r < RPC; ++r) acc[r] = 0.f;
+  bool ok = true;
+  int ch = 0;
+  for (; ch < C::NCH; ++ch) {
+    const int s = ch % C::NSTG;
+    const bool got = mbar_wait(bar0 + 8 * s, (ch / C::NSTG) & 1);
+    if (__syncthreads_or(!got)) {
+      ok = false;
+      break;
+    }
+    const float* Rc = Rs + size_t(s) * C::CH_ROWS * kGroup;
+#pragma unroll 4
+    for (int kk = 0; kk < C::CH_ROWS; ++kk) {
+      const int k = ch * C::CH_ROWS + kk;
+      float xv[RPC];
+#pragma unroll
+      for (int r4 = 0; r4 < RPC / 4; ++r4) {
+        const float4 x4 = *reinterpret_cast<const float4*>(xs + k * RPC + 4 * r4);
+        xv[4 * r4 + 0] = x4.x;
+        xv[4 * r4 + 1] = x4.y;
+        xv[4 * r4 + 2] = x4.z;
+        xv[4 * r4 + 3] = x4.w;
+      }
+      const float rv = Rc[kk * kGroup + tid];
+#pragma unroll
+      for (int r = 0; r < RPC; ++r) acc[r] = fmaf(xv[r], rv, acc[r]);
+    }
+    __syncthreads();  // every thread is done with stage s
+    if (tid == 0 && ch + C::NSTG < C::NCH) issue_chunk(ch + C::NSTG, s);
+  }
+  if (!ok && tid == 0) {
+    status_or(a.status, OSCAR_DEV_TIMEOUT);
+    for (int c2 = ch; c2 < C::NCH && c2 < ch + C::NSTG; ++c2)
+      (void)mbar_wait(bar0 + 8 * (c2 % C::NSTG), (c2 / C::NSTG) & 1);
+  }
+#pragma unroll
+  for (int r = 0; r < RPC; ++r) ys[r * kGroup + tid] = acc[r];
+  __syncthreads();
+
+  // 3. this slice's max |y| and finiteness per row, then the row's over the cluster
+  for (int r = warp; r < RPC; r += kAppendThreads / 32) {
+    float amax = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float v = ys[r * kGroup + lane + 32 * e];
+      finite &= isfinite(v);
+      amax = fmaxf(amax, fabsf(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    finite = __all_sync(0xffffffffu, finite);
+    if (lane == 0) {
+      ms[r] = __float_as_uint(amax);
+      ms[RPC + r] = finite ? 1u : 0u;
+    }
+  }
+  cluster_barrier();
+  float row_amax[RPC / 4];
+  bool row_finite[RPC / 4];
+#pragma unroll
+  for (int i = 0; i < RPC / 4; ++i) {
+    const int r = warp + 4 * i;
+    float m = 0.f;
+    bool f = true;
+    if (lane < C::SL) {
+      m = __uint_as_float(ld_cluster_u32(smem_u32(ms + r), uint32_t(lane)));
+      f = ld_cluster_u32(smem_u32(ms + RPC + r), uint32_t(lane)) != 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    row_amax[i] = m;
+    row_finite[i] = __all_sync(0xffffffffu, f);
+  }
+  cluster_barrier();  // no CTA leaves while another reads its shared memory
+  if (!ok) return;
+
+  // 4. codec of this CTA's group, one warp per row
+  const float ratio = role ? a.v_clip : a.k_clip;
+  const Geom& g = a.g;
+  uint8_t* role_base = a.layer_base + role * g.role_bytes;
+#pragma unroll
+  for (int i = 0; i < RPC / 4; ++i) {
+    const int r = warp + 4 * i;
+    const int64_t row = row0 + r;
+    if (row >= a.rows) break;
+    const float* y = ys + r * kGroup;
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = y[lane + 32 * e];
+    if (a.debug_rot) {
+      float* dst = a.debug_rot + (row * 2 + role) * D + col0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[lane + 32 * e] = v[e];
+    }
+    const int h = int(row % g.Hkv);
+    const int64_t bt = row / g.Hkv;
+    const int t = int(bt % a.n_new);
+    const int b = int(bt / a.n_new);
+    const int p = a.start_pos[b] + t;
+    const int newlen = a.start_pos[b] + a.n_new;
+    if (p < 0 || p >= g.cap) {
+      if (lane == 0) status_or(a.status, OSCAR_DEV_OVER_CAPACITY);
+      continue;
+    }
+    const int64_t bh = int64_t(b) * g.Hkv + h;
+    if (!row_finite[i] && lane == 0) status_or(a.status, OSCAR_DEV_NONFINITE);
+    const float tclip = __fmul_rn(ratio, row_amax[i]);
+
+    if (role == 1 && g.vb) {  // K-only INT2: the V row is kept BF16 at its position
+      __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(role_base + (bh * g.cap + p) * (2 * D)) + col0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dv[lane + 32 * e] = __float2bfloat16_rn(v[e]);
+      continue;
+    }
+    const bool to_sink = p < g.S;
+    const bool to_ring = g.W > 0 && p >= newlen - g.W;
+    if (to_sink || to_ring) {
+      __nv_bfloat16* d0 = reinterpret_cast<__nv_bfloat16*>(
+          to_sink ? role_base + (bh * g.S + p) * (2 * D) : role_base + g.sink_bytes + (bh * g.W + (p % g.W)) * (2 * D));
+      __nv_bfloat16* d1 = (to_sink && to_ring)
+                              ? reinterpret_cast<__nv_bfloat16*>(role_base + g.sink_bytes + (bh * g.W + (p % g.W)) * (2 * D))
+                              : nullptr;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 bv = __float2bfloat16_rn(v[e]);
+        d0[col0 + lane + 32 * e] = bv;
+        if (d1) d1[col0 + lane + 32 * e] = bv;
+      }
+    }
+    if (to_sink) continue;
+
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = fminf(fmaxf(v[e], -tclip), tclip);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), g.lm ? kLmSpan : 3.0f);
+    const __half sh = __float2half_rn(s32);
+    const __half zh = __float2half_rn(mn);
+    const float sf = __half2float(sh), zf = __half2float(zh);
+    const bool rng_ok = isfinite(sf) && isfinite(zf);
+    if (!rng_ok && lane == 0) status_or(a.status, OSCAR_DEV_FP16_RANGE);
+    const bool gok = rng_ok && sf != 0.f;
+    const float inv = gok ? __frcp_rn(sf) : 0.f;
+
+    // word w = lane / 4 of the group, slots 4 (lane % 4) .. + 3
+    const int64_t irow = bh * g.ncap + (p - g.S);
+    uint32_t* codes = reinterpret_cast<uint32_t*>(role_base + g.sink_bytes + g.ring_bytes + irow * (D / 4));
+    uint32_t* sz = reinterpret_cast<uint32_t*>(role_base + g.sink_bytes + g.ring_bytes + g.codes_bytes) +
+                   irow * (D / kGroup);
+    const int wi = lane >> 2, part = lane & 3;
+    uint32_t word = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int sl = part * 4 + k;
+      const float x = fminf(fmaxf(y[slot_channel(role, wi, sl)], -tclip), tclip);
+      const float yq = __fmul_rn(__fsub_rn(x, zf), inv);
+      int c = g.lm ? lm_code(yq) : min(max(__float2int_rn(yq), 0), 3);
+      c = gok ? c : 0;
+      word |= uint32_t(c) << (2 * sl);
+    }
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (part == 0) codes[8 * q + wi] = word;
+    if (lane == 0) sz[q] = pack_half2(sh, zh);
+  }
+}
+
 template <int D, int RPC, bool HAD>
 int launch_append_rows(const AppendArgs& a, cudaStream_t stream) {
   using C = RowsCfg<D, RPC>;
@@ -525,8 +811,51 @@ int launch_append_rows(const AppendArgs& a, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
 }
 
+template <int D, int RPC>
+int launch_append_slices(const AppendArgs& a, cudaStream_t stream) {
+  using C = SliceCfg<D, RPC>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kv_append_slices_kernel<D, RPC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return OSCAR_ERR_LAUNCH;
+    attr_set[dev] = 1;
+  }
+  const int64_t blocks = (a.rows + RPC - 1) / RPC;
+  if (blocks * C::SL > (int64_t(1) << 31) - 1) return OSCAR_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks * C::SL), 2, 1);
+  cfg.blockDim = dim3(kAppendThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::SL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  CUtensorMap mk, mv;
+  if (!encode_f32_tiles(&mk, a.R_K, D, D, kGroup, C::CH_ROWS) || !encode_f32_tiles(&mv, a.R_V, D, D, kGroup, C::CH_ROWS))
+    return OSCAR_ERR_LAUNCH;
+  return cudaLaunchKernelEx(&cfg, kv_append_slices_kernel<D, RPC>, mk, mv, a) == cudaSuccess ? OSCAR_OK
+                                                                                            : OSCAR_ERR_LAUNCH;
+}
+
+// Row-parallel appends: at head_dim 256 / 512 and up to kSmallAppendRows rows
+// per role (a decode step) a cluster of D / 128 CTAs, one per quant group, per
+// RPC rows (decode-step append of 32 rows per role at head_dim 512: 37.5 ->
+// 17.1 us); otherwise one CTA per RPC rows (larger K-only-INT2 or Lloyd-Max
+// appends, where the sliced grid's per-CTA set-up costs more than the shared
+// stream of R saves: 65,536 rows per role 3.3 vs 4.7 ms).
 template <int D>
 int launch_append_small(const AppendArgs& a, cudaStream_t stream) {
+  if constexpr (D >= 256) {
+    if (a.rows <= kSmallAppendRows)
+      return a.rows > 512 ? launch_append_slices<D, 8>(a, stream) : launch_append_slices<D, 4>(a, stream);
+  }
   return a.rows > 512 ? launch_append_rows<D, 8, false>(a, stream) : launch_append_rows<D, 4, false>(a, stream);
 }
 
