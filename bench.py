@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--v-bf16", action="store_true", help="K-only INT2: V kept BF16 at every position")
     ap.add_argument("--lloyd-max", action="store_true",
                     help="INT2 codes index the Lloyd-Max levels (0, rho, rho + 1, 2 rho + 1) instead of evenly spaced ones")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured once as a CUDA graph and replayed (reported under `graph`)")
     ap.add_argument("--calibrate", action="store_true",
                     help="time the R_K calibration (Sigma, eigenvectors, H P_br) instead of the decode step")
     ap.add_argument("--cpu-sample-worker", action="store_true", help=argparse.SUPPRESS)
@@ -511,6 +513,30 @@ def ours(args):
     split_share = sum(split_ms) / sum(a.elapsed_time(b) for a, b in pev)
     clocks.stop()
 
+    # ---- optional: the same step captured as one CUDA graph, replayed K times
+    graph_line = None
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        stream.wait_stream(side)
+        for _ in range(3):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_)]
+        for i in range(K_):
+            flush.zero_()
+            gev[i][0].record(stream)
+            graph.replay()
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        g_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in gev))
+        graph_line = {"ms_per_step": g_ms, "value": whole_job_tokens_per_s(Bsz, world, g_ms),
+                      "kernels_per_replay": (1 + decode_kernels) * L}
+
     # ---- end-to-end through the public API with host buffers
     q_h = q.cpu().pin_memory()
     k_h = k1.cpu().pin_memory()
@@ -574,6 +600,7 @@ def ours(args):
         "gpu_launches": (1 + decode_kernels) * L * K_,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
+        "graph": graph_line,
         "dev_status": st,
         "wall_s_timed": wall,
     }
