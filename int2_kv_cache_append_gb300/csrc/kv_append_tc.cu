@@ -482,19 +482,6 @@ bool encode_rows_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t c
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_f32_tiles(CUtensorMap* m, const float* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                      uint32_t box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || rows == 0 || cols == 0) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(cols) * 4};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool encode_code_rows(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t rowb, uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || rows == 0) return false;
