@@ -241,7 +241,9 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  * split kernel's MMA fragments), then split attention whose last CTA per
  * (sequence, KV head) merges that unit's partials and un-rotates V; at
  * head_dim 256 and 512 with V neither absorbed nor Hadamard-rotated a third
- * kernel applies R_V^T to every merged output instead.  All use programmatic
+ * kernel applies R_V^T to every merged output instead (also at head_dim 128
+ * with G > 4 and at most 16 (sequence, KV head) pairs; see
+ * oscar_kv_decode_kernels).  All use programmatic
  * dependent launch; the first waits for all prior work on the stream before
  * reading q.  Concurrent calls must not share a workspace.
  */
@@ -315,8 +317,9 @@ int oscar_kv_set_profile_events(void* split_start, void* split_stop);
  * oscar_kv_decode_kernels — how many kernels one attn_decode call with this
  * configuration launches (no counterpart on the pages; for launch accounting
  * and graph planning): query rotation and split attention, plus an
- * un-rotation kernel at head_dim 256 / 512 with V neither absorbed nor
- * Hadamard-rotated.  decode_step launches one kernel more (the append).
+ * un-rotation kernel when V is neither absorbed nor Hadamard-rotated and
+ * either head_dim is 256 / 512 or more than four query heads share a KV head
+ * with at most 16 (sequence, KV head) pairs in the batch.  decode_step launches one kernel more (the append).
  * Needs no device.  Returns 2 or 3, or OSCAR_ERR_INVALID for an invalid
  * configuration.
  */

@@ -57,6 +57,17 @@ namespace {
 constexpr int kNCW = 4;                    // warps per CTA (each team issues its own copies)
 constexpr int kThreads = kNCW * 32;
 constexpr int kI2Tok = 128;                // tokens per INT2 block (one set of bulk copies)
+
+// Is o = o' R_V^T applied by unrot_kernel after the split kernel (the merging
+// CTA then leaves o' in workspace slot 0)?  At head_dim 256 / 512 always (one
+// CTA per unit would read all of R_V through L2); at head_dim 128 when G > 4
+// heads share a KV head and there are few units (every unit is then shared by
+// tens of CTAs and all merge at the very end, where the 8-head un-rotation is
+// ~40 % of the merge).
+constexpr int kFewUnits = 16;
+__host__ __device__ inline bool unrot_separate(const Geom& g, bool absorb_v, bool hadamard) {
+  return !absorb_v && !hadamard && (g.D >= 256 || (g.G > 4 && g.B * g.Hkv <= kFewUnits));
+}
 constexpr int kSub = 64;                   // tokens per INT2 compute sub-block
 constexpr int kBfTok = 16;                 // tokens per BF16 block
 constexpr int kMaxSeg = 48;                // segments (units) one window of a CTA's slice lists
@@ -1427,8 +1438,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // R_V: in the CTA's last segment no copy is in flight, so at D = 128 it
         // comes into the idle stage area with one bulk copy, landing while the
         // slots are merged; otherwise its rows are read through L2
-        const bool rv_smem = D == 128 && !a.absorb_v && !a.hadamard && !more && sg == nwin - 1 &&
-                             C::NST * C::STAGE >= D * D * 4;
+        const bool rv_smem = D == 128 && !unrot_separate(g, a.absorb_v, a.hadamard) && !a.absorb_v && !a.hadamard &&
+                             !more && sg == nwin - 1 && C::NST * C::STAGE >= D * D * 4;
         const uint32_t rv_bar = smem_u32(&bars[C::NST]);
         if (rv_smem && threadIdx.x == 0) {
           mbar_arrive_expect_tx(rv_bar, D * D * 4);
@@ -1538,7 +1549,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) store(i, j * kGroup + lane + 32 * e, x[e]);
           }
-        } else if (a.absorb_v || D == 128) {
+        } else if (!unrot_separate(g, a.absorb_v, a.hadamard)) {
           // o = o' R_V^T (or o' when absorbed): one thread per output channel r.
           // At head_dim 128, R_V comes from the stage area when it was
           // prefetched there, else from L2, through the same arithmetic in the
@@ -1575,10 +1586,9 @@ __global__ void __launch_bounds__(kThreads, 2)
               if (i < Gh) store(i, r, res[i]);
           }
         } else {
-          // head_dim 256 / 512: o' goes to the unit's workspace slot 0 (every
-          // slot has been read) and unrot_kernel applies R_V^T for all units
-          // at once, spread over the GPU (here one CTA per unit would read all
-          // of R_V through L2, one row round trip at a time)
+          // o' goes to the unit's workspace slot 0 (every slot has been read)
+          // and unrot_kernel applies R_V^T for all units at once, spread over
+          // the GPU (see unrot_separate)
           for (int e = threadIdx.x; e < Gh * (D / 4); e += kThreads) {
             const int i = e / (D / 4), j4 = e % (D / 4);
             const int64_t si = (int64_t(b) * g.Hq + head0 + i) * a.ns;
@@ -1624,7 +1634,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ---------------------------------------------------------------------------
 constexpr int kUnrotRows = 16;
 // unrot_kernel runs after the split kernel (the decode's fourth launch)
-inline bool unrot_launched(int D, const DecodeArgs& a) { return D >= 256 && !a.absorb_v && !a.hadamard; }
+inline bool unrot_launched(const DecodeArgs& a) { return unrot_separate(a.g, a.absorb_v, a.hadamard); }
 constexpr int kUnrotThreads = 256;
 
 template <int W, int SH>
@@ -1791,7 +1801,7 @@ int launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   if (launch_pdl(split_kernel<D, NQT, VB, LM>, dim3(unsigned(a.ctas)), dim3(kThreads), C::SMEM, stream, maps[0], maps[1],
                  maps[2], maps[3], cmaps[0], cmaps[1], a) != cudaSuccess)
     return OSCAR_ERR_LAUNCH;
-  if (unrot_launched(D, a)) {
+  if (unrot_launched(a)) {
     const int nvec = g.B * g.Hq, wpc = kUnrotThreads / 32;
     const int gy = std::max(1, std::min((nvec + wpc - 1) / wpc, 8));
     if (launch_pdl(unrot_kernel<D>, dim3(D / kUnrotRows, unsigned(gy)), dim3(kUnrotThreads), 0, stream, a) !=
@@ -1809,7 +1819,7 @@ thread_local uint64_t g_test_wait_ns = 0;
 thread_local int g_test_wait_poison = 0;
 
 int decode_kernel_count(const Geom& g, bool absorb_v, bool hadamard) {
-  return 2 + (g.D >= 256 && !absorb_v && !hadamard ? 1 : 0);
+  return 2 + (unrot_separate(g, absorb_v, hadamard) ? 1 : 0);
 }
 
 uint64_t decode_workspace_bytes(const Geom& g, int ns) {

@@ -96,5 +96,9 @@ def test_decode_kernel_count():
     assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 512, 4, 8, 64)) == 3
     assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 512, 4, 8, 64, flags=K.FLAG_ABSORB_V)) == 2
     assert K.decode_kernels(K.KVConfig(1, 2, 8, 2, 512, 4, 8, 64, flags=K.FLAG_HADAMARD)) == 2
+    # head_dim 128: only with G > 4 and at most 16 (sequence, KV head) pairs
+    assert K.decode_kernels(K.KVConfig(1, 1, 64, 8, 128, 4, 8, 64)) == 3
+    assert K.decode_kernels(K.KVConfig(1, 4, 64, 8, 128, 4, 8, 64)) == 2
+    assert K.decode_kernels(K.KVConfig(1, 1, 64, 8, 128, 4, 8, 64, flags=K.FLAG_ABSORB_V)) == 2
     with pytest.raises(K.OscarError):
         K.decode_kernels(K.KVConfig(1, 2, 8, 3, 128, 4, 8, 64))  # 8 query heads over 3 KV heads

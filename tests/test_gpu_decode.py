@@ -251,3 +251,15 @@ def test_decode_merge_paths(D, flags, splits):
     _check(c, cache, q, lens, RK, RV, num_splits=splits)
     from tests.gpu_helpers import kcfg
     assert K.decode_kernels(kcfg(c)) == 2 + (D >= 256 and not flags & K.FLAG_ABSORB_V)
+
+
+@pytest.mark.parametrize("splits", [0, 4, 16])
+def test_decode_g8_few_units(splits):
+    # G = 8 with few (sequence, KV head) units: the merging CTA leaves o' in
+    # slot 0 and unrot_kernel applies R_V^T (three kernels)
+    c = O.Config(1, 1, 32, 4, 128, 16, 64, 3000, 0.96, 0.92)
+    lens = [2900]
+    cache, q, RK, RV = _build(c, lens, seed=80 + splits)
+    _check(c, cache, q, lens, RK, RV, num_splits=splits)
+    from tests.gpu_helpers import kcfg
+    assert K.decode_kernels(kcfg(c)) == 3
