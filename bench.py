@@ -129,9 +129,9 @@ def measured_peaks():
 # figure is the split kernel's alone (unrot_kernel reads R_V and the merged
 # outputs, a few MB from L2).
 MEASURED_TRAFFIC = {
-    "qwen3-8b-36L": ("attn_decode.cu", "a66eff6947186d2c", 647630080),
-    "hd512": ("attn_decode.cu", "a66eff6947186d2c", 753272832),
-    "qwen3-32b-decode": ("attn_decode.cu", "a66eff6947186d2c", 78338560),
+    "qwen3-8b-36L": ("attn_decode.cu", "d9887dbcf45ab200", 647457792),
+    "hd512": ("attn_decode.cu", "d9887dbcf45ab200", 753049088),
+    "qwen3-32b-decode": ("attn_decode.cu", "d9887dbcf45ab200", 78135296),
     "qwen3-32b-append": ("kv_append_tc.cu", "da55696891866101", 143004928),
 }
 
