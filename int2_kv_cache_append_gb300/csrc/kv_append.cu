@@ -362,6 +362,12 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_rows_kernel(const Ap
   extern __shared__ __align__(128) unsigned char sm[];
   float* ys = reinterpret_cast<float*>(sm + (HAD ? 0 : C::OFF_Y));  // [RPC][D] rotated rows
 
+  // Launched with programmatic dependent launch, so the CTAs can be resident
+  // before the preceding kernel ends (a decode step's append follows the
+  // previous layer's attention); nothing is read before the wait, and the
+  // dependents (qrot) are released only after it, so they never run ahead of
+  // the kernel that produced this call's inputs.
+  pdl_wait();
   pdl_trigger();
   const int role = blockIdx.y;
   const int64_t row0 = int64_t(blockIdx.x) * RPC;
@@ -564,6 +570,7 @@ __global__ void __launch_bounds__(kAppendThreads)
   uint32_t* ms = reinterpret_cast<uint32_t*>(sm + C::OFF_M);   // [RPC] max |y| bits, [RPC] finite
   const uint32_t bar0 = smem_u32(sm + C::OFF_BAR);
 
+  pdl_wait();  // as in kv_append_rows_kernel
   pdl_trigger();
   const int role = blockIdx.y;
   const int q = int(cluster_rank());                  // quant group of this CTA
@@ -806,9 +813,18 @@ int launch_append_rows(const AppendArgs& a, cudaStream_t stream) {
       return OSCAR_ERR_LAUNCH;
     attr_set[dev] = 1;
   }
-  const dim3 grid(unsigned((a.rows + RPC - 1) / RPC), 2, 1);
-  kv_append_rows_kernel<D, RPC, HAD><<<grid, kAppendThreads, smem, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((a.rows + RPC - 1) / RPC), 2, 1);
+  cfg.blockDim = dim3(kAppendThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_append_rows_kernel<D, RPC, HAD>, a) == cudaSuccess ? OSCAR_OK
+                                                                                       : OSCAR_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -859,13 +875,15 @@ int launch_append_slices(const AppendArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kAppendThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C::SL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   CUtensorMap mk, mv;
   if (!encode_f32_tiles(&mk, a.R_K, D, D, kGroup, C::CH_ROWS) || !encode_f32_tiles(&mv, a.R_V, D, D, kGroup, C::CH_ROWS))
     return OSCAR_ERR_LAUNCH;
