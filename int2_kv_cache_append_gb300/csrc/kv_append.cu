@@ -7,7 +7,7 @@
 // high-precision sink/recent tokens) and "OSCAR-RotationZoo" (Available
 // rotations: group 128 along head_dim; How to use: K/V clip 0.96/0.92).
 //
-// Two CUDA-core kernels (the tensor-core kernel for large head_dim-128 bf16
+// Three CUDA-core kernels (the tensor-core kernel for large head_dim-128 bf16
 // appends is in kv_append_tc.cu):
 //
 // kv_append_kernel, tiled: one CTA of 128 threads handles RPC = 64*128/D rows
@@ -25,8 +25,13 @@
 // at their positions) and of the Lloyd-Max levels (span 2 rho + 1, codes by
 // comparison with the level midpoints, lm_code).
 //
-// Both accumulate each rotated value with fp32 FMAs in increasing input-channel
-// order and run the same codec operations, so they write identical bytes.
+// kv_append_slices_kernel, the row-parallel append at head_dim 256 / 512 for
+// up to 1024 rows per role: a thread-block cluster of one CTA per quant group
+// shares a few rows, each CTA streaming only its column slice of R (below).
+//
+// All three accumulate each rotated value with fp32 FMAs in increasing
+// input-channel order and run the same codec operations, so they write
+// identical bytes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
