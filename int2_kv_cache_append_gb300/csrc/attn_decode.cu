@@ -608,15 +608,16 @@ __global__ void __launch_bounds__(kQrotThreads) qrot_kernel(const DecodeArgs a) 
   // holds column gq and k-rows 2cq, 2cq + 1 (+ 8 for the second register).
   const int NQT = G > 4 ? 2 : 1, NQB = 2 * NQT;
   const int64_t grp = int64_t(bh) * (D / kGroup) + chunk;
-  // INT2 blocks: channel d of a code at mantissa bit 2k meets q'[d] * 4^-k * 2^X
-  // as an fp16 hi/lo pair (see unpack16), entry ((nq * 8 + kk) * 2 + half) * 32 + lane
+  // INT2 blocks: channel d of a K code at mantissa bit 2k meets q'[d] * 4^-k * 2^X
+  // as an fp16 hi/lo pair (k = unpack_kq of its register, see unpack16), entry
+  // ((nq * 8 + kk) * 2 + half) * 32 + lane
   for (int e = threadIdx.x; e < NQT * 512; e += kQrotThreads) {
     const int ln = e & 31, half = (e >> 5) & 1, kk = (e >> 6) & 7, nq = e >> 9;
     const int gq = ln >> 2, cq = ln & 3, hb = 4 * nq + (gq >> 1);
     const int d0 = 16 * kk + 2 * cq + 8 * half;
     uint32_t v16 = 0;
     if (hb < G) {
-      const float f = pow2f(Xs[hb] - 2 * unpack_k(2 * (kk & 3) + half));
+      const float f = pow2f(Xs[hb] - 2 * unpack_kq(2 * (kk & 3) + half));
       const uint32_t s0 = split_f16(qv[hb][d0] * f), s1 = split_f16(qv[hb][d0 + 1] * f);
       v16 = (gq & 1) ? ((s0 >> 16) | (s1 & 0xffff0000u)) : ((s0 & 0xffffu) | (s1 << 16));
     }
@@ -957,8 +958,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
       int xbuf = 0;
 
-      // INT2 P.V takes V codes from unpack16_v: the code of output row r arrives
-      // as code * 2^e(r), e(r) = unpack_v_exp(p) with p = 2 * (mtd % 4) for rows gq
+      // INT2 P.V takes V codes from unpack16: the code of output row r arrives
+      // as code * 2^e(r), e(r) = unpack_exp(p) with p = 2 * (mtd % 4) for rows gq
       // and 2 * (mtd % 4) + 1 for rows gq + 8.  While INT2 blocks are consumed, row
       // r of o holds (real value) * 2^e(r); it is converted by exact powers of two
       // at a switch between INT2 and BF16 blocks and at the end.
@@ -966,8 +967,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       auto scale_o = [&](int sign) {  // o *= 2^(sign * e(r)) per row
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          const float f0 = pow2f(sign * unpack_v_exp(2 * (mt & 3)));
-          const float f1 = pow2f(sign * unpack_v_exp(2 * (mt & 3) + 1));
+          const float f0 = pow2f(sign * unpack_exp(2 * (mt & 3)));
+          const float f1 = pow2f(sign * unpack_exp(2 * (mt & 3) + 1));
 #pragma unroll
           for (int nq = 0; nq < NQT; ++nq) {
             o[mt][nq][0] *= f0; o[mt][nq][1] *= f0;
@@ -1306,8 +1307,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               uint32_t rx[8], ry[8];
-              unpack16_v(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
-              unpack16_v(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+              unpack16(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
+              unpack16(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
 #pragma unroll
               for (int m4 = 0; m4 < 4; ++m4) {
                 const int mtd = 4 * hh + m4;
@@ -1320,8 +1321,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 uint32_t rx[8], ry[8];
-                unpack16_v_hi(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
-                unpack16_v_hi(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
+                unpack16_hi(prmt(wa, wb, hh ? 0x7632u : 0x5410u), rx);
+                unpack16_hi(prmt(wc, wd, hh ? 0x7632u : 0x5410u), ry);
 #pragma unroll
                 for (int m4 = 0; m4 < 4; ++m4) {
                   const int mtd = 4 * hh + m4;

@@ -63,55 +63,41 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Unpack 16 two-bit codes into 8 f16x2 registers of fp16 subnormals.
-// Register p holds the codes at bits 2p and 16 + 2p (low and high half) for
-// p < 5, and the codes at bits 10 + 2(p-5) and 26 + 2(p-5) for p >= 5, each
-// left at mantissa bit 2k(p) of an otherwise zero half, k(p) = p < 5 ? p : p - 5:
-// the half's value is exactly code * 4^k(p) * 2^-24 (an fp16 subnormal; the
-// tensor cores multiply subnormal inputs exactly).  One AND per register (and
-// one shift for the top three): the factor 4^k(p) * 2^-24 is constant per
-// register index, so callers fold it into the other operand or the accumulator.
-// Precision: the tensor cores align the products of one MMA by the operands'
-// exponent fields, and a subnormal's field says 2^-14 whatever its leading bit,
-// so a code at bit 2k keeps about 15 + 2k significant bits of the accumulation
-// window instead of ~25 (measured on GB300: ~2e-5 relative error on sums of
-// k = 0 codes, ~2e-6 from k = 1 up).  unpack16_v therefore converts the two
-// k = 0 registers exactly instead.
-__device__ __forceinline__ constexpr int unpack_k(int p) { return p < 5 ? p : p - 5; }
+// Precision of two-bit codes as fp16 subnormal operands: a half whose only
+// bits are a code at mantissa bit 2k has the exact value code * 4^k * 2^-24,
+// and the tensor cores multiply subnormal inputs exactly, but they align the
+// products of one MMA by the operands' exponent fields, and a subnormal's
+// field says 2^-14 whatever its leading bit: a code at bit 2k keeps about
+// 15 + 2k significant bits of the accumulation window instead of ~25
+// (measured on GB300: ~2e-5 relative error on sums of k = 0 codes, ~2e-6 from
+// k = 1 up).  So codes are unpacked to mantissa bits 4..9 only (k = 2, 3, 4),
+// for K (QK^T, where one MMA mixes the k of two registers) and V (P.V, where
+// each output row takes one register index) alike: register p holds the codes
+// at bits 2p and 16 + 2p (the word's low and high half) moved to mantissa bit
+// 2 kq(p):
+//   p = 0, 1: the word shifted left by 4 (k = 2, 3);
+//   p = 2, 3, 4: the word itself (k = 2, 3, 4);
+//   p = 5, 6, 7: the word shifted right by 6 (k = 2, 3, 4).
+// The masks keep bits 4..9 of each half, so bits a shift carries across the
+// halves are never kept.  Two shifts and eight ANDs per 16 codes; the factor
+// 4^kq(p) * 2^-24 is constant per register index, so the caller folds it into
+// the other operand.
+__device__ __forceinline__ constexpr int unpack_kq(int p) { return p < 2 ? p + 2 : (p < 5 ? p : p - 3); }
 
 __device__ __forceinline__ void unpack16(uint32_t w, uint32_t (&r)[8]) {
-  r[0] = w & 0x00030003u;
-  r[1] = w & 0x000C000Cu;
+  const uint32_t wl = w << 4, wr = w >> 6;
+  r[0] = wl & 0x00300030u;
+  r[1] = wl & 0x00C000C0u;
   r[2] = w & 0x00300030u;
   r[3] = w & 0x00C000C0u;
   r[4] = w & 0x03000300u;
-  const uint32_t w2 = w >> 10;
-  r[5] = w2 & 0x00030003u;
-  r[6] = w2 & 0x000C000Cu;
-  r[7] = w2 & 0x00300030u;
+  r[5] = wr & 0x00300030u;
+  r[6] = wr & 0x00C000C0u;
+  r[7] = wr & 0x03000300u;
 }
 
-// As unpack16, except registers 0 and 5 (the codes at bit 0 of each half) hold
-// the codes as exact fp16 integers: OR-ed into the mantissa of 1024 (0x6400)
-// and shifted back by one fp16x2 subtraction, which is exact.
-__device__ __forceinline__ void unpack16_v(uint32_t w, uint32_t (&r)[8]) {
-  const uint32_t M = 0x64006400u;
-  uint32_t t0, t5;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t0) : "r"(w), "r"(0x00030003u), "r"(M));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(M));
-  r[1] = w & 0x000C000Cu;
-  r[2] = w & 0x00300030u;
-  r[3] = w & 0x00C000C0u;
-  r[4] = w & 0x03000300u;
-  const uint32_t w2 = w >> 10;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t5) : "r"(w2), "r"(0x00030003u), "r"(M));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[5]) : "r"(t5), "r"(M));
-  r[6] = w2 & 0x000C000Cu;
-  r[7] = w2 & 0x00300030u;
-}
-
-// log2 of the value unpack16_v gives a code of register p, per unit of code
-__device__ __forceinline__ constexpr int unpack_v_exp(int p) { return (p == 0 || p == 5) ? 0 : 2 * unpack_k(p) - 24; }
+// log2 of the value unpack16 gives a code of register p, per unit of code
+__device__ __forceinline__ constexpr int unpack_exp(int p) { return 2 * unpack_kq(p) - 24; }
 
 // Lloyd-Max levels: level(c) = (0, rho, rho + 1, 2 rho + 1)[c] with rho = 1.16
 // (LM_RATIO as printed, rounded to float32).  Writing c = c0 + 2 c1,
@@ -134,36 +120,19 @@ constexpr float kLmMid2 = kLmSpan - kLmMid0;
 __device__ __forceinline__ int lm_code(float y) { return (y > kLmMid0) + (y > kLmMid1) + (y > kLmMid2); }
 
 // As unpack16, keeping only the high bit of each code: register p holds
-// 2 * c1 * 4^k(p) * 2^-24 where unpack16 holds c * 4^k(p) * 2^-24.
+// 2 * c1 * 4^kq(p) * 2^-24 where unpack16 holds c * 4^kq(p) * 2^-24.
 __device__ __forceinline__ void unpack16_hi(uint32_t w, uint32_t (&r)[8]) {
-  r[0] = w & 0x00020002u;
-  r[1] = w & 0x00080008u;
+  const uint32_t wl = w << 4, wr = w >> 6;
+  r[0] = wl & 0x00200020u;
+  r[1] = wl & 0x00800080u;
   r[2] = w & 0x00200020u;
   r[3] = w & 0x00800080u;
   r[4] = w & 0x02000200u;
-  const uint32_t w2 = w >> 10;
-  r[5] = w2 & 0x00020002u;
-  r[6] = w2 & 0x00080008u;
-  r[7] = w2 & 0x00200020u;
+  r[5] = wr & 0x00200020u;
+  r[6] = wr & 0x00800080u;
+  r[7] = wr & 0x02000200u;
 }
 
-// As unpack16_v for the high bits: registers 0 and 5 hold 2 * c1 as exact fp16
-// integers, the others 2 * c1 at the code's subnormal position.
-__device__ __forceinline__ void unpack16_v_hi(uint32_t w, uint32_t (&r)[8]) {
-  const uint32_t M = 0x64006400u;
-  uint32_t t0, t5;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t0) : "r"(w), "r"(0x00020002u), "r"(M));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(M));
-  r[1] = w & 0x00080008u;
-  r[2] = w & 0x00200020u;
-  r[3] = w & 0x00800080u;
-  r[4] = w & 0x02000200u;
-  const uint32_t w2 = w >> 10;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t5) : "r"(w2), "r"(0x00020002u), "r"(M));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[5]) : "r"(t5), "r"(M));
-  r[6] = w2 & 0x00080008u;
-  r[7] = w2 & 0x00200020u;
-}
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -1,0 +1,184 @@
+"""GPU parity over seeded random configurations of the whole path.
+
+Each case draws, from its seed alone: head_dim, the GQA shape (G = 1..8),
+batch, sink and ring sizes, the mode flags (absorbed V, V kept BF16, Lloyd-Max
+levels, float32 inputs), how the rows are appended (one to three kv_append
+calls of different sizes, a start offset per sequence), the decode lengths
+(empty sequences, lengths inside the BF16 windows, full lengths) and the split
+count.  The rotations are exact signed permutations, so every rotated value,
+and hence the cache, is exact on both sides:
+
+  * the GPU cache after the kv_append calls equals the oracle's byte for byte;
+  * attn_decode of those bytes agrees with the oracle's decode within the
+    tolerances of the decode tests (bf16 output rel-L2 <= 1e-3 against the
+    oracle rounded to bf16; float32 output max-abs <= 5e-3, rel-L2 <= 2e-4;
+    lse within 1e-4 + 1e-5 |lse|);
+  * decode_step (one more append of 1..6 tokens fused with the decode) leaves
+    the oracle's cache bytes and agrees with the oracle's append + decode
+    within the same tolerances.
+
+The in-quant Hadamard is not an exact rotation in float32, so its cases decode
+the oracle's cache bytes on both sides instead (the Hadamard tests check its
+append on the GPU's own rotated rows)."""
+import numpy as np
+import pytest
+import torch
+
+from int2_kv_cache_append_gb300 import oscar_kv as K
+from int2_kv_cache_append_gb300 import synth as S
+from oracle import oscar_oracle as O
+from tests.gpu_helpers import bf16_round64, dev, dev_i32, dev_rot, gpu_append, gpu_decode, kcfg, new_cache, rel_l2
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int2_kv_cache_append_gb300 import build
+    build.build()
+
+
+def draw(seed: int, hadamard: bool = False) -> dict:
+    """One random configuration, a pure function of the seed."""
+    r = np.random.default_rng(seed)
+    D = int(r.choice([128, 128, 128, 256, 512]))
+    G = int(r.choice([1, 2, 4, 8]))
+    Hkv = int(r.choice([1, 2, 4])) if D == 128 else int(r.choice([1, 2]))
+    B = int(r.integers(1, 5))
+    S_ = int(r.choice([0, 8, 16, 64]))
+    W = int(r.choice([16, 64, 256])) if S_ == 0 else int(r.choice([0, 16, 64, 256]))
+    flags = K.FLAG_HADAMARD if hadamard else 0
+    for f, p in ((K.FLAG_ABSORB_V, 0.3), (K.FLAG_V_BF16, 0.25), (K.FLAG_LLOYD_MAX, 0.25), (K.FLAG_IN_FP32, 0.3)):
+        if r.random() < p:
+            flags |= f
+    total = int(r.integers(1, 2500 if D == 128 else 1200))  # rows appended per sequence
+    nch = int(r.integers(1, 4))
+    cuts = sorted(set(int(x) for x in r.integers(1, total, nch - 1))) if total > 1 else []
+    chunks = [b - a for a, b in zip([0] + cuts, cuts + [total])]
+    offs = [int(x) for x in r.integers(0, 40, B)]
+    n_step = int(r.integers(1, 7))
+    cap = max(offs) + total + n_step + int(r.integers(0, 50))
+    lens = []
+    for b in range(B):
+        end = offs[b] + total
+        kind = r.integers(0, 4)
+        lens.append(0 if kind == 0 else (int(r.integers(1, end + 1)) if kind == 1 else end))
+    splits = int(r.choice([0, 0, 0, 1, 3, 9]))
+    return dict(D=D, Hq=G * Hkv, Hkv=Hkv, B=B, S=S_, W=W, flags=flags, chunks=chunks, offs=offs, cap=cap,
+                lens=lens, splits=splits, n_step=n_step, seed=seed)
+
+
+def _rows(rng, shape, ch, fp32):
+    x = S.activations(rng, shape, ch)
+    return x if fp32 else S.to_bf16_values(x)
+
+
+def _oracle_decode(c, cache, q, lens, RK, RV, absorb):
+    """The oracle's decode; an empty sequence has its defined output (zeros,
+    lse = -inf), which the oracle does not evaluate."""
+    ref, ref_lse = O.decode(c, cache, 0, q, [max(1, t) for t in lens], RK, RV, absorb_v=absorb)
+    for b, t in enumerate(lens):
+        if t == 0:
+            ref[b] = 0.0
+            ref_lse[b] = -np.inf
+    return ref, ref_lse
+
+
+def _compare(c, ref, ref_lse, o16, o32, lse, lse32, what):
+    r16 = rel_l2(o16, bf16_round64(ref))
+    r32 = rel_l2(o32, ref)
+    m32 = float(np.abs(o32 - ref).max()) if ref.size else 0.0
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: empty sequences differ"
+    dl = float(np.max(np.abs(lse[fin] - ref_lse[fin]) - 1e-5 * np.abs(ref_lse[fin]))) if fin.any() else 0.0
+    assert r16 <= 1e-3, f"{what}: bf16 rel-L2 {r16}"
+    assert m32 <= 5e-3 and r32 <= 2e-4, f"{what}: fp32 max-abs {m32} rel-L2 {r32}"
+    assert dl <= 1e-4, f"{what}: lse {dl}"
+    assert np.array_equal(lse, lse32), f"{what}: lse depends on the output type"
+
+
+SEEDS = list(range(24))
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_sweep_chain(seed):
+    p = draw(seed)
+    D, B, Hq, Hkv = p["D"], p["B"], p["Hq"], p["Hkv"]
+    c = O.Config(1, B, Hq, Hkv, D, p["S"], p["W"], p["cap"], 0.96, 0.92, flags=p["flags"])
+    fp32 = bool(p["flags"] & K.FLAG_IN_FP32)
+    absorb = bool(p["flags"] & K.FLAG_ABSORB_V)
+    rng = np.random.default_rng(1000 + seed)
+    RK = S.signed_permutation(rng, D).astype(np.float32)
+    RV = S.signed_permutation(rng, D).astype(np.float32)
+    ch = rng.choice(D, max(1, round(0.02 * D)), replace=False)
+
+    # appends: the same rows through the oracle and the GPU
+    ocache, gcache = O.new_cache(c), new_cache(c)
+    pos = list(p["offs"])
+    for n in p["chunks"]:
+        k, v = _rows(rng, (B, n, Hkv, D), ch, fp32), _rows(rng, (B, n, Hkv, D), ch, fp32)
+        O.append(c, ocache, 0, k, v, pos, RK, RV)
+        gpu_append(c, gcache, 0, k, v, pos, RK, RV)
+        pos = [x + n for x in pos]
+    got = gcache.cpu().numpy()
+    diff = np.nonzero(got != ocache)[0]
+    assert diff.size == 0, f"{p}: {diff.size} cache bytes differ, first at {diff[:8]}"
+
+    # decode of those bytes
+    q = _rows(rng, (B, Hq, D), ch, fp32)
+    ref, ref_lse = _oracle_decode(c, ocache, q, p["lens"], RK, RV, absorb)
+    o16, lse = gpu_decode(c, gcache, 0, q, p["lens"], RK, RV, num_splits=p["splits"], hint=p["cap"], out_fp32=False)
+    o32, lse32 = gpu_decode(c, gcache, 0, q, p["lens"], RK, RV, num_splits=p["splits"], hint=p["cap"],
+                            out_fp32=True)
+    _compare(c, ref, ref_lse, o16, o32, lse, lse32, f"attn_decode {p}")
+
+    # decode_step: n_step more rows at each sequence's end, then the decode of
+    # the new lengths, in one call
+    n = p["n_step"]
+    k, v = _rows(rng, (B, n, Hkv, D), ch, fp32), _rows(rng, (B, n, Hkv, D), ch, fp32)
+    q = _rows(rng, (B, Hq, D), ch, fp32)
+    lens = [x + n for x in pos]
+    O.append(c, ocache, 0, k, v, pos, RK, RV)
+    ref, ref_lse = _oracle_decode(c, ocache, q, lens, RK, RV, absorb)
+    kc = kcfg(c)
+    lay = K.layout_query(kc)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    outs = []
+    for out_fp32 in (False, True):
+        kc.flags = (c.flags & ~K.FLAG_OUT_FP32) | (K.FLAG_OUT_FP32 if out_fp32 else 0)
+        gc = gcache.clone()
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32 if out_fp32 else torch.bfloat16, device="cuda")
+        lse_t = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+        ws = torch.empty(lay["decode_workspace_bytes"], dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        K.decode_step(kc, gc, 0, dev(k, dt), dev(v, dt), dev_i32(pos), dev(q, dt), dev_i32(lens), dev_rot(RK),
+                      dev_rot(RV), out, ws, lse=lse_t, seq_len_hint=p["cap"], num_splits=p["splits"], status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, f"decode_step status {int(st.item())}"
+        diff = np.nonzero(gc.cpu().numpy() != ocache)[0]
+        assert diff.size == 0, f"{p}: decode_step cache: {diff.size} bytes differ, first at {diff[:8]}"
+        outs.append((out.float().cpu().numpy().astype(np.float64), lse_t.cpu().numpy().astype(np.float64)))
+    (o16, lse), (o32, lse32) = outs
+    _compare(c, ref, ref_lse, o16, o32, lse, lse32, f"decode_step {p}")
+
+
+@pytest.mark.parametrize("seed", range(100, 106))
+def test_sweep_hadamard_decode(seed):
+    p = draw(seed, hadamard=True)
+    D, B, Hq, Hkv = p["D"], p["B"], p["Hq"], p["Hkv"]
+    c = O.Config(1, B, Hq, Hkv, D, p["S"], p["W"], p["cap"], 0.96, 0.92, flags=p["flags"])
+    fp32 = bool(p["flags"] & K.FLAG_IN_FP32)
+    rng = np.random.default_rng(1000 + seed)
+    ch = rng.choice(D, max(1, round(0.02 * D)), replace=False)
+    cache = O.new_cache(c)
+    pos = list(p["offs"])
+    for n in p["chunks"]:
+        k, v = _rows(rng, (B, n, Hkv, D), ch, fp32), _rows(rng, (B, n, Hkv, D), ch, fp32)
+        O.append(c, cache, 0, k, v, pos, None, None)
+        pos = [x + n for x in pos]
+    q = _rows(rng, (B, Hq, D), ch, fp32)
+    ref, ref_lse = _oracle_decode(c, cache, q, p["lens"], None, None, bool(p["flags"] & K.FLAG_ABSORB_V))
+    gc = torch.from_numpy(cache).cuda()
+    o16, lse = gpu_decode(c, gc, 0, q, p["lens"], None, None, num_splits=p["splits"], hint=p["cap"], out_fp32=False)
+    o32, lse32 = gpu_decode(c, gc, 0, q, p["lens"], None, None, num_splits=p["splits"], hint=p["cap"], out_fp32=True)
+    _compare(c, ref, ref_lse, o16, o32, lse, lse32, f"attn_decode {p}")
