@@ -152,13 +152,14 @@ __host__ __device__ inline Regions make_regions(int T, int S, int W, int D, int 
   r.nrb1 = (r.rlen1 + kBfTok - 1) / kBfTok;
   r.nrb = r.nrb1 + (r.n_ring - r.rlen1 + kBfTok - 1) / kBfTok;
   // work weights of one block, in proportion to its measured processing time
-  // (a 128-token INT2 block takes ~1.7x a 16-token BF16 block for ~1.1x the
+  // (a 128-token INT2 block takes ~1.8x a 16-token BF16 block for ~1.1x the
   // bytes: the codes are unpacked and the scale/zero algebra is extra work;
-  // with Lloyd-Max levels every INT2 product runs a second time over the
-  // codes' high bits, ~1.7x again: split kernel 61.4 -> 85.5 us on the
-  // qwen3-4b layer, whose weighted cost is 53 % INT2)
+  // INT2 weights of 9, 10, 11, 12 and 13 x D timed on the qwen3-4b layer and
+  // at head_dim 512: 11 is the best for both; with Lloyd-Max levels every
+  // INT2 product runs a second time over the codes' high bits, ~1.7x again:
+  // split kernel 61.4 -> 85.5 us on the qwen3-4b layer at 10 and 17)
   r.cbf = int64_t(6) * D;
-  r.ci2 = vb ? r.cbf : int64_t(lm ? 17 : 10) * D;
+  r.ci2 = vb ? r.cbf : int64_t(lm ? 17 : 11) * D;
   return r;
 }
 
