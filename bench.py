@@ -129,10 +129,10 @@ def measured_peaks():
 # figure is the split kernel's alone (unrot_kernel reads R_V and the merged
 # outputs, a few MB from L2).
 MEASURED_TRAFFIC = {
-    "qwen3-8b-36L": ("attn_decode.cu", "42bc793c36524aa7", 647701504),
-    "hd512": ("attn_decode.cu", "42bc793c36524aa7", 753161216),
-    "qwen3-32b-decode": ("attn_decode.cu", "42bc793c36524aa7", 78010880),
-    "qwen3-4b-layer": ("attn_decode.cu", "42bc793c36524aa7", 151966208),
+    "qwen3-8b-36L": ("attn_decode.cu", "3cdce9215ee18187", 647665664),
+    "hd512": ("attn_decode.cu", "3cdce9215ee18187", 753083136),
+    "qwen3-32b-decode": ("attn_decode.cu", "3cdce9215ee18187", 77965824),
+    "qwen3-4b-layer": ("attn_decode.cu", "3cdce9215ee18187", 152292352),
     "qwen3-32b-append": ("kv_append_tc.cu", "da55696891866101", 143004928),
 }
 
