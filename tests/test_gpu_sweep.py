@@ -16,8 +16,10 @@ cache, is exact on both sides:
     <= 2e-4; lse within 1e-4 + 1e-5 |lse|), and its bf16 output is the float32
     output rounded to nearest (see _compare);
   * decode_step (one more append of 1..6 tokens fused with the decode) leaves
-    the oracle's cache bytes and agrees with the oracle's append + decode
-    within the same tolerances.
+    the oracle's cache bytes, agrees with the oracle's append + decode within
+    the same tolerances, and gives the same output and lse bits as kv_append
+    followed by attn_decode (it streams the blocks the append leaves alone
+    before the append completes, so a block read too early would show).
 
 The in-quant Hadamard is not an exact rotation in float32, so its cases decode
 the oracle's cache bytes on both sides instead (the Hadamard tests check its
@@ -29,8 +31,8 @@ import torch
 from int2_kv_cache_append_gb300 import oscar_kv as K
 from int2_kv_cache_append_gb300 import synth as S
 from oracle import oscar_oracle as O
-from tests.gpu_helpers import (bf16_round64, dev, dev_i32, dev_rot, gpu_append, gpu_decode, kcfg, new_cache, rel_l2,
-                               workspace_bytes)
+from tests.gpu_helpers import (assert_same_decode, bf16_round64, dev, dev_i32, dev_rot, gpu_append, gpu_decode, kcfg,
+                               new_cache, rel_l2, workspace_bytes)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not torch.cuda.is_available(), reason="needs CUDA")]
 
@@ -180,20 +182,32 @@ def test_sweep_chain(seed):
     outs = []
     for out_fp32 in (False, True):
         kc.flags = (c.flags & ~K.FLAG_OUT_FP32) | (K.FLAG_OUT_FP32 if out_fp32 else 0)
-        gc = gcache.clone()
-        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32 if out_fp32 else torch.bfloat16, device="cuda")
-        lse_t = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
-        ws = torch.empty(workspace_bytes(c, p["slots"]) if p["slots"] else lay["decode_workspace_bytes"],
-                         dtype=torch.uint8, device="cuda")
-        st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        K.decode_step(kc, gc, L, dev(k, dt), dev(v, dt), dev_i32(pos), dev(q, dt), dev_i32(lens), dev_rot(RK),
-                      dev_rot(RV), out, ws, lse=lse_t, seq_len_hint=p["hint"], sm_scale=p["sm_scale"],
-                      num_splits=p["splits"], status=st)
-        torch.cuda.synchronize()
-        assert int(st.item()) == 0, f"decode_step status {int(st.item())}"
-        diff = np.nonzero(gc.cpu().numpy() != ocache)[0]
-        assert diff.size == 0, f"{p}: decode_step cache: {diff.size} bytes differ, first at {diff[:8]}"
-        outs.append((out.float().cpu().numpy().astype(np.float64), lse_t.cpu().numpy().astype(np.float64)))
+        res = []
+        for fused in (True, False):
+            gc = gcache.clone()
+            out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                             device="cuda")
+            lse_t = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+            ws = torch.empty(workspace_bytes(c, p["slots"]) if p["slots"] else lay["decode_workspace_bytes"],
+                             dtype=torch.uint8, device="cuda")
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            new_rows = (dev(k, dt), dev(v, dt), dev_i32(pos))
+            dec = dict(lse=lse_t, seq_len_hint=p["hint"], sm_scale=p["sm_scale"], num_splits=p["splits"], status=st)
+            if fused:
+                K.decode_step(kc, gc, L, *new_rows, dev(q, dt), dev_i32(lens), dev_rot(RK), dev_rot(RV), out, ws, **dec)
+            else:
+                K.kv_append(kc, gc, L, *new_rows, dev_rot(RK), dev_rot(RV), status=st)
+                K.attn_decode(kc, gc, L, dev(q, dt), dev_i32(lens), dev_rot(RK), dev_rot(RV), out, ws, **dec)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0, f"{'decode_step' if fused else 'append + decode'} status {int(st.item())}"
+            diff = np.nonzero(gc.cpu().numpy() != ocache)[0]
+            assert diff.size == 0, f"{p}: fused {fused}: {diff.size} cache bytes differ, first at {diff[:8]}"
+            res.append((out.float().cpu().numpy(), lse_t.cpu().numpy()))
+        # the fused call streams blocks the append leaves alone before it completes:
+        # it must read exactly what the sequential calls read
+        (of, lf), (os_, ls) = res
+        assert_same_decode(of, os_, lf, ls)
+        outs.append((of.astype(np.float64), lf.astype(np.float64)))
     (o16, lse), (o32, lse32) = outs
     _compare(c, ref, ref_lse, o16, o32, lse, lse32, f"decode_step {p}")
 
