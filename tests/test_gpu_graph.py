@@ -3,7 +3,9 @@
 replayed must write the same cache bytes, outputs and lse as the same calls
 run eagerly, and replaying it again (same positions, same inputs) must leave
 them unchanged.  The step's launches use programmatic dependent launch and, at
-head_dim 256, a thread-block cluster; both must survive capture."""
+head_dim 256/512, a thread-block cluster; both must survive capture.  Cases
+cover G = 8 with the separate V un-rotation kernel and the Lloyd-Max, K-only
+INT2 and in-quant Hadamard modes."""
 import numpy as np
 import pytest
 import torch
@@ -20,17 +22,27 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("D,B,Hq,Hkv", [(128, 4, 16, 4), (256, 2, 8, 2)])
-def test_graph_replay_equals_eager(D, B, Hq, Hkv):
+@pytest.mark.parametrize("D,B,Hq,Hkv,flags", [
+    (128, 4, 16, 4, 0),
+    (256, 2, 8, 2, 0),
+    (512, 2, 16, 2, 0),                     # G = 8, V un-rotated by unrot_kernel
+    (128, 2, 16, 2, K.FLAG_LLOYD_MAX),
+    (128, 2, 8, 2, K.FLAG_V_BF16),
+    (128, 2, 8, 2, K.FLAG_HADAMARD | K.FLAG_ABSORB_V),
+])
+def test_graph_replay_equals_eager(D, B, Hq, Hkv, flags):
     L, S_, W, cap = 3, 16, 64, 1500
-    kc = K.KVConfig(L, B, Hq, Hkv, D, S_, W, cap, 0.96, 0.92, K.FLAG_OUT_FP32)
+    kc = K.KVConfig(L, B, Hq, Hkv, D, S_, W, cap, 0.96, 0.92, K.FLAG_OUT_FP32 | flags)
     lay = K.layout_query(kc)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(77 + D)
     ch = np.array([3, 40])
     rng = np.random.default_rng(D)
-    rots = [(torch.from_numpy(S.qr_rotation(rng, D).astype(np.float32)).cuda(),
-             torch.from_numpy(S.qr_rotation(rng, D).astype(np.float32)).cuda()) for _ in range(L)]
+    if flags & K.FLAG_HADAMARD:
+        rots = [(None, None)] * L
+    else:
+        rots = [(torch.from_numpy(S.qr_rotation(rng, D).astype(np.float32)).cuda(),
+                 torch.from_numpy(S.qr_rotation(rng, D).astype(np.float32)).cuda()) for _ in range(L)]
     cache0 = torch.zeros(lay["total_bytes"], dtype=torch.uint8, device="cuda")
     T0 = 1200
     for layer in range(L):
