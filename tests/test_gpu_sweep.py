@@ -263,11 +263,17 @@ def draw_append(seed: int) -> dict:
 @pytest.mark.parametrize("seed", range(200, 224))
 def test_sweep_append_codec_on_gpu_rows(seed):
     """General rotations (calibrated R_K, random orthogonal R_V, or the in-quant
-    Hadamard): the GPU's float32 rotation is within 2e-6 of the float64
-    product (max-norm, relative to the largest element) but not correctly
-    rounded, so the codec is checked on the GPU's own rows: the oracle
-    quantises the rows each call exports through debug_rot_out (identity
-    rotation, no Hadamard) and the two caches must match byte for byte."""
+    Hadamard).  The GPU's float32 rotation is checked against the float64
+    product with the error bounds of a D-term float32 dot product: every
+    element within gamma_D = D u (u = 2^-24) times sum_i |x_i R_ij| (the
+    worst case of any summation order), and the root-mean-square error within
+    2 sqrt(D) u times the root mean square of those sums (rounding errors that
+    add as a random walk; a product in bf16 arithmetic would exceed it by four
+    orders of magnitude).  The
+    rows are not correctly rounded, so the codec is checked on the GPU's own
+    rows: the oracle quantises the rows each call exports through
+    debug_rot_out (identity rotation, no Hadamard) and the two caches must
+    match byte for byte."""
     p = draw_append(seed)
     D, B, Hkv = p["D"], p["B"], p["Hkv"]
     had = bool(p["flags"] & K.FLAG_HADAMARD)
@@ -290,10 +296,15 @@ def test_sweep_append_codec_on_gpu_rows(seed):
     for n in p["chunks"]:
         k, v = _rows(rng, (B, n, Hkv, D), ch, fp32), _rows(rng, (B, n, Hkv, D), ch, fp32)
         rot = gpu_append(c, gcache, 0, k, v, pos, RK, RV, want_rot=True).cpu().numpy()
+        u = 2.0 ** -24
         for role, (x, R) in enumerate(((k, Rk64), (v, Rv64))):
             exact = x.astype(np.float64) @ R
-            err = np.abs(rot[:, :, :, role] - exact).max()
-            assert err <= 2e-6 * np.abs(exact).max(), f"{p}: role {role} rotation error {err}"
+            terms = np.abs(x.astype(np.float64)) @ np.abs(R)
+            err = np.abs(rot[:, :, :, role] - exact)
+            worst = float(np.max(err - D * u * terms))
+            assert worst <= 1e-30, f"{p}: role {role} rotation error beyond gamma_D: {worst}"
+            rms, rms_terms = float(np.sqrt(np.mean(err ** 2))), float(np.sqrt(np.mean(terms ** 2)))
+            assert rms <= 2 * np.sqrt(D) * u * rms_terms, f"{p}: role {role} rotation rms error {rms} ({rms_terms})"
         O.append(plain, ocache, 0, rot[:, :, :, 0], rot[:, :, :, 1], pos, eye, eye)
         pos = [x + n for x in pos]
     got = gcache.cpu().numpy()
