@@ -212,7 +212,10 @@ int kv_append(const oscar_kv_config* cfg, void* cache, int32_t layer, const void
  * attn_decode — one query token per sequence attends to all seq_lens[b]
  * cached positions of layer `layer` (append the current token first).
  *   q          device [B][Hq][D] bf16 (float32 with OSCAR_FLAG_IN_FP32), not rotated.
- *   seq_lens   device int32 [B], 1 <= seq_len <= capacity.
+ *   seq_lens   device int32 [B], 1 <= seq_len <= capacity; a seq_len < 1
+ *              gives that sequence a zero output and lse = -inf and sets
+ *              OSCAR_DEV_EMPTY, one above capacity is clamped to it and sets
+ *              OSCAR_DEV_OVER_CAPACITY.
  *   seq_len_hint host upper bound on seq_lens (0 = capacity); only used to
  *              size the grid when the contexts are short.
  *   R_K, R_V   device float32 [D][D] rotations of this layer (not read
