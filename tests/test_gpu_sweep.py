@@ -23,7 +23,12 @@ cache, is exact on both sides:
 
 The in-quant Hadamard is not an exact rotation in float32, so its cases decode
 the oracle's cache bytes on both sides instead (the Hadamard tests check its
-append on the GPU's own rotated rows)."""
+append on the GPU's own rotated rows).
+
+OSCAR_SWEEP_SEEDS=a-b runs every test of this file over seeds a to b - 1
+instead of the committed ones, e.g. for a long stress run."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -123,7 +128,17 @@ def _compare(c, ref, ref_lse, o16, o32, lse, lse32, what):
     assert np.array_equal(lse, lse32), f"{what}: lse depends on the output type"
 
 
-SEEDS = list(range(48))
+def _seeds(default):
+    """The committed seeds, or those of OSCAR_SWEEP_SEEDS ("a-b": seeds a to
+    b - 1, every test of this file) for a longer stress run."""
+    spec = os.environ.get("OSCAR_SWEEP_SEEDS", "")
+    if spec:
+        a, b = (int(x) for x in spec.split("-"))
+        return list(range(a, b))
+    return list(default)
+
+
+SEEDS = _seeds(range(48))
 
 
 def _config(p):
@@ -212,7 +227,7 @@ def test_sweep_chain(seed):
     _compare(c, ref, ref_lse, o16, o32, lse, lse32, f"decode_step {p}")
 
 
-@pytest.mark.parametrize("seed", range(100, 112))
+@pytest.mark.parametrize("seed", _seeds(range(100, 112)))
 def test_sweep_hadamard_decode(seed):
     p = draw(seed, hadamard=True)
     D, B, Hq, Hkv, L = p["D"], p["B"], p["Hq"], p["Hkv"], p["layer"]
@@ -260,7 +275,7 @@ def draw_append(seed: int) -> dict:
     return dict(D=D, Hkv=Hkv, B=B, S=S_, W=W, flags=flags, chunks=chunks, offs=offs, cap=cap, seed=seed)
 
 
-@pytest.mark.parametrize("seed", range(200, 224))
+@pytest.mark.parametrize("seed", _seeds(range(200, 224)))
 def test_sweep_append_codec_on_gpu_rows(seed):
     """General rotations (calibrated R_K, random orthogonal R_V, or the in-quant
     Hadamard).  The GPU's float32 rotation is checked against the float64
